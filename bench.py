@@ -1,0 +1,465 @@
+#!/usr/bin/env python3
+"""Benchmark of the Q2_0 hot path on one or more GB300s (one process per GPU).
+
+One step = one pass of the whole hot path over one batch of synthetic input of
+the 1.7B-class decoder (hidden 2048, 28 layers):
+  1. get_rows: 512 seeded token ids from a 151936 x 2048 Q2_0 embedding table;
+  2. prefill GEMM at M = 512 tokens over the layer's Q2_0 shapes gate/up
+     (6144 x 2048) and down (2048 x 6144), F32 activations, split fp16 hi+lo;
+  3. decode step: the 196 Q2_0 mat-vecs (q, k, v, o, gate, up, down x 28) at
+     ncols = 1, each matrix with its own activation vector, as one batched plan.
+value = packed-weight bytes of the decode step / the decode part's device time
+(GB/s); the GEMM's TFLOP/s (2*M*N*K per product) and get_rows' bytes/s are
+reported beside it. Inputs are resident in HBM before timing; the 396 MB of
+packed decode weights streamed every step exceed the 129 MB L2, so no kernel
+sees its inputs cached from the previous step.
+
+--impl reference runs the CPU oracle on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "Q2_0 mat-vec weight GB/s (% of HBM peak); GEMM TFLOP/s at M=512"
+WORKLOAD = "1.7B-class decoder, hidden 2048 x 28 layers: decode step (196 Q2_0 mat-vecs, ncols=1) " \
+           "+ prefill GEMM M=512 (6144x2048, 6144x2048, 2048x6144) + get_rows 512 of 151936x2048"
+VOCAB = 151936
+HIDDEN = 2048
+PREFILL_M = 512
+GEMM_SHAPES = [("gate", 6144, 2048), ("up", 6144, 2048), ("down", 2048, 6144)]
+N_IDS = 512
+SEED = 1002
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(dist, value: float, device=None) -> float:
+    """Max over ranks (identity with one rank)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"q2_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload construction (host arrays; identical for both arms)
+# ---------------------------------------------------------------------------
+def decode_inputs(ncols: int = 1):
+    mats = synth.decode_step_1p7b()
+    out = []
+    for idx, (layer, m) in enumerate(mats):
+        g = synth.rng(SEED, idx)
+        w = synth.packed_matrix(g, m.N, m.K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+        x = synth.activations(g, ncols, m.K)
+        out.append((m, w, x))
+    return out
+
+
+def gemm_inputs():
+    out = []
+    for i, (name, N, K) in enumerate(GEMM_SHAPES):
+        g = synth.rng(SEED + 3, i)
+        w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+        x = synth.activations(g, PREFILL_M, K, synth.PREFILL_OUTLIER_FRAC, synth.PREFILL_OUTLIER)
+        out.append((name, N, K, w, x))
+    return out
+
+
+def rows_inputs():
+    g = synth.rng(SEED + 5)
+    table = synth.packed_matrix(g, VOCAB, HIDDEN, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    ids = synth.token_ids(g, N_IDS, VOCAB, 0.05)
+    return table, ids
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import bit_ternary_matmul_gb300 as q
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    q.build()
+    if q.q2_0_device_check() != q.Q2_0_OK:
+        raise SystemExit("q2_0: current device is not compute capability 10.3")
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(device=dev)
+
+    # ---- resident inputs -------------------------------------------------
+    dec = decode_inputs(1)
+    dec_bytes = sum(w.size for _, w, _ in dec)
+    dec_x_bytes = sum(x.nbytes for _, _, x in dec)
+    dec_y_bytes = sum(m.N * 4 for m, _, _ in dec)
+    d_dec = []
+    for m, w, x in dec:
+        d_dec.append((torch.from_numpy(w).to(dev), torch.from_numpy(x).to(dev),
+                      torch.empty((1, m.N), dtype=torch.float32, device=dev), m.N, m.K))
+    plan = q.MvPlan(d_dec, 1)
+
+    gm = gemm_inputs()
+    d_gm = []
+    for name, N, K, w, x in gm:
+        ws = torch.empty(q.q2_0_mul_mat_workspace_size(PREFILL_M, N, K), dtype=torch.uint8,
+                         device=dev)
+        d_gm.append((torch.from_numpy(w).to(dev), torch.from_numpy(x).to(dev),
+                     torch.empty((PREFILL_M, N), dtype=torch.float32, device=dev), N, K, ws))
+    gemm_flops = sum(2.0 * PREFILL_M * N * K for _, N, K, _, _ in gm)
+
+    table, ids = rows_inputs()
+    d_table = torch.from_numpy(table).to(dev)
+    d_ids = torch.from_numpy(ids).to(dev)
+    d_rows = torch.empty((N_IDS, HIDDEN), dtype=torch.float32, device=dev)
+    rows_bytes = N_IDS * (HIDDEN // 64) * 18 + N_IDS * HIDDEN * 4
+    del dec, gm, table
+    torch.cuda.synchronize()
+
+    launches_per_step = 1 + 2 * len(d_gm) + plan.launches
+
+    def step(ev=None):
+        with torch.cuda.stream(stream):
+            if ev:
+                ev[0].record(stream)
+            q.q2_0_get_rows(d_table, VOCAB, HIDDEN, d_ids, out=d_rows, stream=stream)
+            if ev:
+                ev[1].record(stream)
+            for w, x, y, N, K, ws in d_gm:
+                q.q2_0_mul_mat(w, x, N, K, PREFILL_M, q.Q2_0_PREC_F16_SPLIT, y=y, workspace=ws,
+                               stream=stream)
+            if ev:
+                ev[2].record(stream)
+            plan.execute(stream)
+            if ev:
+                ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    code, info = q.q2_0_get_error(stream)
+    if code != 0:
+        raise SystemExit(f"device error word {code} (info {info}) after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)  # first clock sample lands before the timed region
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+
+    total_ms = t_start.elapsed_time(t_end)
+    rows_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    gemm_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    dec_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    ms_per_step = total_ms / args.steps
+    # max over ranks (each rank runs its own decoder replica: weak scaling)
+    ms_per_step = reduce_max(dist, ms_per_step, dev)
+    dec_ms = reduce_max(dist, dec_ms, dev)
+    gemm_ms = reduce_max(dist, gemm_ms, dev)
+    rows_ms = reduce_max(dist, rows_ms, dev)
+
+    value = world * dec_bytes / (dec_ms * 1e-3) / 1e9
+    gemm_tflops = world * gemm_flops / (gemm_ms * 1e-3) / 1e12
+    rows_gbs = world * rows_bytes / (rows_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers --------------
+    e2e = measure_e2e(args, q, torch, dev, stream, d_dec, plan, dec_bytes, dec_x_bytes,
+                      dec_y_bytes)
+    e2e_val = reduce_sum(dist, e2e["value"], dev) if dist else e2e["value"]
+    e2e["value"] = e2e_val
+
+    code, info = q.q2_0_get_error(stream)
+    if code != 0:
+        raise SystemExit(f"device error word {code} (info {info}) after timing")
+
+    # ---- roofline of the dominant kernels -----------------------------------
+    per_gpu_dec = dec_bytes / (dec_ms * 1e-3) / 1e9
+    hbm = peaks["hbm_gbs"]
+    roof_mv = {"bound": "hbm", "achieved": round(per_gpu_dec, 1), "peak": hbm, "unit": "GB/s",
+               "frac": round(per_gpu_dec / hbm, 4), "traffic": None,
+               "kernel": "mv_tc_kernel (decode mat-vec plan, incl. its activation prep launch)",
+               "peak_source": peaks["source"]}
+    per_gpu_gemm = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    # fp16 dense peak = measured bf16 peak (same nominal rate); split path does 2x tensor work
+    tpk = peaks["bf16_tflops_sustained"]
+    roof_gemm = {"bound": "tensor", "achieved": round(per_gpu_gemm, 2), "peak": tpk,
+                 "unit": "TFLOP/s", "frac": round(per_gpu_gemm / tpk, 4), "traffic": None,
+                 "tensor_frac_hi_lo": round(2 * per_gpu_gemm / tpk, 4),
+                 "kernel": "gemm_tc_kernel (M=512, fp16 hi+lo split, incl. prepass)",
+                 "peak_source": peaks["source"] + " bf16 (fp16 dense rate is the same)"}
+    dominant, other = (roof_mv, roof_gemm) if dec_ms >= gemm_ms else (roof_gemm, roof_mv)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "u8 weights (2-bit codes), f32 activations, fp16 tensor-core operands",
+            "data": "synthetic (seeded; no trained weights)",
+            "config": {"workload": WORKLOAD, "ncols": 1, "decode_matrices": len(d_dec),
+                       "decode_weight_bytes": dec_bytes, "prefill_M": PREFILL_M,
+                       "gemm_prec": "f16_split", "get_rows_ids": N_IDS,
+                       "l2": "inputs larger than L2 (396 MB packed weights streamed per step)",
+                       "parallelism": f"replicas x{world}"},
+            "hbm_frac": round(per_gpu_dec / hbm, 4),
+            "gemm_tflops": round(gemm_tflops, 2),
+            "get_rows_gbs": round(rows_gbs, 2),
+            "parts_ms": {"get_rows": round(rows_ms, 5), "gemm": round(gemm_ms, 5),
+                         "decode_matvec": round(dec_ms, 5)},
+            "roofline": dominant, "roofline_other": other,
+            "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk, "cpu_baseline": cpu, "impl": "ours",
+        }
+        print(json.dumps(line), flush=True)
+    plan.close()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def measure_e2e(args, q, torch, dev, stream, d_dec, plan, dec_bytes, x_bytes, y_bytes):
+    """Decode step through the public API with host buffers: per step, copy every
+    matrix's activations host->device (pinned), run the plan, copy every output
+    device->host; timed with CUDA events on the stream."""
+    hx = [torch.empty_like(x, device="cpu").pin_memory() for _, x, _, _, _ in d_dec]
+    hy = [torch.empty_like(y, device="cpu").pin_memory() for _, _, y, _, _ in d_dec]
+    for h, (_, x, _, _, _) in zip(hx, d_dec):
+        h.copy_(x.cpu())
+    steps = max(3, min(args.steps, 50))
+
+    def one():
+        with torch.cuda.stream(stream):
+            for h, (_, x, _, _, _) in zip(hx, d_dec):
+                x.copy_(h, non_blocking=True)
+            plan.execute(stream)
+            for h, (_, _, y, _, _) in zip(hy, d_dec):
+                h.copy_(y, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": round(dec_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": x_bytes, "d2h_bytes_per_step": y_bytes,
+            "ms_per_step": round(ms, 5), "steps": steps,
+            "what": "decode step: pinned H2D of 196 activation vectors + plan + D2H of outputs"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timings (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def cpu_sample_decode(budget_s: float):
+    """Oracle mat-vec over whole matrices of the decode step, in order, until about
+    budget_s seconds are spent. Returns (bytes, seconds, n_matrices)."""
+    import oracle
+    oracle.build()
+    dec_mats = synth.decode_step_1p7b()
+    done_bytes, spent, n = 0, 0.0, 0
+    for idx, (layer, m) in enumerate(dec_mats):
+        g = synth.rng(SEED, idx)
+        w = synth.packed_matrix(g, m.N, m.K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+        x = synth.activations(g, 1, m.K)
+        t0 = time.perf_counter()
+        oracle.matmul(w, m.N, m.K, x)
+        spent += time.perf_counter() - t0
+        done_bytes += w.size
+        n += 1
+        if spent >= budget_s:
+            break
+    return done_bytes, spent, n
+
+
+def cpu_baseline(budget_s: float):
+    import oracle
+    oracle.build()
+    b, s, n = cpu_sample_decode(budget_s)
+    return {"value": round(b / s / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 oracle mat-vec over the first {n} of 196 decode-step matrices "
+                      f"({b} packed bytes, {s:.1f} s), OpenMP over rows"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    budget = max(0.5, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_sample_decode(budget)
+    tot_b, tot_s = 0, 0.0
+    nmat = 0
+    for _ in range(args.steps):
+        b, s, n = cpu_sample_decode(budget)
+        tot_b += b
+        tot_s += s
+        nmat = n
+    value = tot_b / tot_s / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_s / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (CPU oracle)",
+        "data": "synthetic (seeded; no trained weights)",
+        "config": {"workload": WORKLOAD, "ncols": 1,
+                   "sample": f"each step: oracle mat-vec over the first {nmat} decode-step matrices"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"first {nmat} of 196 decode-step matrices per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

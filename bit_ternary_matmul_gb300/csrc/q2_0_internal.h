@@ -1,0 +1,58 @@
+// Host-side internals shared by the translation units of libq2_0: launch
+// helpers, TMA descriptor encoding and the kernel entry points each .cu file
+// exposes to the C-ABI layer (api.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/q2_0.h"
+
+namespace q2 {
+
+// Status of the last CUDA call -> q2_0_status.
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? Q2_0_OK : Q2_0_ECUDA; }
+
+// Checks the current device (cached per device): compute capability 10.3.
+int check_device(int *device_out);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Device address of the current device's error word (2 x u64), or nullptr.
+unsigned long long *error_word_ptr();
+
+// Encodes a 2-D tiled tensor map; returns false on failure.
+//   dtype: CU_TENSOR_MAP_DATA_TYPE_*; dims/strides in elements/bytes as the
+//   driver API defines them (dim0 innermost; stride1 = bytes between rows).
+bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t dim0,
+                    uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1,
+                    CUtensorMapSwizzle swizzle);
+
+// ---- kernels' host launchers -------------------------------------------------
+cudaError_t launch_get_rows(const uint8_t *table, int64_t n_rows, int64_t K, const int32_t *ids,
+                            int64_t n_ids, float *out, unsigned long long *err, cudaStream_t s);
+
+cudaError_t launch_quantize(const float *src, uint8_t *dst, int64_t nrows, int64_t K,
+                            cudaStream_t s);
+
+// mat-vec
+size_t matvec_workspace_bytes(int64_t K, int ncols);
+bool matvec_fast_path_ok(const void *w, int64_t K);
+int matvec_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
+               void *ws, size_t ws_bytes, cudaStream_t s);
+
+// batched mat-vec plans (opaque to the C ABI)
+int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **plan);
+int mv_plan_execute(const q2_0_mv_plan *plan, cudaStream_t s);
+int mv_plan_launches(const q2_0_mv_plan *plan);
+void mv_plan_destroy(q2_0_mv_plan *plan);
+
+// GEMM
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int prec);
+int gemm_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, int64_t M, int prec,
+             void *ws, size_t ws_bytes, cudaStream_t s);
+
+}  // namespace q2

@@ -1,0 +1,178 @@
+/*
+ * q2_0.h — C ABI of the GB300 (sm_103a) Q2_0 dequantize-fused matmul library.
+ *
+ * Q2_0 format. Sources: "WebGPU: add Q2_0 support" (bisque.today write-up of
+ * llama.cpp PR 30914), format paragraph; "Llama.cpp umí dvoubitový Q2_0 i na
+ * kartách NVIDIA" (aisvetem.cz), section "Osmnáct bajtů na čtyřiašedesát vah".
+ *   A block packs 64 weights into 18 bytes: a little-endian IEEE fp16 scale d at
+ *   byte 0, then four little-endian u32 words at bytes 2, 6, 10, 14. Element
+ *   16*w + i of the block is the code q = (word_w >> 2i) & 3, and decodes to
+ *   (q - 1) * d: codes 0/1/2/3 give -d / 0 / +d / +2d (3 is reserved by the
+ *   format but decoded by the same rule).
+ *   A weight matrix W has N rows of K weights (K a multiple of 64) stored as
+ *   N * K/64 consecutive blocks, row-major: block b of row n is at byte offset
+ *   (n * K/64 + b) * 18. No alignment is required of W.
+ *
+ * Activations and outputs follow ggml's mul_mat(src0 = W, src1 = X):
+ *   X is F32 [C][K] row-major (C = ncols or M), Y is F32 [C][N] row-major,
+ *   Y[c][n] = sum_k W[n][k] * X[c][k].
+ *
+ * Conventions for every call:
+ *   - All pointers are device pointers owned by the caller, unless stated.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *     asynchronous on it; nothing synchronises the host except
+ *     q2_0_get_error().
+ *   - The calls act on the device current to the calling thread. That device
+ *     must be compute capability 10.3 (GB300); otherwise Q2_0_EUNSUPPORTED.
+ *   - Argument errors return Q2_0_EINVAL before anything is launched. A failed
+ *     launch or runtime call returns Q2_0_ECUDA. No exception crosses the ABI.
+ *     There is no CPU fallback: every result is computed by a CUDA kernel.
+ *   - Data-dependent errors found by a kernel (an id out of range in get_rows,
+ *     a pipeline wait that timed out) are recorded in a per-device error word;
+ *     q2_0_get_error() reads and clears it.
+ */
+#ifndef Q2_0_H
+#define Q2_0_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q2_0_BLOCK_WEIGHTS 64
+#define Q2_0_BLOCK_BYTES 18
+
+typedef enum q2_0_status {
+    Q2_0_OK = 0,
+    Q2_0_EINVAL = 1,       /* bad argument; nothing was launched */
+    Q2_0_ECUDA = 2,        /* a CUDA runtime call or kernel launch failed */
+    Q2_0_EUNSUPPORTED = 3, /* the current device is not compute capability 10.3 */
+    Q2_0_EDEVICE = 4       /* a kernel recorded an error: see q2_0_get_error() */
+} q2_0_status;
+
+/* Device error codes (first error wins until cleared). */
+#define Q2_0_DEVERR_NONE 0
+#define Q2_0_DEVERR_BAD_ID 1  /* get_rows: ids[info] outside [0, n_rows) */
+#define Q2_0_DEVERR_TIMEOUT 2 /* a pipeline wait gave up; info = kernel tag */
+
+/* GEMM activation precision. F32 activations are used by the tensor cores as
+ * fp16 operands (the weights (q-1)*d are exact in fp16):
+ *   Q2_0_PREC_F16_SPLIT: x = hi + lo with hi = fp16(x), lo = fp16(x - hi); two
+ *     tensor-core products. Bound: |y - exact| <= 1e-5 * sum|w*x| + 1e-7.
+ *   Q2_0_PREC_F16: x rounded once to fp16. Bound: <= 4e-3 * sum|w*x|.
+ * Precondition of both: finite x with |x| < 65504 and |2d| <= 65504. */
+typedef enum q2_0_prec { Q2_0_PREC_F16_SPLIT = 0, Q2_0_PREC_F16 = 1 } q2_0_prec;
+
+/* Library version string (static storage). */
+const char *q2_0_version(void);
+
+/* Checks that the current device is a compute capability 10.3 GPU.
+ * Returns Q2_0_OK, Q2_0_EUNSUPPORTED or Q2_0_ECUDA. */
+int q2_0_device_check(void);
+
+/*
+ * q2_0_mul_mat_vec — decode mat-vec, Y[c][n] = sum_k W[n][k] X[c][k].
+ * Source: the mat-vec kernel of "WebGPU: add Q2_0 support" (each block's codes
+ * are multiplied by the activations and the scale d is applied once per block
+ * sum).
+ *   w      N x K Q2_0 matrix (N*K/64*18 bytes), any alignment.
+ *   x      F32 [ncols][K].   y  F32 [ncols][N] (written, not accumulated).
+ *   N >= 1, K >= 64 with K % 64 == 0, 1 <= ncols <= 8.
+ * Error bound: |y - exact| <= 1e-5 * sum_k |W[n][k] X[c][k]| + 1e-7 for finite x.
+ * Scratch: the call takes q2_0_mul_mat_vec_workspace_size(K, ncols) bytes of
+ * stream-ordered memory from the device's default memory pool
+ * (cudaMallocAsync/cudaFreeAsync on `stream`); use q2_0_mul_mat_vec_ws to
+ * supply it instead.
+ */
+int q2_0_mul_mat_vec(const void *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
+                     void *stream);
+
+/* Scratch bytes q2_0_mul_mat_vec_ws needs for (K, ncols); 0 on bad arguments. */
+size_t q2_0_mul_mat_vec_workspace_size(int64_t K, int ncols);
+
+/* As q2_0_mul_mat_vec, with caller-owned scratch `workspace` (device memory,
+ * 256-byte aligned, at least workspace_size bytes; contents are overwritten and
+ * must not be used by other work in flight). */
+int q2_0_mul_mat_vec_ws(const void *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Batched decode mat-vec: many independent (W, x, y) products, e.g. all the
+ * projections of one decoder step, run by one persistent launch with a static,
+ * cost-balanced schedule of row tiles over the GPU's SMs.
+ * q2_0_mv_plan_create records the descriptors (the pointers are kept, not the
+ * data), encodes per-matrix TMA descriptors, builds the schedule and allocates
+ * the plan's device memory and scratch. q2_0_mv_plan_execute launches the work
+ * on `stream` (two kernels: activation preparation, then the mat-vecs); it
+ * allocates nothing and may be captured in a CUDA graph. Each descriptor
+ * obeys q2_0_mul_mat_vec's rules; all share ncols.
+ */
+typedef struct q2_0_mv_desc {
+    const void *w; /* N x K Q2_0 matrix */
+    const float *x; /* F32 [ncols][K] */
+    float *y;       /* F32 [ncols][N] */
+    int64_t N;
+    int64_t K;
+} q2_0_mv_desc;
+
+typedef struct q2_0_mv_plan q2_0_mv_plan;
+
+int q2_0_mv_plan_create(const q2_0_mv_desc *descs, int n_desc, int ncols, q2_0_mv_plan **plan);
+int q2_0_mv_plan_execute(const q2_0_mv_plan *plan, void *stream);
+/* Number of kernel launches one execute performs. */
+int q2_0_mv_plan_launches(const q2_0_mv_plan *plan);
+void q2_0_mv_plan_destroy(q2_0_mv_plan *plan);
+
+/*
+ * q2_0_mul_mat — prefill GEMM, Y[m][n] = sum_k W[n][k] X[m][k], M tokens.
+ * Source: the tiled matrix multiply of "WebGPU: add Q2_0 support" (codes are
+ * unpacked into shared memory as half precision before the product).
+ *   w      N x K Q2_0 matrix.  x  F32 [M][K].  y  F32 [M][N] (written).
+ *   N, M >= 1, K >= 64 with K % 64 == 0. prec is a q2_0_prec.
+ * workspace: device memory of at least q2_0_mul_mat_workspace_size(M, N, K,
+ * prec) bytes, 256-byte aligned, or NULL to take it from the device's default
+ * memory pool on `stream` (stream-ordered).
+ */
+size_t q2_0_mul_mat_workspace_size(int64_t M, int64_t N, int64_t K, int prec);
+int q2_0_mul_mat(const void *w, const float *x, float *y, int64_t N, int64_t K, int64_t M, int prec,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * q2_0_get_rows — gather rows of a Q2_0 table into F32, bit-exact.
+ * Source: the get-rows shader of "WebGPU: add Q2_0 support" (copies rows of a
+ * Q2_0 tensor out, 64 floats per block).
+ *   table  n_rows x K Q2_0 matrix.  ids  int32 [n_ids] (repeats allowed).
+ *   out    F32 [n_ids][K]: out[r][k] = f32(q - 1) * f32(d), the IEEE product
+ *          (signed zeros kept).
+ * An id outside [0, n_rows) leaves its output row unwritten and records
+ * Q2_0_DEVERR_BAD_ID with info = its position r. n_ids == 0 is a no-op.
+ */
+int q2_0_get_rows(const void *table, int64_t n_rows, int64_t K, const int32_t *ids, int64_t n_ids,
+                  float *out, void *stream);
+
+/*
+ * q2_0_quantize_ref — the reference quantizer, bit-exact.
+ * Source: "Llama.cpp umí dvoubitový Q2_0 i na kartách NVIDIA" (aisvetem.cz),
+ * section "Na běžný model to není": the block's largest |w| is the scale and
+ * each weight is rounded to the nearest of the four levels.
+ *   src  F32 [nrows][K] (finite).  dst  nrows x K Q2_0 matrix (written).
+ * Per block: amax = max |w|; d = fp16(amax) rounded to nearest even; code 2 if
+ * 2w >= amax, code 0 if 2w <= -amax, else code 1 (ties away from zero; the
+ * decisions use the unrounded amax); amax == 0 gives d = 0 and code 1.
+ */
+int q2_0_quantize_ref(const float *src, void *dst, int64_t nrows, int64_t K, void *stream);
+
+/*
+ * q2_0_get_error — synchronises `stream`, then reads and clears the current
+ * device's error word. Returns a Q2_0_DEVERR_* code; *info (if not NULL)
+ * receives its detail. Returns -1 if the read itself failed.
+ */
+int q2_0_get_error(void *stream, int64_t *info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q2_0_H */

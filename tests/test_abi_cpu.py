@@ -1,0 +1,79 @@
+"""Host-side checks of the C-ABI library: it builds for sm_103a, loads, exports
+every symbol include/q2_0.h declares, and rejects bad arguments before touching
+a GPU. No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_ternary_matmul_gb300 as q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q2_0.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    q.build()
+    return q.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(q2_0_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_symbols_exported(L):
+    names = _declared()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(q.EXPORTS) == names
+
+
+def test_version_and_no_device(L):
+    assert "sm_103a" in q.q2_0_version()
+    import torch
+    if not torch.cuda.is_available():
+        assert q.q2_0_device_check() in (q.Q2_0_ECUDA, q.Q2_0_EUNSUPPORTED)
+
+
+def test_argument_validation_without_gpu(L):
+    p = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    null = ctypes.c_void_p(0)
+    EINVAL = q.Q2_0_EINVAL
+    # mat-vec: null pointers, K not a multiple of 64, ncols out of range, N < 1
+    assert L.q2_0_mul_mat_vec(null, p, p, 4, 64, 1, null) == EINVAL
+    assert L.q2_0_mul_mat_vec(p, p, p, 4, 100, 1, null) == EINVAL
+    assert L.q2_0_mul_mat_vec(p, p, p, 4, 64, 0, null) == EINVAL
+    assert L.q2_0_mul_mat_vec(p, p, p, 4, 64, 9, null) == EINVAL
+    assert L.q2_0_mul_mat_vec(p, p, p, 0, 64, 1, null) == EINVAL
+    # mat-vec with workspace: too small, misaligned
+    need = L.q2_0_mul_mat_vec_workspace_size(512, 1)
+    assert need > 0 and need % 256 == 0
+    assert L.q2_0_mul_mat_vec_ws(p, p, p, 4, 512, 1, p, need - 1, null) == EINVAL
+    assert L.q2_0_mul_mat_vec_ws(p, p, p, 4, 512, 1, ctypes.c_void_p(0x1010), need, null) == EINVAL
+    assert L.q2_0_mul_mat_vec_workspace_size(100, 1) == 0
+    assert L.q2_0_mul_mat_vec_workspace_size(512, 9) == 0
+    # GEMM: bad precision, bad K, small workspace
+    assert L.q2_0_mul_mat(p, p, p, 4, 64, 4, 7, null, 0, null) == EINVAL
+    assert L.q2_0_mul_mat(p, p, p, 4, 65, 4, 0, null, 0, null) == EINVAL
+    ws = L.q2_0_mul_mat_workspace_size(4, 4, 512, 0)
+    assert ws >= 2 * 4 * 512 * 2
+    assert L.q2_0_mul_mat_workspace_size(4, 4, 512, 1) * 2 == ws
+    assert L.q2_0_mul_mat(p, p, p, 4, 512, 4, 0, ctypes.c_void_p(0x100000), ws - 1, null) == EINVAL
+    # get_rows: n_ids == 0 is a no-op, negative is invalid
+    assert L.q2_0_get_rows(p, 4, 64, p, 0, p, null) == q.Q2_0_OK
+    assert L.q2_0_get_rows(p, 4, 64, p, -1, p, null) == EINVAL
+    assert L.q2_0_get_rows(null, 4, 64, p, 3, p, null) == EINVAL
+    # quantize
+    assert L.q2_0_quantize_ref(p, p, 0, 64, null) == EINVAL
+    assert L.q2_0_quantize_ref(p, p, 2, 96, null) == EINVAL
+    # plans
+    h = ctypes.c_void_p()
+    assert L.q2_0_mv_plan_create(None, 1, 1, ctypes.byref(h)) == EINVAL
+    assert L.q2_0_mv_plan_execute(null, null) == EINVAL
+    assert L.q2_0_mv_plan_launches(null) == 0
+    L.q2_0_mv_plan_destroy(null)

@@ -1,0 +1,351 @@
+"""GPU parity: every C-ABI entry point against the CPU oracle on the same seeded
+inputs. Bit-exact for get_rows and the quantizer; for the matmuls
+|gpu - oracle| <= 1e-5 * sum|w*x| + 1e-7 (split / mat-vec paths) or
+<= 4e-3 * sum|w*x| (single-fp16 GEMM path), with the oracle's fp64 values."""
+import numpy as np
+import pytest
+import torch
+
+import bit_ternary_matmul_gb300 as q
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL_SPLIT = (1e-5, 1e-7)
+TOL_F16 = (4e-3, 0.0)
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    q.build()
+    oracle.build()
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    assert q.q2_0_device_check() == q.Q2_0_OK
+    code, _ = q.q2_0_get_error()
+    assert code == 0
+    return d
+
+
+def _to(dev, a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def _assert_close(gpu, y, acc, tol, what):
+    ok = oracle.within_tolerance(gpu, y, acc, tol[0], tol[1])
+    if not ok.all():
+        bad = np.argwhere(~ok)[:5]
+        msgs = [f"{tuple(i)}: gpu={gpu[tuple(i)]!r} ref={y[tuple(i)]!r} acc={acc[tuple(i)]!r}"
+                for i in bad]
+        raise AssertionError(f"{what}: {int((~ok).sum())} of {ok.size} outside tolerance\n" +
+                             "\n".join(msgs))
+
+
+def _no_device_error():
+    code, info = q.q2_0_get_error()
+    assert code == 0, (code, info)
+
+
+# ---------------------------------------------------------------------------
+# get_rows
+# ---------------------------------------------------------------------------
+def _edge_table(g, n_rows, K, edge_rows):
+    t = synth.packed_matrix(g, n_rows, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    edges = synth.edge_blocks()
+    nb = K // 64
+    tv = t.reshape(n_rows, nb, 18)
+    for i, r in enumerate(edge_rows):
+        # whole row of one edge pattern, then every pattern in turn
+        tv[r, :, :] = edges[i % len(edges)]
+        for j in range(min(nb, len(edges))):
+            tv[r, j] = edges[(i + j) % len(edges)]
+    return t
+
+
+def test_get_rows_embedding_table(dev):
+    """151936 x 4096 table, 512 seeded ids with repeats; ids[0..8] hit edge rows."""
+    g = synth.rng(1005, 1)
+    n_rows, K = 151936, 4096
+    head = np.array([7, 151935, 0, 77777, 4242, 123, 99999, 31, 5], dtype=np.int32)
+    t = _edge_table(g, n_rows, K, head)
+    ids = synth.token_ids(g, 512, n_rows, 0.05, head)
+    out = q.q2_0_get_rows(_to(dev, t), n_rows, K, _to(dev, ids)).cpu().numpy()
+    ref, bad = oracle.get_rows(t, n_rows, K, ids)
+    assert bad == 0
+    assert np.array_equal(out.view(np.uint32), ref.view(np.uint32))
+    _no_device_error()
+
+
+@pytest.mark.parametrize("K,offset", [(64, 0), (576, 0), (1024, 1), (2048, 4)])
+def test_get_rows_shapes_and_alignment(dev, K, offset):
+    g = synth.rng(77, K, offset)
+    n_rows = 37
+    t = _edge_table(g, n_rows, K, [0, 5, 36])
+    ids = np.array([0, 36, 5, 5, 1, 0, 20], dtype=np.int32)
+    # packed table at a byte offset (any alignment), output at a float offset
+    tb = torch.zeros(t.size + 16, dtype=torch.uint8, device=dev)
+    tb[offset:offset + t.size] = _to(dev, t)
+    ob = torch.full((ids.size * K + 1,), float("nan"), device=dev)
+    out = ob[1:] if offset else ob[:-1]
+    q.q2_0_get_rows(tb[offset:offset + t.size], n_rows, K, _to(dev, ids), out=out)
+    ref, _ = oracle.get_rows(t, n_rows, K, ids)
+    got = out.cpu().numpy().reshape(ids.size, K)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    # the guard element next to the output is untouched
+    guard = ob[0] if offset else ob[-1]
+    assert torch.isnan(guard)
+    _no_device_error()
+
+
+def test_get_rows_bad_ids_recorded(dev):
+    g = synth.rng(78)
+    n_rows, K = 10, 128
+    t = synth.packed_matrix(g, n_rows, K, 0.1, 0.2)
+    ids = np.array([3, 10, 9, -1], dtype=np.int32)
+    out = torch.full((4, K), 7.0, device=dev)
+    q.q2_0_get_rows(_to(dev, t), n_rows, K, _to(dev, ids), out=out)
+    code, info = q.q2_0_get_error()
+    assert code == q.Q2_0_DEVERR_BAD_ID and info in (1, 3)
+    o = out.cpu().numpy()
+    ref, bad = oracle.get_rows(t, n_rows, K, ids)
+    assert bad == 2
+    assert np.array_equal(o[0].view(np.uint32), ref[0].view(np.uint32))
+    assert np.array_equal(o[2].view(np.uint32), ref[2].view(np.uint32))
+    assert np.all(o[1] == 7.0) and np.all(o[3] == 7.0)   # rows of bad ids untouched
+    _no_device_error()
+
+
+# ---------------------------------------------------------------------------
+# reference quantizer
+# ---------------------------------------------------------------------------
+def test_quantize_random_blocks_bitexact(dev):
+    """>= 14,000 random blocks (normal, uniform, heavy-tailed, ties, zeros), bit-exact."""
+    g = synth.rng(31337)
+    rows = []
+    rows.append(g.standard_normal((4000, 64)))
+    rows.append(g.uniform(-1, 1, (4000, 64)))
+    rows.append(g.standard_cauchy((4000, 64)) * 1e-3)
+    tie = g.uniform(-1, 1, (2000, 64))
+    amax = np.max(np.abs(tie), axis=1, keepdims=True)
+    sel = g.integers(0, 64, (2000, 8))
+    for r in range(2000):
+        tie[r, sel[r, :4]] = amax[r] / 2
+        tie[r, sel[r, 4:]] = -amax[r] / 2
+    rows.append(tie)
+    rows.append(np.zeros((50, 64)))
+    rows.append(g.standard_normal((100, 64)) * 1e-7)    # scale rounds to subnormal fp16
+    rows.append(g.standard_normal((100, 64)) * 1e4)     # scale near the fp16 top
+    src = np.concatenate(rows).astype(np.float32)
+    n = src.shape[0]
+    assert n >= 14000
+    got = q.q2_0_quantize_ref(_to(dev, src), n, 64).cpu().numpy()
+    ref = oracle.quantize(src, n, 64)
+    assert np.array_equal(got, ref)
+    _no_device_error()
+
+
+def test_quantize_rows_misaligned_dst(dev):
+    g = synth.rng(31338)
+    src = g.standard_normal((9, 576)).astype(np.float32)
+    nbytes = 9 * 9 * 18
+    buf = torch.zeros(nbytes + 3, dtype=torch.uint8, device=dev)
+    q.q2_0_quantize_ref(_to(dev, src), 9, 576, dst=buf[1:1 + nbytes])
+    assert np.array_equal(buf[1:1 + nbytes].cpu().numpy(), oracle.quantize(src, 9, 576))
+    assert int(buf[0]) == 0 and int(buf[-1]) == 0
+    _no_device_error()
+
+
+# ---------------------------------------------------------------------------
+# decode mat-vec
+# ---------------------------------------------------------------------------
+MV_CASES = [
+    (2048, 2048, 1),   # the 2048 x 2048 single-matrix workload
+    (1, 512, 1), (3, 1024, 2), (127, 512, 3), (300, 2048, 4), (257, 1536, 5),
+    (64, 512, 8), (1000, 6144, 7), (513, 4096, 6),
+    (33, 576, 1), (5, 64, 3), (130, 1088, 8),   # K % 512 != 0: CUDA-core path
+]
+
+
+@pytest.mark.parametrize("N,K,ncols", MV_CASES)
+def test_matvec_parity(dev, N, K, ncols):
+    g = synth.rng(2001, N, K, ncols)
+    w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    x = synth.activations(g, ncols, K, 0.001, 30.0)
+    y = q.q2_0_mul_mat_vec(_to(dev, w), _to(dev, x), N, K, ncols).cpu().numpy()
+    yo, acc = oracle.matmul(w, N, K, x)
+    _assert_close(y, yo, acc, TOL_SPLIT, f"mat-vec {N}x{K} ncols={ncols}")
+    _no_device_error()
+
+
+@pytest.mark.parametrize("offset", [1, 2, 8])
+def test_matvec_unaligned_weights(dev, offset):
+    g = synth.rng(2002, offset)
+    N, K, ncols = 70, 1024, 2
+    w = synth.packed_matrix(g, N, K, 0.01, 0.05, 0.01)
+    x = synth.activations(g, ncols, K)
+    buf = torch.zeros(w.size + 16, dtype=torch.uint8, device=dev)
+    buf[offset:offset + w.size] = _to(dev, w)
+    y = q.q2_0_mul_mat_vec(buf[offset:offset + w.size], _to(dev, x), N, K, ncols).cpu().numpy()
+    yo, acc = oracle.matmul(w, N, K, x)
+    _assert_close(y, yo, acc, TOL_SPLIT, f"mat-vec offset {offset}")
+
+
+@pytest.mark.parametrize("kind", ["tiny", "huge", "zero_col", "outliers", "edge_blocks", "code3"])
+def test_matvec_value_ranges(dev, kind):
+    g = synth.rng(2003, hash(kind) % 1000)
+    N, K, ncols = 260, 2048, 4
+    w = synth.packed_matrix(g, N, K, 0.005, 0.05, 0.01)
+    x = synth.activations(g, ncols, K)
+    if kind == "tiny":
+        x *= np.float32(1e-6)
+    elif kind == "huge":
+        x *= np.float32(1e3)
+    elif kind == "zero_col":
+        x[1] = 0
+        x[3, ::7] = 0
+    elif kind == "outliers":
+        x = synth.activations(g, ncols, K, 0.01, 30.0)
+    elif kind == "edge_blocks":
+        edges = synth.edge_blocks()
+        wv = w.reshape(N, K // 64, 18)
+        # finite edge blocks only (the 65504 scale keeps |2d| finite in f32)
+        for r in range(0, N, 3):
+            wv[r, r % (K // 64)] = edges[r % len(edges)]
+    elif kind == "code3":
+        w = synth.packed_matrix(g, N, K, 0.005, 0.05, 0.3)
+    y = q.q2_0_mul_mat_vec(_to(dev, w), _to(dev, x), N, K, ncols).cpu().numpy()
+    yo, acc = oracle.matmul(w, N, K, x)
+    _assert_close(y, yo, acc, TOL_SPLIT, f"mat-vec {kind}")
+
+
+def test_matvec_ws_entry_point(dev):
+    g = synth.rng(2004)
+    N, K, ncols = 400, 3072, 3
+    w = synth.packed_matrix(g, N, K, 0.01, 0.05)
+    x = synth.activations(g, ncols, K)
+    need = q.q2_0_mul_mat_vec_workspace_size(K, ncols)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    y = q.q2_0_mul_mat_vec_ws(_to(dev, w), _to(dev, x), N, K, ncols, ws).cpu().numpy()
+    yo, acc = oracle.matmul(w, N, K, x)
+    _assert_close(y, yo, acc, TOL_SPLIT, "mat-vec ws")
+
+
+@pytest.mark.parametrize("ncols", [1, 2, 4, 8])
+def test_plan_mixed_shapes(dev, ncols):
+    g = synth.rng(2005, ncols)
+    shapes = [(256, 512), (1000, 2048), (1, 1024), (777, 1536), (96, 576), (2048, 6144), (33, 64)]
+    ents, host = [], []
+    for (N, K) in shapes:
+        w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+        x = synth.activations(g, ncols, K)
+        yd = torch.full((ncols, N), float("nan"), device=dev)
+        ents.append((_to(dev, w), _to(dev, x), yd, N, K))
+        host.append((w, x))
+    plan = q.MvPlan(ents, ncols)
+    assert plan.launches == 2 + 2   # prep + tensor-core kernel, two CUDA-core matrices
+    for rep in range(2):
+        plan.execute()
+        torch.cuda.synchronize()
+        for (w, x), (_, _, yd, N, K) in zip(host, ents):
+            yo, acc = oracle.matmul(w, N, K, x)
+            _assert_close(yd.cpu().numpy(), yo, acc, TOL_SPLIT, f"plan {N}x{K} rep {rep}")
+    plan.close()
+    _no_device_error()
+
+
+def _decode_step(dev, mats, seed, ncols):
+    ents, host = [], []
+    for idx, (layer, m) in enumerate(mats):
+        g = synth.rng(seed, idx)
+        w = synth.packed_matrix(g, m.N, m.K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+        x = synth.activations(g, ncols, m.K)
+        ents.append((_to(dev, w), _to(dev, x), torch.empty((ncols, m.N), device=dev), m.N, m.K))
+        host.append((w, x))
+    return ents, host
+
+
+@pytest.mark.parametrize("ncols", [1, 8])
+def test_plan_1p7b_decode_step_sampled(dev, ncols):
+    """All 196 matrices of the 1.7B-class step; 24 sampled rows of each checked."""
+    mats = synth.decode_step_1p7b()
+    ents, host = _decode_step(dev, mats, 1002, ncols)
+    plan = q.MvPlan(ents, ncols)
+    plan.execute()
+    torch.cuda.synchronize()
+    g = synth.rng(1002, 999)
+    for (w, x), (_, _, yd, N, K) in zip(host, ents):
+        rows = np.unique(np.concatenate([[0, N - 1], g.integers(0, N, 22)]))
+        yo, acc = oracle.matmul(w, N, K, x, rows=rows)
+        _assert_close(yd[:, rows].cpu().numpy(), yo, acc, TOL_SPLIT, f"1.7B step {N}x{K}")
+    plan.close()
+    _no_device_error()
+
+
+def test_plan_8b_decode_step_sampled(dev):
+    """All 253 matrices of the 8B-class step with the 151936 x 4096 head, ncols = 1."""
+    mats = synth.decode_step_8b(with_head=True)
+    ents, host = _decode_step(dev, mats, 1003, 1)
+    plan = q.MvPlan(ents, 1)
+    plan.execute()
+    torch.cuda.synchronize()
+    g = synth.rng(1003, 999)
+    for (w, x), (_, _, yd, N, K) in zip(host, ents):
+        rows = np.unique(np.concatenate([[0, N - 1], g.integers(0, N, 14)]))
+        yo, acc = oracle.matmul(w, N, K, x, rows=rows)
+        _assert_close(yd[:, rows].cpu().numpy(), yo, acc, TOL_SPLIT, f"8B step {N}x{K}")
+    plan.close()
+    _no_device_error()
+
+
+# ---------------------------------------------------------------------------
+# prefill GEMM
+# ---------------------------------------------------------------------------
+GEMM_SMALL = [(128, 512, 128), (300, 1024, 70), (1, 512, 1), (200, 1536, 17), (130, 2048, 257),
+              (256, 512, 300), (40, 576, 9), (17, 64, 5)]
+
+
+@pytest.mark.parametrize("prec", [q.Q2_0_PREC_F16_SPLIT, q.Q2_0_PREC_F16])
+@pytest.mark.parametrize("N,K,M", GEMM_SMALL)
+def test_gemm_parity_small(dev, N, K, M, prec):
+    g = synth.rng(3001, N, K, M)
+    w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    x = synth.activations(g, M, K, synth.PREFILL_OUTLIER_FRAC, synth.PREFILL_OUTLIER)
+    y = q.q2_0_mul_mat(_to(dev, w), _to(dev, x), N, K, M, prec).cpu().numpy()
+    yo, acc = oracle.matmul(w, N, K, x)
+    tol = TOL_SPLIT if prec == q.Q2_0_PREC_F16_SPLIT else TOL_F16
+    _assert_close(y, yo.T, acc.T, tol, f"GEMM {N}x{K} M={M} prec={prec}")
+    _no_device_error()
+
+
+def test_gemm_caller_workspace_and_unaligned(dev):
+    g = synth.rng(3002)
+    N, K, M = 200, 1024, 33
+    w = synth.packed_matrix(g, N, K, 0.01, 0.05)
+    x = synth.activations(g, M, K)
+    ws = torch.empty(q.q2_0_mul_mat_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+    y = q.q2_0_mul_mat(_to(dev, w), _to(dev, x), N, K, M, workspace=ws).cpu().numpy()
+    yo, acc = oracle.matmul(w, N, K, x)
+    _assert_close(y, yo.T, acc.T, TOL_SPLIT, "GEMM caller workspace")
+    buf = torch.zeros(w.size + 8, dtype=torch.uint8, device=dev)
+    buf[3:3 + w.size] = _to(dev, w)
+    y = q.q2_0_mul_mat(buf[3:3 + w.size], _to(dev, x), N, K, M).cpu().numpy()
+    _assert_close(y, yo.T, acc.T, TOL_SPLIT, "GEMM unaligned weights")
+
+
+@pytest.mark.parametrize("prec", [q.Q2_0_PREC_F16_SPLIT, q.Q2_0_PREC_F16])
+@pytest.mark.parametrize("N,K,M", [(6144, 2048, 512), (2048, 6144, 512), (4096, 4096, 2048),
+                                   (12288, 4096, 2048), (4096, 12288, 2048)])
+def test_gemm_prefill_shapes_sampled(dev, N, K, M, prec):
+    """The 1.7B (M=512) and 8B (M=2048) prefill shapes; 96 sampled weight rows x all M."""
+    g = synth.rng(3003, N, K, M)
+    w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    x = synth.activations(g, M, K, synth.PREFILL_OUTLIER_FRAC, synth.PREFILL_OUTLIER)
+    y = q.q2_0_mul_mat(_to(dev, w), _to(dev, x), N, K, M, prec)
+    rows = np.unique(np.concatenate([[0, 127, 128, N - 1], g.integers(0, N, 92)]))
+    yo, acc = oracle.matmul(w, N, K, x, rows=rows)
+    got = y[:, torch.from_numpy(rows).to(dev)].cpu().numpy()
+    tol = TOL_SPLIT if prec == q.Q2_0_PREC_F16_SPLIT else TOL_F16
+    _assert_close(got, yo, acc, tol, f"GEMM {N}x{K} M={M} prec={prec}")
+    _no_device_error()
