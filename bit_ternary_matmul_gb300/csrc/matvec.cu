@@ -51,12 +51,18 @@ namespace {
 constexpr int kTileRows = 256;
 constexpr int kChunkBlocks = 8;
 constexpr int kChunkBytes = kChunkBlocks * 18;  // 144
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kWStageBytes = kTileRows * kChunkBytes;  // 36864
-constexpr int kRecBytes = 1056;  // per block per n-tile: 32 lanes x 8 u32 + 8 f32
+// Record per block per n-tile, for S = lane slots that carry data (8 per column
+// for ncols <= 4, 4 per column for 5..8): B-fragment registers 0..3 of the S
+// slots (16 B each), registers 4..7 of the slots, then for each lane group c
+// the accumulator start (s[2c], s[2c+1], s[2c], s[2c+1]) (64 B). Data lanes
+// occupy consecutive slots, so their 16-byte loads are dense.
 constexpr int kPrepHeader = 64;  // float out_scale[8] (+ pad)
-constexpr int kStages = 4;
+constexpr int kMaxStages = 8;
+// Dynamic shared memory the ring may use: the opt-in maximum less the static
+// part and the barriers.
+constexpr int kSmemBudget = 232448 - 1024 - 2 * kMaxStages * 8;
+constexpr int kPrepThreads = 512;
 
 // Timeout tags (info of Q2_0_DEVERR_TIMEOUT).
 constexpr int kTagMvFull = 101;
@@ -88,44 +94,100 @@ struct MvParams {
     const MvItem *items;      // per-CTA work lists (schedule), when jobs != nullptr
     const int *cta_begin;     // [gridDim.x + 1]
     int ncols;
+    int n_stages;             // pipeline depth (n_stages_for(ncols))
     unsigned long long *err;
 };
 
 __host__ __device__ constexpr int n_tiles_for(int ncols) { return ncols <= 4 ? 1 : 2; }
+__host__ __device__ constexpr int used_slots(int ncols) {
+    return n_tiles_for(ncols) == 1 ? 8 * ncols : 4 * ncols;
+}
+__host__ __device__ constexpr int rec_bytes(int ncols) { return 32 * used_slots(ncols) + 64; }
+__host__ __device__ constexpr int rstage_bytes(int ncols) {
+    return kChunkBlocks * n_tiles_for(ncols) * rec_bytes(ncols);
+}
+constexpr int n_stages_for(int ncols) {
+    return kSmemBudget / (kWStageBytes + rstage_bytes(ncols)) < kMaxStages
+               ? kSmemBudget / (kWStageBytes + rstage_bytes(ncols))
+               : kMaxStages;
+}
+constexpr int smem_bytes_for(int ncols) {
+    return n_stages_for(ncols) * (kWStageBytes + rstage_bytes(ncols)) + 2 * kMaxStages * 8;
+}
 
 size_t prep_bytes_for(int64_t K, int ncols) {
-    size_t b = kPrepHeader + size_t(K / 64) * n_tiles_for(ncols) * kRecBytes;
+    size_t b = kPrepHeader + size_t(K / 64) * n_tiles_for(ncols) * rec_bytes(ncols);
     return (b + 255) & ~size_t(255);
 }
 
 // ---------------------------------------------------------------------------
 // Activation preparation: grid (ncols, n_jobs), 256 threads.
 // ---------------------------------------------------------------------------
+// Lane slot of MMA lane L = 4g + c in a record. NT == 1: column groups g < 4
+// carry hi parts of columns 0..ncols-1, g >= 4 the lo parts; NT == 2: g < ncols.
+__host__ __device__ __forceinline__ int lane_slot(int nt, int lane, int ncols) {
+    const int g = lane >> 2, c = lane & 3;
+    return nt == 1 ? (((g & 3) + (g >> 2) * ncols) * 4 + c) : lane;
+}
+
+// Accumulator start of MMA column n (the -sum for all-ones codes): stored at
+// both places lane group n/2 loads it from.
+__device__ __forceinline__ void put_start(uint8_t *rec, int s_used, int n, float v) {
+    float *q = reinterpret_cast<float *>(rec + 32 * s_used + (n >> 1) * 16) + (n & 1);
+    q[0] = v;
+    q[2] = v;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
     return uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
 }
 
 template <int NT>
-__global__ void __launch_bounds__(256) mv_prep_kernel(const __grid_constant__ MvPrepJob single,
-                                                      const MvPrepJob *__restrict__ jobs,
-                                                      int ncols) {
+__global__ void __launch_bounds__(kPrepThreads) mv_prep_kernel(
+    const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs, int ncols) {
+    // The mat-vec kernel that follows may start its prologue (barrier set-up,
+    // weight loads) now; it waits for this grid before reading the fragments.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const MvPrepJob &J = jobs ? jobs[blockIdx.y] : single;
     const int K = J.K;
     const int j = blockIdx.x;  // activation column
     const float *xj = J.x + size_t(j) * K;
     const int tid = threadIdx.x;
+    const int nb = K / 64;
 
-    // 1) column scale 2^s with max|x * 2^s| in [2^14, 2^15)
+    // 1) column scale 2^s with max|x * 2^s| in [2^14, 2^15). The thread's first
+    //    16-element group stays in registers for step 2.
+    float first[16];
     float m = 0.0f;
-    for (int k = tid; k < K; k += 256) m = fmaxf(m, fabsf(xj[k]));
+    if (tid < nb * 4) {
+        if ((reinterpret_cast<uintptr_t>(xj) & 15u) == 0) {
+            const float4 *src = reinterpret_cast<const float4 *>(xj + tid * 16);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const float4 f = src[q4];
+                first[4 * q4] = f.x;
+                first[4 * q4 + 1] = f.y;
+                first[4 * q4 + 2] = f.z;
+                first[4 * q4 + 3] = f.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) first[i] = xj[tid * 16 + i];
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(first[i]));
+    }
+    for (int k = (kPrepThreads + tid) * 16; k < K; k += kPrepThreads * 16)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(xj[k + i]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    __shared__ float red[8];
+    __shared__ float red[kPrepThreads / 32];
     if ((tid & 31) == 0) red[tid >> 5] = m;
     __syncthreads();
     float amax = red[0];
 #pragma unroll
-    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+    for (int w = 1; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
     int s = 0;
     if (amax > 0.0f && amax <= 3.4e38f) {
         int e;
@@ -137,18 +199,18 @@ __global__ void __launch_bounds__(256) mv_prep_kernel(const __grid_constant__ Mv
     if (j == 0 && tid < 8 && tid >= ncols) out_scale[tid] = 0.0f;
 
     // 2) fragments. Thread handles (block b, word c): the 16 elements 16c..16c+15.
-    const int nb = K / 64;
     const float fscale[4] = {ldexpf(1.0f, s), ldexpf(1.0f, s - 2), ldexpf(1.0f, s - 4),
                              ldexpf(1.0f, s - 6)};
     const int lane = tid & 31;
-    for (int idx = tid; idx < nb * 4; idx += 256) {
+    for (int idx = tid; idx < nb * 4; idx += kPrepThreads) {
         const int b = idx >> 2, c = idx & 3;
         const float *xe = xj + b * 64 + c * 16;
         __half hi[16], lo[16];
         float base_hi = 0.0f, base_lo = 0.0f;  // sum over the block of part * 4^m * 2^-24
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const float v = xe[i] * fscale[i & 3];
+            const float xv = idx == tid ? first[i] : xe[i];
+            const float v = xv * fscale[i & 3];
             hi[i] = __float2half_rn(v);
             lo[i] = __float2half_rn(v - __half2float(hi[i]));
             const float wgt = ldexpf(1.0f, 2 * (i & 3) - 24);
@@ -170,7 +232,8 @@ __global__ void __launch_bounds__(256) mv_prep_kernel(const __grid_constant__ Mv
         base_lo += __shfl_xor_sync(grp, base_lo, 1);
         base_lo += __shfl_xor_sync(grp, base_lo, 2);
 
-        uint8_t *rec0 = J.prep + kPrepHeader + size_t(b) * NT * kRecBytes;
+        const int su = used_slots(ncols), rb = rec_bytes(ncols);
+        uint8_t *rec0 = J.prep + kPrepHeader + size_t(b) * NT * rb;
         int lane_hi, lane_lo, slot_hi, slot_lo;
         uint8_t *rec_hi, *rec_lo;
         if (NT == 1) {
@@ -181,37 +244,26 @@ __global__ void __launch_bounds__(256) mv_prep_kernel(const __grid_constant__ Mv
             slot_lo = 4 + j;
         } else {
             rec_hi = rec0;
-            rec_lo = rec0 + kRecBytes;
+            rec_lo = rec0 + rb;
             lane_hi = lane_lo = 4 * j + c;
             slot_hi = slot_lo = j;
         }
-        uint4 *fh = reinterpret_cast<uint4 *>(rec_hi + lane_hi * 32);
-        uint4 *fl = reinterpret_cast<uint4 *>(rec_lo + lane_lo * 32);
-        fh[0] = make_uint4(rh[0], rh[1], rh[2], rh[3]);
-        fh[1] = make_uint4(rh[4], rh[5], rh[6], rh[7]);
-        fl[0] = make_uint4(rl[0], rl[1], rl[2], rl[3]);
-        fl[1] = make_uint4(rl[4], rl[5], rl[6], rl[7]);
+        const int sh = lane_slot(NT, lane_hi, ncols), sl = lane_slot(NT, lane_lo, ncols);
+        *reinterpret_cast<uint4 *>(rec_hi + sh * 16) = make_uint4(rh[0], rh[1], rh[2], rh[3]);
+        *reinterpret_cast<uint4 *>(rec_hi + 16 * su + sh * 16) = make_uint4(rh[4], rh[5], rh[6], rh[7]);
+        *reinterpret_cast<uint4 *>(rec_lo + sl * 16) = make_uint4(rl[0], rl[1], rl[2], rl[3]);
+        *reinterpret_cast<uint4 *>(rec_lo + 16 * su + sl * 16) = make_uint4(rl[4], rl[5], rl[6], rl[7]);
         if (c == 0) {
-            reinterpret_cast<float *>(rec_hi + 1024)[slot_hi] = -base_hi;
-            reinterpret_cast<float *>(rec_lo + 1024)[slot_lo] = -base_lo;
+            put_start(rec_hi, su, slot_hi, -base_hi);
+            put_start(rec_lo, su, slot_lo, -base_lo);
         }
-        // Column 0's CTA also zeroes the lanes and slots of unused columns.
-        if (j == 0) {
-            for (int u = ncols; u < (NT == 1 ? 4 : 8); ++u) {
-                if (NT == 1) {
-                    uint4 *z0 = reinterpret_cast<uint4 *>(rec0 + (4 * u + c) * 32);
-                    uint4 *z1 = reinterpret_cast<uint4 *>(rec0 + (4 * (4 + u) + c) * 32);
-                    z0[0] = z0[1] = z1[0] = z1[1] = make_uint4(0, 0, 0, 0);
-                    if (c == 0) {
-                        reinterpret_cast<float *>(rec0 + 1024)[u] = 0.0f;
-                        reinterpret_cast<float *>(rec0 + 1024)[4 + u] = 0.0f;
-                    }
-                } else {
-                    for (int t = 0; t < 2; ++t) {
-                        uint4 *z = reinterpret_cast<uint4 *>(rec0 + t * kRecBytes + (4 * u + c) * 32);
-                        z[0] = z[1] = make_uint4(0, 0, 0, 0);
-                        if (c == 0) reinterpret_cast<float *>(rec0 + t * kRecBytes + 1024)[u] = 0.0f;
-                    }
+        // Column 0's CTA also zeroes the column starts of unused columns.
+        if (j == 0 && c == 0) {
+            for (int t = 0; t < NT; ++t) {
+                uint8_t *rt = rec0 + t * rb;
+                for (int u = ncols; u < (NT == 1 ? 4 : 8); ++u) {
+                    put_start(rt, su, u, 0.0f);
+                    if (NT == 1) put_start(rt, su, 4 + u, 0.0f);
                 }
             }
         }
@@ -231,28 +283,10 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
           "f"(c3));
 }
 
-// The 8 A registers of one word: in[m] = word & (0x00030003 << 2m) (elements m,
-// 8+m), sh[m] = (word >> 8) & (0x00030003 << 2m) (elements 4+m, 12+m).
-struct WordRegs {
-    uint32_t in[4], sh[4];
-};
-
-__device__ __forceinline__ WordRegs split_word(uint32_t w) {
-    WordRegs r;
-    const uint32_t ws = w >> 8;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        r.in[m] = w & (0x00030003u << (2 * m));
-        r.sh[m] = ws & (0x00030003u << (2 * m));
-    }
-    return r;
+// fp16 scale at a shared-memory address, as f32 (16-bit load + convert).
+__device__ __forceinline__ float lds_half_as_float(const uint8_t *p) {
+    return __half2float(*reinterpret_cast<const __half *>(p));
 }
-
-template <int NT>
-struct BFrag {
-    uint4 f0[NT], f1[NT];  // 8 u32 per n-tile (MMA m uses regs 2m, 2m+1)
-    float2 base[NT];       // -(all-ones sum) for columns 2c, 2c+1
-};
 
 __device__ __forceinline__ uint32_t pick(const uint4 &a, const uint4 &b, int r) {
     switch (r) {
@@ -267,40 +301,55 @@ __device__ __forceinline__ uint32_t pick(const uint4 &a, const uint4 &b, int r) 
     }
 }
 
-// One block (64 weights) for one 16-row group: rows ra (regs c0,c1) and rb (c2,c3).
-template <int NT>
-__device__ __forceinline__ void block_mma(float (&acc)[NT][4], const WordRegs &wa,
-                                          const WordRegs &wb, float da, float db,
-                                          const BFrag<NT> &B) {
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        float cc[4] = {B.base[t].x, B.base[t].y, B.base[t].x, B.base[t].y};
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            float dd[4];
-            mma_16816(dd, wa.in[m], wb.in[m], wa.sh[m], wb.sh[m], pick(B.f0[t], B.f1[t], 2 * m),
-                      pick(B.f0[t], B.f1[t], 2 * m + 1), cc[0], cc[1], cc[2], cc[3]);
-            cc[0] = dd[0];
-            cc[1] = dd[1];
-            cc[2] = dd[2];
-            cc[3] = dd[3];
-        }
-        acc[t][0] = fmaf(da, cc[0], acc[t][0]);
-        acc[t][1] = fmaf(da, cc[1], acc[t][1]);
-        acc[t][2] = fmaf(db, cc[2], acc[t][2]);
-        acc[t][3] = fmaf(db, cc[3], acc[t][3]);
-    }
+// Code words and scales of one block pair for a thread's two rows (a, b):
+// element u = 0 is the even block (words straddle two aligned words), u = 1 the
+// odd block (words aligned).
+struct PairRegs {
+    uint32_t wa[2], wb[2];
+    float da[2], db[2];
+};
+
+__device__ __forceinline__ PairRegs load_pair(const uint8_t *row_a, const uint8_t *row_b, int pr,
+                                              int c) {
+    PairRegs r;
+    const uint8_t *pa = row_a + 36 * pr;
+    const uint8_t *pb = row_b + 36 * pr;
+    r.wa[0] = __byte_perm(*reinterpret_cast<const uint32_t *>(pa + 4 * c),
+                          *reinterpret_cast<const uint32_t *>(pa + 4 * c + 4), 0x5432);
+    r.wb[0] = __byte_perm(*reinterpret_cast<const uint32_t *>(pb + 4 * c),
+                          *reinterpret_cast<const uint32_t *>(pb + 4 * c + 4), 0x5432);
+    r.wa[1] = *reinterpret_cast<const uint32_t *>(pa + 20 + 4 * c);
+    r.wb[1] = *reinterpret_cast<const uint32_t *>(pb + 20 + 4 * c);
+    r.da[0] = lds_half_as_float(pa);
+    r.db[0] = lds_half_as_float(pb);
+    r.da[1] = lds_half_as_float(pa + 18);
+    r.db[1] = lds_half_as_float(pb + 18);
+    return r;
 }
 
-template <int NT>
-__global__ void __launch_bounds__(kThreads, 1) mv_tc_kernel(const __grid_constant__ MvJob single,
-                                                            const MvParams p) {
+// Consumer warps per CTA for RG 16-row groups per warp (256-row tiles).
+template <int RG>
+constexpr int consumer_warps() { return kTileRows / (16 * RG); }
+template <int RG>
+constexpr int cta_threads() { return (consumer_warps<RG>() + 1) * 32; }
+
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// NT: MMA n-tiles (1 for ncols <= 4, 2 for 5..8); RG: 16-row groups per warp.
+template <int NT, int RG>
+__global__ void __launch_bounds__(cta_threads<RG>(), 1)
+    mv_tc_kernel(const __grid_constant__ MvJob single, const MvParams p) {
+    constexpr int kCW = consumer_warps<RG>();
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t *w_stage = smem;                                  // kStages x kWStageBytes
-    uint8_t *r_stage = smem + kStages * kWStageBytes;         // kStages x 8*NT*kRecBytes
-    constexpr int kRStageBytes = kChunkBlocks * NT * kRecBytes;
+    const int kStages = p.n_stages;
+    const int su = used_slots(p.ncols), kRecBytes = rec_bytes(p.ncols);
+    const int kRStageBytes = kChunkBlocks * NT * kRecBytes;
+    uint8_t *w_stage = smem;                               // kStages x kWStageBytes
+    uint8_t *r_stage = smem + kStages * kWStageBytes;      // kStages x kRStageBytes
     uint64_t *full = reinterpret_cast<uint64_t *>(r_stage + kStages * kRStageBytes);
-    uint64_t *empty = full + kStages;
+    uint64_t *empty = full + kMaxStages;
     __shared__ int s_abort;
 
     const int warp = threadIdx.x >> 5;
@@ -309,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) mv_tc_kernel(const __grid_constan
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kConsumerWarps);
+            mbar_init(&empty[i], kCW);
         }
         s_abort = 0;
         fence_barrier_init();
@@ -337,13 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1) mv_tc_kernel(const __grid_constan
         }
     };
 
-    if (warp == kConsumerWarps) {
+    if (warp == kCW) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
             int stage = 0;
             uint32_t ph = 0;
             int issued = 0;
-            bool ok = true;
+            bool ok = true, prep_ready = false;
             for (int i = 0; i < n_items && ok; ++i) {
                 const MvJob *J;
                 int tile;
@@ -358,8 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1) mv_tc_kernel(const __grid_constan
                     mbar_arrive_expect_tx(&full[stage], kWStageBytes + kRStageBytes);
                     tma_load_2d(w_stage + stage * kWStageBytes, &J->tmap, ch * kChunkBytes,
                                 tile * kTileRows, &full[stage]);
+                    if (!prep_ready) {
+                        // The activation fragments come from the preceding kernel.
+                        grid_dependency_wait();
+                        prep_ready = true;
+                    }
                     bulk_g2s(r_stage + stage * kRStageBytes,
-                             J->prep + kPrepHeader + size_t(ch) * kChunkBlocks * NT * kRecBytes,
+                             J->prep + kPrepHeader + size_t(ch) * kRStageBytes,
                              kRStageBytes, &full[stage]);
                     ++issued;
                     if (++stage == kStages) {
@@ -384,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) mv_tc_kernel(const __grid_constan
     }
 
     // ------------------------------ consumers ------------------------------
+    grid_dependency_wait();  // the epilogue reads the column scales written by prep
     const int g = lane >> 2, c = lane & 3;
     // B lanes that carry data: NT==1 -> groups g < ncols (hi) and 4 <= g < 4+ncols (lo)
     bool lane_used[NT];
@@ -391,22 +446,31 @@ __global__ void __launch_bounds__(kThreads, 1) mv_tc_kernel(const __grid_constan
     for (int t = 0; t < NT; ++t)
         lane_used[t] = (NT == 1) ? ((g & 3) < p.ncols) : (g < p.ncols);
 
+    const int slot = lane_slot(NT, lane, p.ncols);
+    // B-fragment registers of a block pair; lanes that carry no column keep zeros.
+    uint4 fr0[2][NT], fr1[2][NT];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int t = 0; t < NT; ++t) fr0[u][t] = fr1[u][t] = make_uint4(0, 0, 0, 0);
+
     int stage = 0;
     uint32_t ph = 0;
     for (int i = 0; i < n_items; ++i) {
         const MvJob *J;
         int tile;
         item_at(i, J, tile);
-        float acc[2][NT][4];
+        const int n_chunks = J->n_chunks;
+        float acc[RG][NT][4];
 #pragma unroll
-        for (int rg = 0; rg < 2; ++rg)
+        for (int rg = 0; rg < RG; ++rg)
 #pragma unroll
             for (int t = 0; t < NT; ++t)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) acc[rg][t][k] = 0.0f;
 
         bool ok = true;
-        for (int ch = 0; ch < J->n_chunks; ++ch) {
+        for (int ch = 0; ch < n_chunks; ++ch) {
             const bool got = mbar_wait(&full[stage], ph, p.err, kTagMvFull) &&
                              !*(volatile int *)&s_abort;
             if (!__all_sync(0xffffffffu, got)) {  // warp-uniform decision
@@ -416,46 +480,59 @@ __global__ void __launch_bounds__(kThreads, 1) mv_tc_kernel(const __grid_constan
             }
             const uint8_t *ws = w_stage + stage * kWStageBytes;
             const uint8_t *rs = r_stage + stage * kRStageBytes;
-#pragma unroll 2
-            for (int pr = 0; pr < kChunkBlocks / 2; ++pr) {
+            // Block pairs (36 bytes per row). The words and scales of pair pr+1 are
+            // loaded before pair pr's MMAs, which are issued step-major across the
+            // pair's two accumulation chains.
+            const int ra = warp * 16 + g;
+            const uint8_t *row_a = ws + ra * kChunkBytes;
+            const uint8_t *row_b = row_a + 8 * kChunkBytes;
+            PairRegs nxt = load_pair(row_a, row_b, 0, c);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int blk = 2 * pr + half;
-                    BFrag<NT> B;
+            for (int pr = 0; pr < kChunkBlocks / 2; ++pr) {
+                const PairRegs cur = nxt;
+                if (pr + 1 < kChunkBlocks / 2) nxt = load_pair(row_a, row_b, pr + 1, c);
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
-                        const uint8_t *rec = rs + (blk * NT + t) * kRecBytes;
-                        if (lane_used[t]) {
-                            B.f0[t] = *reinterpret_cast<const uint4 *>(rec + lane * 32);
-                            B.f1[t] = *reinterpret_cast<const uint4 *>(rec + lane * 32 + 16);
-                        } else {
-                            B.f0[t] = B.f1[t] = make_uint4(0, 0, 0, 0);
+                        const uint8_t *rec = rs + ((2 * pr + u) * NT + t) * kRecBytes;
+                        if (lane_used[t]) {  // unused lanes keep their zero registers
+                            fr0[u][t] = *reinterpret_cast<const uint4 *>(rec + slot * 16);
+                            fr1[u][t] = *reinterpret_cast<const uint4 *>(rec + 16 * su + slot * 16);
                         }
-                        B.base[t] = *reinterpret_cast<const float2 *>(rec + 1024 + 8 * c);
+                    }
+                uint32_t sa[2], sb[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    sa[u] = __umulhi(cur.wa[u], 0x01000000u);  // >> 8 on the FMA pipe
+                    sb[u] = __umulhi(cur.wb[u], 0x01000000u);
+                }
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    float4 cc[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        cc[u] = *reinterpret_cast<const float4 *>(
+                            rs + ((2 * pr + u) * NT + t) * kRecBytes + 32 * su + 16 * c);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const uint32_t mask = 0x00030003u << (2 * m);
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            float dd[4];
+                            mma_16816(dd, cur.wa[u] & mask, cur.wb[u] & mask, sa[u] & mask,
+                                      sb[u] & mask, pick(fr0[u][t], fr1[u][t], 2 * m),
+                                      pick(fr0[u][t], fr1[u][t], 2 * m + 1), cc[u].x, cc[u].y,
+                                      cc[u].z, cc[u].w);
+                            cc[u] = make_float4(dd[0], dd[1], dd[2], dd[3]);
+                        }
                     }
 #pragma unroll
-                    for (int rg = 0; rg < 2; ++rg) {
-                        const int ra = warp * 32 + rg * 16 + g;
-                        const uint8_t *pa = ws + ra * kChunkBytes + 36 * pr;
-                        const uint8_t *pb = pa + 8 * kChunkBytes;
-                        uint32_t wa, wb, dab, dbb;
-                        if (half == 0) {
-                            const uint32_t a0 = *reinterpret_cast<const uint32_t *>(pa + 4 * c);
-                            const uint32_t a1 = *reinterpret_cast<const uint32_t *>(pa + 4 * c + 4);
-                            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(pb + 4 * c);
-                            const uint32_t b1 = *reinterpret_cast<const uint32_t *>(pb + 4 * c + 4);
-                            wa = __byte_perm(a0, a1, 0x5432);
-                            wb = __byte_perm(b0, b1, 0x5432);
-                            dab = *reinterpret_cast<const uint16_t *>(pa);
-                            dbb = *reinterpret_cast<const uint16_t *>(pb);
-                        } else {
-                            wa = *reinterpret_cast<const uint32_t *>(pa + 20 + 4 * c);
-                            wb = *reinterpret_cast<const uint32_t *>(pb + 20 + 4 * c);
-                            dab = *reinterpret_cast<const uint16_t *>(pa + 18);
-                            dbb = *reinterpret_cast<const uint16_t *>(pb + 18);
-                        }
-                        block_mma<NT>(acc[rg], split_word(wa), split_word(wb),
-                                      half_bits_to_float(dab), half_bits_to_float(dbb), B);
+                    for (int u = 0; u < 2; ++u) {
+                        acc[0][t][0] = fmaf(cur.da[u], cc[u].x, acc[0][t][0]);
+                        acc[0][t][1] = fmaf(cur.da[u], cc[u].y, acc[0][t][1]);
+                        acc[0][t][2] = fmaf(cur.db[u], cc[u].z, acc[0][t][2]);
+                        acc[0][t][3] = fmaf(cur.db[u], cc[u].w, acc[0][t][3]);
                     }
                 }
             }
@@ -472,8 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1) mv_tc_kernel(const __grid_constan
         const float *out_scale = reinterpret_cast<const float *>(J->prep);
         const int N = J->N;
 #pragma unroll
-        for (int rg = 0; rg < 2; ++rg) {
-            const int row_a = tile * kTileRows + warp * 32 + rg * 16 + g;
+        for (int rg = 0; rg < RG; ++rg) {
+            const int row_a = tile * kTileRows + warp * (16 * RG) + rg * 16 + g;
             const int row_b = row_a + 8;
             float v[4];
 #pragma unroll
@@ -543,10 +620,10 @@ __global__ void __launch_bounds__(256) mv_generic_kernel(const uint8_t *__restri
         for (int cc = 0; cc < ncols; ++cc) y[size_t(cc) * N + row] = acc[cc];
 }
 
-template <int NT>
-constexpr int smem_bytes() {
-    return kStages * (kWStageBytes + kChunkBlocks * NT * kRecBytes) + 2 * kStages * 8;
-}
+// One 16-row group per consumer warp: 16 consumer warps per CTA for both
+// n-tile counts.
+constexpr int kRG1 = 1;
+constexpr int kRG2 = 1;
 
 std::mutex g_attr_mu;
 bool g_attr_done[64][2];
@@ -558,11 +635,11 @@ cudaError_t ensure_attrs(int nt) {
     std::lock_guard<std::mutex> lk(g_attr_mu);
     if (dev < 64 && g_attr_done[dev][nt - 1]) return cudaSuccess;
     if (nt == 1)
-        e = cudaFuncSetAttribute(mv_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_bytes<1>());
+        e = cudaFuncSetAttribute(mv_tc_kernel<1, kRG1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBudget + 2 * kMaxStages * 8);
     else
-        e = cudaFuncSetAttribute(mv_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_bytes<2>());
+        e = cudaFuncSetAttribute(mv_tc_kernel<2, kRG2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBudget + 2 * kMaxStages * 8);
     if (e == cudaSuccess && dev < 64) g_attr_done[dev][nt - 1] = true;
     return e;
 }
@@ -586,20 +663,37 @@ cudaError_t launch_prep(const MvPrepJob &single, const MvPrepJob *jobs, int n_jo
                         cudaStream_t s) {
     dim3 grid(ncols, n_jobs);
     if (n_tiles_for(ncols) == 1)
-        mv_prep_kernel<1><<<grid, 256, 0, s>>>(single, jobs, ncols);
+        mv_prep_kernel<1><<<grid, kPrepThreads, 0, s>>>(single, jobs, ncols);
     else
-        mv_prep_kernel<2><<<grid, 256, 0, s>>>(single, jobs, ncols);
+        mv_prep_kernel<2><<<grid, kPrepThreads, 0, s>>>(single, jobs, ncols);
     return cudaGetLastError();
 }
 
+// The tensor-core kernel is launched as a programmatic dependent of the prep
+// kernel: its prologue and first weight loads overlap the prep's tail; its
+// producer waits for the prep grid before loading any activation fragment.
 cudaError_t launch_tc(const MvJob &single, const MvParams &prm, int grid, cudaStream_t s) {
     const int nt = n_tiles_for(prm.ncols);
     cudaError_t e = ensure_attrs(nt);
     if (e != cudaSuccess) return e;
-    if (nt == 1)
-        mv_tc_kernel<1><<<grid, kThreads, smem_bytes<1>(), s>>>(single, prm);
-    else
-        mv_tc_kernel<2><<<grid, kThreads, smem_bytes<2>(), s>>>(single, prm);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (nt == 1) {
+        cfg.blockDim = dim3(cta_threads<kRG1>());
+        cfg.dynamicSmemBytes = smem_bytes_for(prm.ncols);
+        e = cudaLaunchKernelEx(&cfg, mv_tc_kernel<1, kRG1>, single, prm);
+    } else {
+        cfg.blockDim = dim3(cta_threads<kRG2>());
+        cfg.dynamicSmemBytes = smem_bytes_for(prm.ncols);
+        e = cudaLaunchKernelEx(&cfg, mv_tc_kernel<2, kRG2>, single, prm);
+    }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -629,7 +723,7 @@ int matvec_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K,
     if (e != cudaSuccess) return Q2_0_ECUDA;
     MvJob J;
     if (!make_job(J, w, prep, y, N, K)) return Q2_0_ECUDA;
-    MvParams prm{nullptr, nullptr, nullptr, ncols, err};
+    MvParams prm{nullptr, nullptr, nullptr, ncols, n_stages_for(ncols), err};
     const int grid = std::max(1, std::min(J.n_tiles, sm_count()));
     return cuda_status(launch_tc(J, prm, grid, s));
 }
@@ -776,7 +870,8 @@ int mv_plan_execute(const q2_0_mv_plan *P, cudaStream_t s) {
             return Q2_0_ECUDA;
         MvJob dummy;
         std::memset(&dummy, 0, sizeof(dummy));
-        MvParams prm{P->d_jobs, P->d_items, P->d_cta_begin, P->ncols, P->err};
+        MvParams prm{P->d_jobs, P->d_items, P->d_cta_begin, P->ncols, n_stages_for(P->ncols),
+                     P->err};
         if (launch_tc(dummy, prm, P->grid, s) != cudaSuccess) return Q2_0_ECUDA;
     }
     for (const q2_0_mv_desc &d : P->generic)

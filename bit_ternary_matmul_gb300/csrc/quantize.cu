@@ -11,8 +11,8 @@
 //
 // One warp per 64-weight block: lane l owns elements 2l and 2l+1; the packed
 // word w (elements 16w..16w+15, code of element 16w+i at bits 2i) is OR-reduced
-// over the 8 lanes that own it and written little-endian byte by byte, so the
-// destination may have any alignment.
+// over the 8 lanes that own it; lanes 0..17 then write the block's 18 bytes
+// (little-endian), so the destination may have any alignment.
 #include "q2_0_device.cuh"
 #include "q2_0_internal.h"
 
@@ -47,18 +47,22 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float *__restrict__
         part |= __shfl_xor_sync(0xffffffffu, part, 1);
         part |= __shfl_xor_sync(0xffffffffu, part, 2);
         part |= __shfl_xor_sync(0xffffffffu, part, 4);
-        uint8_t *blk = dst + b * 18;
-        if ((lane & 7) == 0) {
-            uint8_t *p = blk + 2 + 4 * (lane >> 3);
-            p[0] = static_cast<uint8_t>(part);
-            p[1] = static_cast<uint8_t>(part >> 8);
-            p[2] = static_cast<uint8_t>(part >> 16);
-            p[3] = static_cast<uint8_t>(part >> 24);
-        }
-        if (lane == 1) {
-            const uint32_t dbits = __half_as_ushort(__float2half_rn(a));
-            blk[0] = static_cast<uint8_t>(dbits);
-            blk[1] = static_cast<uint8_t>(dbits >> 8);
+        // gather the four words, then lanes 0..17 write the block's 18 bytes
+        const uint32_t word0 = __shfl_sync(0xffffffffu, part, 0);
+        const uint32_t word1 = __shfl_sync(0xffffffffu, part, 8);
+        const uint32_t word2 = __shfl_sync(0xffffffffu, part, 16);
+        const uint32_t word3 = __shfl_sync(0xffffffffu, part, 24);
+        const uint32_t dbits = __half_as_ushort(__float2half_rn(a));
+        if (lane < 18) {
+            uint32_t v;
+            if (lane < 2) {
+                v = dbits >> (8 * lane);
+            } else {
+                const int j = lane - 2;  // code byte j = byte j%4 of word j/4
+                const uint32_t wsel = j < 4 ? word0 : (j < 8 ? word1 : (j < 12 ? word2 : word3));
+                v = wsel >> (8 * (j & 3));
+            }
+            dst[b * 18 + lane] = static_cast<uint8_t>(v & 0xFFu);
         }
     }
 }

@@ -43,6 +43,18 @@ def _assert_close(gpu, y, acc, tol, what):
                              "\n".join(msgs))
 
 
+def _assert_same_blocks(got, ref, what):
+    if np.array_equal(got, ref):
+        return
+    g = got.reshape(-1, 18)
+    r = ref.reshape(-1, 18)
+    bad = np.nonzero(np.any(g != r, axis=1))[0]
+    b = bad[0]
+    raise AssertionError(f"{what}: {bad.size} of {r.shape[0]} blocks differ; first block {b}: "
+                         f"gpu={g[b].tobytes().hex()} ref={r[b].tobytes().hex()}; "
+                         f"d differs in {int(np.sum(np.any(g[bad, :2] != r[bad, :2], axis=1)))}")
+
+
 def _no_device_error():
     code, info = q.q2_0_get_error()
     assert code == 0, (code, info)
@@ -142,7 +154,7 @@ def test_quantize_random_blocks_bitexact(dev):
     assert n >= 14000
     got = q.q2_0_quantize_ref(_to(dev, src), n, 64).cpu().numpy()
     ref = oracle.quantize(src, n, 64)
-    assert np.array_equal(got, ref)
+    _assert_same_blocks(got, ref, "quantize random blocks")
     _no_device_error()
 
 
@@ -152,7 +164,8 @@ def test_quantize_rows_misaligned_dst(dev):
     nbytes = 9 * 9 * 18
     buf = torch.zeros(nbytes + 3, dtype=torch.uint8, device=dev)
     q.q2_0_quantize_ref(_to(dev, src), 9, 576, dst=buf[1:1 + nbytes])
-    assert np.array_equal(buf[1:1 + nbytes].cpu().numpy(), oracle.quantize(src, 9, 576))
+    _assert_same_blocks(buf[1:1 + nbytes].cpu().numpy(), oracle.quantize(src, 9, 576),
+                        "quantize misaligned")
     assert int(buf[0]) == 0 and int(buf[-1]) == 0
     _no_device_error()
 
@@ -315,7 +328,7 @@ def test_gemm_parity_small(dev, N, K, M, prec):
     y = q.q2_0_mul_mat(_to(dev, w), _to(dev, x), N, K, M, prec).cpu().numpy()
     yo, acc = oracle.matmul(w, N, K, x)
     tol = TOL_SPLIT if prec == q.Q2_0_PREC_F16_SPLIT else TOL_F16
-    _assert_close(y, yo.T, acc.T, tol, f"GEMM {N}x{K} M={M} prec={prec}")
+    _assert_close(y, yo, acc, tol, f"GEMM {N}x{K} M={M} prec={prec}")
     _no_device_error()
 
 
@@ -327,11 +340,11 @@ def test_gemm_caller_workspace_and_unaligned(dev):
     ws = torch.empty(q.q2_0_mul_mat_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
     y = q.q2_0_mul_mat(_to(dev, w), _to(dev, x), N, K, M, workspace=ws).cpu().numpy()
     yo, acc = oracle.matmul(w, N, K, x)
-    _assert_close(y, yo.T, acc.T, TOL_SPLIT, "GEMM caller workspace")
+    _assert_close(y, yo, acc, TOL_SPLIT, "GEMM caller workspace")
     buf = torch.zeros(w.size + 8, dtype=torch.uint8, device=dev)
     buf[3:3 + w.size] = _to(dev, w)
     y = q.q2_0_mul_mat(buf[3:3 + w.size], _to(dev, x), N, K, M).cpu().numpy()
-    _assert_close(y, yo.T, acc.T, TOL_SPLIT, "GEMM unaligned weights")
+    _assert_close(y, yo, acc, TOL_SPLIT, "GEMM unaligned weights")
 
 
 @pytest.mark.parametrize("prec", [q.Q2_0_PREC_F16_SPLIT, q.Q2_0_PREC_F16])
