@@ -31,6 +31,8 @@ Q2_0_EINVAL = 1
 Q2_0_ECUDA = 2
 Q2_0_EUNSUPPORTED = 3
 Q2_0_EDEVICE = 4
+Q2_0_ENOSPACE = 5
+Q2_0_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 Q2_0_PREC_F16_SPLIT = 0
 Q2_0_PREC_F16 = 1
@@ -40,12 +42,12 @@ Q2_0_DEVERR_BAD_ID = 1
 Q2_0_DEVERR_TIMEOUT = 2
 
 _STATUS = {0: "Q2_0_OK", 1: "Q2_0_EINVAL", 2: "Q2_0_ECUDA", 3: "Q2_0_EUNSUPPORTED",
-           4: "Q2_0_EDEVICE"}
+           4: "Q2_0_EDEVICE", 5: "Q2_0_ENOSPACE"}
 
 # Every symbol include/q2_0.h declares.
 EXPORTS = (
     "q2_0_version", "q2_0_device_check", "q2_0_mul_mat_vec", "q2_0_mul_mat_vec_workspace_size",
-    "q2_0_mul_mat_vec_ws", "q2_0_mv_plan_create", "q2_0_mv_plan_execute",
+    "q2_0_mul_mat_vec_ws", "q2_0_mul_mat_vec_noalloc", "q2_0_mv_plan_create", "q2_0_mv_plan_execute",
     "q2_0_mv_plan_launches", "q2_0_mv_plan_destroy", "q2_0_mul_mat_workspace_size",
     "q2_0_mul_mat", "q2_0_get_rows", "q2_0_quantize_ref", "q2_0_get_error",
 )
@@ -94,6 +96,8 @@ def lib():
             L.q2_0_mul_mat_vec_workspace_size.restype = sz
             L.q2_0_mul_mat_vec_ws.argtypes = [vp, vp, vp, i64, i64, i32, vp, sz, vp]
             L.q2_0_mul_mat_vec_ws.restype = i32
+            L.q2_0_mul_mat_vec_noalloc.argtypes = [vp, vp, vp, i64, i64, i32, vp]
+            L.q2_0_mul_mat_vec_noalloc.restype = i32
             L.q2_0_mv_plan_create.argtypes = [ctypes.POINTER(_MvDesc), i32, i32,
                                               ctypes.POINTER(vp)]
             L.q2_0_mv_plan_create.restype = i32
@@ -183,6 +187,26 @@ def q2_0_mul_mat_vec_ws(w, x, N, K, ncols, workspace: torch.Tensor, y=None, stre
                                    _dev(workspace, "workspace", torch.uint8, need),
                                    workspace.numel(), _stream(stream))
     _check("q2_0_mul_mat_vec_ws", st)
+    return y
+
+
+def q2_0_mul_mat_vec_noalloc(w: torch.Tensor, x: torch.Tensor, N: int, K: int,
+                             ncols: int | None = None, y: torch.Tensor | None = None,
+                             stream=None) -> torch.Tensor:
+    """q2_0_mul_mat_vec whose scratch is the library's static device array.
+
+    For callers that cannot allocate device memory at call time. The output
+    tensor is allocated here only when ``y`` is None; pass ``y`` to keep the call
+    allocation-free. Calls that overlap on the GPU share the array and race.
+    """
+    ncols = x.shape[0] if (ncols is None and x.dim() == 2) else (ncols or 1)
+    if y is None:
+        y = torch.empty((ncols, N), dtype=torch.float32, device=x.device)
+    st = lib().q2_0_mul_mat_vec_noalloc(_dev(w, "w", torch.uint8, packed_bytes(N, K)),
+                                        _dev(x, "x", torch.float32, ncols * K),
+                                        _dev(y, "y", torch.float32, ncols * N), N, K, ncols,
+                                        _stream(stream))
+    _check("q2_0_mul_mat_vec_noalloc", st)
     return y
 
 

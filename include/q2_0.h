@@ -49,7 +49,9 @@ typedef enum q2_0_status {
     Q2_0_EINVAL = 1,       /* bad argument; nothing was launched */
     Q2_0_ECUDA = 2,        /* a CUDA runtime call or kernel launch failed */
     Q2_0_EUNSUPPORTED = 3, /* the current device is not compute capability 10.3 */
-    Q2_0_EDEVICE = 4       /* a kernel recorded an error: see q2_0_get_error() */
+    Q2_0_EDEVICE = 4,      /* a kernel recorded an error: see q2_0_get_error() */
+    Q2_0_ENOSPACE = 5      /* q2_0_mul_mat_vec_noalloc: the call needs more scratch than
+                              Q2_0_NOALLOC_SCRATCH_BYTES; nothing was launched */
 } q2_0_status;
 
 /* Device error codes (first error wins until cleared). */
@@ -97,6 +99,32 @@ size_t q2_0_mul_mat_vec_workspace_size(int64_t K, int ncols);
  * must not be used by other work in flight). */
 int q2_0_mul_mat_vec_ws(const void *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * q2_0_mul_mat_vec_noalloc — q2_0_mul_mat_vec for callers that cannot allocate
+ * device memory at call time. (The Q2_0 pages have no counterpart: this is a
+ * deployment variant of the decode mat-vec above, with the same arguments and
+ * the same result and error bound.)
+ *   Who needs it: an inference server or framework that reserves all of HBM
+ *   for its own allocator leaves nothing for cudaMalloc or the default memory
+ *   pool, and a latency-critical decode loop should not call an allocator at
+ *   all. This call allocates nothing: its scratch (the prepared activation
+ *   fragments) lives in a static device array of Q2_0_NOALLOC_SCRATCH_BYTES
+ *   that every GPU which loads the library holds until the process exits.
+ *   Limit: if q2_0_mul_mat_vec_workspace_size(K, ncols) exceeds
+ *   Q2_0_NOALLOC_SCRATCH_BYTES the call returns Q2_0_ENOSPACE (1 MiB covers K up
+ *   to 61,632 for ncols <= 4 and K up to 30,784 for ncols 5..8).
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Sharing: every call uses the same array and leaves its contents behind.
+ *   Each call rewrites all of the scratch it reads, so nothing needs clearing,
+ *   but calls whose executions overlap on the GPU (e.g. on two streams) race
+ *   on the array: serialise them.
+ */
+#define Q2_0_NOALLOC_SCRATCH_BYTES ((size_t)1 << 20)
+int q2_0_mul_mat_vec_noalloc(const void *w, const float *x, float *y, int64_t N, int64_t K,
+                             int ncols, void *stream);
 
 /*
  * Batched decode mat-vec: many independent (W, x, y) products, e.g. all the
