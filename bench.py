@@ -92,6 +92,30 @@ def load_peaks():
             "source": "fallback"}
 
 
+def source_sha256(paths) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def committed_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/traffic.json), or None when absent or when the kernel's sources
+    have changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            entry = json.load(f).get(kernel)
+        if entry and source_sha256(entry["sources"]) == entry["sha256"]:
+            return int(entry["bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle sampling during the timed region."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -317,14 +341,16 @@ def run_ours(args):
     per_gpu_dec = dec_bytes / (dec_ms * 1e-3) / 1e9
     hbm = peaks["hbm_gbs"]
     roof_mv = {"bound": "hbm", "achieved": round(per_gpu_dec, 1), "peak": hbm, "unit": "GB/s",
-               "frac": round(per_gpu_dec / hbm, 4), "traffic": None,
+               "frac": round(per_gpu_dec / hbm, 4),
+               "traffic": committed_traffic("mv_tc_kernel/decoder_1p7b_step_ncols1"),
                "kernel": "mv_tc_kernel (decode mat-vec plan, incl. its activation prep launch)",
                "peak_source": peaks["source"]}
     per_gpu_gemm = gemm_flops / (gemm_ms * 1e-3) / 1e12
     # fp16 dense peak = measured bf16 peak (same nominal rate); split path does 2x tensor work
     tpk = peaks["bf16_tflops_sustained"]
     roof_gemm = {"bound": "tensor", "achieved": round(per_gpu_gemm, 2), "peak": tpk,
-                 "unit": "TFLOP/s", "frac": round(per_gpu_gemm / tpk, 4), "traffic": None,
+                 "unit": "TFLOP/s", "frac": round(per_gpu_gemm / tpk, 4),
+                 "traffic": committed_traffic("gemm_tc_kernel/prefill_1p7b_m512"),
                  "tensor_frac_hi_lo": round(2 * per_gpu_gemm / tpk, 4),
                  "kernel": "gemm_tc_kernel (M=512, fp16 hi+lo split, incl. prepass)",
                  "peak_source": peaks["source"] + " bf16 (fp16 dense rate is the same)"}
