@@ -7,118 +7,82 @@
 // unpacked operand is (q - 1) * d in fp16, which is exact for every code and
 // every fp16 d with |2d| <= 65504, so the scale needs no separate pass.
 //
-// Data flow of one CTA (a 128-row x BN-token output tile, K in 64-wide slabs,
-// one Q2_0 block per row per slab):
-//   warp 0  TMA producer: packed W box (128 rows x 144 B = 8 slabs) into a
-//           2-deep ring; per slab the X_hi (and X_lo) tile [BN x 64] fp16 with
-//           128-byte swizzle into a kStages-deep ring.
-//   warp 1  TMEM allocation and the MMA issuer (one thread): 4 K=16 steps per
-//           slab, for hi and lo, tcgen05.mma kind::f16 M=128 N=BN, fp32
-//           accumulator in TMEM; tcgen05.commit frees the slab's ring slot.
-//   warps 2-5  expansion: thread r decodes row r's block of the slab into 64
-//           fp16 and stores them into the A tile (K-major, 128-byte swizzle);
-//           then the epilogue: tcgen05.ld of the accumulator, F32 stores.
+// Data flow of one CTA (persistent over output units of 256 weight rows x 128
+// tokens; K in 64-wide slabs, one Q2_0 block per row per slab):
+//   warp 0   TMA producer: the packed W box (256 rows x 144 B = 8 slabs) into a
+//            2-deep ring; per slab the X_hi (and X_lo) tile [128 x 64] fp16 with
+//            128-byte swizzle into a 4-deep ring.
+//   warp 1   TMEM allocation (all 512 columns) and the MMA issuer (one thread):
+//            per slab, for each of the two 128-row weight tiles, 4 K=16 steps
+//            for hi and lo: tcgen05.mma kind::f16 M=128 N=128 with the A operand
+//            (expanded weights) in TMEM and B (X) in shared memory; the fp32
+//            accumulators are TMEM columns 0..255. tcgen05.commit frees the slab.
+//   warps 2-9   expansion: thread r decodes weight row r's block of the slab
+//            into 64 fp16 values (q - 1) * d and writes them to the slab's TMEM
+//            A slot with one tcgen05.st (32 columns of its lane).
+//   warps 10-17 epilogue: tcgen05.ld of the accumulators, F32 stores, then the
+//            accumulators are released to the MMA issuer for the next unit.
+// Two weight tiles share every X tile, so shared memory carries 96 bytes per
+// clock of MMA work instead of the whole bandwidth a single 128 x 128 tile
+// would need; the weights never pass through shared memory once expanded.
 //
-// K order inside a 16-element word group is permuted to (0,8,1,9,...,7,15) on
-// both operands, so that one mask of a code word yields the fp16 pair
-// (element t, element t+8); the prepass writes X in that order.
-//
-// Activations: the prepass writes hi = fp16(x) and lo = fp16(x - hi); the
-// split path issues both products into the same accumulator.
 #include <algorithm>
 #include <cstring>
 #include <mutex>
 
 #include "q2_0_device.cuh"
+#include "q2_0_tcgen05.cuh"
 #include "q2_0_internal.h"
 
 namespace q2 {
 
 namespace {
 
-constexpr int kBM = 128;            // weight rows per tile (MMA M)
-constexpr int kBN = 128;            // tokens per tile (MMA N)
+constexpr int kBM = 128;            // weight rows per MMA tile (MMA M)
+constexpr int kWT = 2;              // weight tiles per CTA unit (256 rows)
+constexpr int kBN = 128;            // tokens per unit (MMA N)
 constexpr int kSlabK = 64;          // one Q2_0 block
-constexpr int kStages = 3;          // X / A ring depth
+constexpr int kStages = 4;          // X ring and TMEM A-slot ring depth
 constexpr int kWStages = 2;         // packed-W ring depth (8 slabs each)
-constexpr int kThreads = 192;       // 6 warps
-constexpr int kATileBytes = kBM * kSlabK * 2;     // 16 KB
+constexpr int kExpandWarps = 8;     // one thread per weight row of the unit
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kExpandWarps + kEpiWarps) * 32;  // 576
 constexpr int kXTileBytes = kBN * kSlabK * 2;     // 16 KB per part
-constexpr int kWBoxBytes = kBM * 144;             // 18 KB
-constexpr int kTmemCols = kBN;                    // fp32 accumulator columns
+constexpr int kWBoxBytes = kWT * kBM * 144;       // 36 KB
+constexpr int kTmemCols = 512;                    // 256 accumulator + 256 A-slot columns
+constexpr int kAccCol = 0;                        // tile t accumulator at t * 128
+constexpr int kASlotCol = 256;                    // slot s, tile t at 256 + (2s + t) * 32
+constexpr int kMaxGrid = 160;                     // stream-K CTAs (>= SMs of a GB300)
+constexpr int kPartialBytes = kBN * kWT * kBM * 4;  // one fp32 unit tile
 
 constexpr int kTagGemm = 200;
 
 struct GemmArgs {
-    CUtensorMap w_map;   // uint8 [N][K/64*18], box {144, 128}
+    CUtensorMap w_map;   // uint8 [N][K/64*18], box {144, 256}
     CUtensorMap xh_map;  // fp16 [M][K], box {64, 128}, 128B swizzle
     CUtensorMap xl_map;
     float *y;
     int M, N, K;
     int split;  // 1: hi + lo, 0: hi only
+    int n_units, n_mtiles;  // units = (N / 256 rounded up) x (M / 128 rounded up)
+    long long total_slabs;  // n_units * K / 64: the stream-K iteration space
+    int *counters;          // per unit: pieces finished (zeroed by the prepass)
+    float *partials;        // 2 slots per CTA of kBN x (kWT * kBM) fp32
     unsigned long long *err;
 };
 
-// ---------------------------------------------------------------------------
-// tcgen05 / TMEM wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void tmem_alloc(uint32_t *smem_dst, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_addr(smem_dst)),
-                 "r"(ncols)
-                 : "memory");
+// Stream-K: CTA c owns global slabs [T*c/G, T*(c+1)/G) of the unit-major slab
+// order; a unit whose slabs span several CTAs is finished by the last of them.
+__host__ __device__ inline long long sk_begin(int c, long long T, int G) {
+    return (T * c) / G;
 }
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+__host__ __device__ inline int sk_owner(long long g, long long T, int G) {
+    return int(((g + 1) * G + T - 1) / T) - 1;  // max c with sk_begin(c) <= g
 }
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                           uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void tc_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_addr(bar))
-        : "memory");
-}
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (SBO), version 1, leading-byte offset unused (1).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= uint64_t((saddr >> 4) & 0x3FFFu);
-    d |= uint64_t(1) << 16;
-    d |= uint64_t(1024 >> 4) << 32;
-    d |= uint64_t(1) << 46;
-    d |= uint64_t(2) << 61;
-    return d;
+// End slab (exclusive, within the unit) of a segment starting at slab kb with
+// rem slabs left in the CTA's range.
+__host__ __device__ inline int seg_end(int n_slabs, int kb, long long rem) {
+    return rem < (long long)(n_slabs - kb) ? kb + int(rem) : n_slabs;
 }
 
 // Instruction descriptor, kind::f16: D f32, A and B f16, both K-major, N, M.
@@ -133,7 +97,12 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
 __global__ void __launch_bounds__(256) gemm_prep_kernel(const float *__restrict__ x,
                                                         __half *__restrict__ xh,
                                                         __half *__restrict__ xl, int64_t groups,
-                                                        int split) {
+                                                        int split, int *counters, int n_counters) {
+    // The GEMM kernel that follows may start its prologue and weight loads now;
+    // it waits for this grid before reading X or the counters.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_counters; i += gridDim.x * blockDim.x)
+        counters[i] = 0;
     for (int64_t gidx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; gidx < groups;
          gidx += int64_t(gridDim.x) * blockDim.x) {
         const float4 *src = reinterpret_cast<const float4 *>(x + gidx * 16);
@@ -170,15 +139,24 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const float *__restrict_
 // ---------------------------------------------------------------------------
 // tcgen05 GEMM kernel
 // ---------------------------------------------------------------------------
+// Two fp16 values (q - 1) * d for k-slots (2j, 2j+1) of the permuted order: the
+// codes of elements t and t+8 of a word (t = j % 8) with the magic exponent
+// 0x6400 give 1024 + q in each half; subtract 1025, multiply by d (exact).
+__device__ __forceinline__ uint32_t expand_pair(uint32_t word, int t, __half2 d2) {
+    const uint32_t bits = ((word >> (2 * t)) & 0x00030003u) | 0x64006400u;
+    __half2 v = *reinterpret_cast<const __half2 *>(&bits);
+    v = __hmul2(__hsub2(v, __floats2half2_rn(1025.0f, 1025.0f)), d2);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // 1024-byte alignment for the swizzled tiles
+    // 1024-byte alignment for the swizzled X tiles
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
     uint8_t *xh_s = smem;                                   // kStages x 16 KB
     uint8_t *xl_s = xh_s + kStages * kXTileBytes;           // kStages x 16 KB
-    uint8_t *a_s = xl_s + kStages * kXTileBytes;            // kStages x 16 KB
-    uint8_t *w_s = a_s + kStages * kATileBytes;             // kWStages x 18 KB
+    uint8_t *w_s = xl_s + kStages * kXTileBytes;            // kWStages x 36 KB
     uint64_t *bars = reinterpret_cast<uint64_t *>(w_s + kWStages * kWBoxBytes);
     uint64_t *x_full = bars;                 // [kStages]
     uint64_t *a_full = x_full + kStages;     // [kStages]
@@ -186,26 +164,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     uint64_t *w_full = slot_free + kStages;  // [kWStages]
     uint64_t *w_free = w_full + kWStages;    // [kWStages]
     uint64_t *acc_full = w_free + kWStages;  // [1]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+    uint64_t *acc_empty = acc_full + 1;      // [1]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+    int *last_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kBM;
-    const int m0 = blockIdx.y * kBN;
     const int n_slabs = a.K / kSlabK;
+    const long long g_begin = sk_begin(blockIdx.x, a.total_slabs, gridDim.x);
+    const long long g_end = sk_begin(blockIdx.x + 1, a.total_slabs, gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&x_full[i], 1);
-            mbar_init(&a_full[i], 128);
+            mbar_init(&a_full[i], kExpandWarps);
             mbar_init(&slot_free[i], 1);
         }
         for (int i = 0; i < kWStages; ++i) {
             mbar_init(&w_full[i], 1);
-            mbar_init(&w_free[i], 128);
+            mbar_init(&w_free[i], kExpandWarps);
         }
         mbar_init(acc_full, 1);
+        mbar_init(acc_empty, kEpiWarps);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -218,152 +199,333 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
+    // Unit u -> (row pair, token tile) with the token tile fastest, so CTAs running
+    // together share weight rows in L2.
+    auto unit_coords = [&](int u, int &n0, int &m0) {
+        n0 = (u / a.n_mtiles) * (kWT * kBM);
+        m0 = (u % a.n_mtiles) * kBN;
+    };
+
     if (warp == 0) {
         // ---------------------------- TMA producer ----------------------------
         if (lane == 0) {
             const uint32_t x_bytes = kXTileBytes * (a.split ? 2 : 1);
             int st = 0, wst = 0;
             uint32_t ph = 0, wph = 0;
-            for (int kk = 0; kk < n_slabs; ++kk) {
-                if ((kk & 7) == 0) {
-                    if (!mbar_wait(&w_free[wst], wph ^ 1u, a.err, kTagGemm + 1)) break;
-                    mbar_arrive_expect_tx(&w_full[wst], kWBoxBytes);
-                    tma_load_2d(w_s + wst * kWBoxBytes, &a.w_map, (kk >> 3) * 144, n0,
-                                &w_full[wst]);
-                }
-                if (!mbar_wait(&slot_free[st], ph ^ 1u, a.err, kTagGemm + 2)) break;
-                mbar_arrive_expect_tx(&x_full[st], x_bytes);
-                tma_load_2d(xh_s + st * kXTileBytes, &a.xh_map, kk * kSlabK, m0, &x_full[st]);
-                if (a.split)
-                    tma_load_2d(xl_s + st * kXTileBytes, &a.xl_map, kk * kSlabK, m0, &x_full[st]);
-                if (++st == kStages) {
-                    st = 0;
-                    ph ^= 1u;
-                }
-                if ((kk & 7) == 7 || kk == n_slabs - 1) {
-                    if (++wst == kWStages) {
-                        wst = 0;
-                        wph ^= 1u;
+            bool ok = true, prep_done = false;
+            for (long long g = g_begin; g < g_end && ok;) {
+                const int u = int(g / n_slabs), kb = int(g % n_slabs);
+                const int ke = seg_end(n_slabs, kb, g_end - g);
+                g += ke - kb;
+                int n0, m0;
+                unit_coords(u, n0, m0);
+                for (int kk = kb; kk < ke; ++kk) {
+                    if ((kk & 7) == 0 || kk == kb) {
+                        if (!mbar_wait(&w_free[wst], wph ^ 1u, a.err, kTagGemm + 1)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&w_full[wst], kWBoxBytes);
+                        tma_load_2d(w_s + wst * kWBoxBytes, &a.w_map, (kk >> 3) * 144, n0,
+                                    &w_full[wst]);
                     }
+                    if (!mbar_wait(&slot_free[st], ph ^ 1u, a.err, kTagGemm + 2)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!prep_done) {  // X (and the counters) come from the prepass
+                        asm volatile("griddepcontrol.wait;" ::: "memory");
+                        prep_done = true;
+                    }
+                    mbar_arrive_expect_tx(&x_full[st], x_bytes);
+                    tma_load_2d(xh_s + st * kXTileBytes, &a.xh_map, kk * kSlabK, m0, &x_full[st]);
+                    if (a.split)
+                        tma_load_2d(xl_s + st * kXTileBytes, &a.xl_map, kk * kSlabK, m0,
+                                    &x_full[st]);
+                    if (++st == kStages) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                    if ((kk & 7) == 7 || kk == ke - 1) {
+                        if (++wst == kWStages) {
+                            wst = 0;
+                            wph ^= 1u;
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                *(volatile int *)abort_flag = 1;
+                // Let the copies already issued land before the CTA exits (bounded).
+                int s2 = st, p2 = int(ph);
+                for (int k = 0; k < kStages; ++k) {
+                    if (--s2 < 0) {
+                        s2 = kStages - 1;
+                        p2 ^= 1;
+                    }
+                    mbar_wait(&x_full[s2], uint32_t(p2), a.err, kTagGemm + 9);
+                }
+                int w2 = wst, q2p = int(wph);
+                for (int k = 0; k < kWStages; ++k) {
+                    if (--w2 < 0) {
+                        w2 = kWStages - 1;
+                        q2p ^= 1;
+                    }
+                    mbar_wait(&w_full[w2], uint32_t(q2p), a.err, kTagGemm + 10);
                 }
             }
         }
     } else if (warp == 1) {
         // ----------------------------- MMA issuer -----------------------------
-        if (lane == 0) {
-            const uint32_t idesc = idesc_f16(kBM, kBN);
-            int st = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            for (int kk = 0; kk < n_slabs && ok; ++kk) {
-                if (!mbar_wait(&x_full[st], ph, a.err, kTagGemm + 3) ||
-                    !mbar_wait(&a_full[st], ph, a.err, kTagGemm + 4)) {
+        // The whole warp runs the loop (addresses and descriptors stay
+        // warp-uniform); the elected lane issues the MMAs and their commits.
+        const uint32_t idesc = idesc_f16(kBM, kBN);
+        const bool leader = elect_one();
+        int st = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        int nu = 0;
+        for (long long g = g_begin; g < g_end && ok; ++nu) {
+            const int kb = int(g % n_slabs);
+            const int ke = seg_end(n_slabs, kb, g_end - g);
+            g += ke - kb;
+            if (nu > 0 &&
+                !__all_sync(0xffffffffu,
+                            mbar_wait(acc_empty, uint32_t((nu - 1) & 1), a.err, kTagGemm + 3))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kk = kb; kk < ke; ++kk) {
+                const bool got = mbar_wait(&x_full[st], ph, a.err, kTagGemm + 4) &&
+                                 mbar_wait(&a_full[st], ph, a.err, kTagGemm + 5);
+                if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a_addr = smem_addr(a_s + st * kATileBytes);
                 const uint32_t h_addr = smem_addr(xh_s + st * kXTileBytes);
                 const uint32_t l_addr = smem_addr(xl_s + st * kXTileBytes);
+                if (leader) {
+                    // consecutive MMAs alternate between the two accumulators
 #pragma unroll
-                for (int ks = 0; ks < kSlabK / 16; ++ks) {
-                    const uint64_t ad = sw128_desc(a_addr + ks * 32);
-                    tc_mma_f16(tmem_base, ad, sw128_desc(h_addr + ks * 32), idesc,
-                               (kk > 0 || ks > 0) ? 1u : 0u);
-                    if (a.split) tc_mma_f16(tmem_base, ad, sw128_desc(l_addr + ks * 32), idesc, 1u);
+                    for (int ks = 0; ks < kSlabK / 16; ++ks) {
+                        const uint64_t hd = sw128_desc(h_addr + ks * 32);
+                        const uint64_t ld = sw128_desc(l_addr + ks * 32);
+#pragma unroll
+                        for (int t = 0; t < kWT; ++t)
+                            tc_mma_f16_ta(tmem_base + kAccCol + t * kBN,
+                                          tmem_base + kASlotCol + (2 * st + t) * 32 + ks * 8, hd,
+                                          idesc, (kk > kb || ks > 0) ? 1u : 0u);
+                        if (a.split) {
+#pragma unroll
+                            for (int t = 0; t < kWT; ++t)
+                                tc_mma_f16_ta(tmem_base + kAccCol + t * kBN,
+                                              tmem_base + kASlotCol + (2 * st + t) * 32 + ks * 8,
+                                              ld, idesc, 1u);
+                        }
+                    }
+                    tc_commit(&slot_free[st]);
                 }
-                tc_commit(&slot_free[st]);
+                __syncwarp();
                 if (++st == kStages) {
                     st = 0;
                     ph ^= 1u;
                 }
             }
-            if (ok) tc_commit(acc_full);
-            else *(volatile int *)abort_flag = 1;
+            if (ok && leader) tc_commit(acc_full);
+            __syncwarp();
         }
-    } else {
-        // ------------------------ expansion, then epilogue ------------------------
-        const int r = threadIdx.x - 64;  // 0..127: tile row
+        if (!ok && leader) *(volatile int *)abort_flag = 1;
+    } else if (warp < 2 + kExpandWarps) {
+        // ------------------------------ expansion ------------------------------
+        // Warp w may access TMEM lanes 32 * (w % 4) .. +31: quarter q = w % 4 of
+        // weight tile t = (w - 2) / 4.
+        const int q = warp & 3, t = (warp - 2) >> 2;
+        const int row = t * kBM + q * 32 + lane;  // row within the 256-row unit
+        const uint32_t lane_addr = uint32_t(q * 32) << 16;
         int st = 0, wst = 0;
         uint32_t ph = 0, wph = 0;
         bool ok = true;
-        for (int kk = 0; kk < n_slabs; ++kk) {
-            bool got = true;
-            if ((kk & 7) == 0) got = mbar_wait(&w_full[wst], wph, a.err, kTagGemm + 5);
-            got = got && mbar_wait(&slot_free[st], ph ^ 1u, a.err, kTagGemm + 6);
-            if (!__all_sync(0xffffffffu, got)) {  // warp-uniform decision
-                ok = false;
-                break;
-            }
-            // row r's block (kk & 7) in the packed box: 18 bytes at r*144 + 18*(kk&7)
-            const int bb = kk & 7;
-            const uint8_t *rowp = w_s + wst * kWBoxBytes + r * 144;
-            const int off = 18 * bb;
-            const uint32_t *u = reinterpret_cast<const uint32_t *>(rowp + (off & ~3));
-            const uint32_t u0 = u[0], u1 = u[1], u2 = u[2], u3 = u[3], u4 = u[4];
-            uint32_t dbits, wd[4];
-            if ((off & 3) == 0) {  // even block: d in u0 low half, words straddle
-                dbits = u0 & 0xFFFFu;
-                wd[0] = __byte_perm(u0, u1, 0x5432);
-                wd[1] = __byte_perm(u1, u2, 0x5432);
-                wd[2] = __byte_perm(u2, u3, 0x5432);
-                wd[3] = __byte_perm(u3, u4, 0x5432);
-            } else {  // odd block: d in u0 high half, words aligned
-                dbits = u0 >> 16;
-                wd[0] = u1;
-                wd[1] = u2;
-                wd[2] = u3;
-                wd[3] = u4;
-            }
-            const __half dh = __ushort_as_half(static_cast<unsigned short>(dbits));
-            const __half2 d2 = __halves2half2(dh, dh);
-            const __half2 k1025 = __floats2half2_rn(1025.0f, 1025.0f);
-            uint8_t *arow = a_s + st * kATileBytes + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {  // 16-byte chunk j = k-slots 8j..8j+7
-                const uint32_t word = wd[j >> 1];
-                uint32_t h[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int t = 4 * (j & 1) + q;  // pair (element t, element t+8)
-                    const uint32_t bits = ((word >> (2 * t)) & 0x00030003u) | 0x64006400u;
-                    __half2 v = *reinterpret_cast<const __half2 *>(&bits);
-                    v = __hmul2(__hsub2(v, k1025), d2);
-                    h[q] = *reinterpret_cast<uint32_t *>(&v);
+        for (long long g = g_begin; g < g_end && ok;) {
+            const int kb = int(g % n_slabs);
+            const int ke = seg_end(n_slabs, kb, g_end - g);
+            g += ke - kb;
+            for (int kk = kb; kk < ke; ++kk) {
+                bool got = true;
+                if ((kk & 7) == 0 || kk == kb) got = mbar_wait(&w_full[wst], wph, a.err, kTagGemm + 6);
+                got = got && mbar_wait(&slot_free[st], ph ^ 1u, a.err, kTagGemm + 7);
+                if (!__all_sync(0xffffffffu, got)) {  // warp-uniform decision
+                    ok = false;
+                    break;
                 }
-                *reinterpret_cast<uint4 *>(arow + ((j ^ (r & 7)) << 4)) =
-                    make_uint4(h[0], h[1], h[2], h[3]);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&a_full[st]);
-            if (bb == 7 || kk == n_slabs - 1) {
-                mbar_arrive(&w_free[wst]);
-                if (++wst == kWStages) {
-                    wst = 0;
-                    wph ^= 1u;
+                // row's block (kk & 7) in the packed box: 18 bytes at row*144 + 18*(kk&7)
+                const int off = 18 * (kk & 7);
+                const uint32_t *up = reinterpret_cast<const uint32_t *>(
+                    w_s + wst * kWBoxBytes + row * 144 + (off & ~3));
+                const uint32_t u0 = up[0], u1 = up[1], u2 = up[2], u3 = up[3], u4 = up[4];
+                uint32_t dbits, wd[4];
+                if ((off & 3) == 0) {  // even block: d in u0 low half, words straddle
+                    dbits = u0 & 0xFFFFu;
+                    wd[0] = __byte_perm(u0, u1, 0x5432);
+                    wd[1] = __byte_perm(u1, u2, 0x5432);
+                    wd[2] = __byte_perm(u2, u3, 0x5432);
+                    wd[3] = __byte_perm(u3, u4, 0x5432);
+                } else {  // odd block: d in u0 high half, words aligned
+                    dbits = u0 >> 16;
+                    wd[0] = u1;
+                    wd[1] = u2;
+                    wd[2] = u3;
+                    wd[3] = u4;
                 }
-            }
-            if (++st == kStages) {
-                st = 0;
-                ph ^= 1u;
+                const __half dh = __ushort_as_half(static_cast<unsigned short>(dbits));
+                const __half2 d2 = __halves2half2(dh, dh);
+                uint32_t r[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = expand_pair(wd[j >> 3], j & 7, d2);
+                tmem_st32(tmem_base + lane_addr + kASlotCol + (2 * st + t) * 32, r);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                const bool box_done = (kk & 7) == 7 || kk == ke - 1;
+                if (lane == 0) {
+                    mbar_arrive(&a_full[st]);
+                    if (box_done) mbar_arrive(&w_free[wst]);
+                }
+                if (box_done) {
+                    if (++wst == kWStages) {
+                        wst = 0;
+                        wph ^= 1u;
+                    }
+                }
+                if (++st == kStages) {
+                    st = 0;
+                    ph ^= 1u;
+                }
             }
         }
-        // epilogue: wait for the accumulator, read TMEM lanes of this warp's quarter
-        const bool acc_ready = ok && mbar_wait(acc_full, 0, a.err, kTagGemm + 7);
-        if (__all_sync(0xffffffffu, acc_ready)) {
+    } else {
+        // ------------------------------- epilogue -------------------------------
+        const int q = warp & 3, t = (warp - 2 - kExpandWarps) >> 2;
+        const uint32_t lane_addr = uint32_t(q * 32) << 16;
+        const int rloc = t * kBM + q * 32 + lane;  // row within the unit
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // counters zeroed by the prepass
+        // A warp whose wait timed out stops reading TMEM and writing, but keeps
+        // taking part in the epilogue barriers so that the other warps finish.
+        bool dead = false;
+        int nu = 0;
+        for (long long g = g_begin; g < g_end; ++nu) {
+            const int u = int(g / n_slabs), kb = int(g % n_slabs);
+            const int ke = seg_end(n_slabs, kb, g_end - g);
+            g += ke - kb;
+            int n0, m0;
+            unit_coords(u, n0, m0);
+            if (!dead) {
+                const bool got = mbar_wait(acc_full, uint32_t(nu & 1), a.err, kTagGemm + 8);
+                dead = !__all_sync(0xffffffffu, got);
+            }
+            const bool whole = kb == 0 && ke == n_slabs;
+            if (dead) {
+                if (!whole) {
+                    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+                    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+                }
+                continue;
+            }
             tc_fence_after();
-            const int quarter = warp & 3;
-            const int n = n0 + quarter * 32 + lane;
-            const uint32_t lane_base = tmem_base + (uint32_t(quarter * 32) << 16);
+            const int n = n0 + rloc;
+            // partial pieces: slot 2c for a CTA's first segment, 2c + 1 for its last
+            const long long ustart = (long long)u * n_slabs;
+            float *mine = a.partials +
+                          size_t(2 * blockIdx.x + (g_begin >= ustart ? 0 : 1)) * (kPartialBytes / 4);
 #pragma unroll 1
             for (int cb = 0; cb < kBN; cb += 32) {
                 uint32_t v[32];
-                tmem_ld32(lane_base + cb, v);
-                if (n < a.N) {
+                tmem_ld32(tmem_base + lane_addr + kAccCol + t * kBN + cb, v);
+                if (whole) {
+                    if (n < a.N) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int m = m0 + cb + j;
-                        if (m < a.M) a.y[size_t(m) * a.N + n] = __uint_as_float(v[j]);
+                        for (int j = 0; j < 32; ++j) {
+                            const int m = m0 + cb + j;
+                            if (m < a.M) a.y[size_t(m) * a.N + n] = __uint_as_float(v[j]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        mine[(cb + j) * (kWT * kBM) + rloc] = __uint_as_float(v[j]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);  // accumulators free for the next segment
+            if (whole) continue;
+            // Publish the piece; the CTA that completes the unit sums its pieces in
+            // K order (deterministic) and writes Y.
+            __threadfence();
+            asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+            const int c_first = sk_owner(ustart, a.total_slabs, gridDim.x);
+            const int c_last = sk_owner(ustart + n_slabs - 1, a.total_slabs, gridDim.x);
+            if (warp == 2 + kExpandWarps && lane == 0)
+                *last_flag = atomicAdd(&a.counters[u], 1) == c_last - c_first;
+            asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+            if (!*(volatile int *)last_flag) continue;
+            __threadfence();
+            // Sum the pieces in K order, all 256 epilogue threads over the unit's
+            // tile as float4 runs of 4 rows; loads of up to 2 pieces in flight.
+            const int tid = (warp - 2 - kExpandWarps) * 32 + lane;
+            constexpr int kRowVec = kWT * kBM / 4;            // float4 per token row
+            constexpr int kTileVec = kBN * kRowVec;           // float4 per tile
+            const bool vec_y = (a.N % 4) == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15u) == 0;
+            const int n_pieces = c_last - c_first + 1;
+#pragma unroll 1
+            for (int i0 = tid; i0 < kTileVec; i0 += kEpiWarps * 32 * 4) {
+                float4 acc[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int p0 = 0; p0 < n_pieces; p0 += 2) {
+                    float4 v[2][4];
+#pragma unroll
+                    for (int pp = 0; pp < 2; ++pp) {
+                        const int cp = c_first + p0 + pp;
+                        if (p0 + pp < n_pieces) {
+                            const float4 *piece = reinterpret_cast<const float4 *>(
+                                a.partials +
+                                size_t(2 * cp + (sk_begin(cp, a.total_slabs, gridDim.x) >= ustart ? 0 : 1)) *
+                                    (kPartialBytes / 4));
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                const int i = i0 + r * kEpiWarps * 32;
+                                v[pp][r] = i < kTileVec ? __ldcg(piece + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int pp = 0; pp < 2; ++pp)
+                        if (p0 + pp < n_pieces)
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                acc[r].x += v[pp][r].x;
+                                acc[r].y += v[pp][r].y;
+                                acc[r].z += v[pp][r].z;
+                                acc[r].w += v[pp][r].w;
+                            }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int i = i0 + r * kEpiWarps * 32;
+                    if (i >= kTileVec) continue;
+                    const int m = m0 + i / kRowVec;
+                    const int nn = n0 + 4 * (i % kRowVec);
+                    if (m >= a.M) continue;
+                    float *yr = a.y + size_t(m) * a.N;
+                    if (vec_y && nn + 3 < a.N) {
+                        *reinterpret_cast<float4 *>(yr + nn) = acc[r];
+                    } else {
+                        if (nn < a.N) yr[nn] = acc[r].x;
+                        if (nn + 1 < a.N) yr[nn + 1] = acc[r].y;
+                        if (nn + 2 < a.N) yr[nn + 2] = acc[r].z;
+                        if (nn + 3 < a.N) yr[nn + 3] = acc[r].w;
                     }
                 }
             }
@@ -408,8 +570,8 @@ __global__ void __launch_bounds__(256) gemm_generic_kernel(const uint8_t *__rest
 }
 
 constexpr int gemm_smem_bytes() {
-    return 1024 /* alignment slack */ + kStages * (2 * kXTileBytes + kATileBytes) +
-           kWStages * kWBoxBytes + 8 * (3 * kStages + 2 * kWStages + 1) + 16;
+    return 1024 /* alignment slack */ + kStages * 2 * kXTileBytes + kWStages * kWBoxBytes +
+           8 * (3 * kStages + 2 * kWStages + 2) + 32;
 }
 
 std::mutex g_mu;
@@ -434,10 +596,40 @@ bool tc_path_ok(const void *w, const float *x, int64_t K) {
 
 }  // namespace
 
+namespace {
+
+struct GemmLayout {
+    size_t part;      // bytes of X_hi (and of X_lo)
+    size_t counters;  // offset of the per-unit counters
+    size_t partials;  // offset of the partial tiles
+    size_t total;
+    int n_units, n_mtiles, grid;
+    long long total_slabs;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Workspace: [X_hi][X_lo (split)][unit counters][2 partial tiles per stream-K CTA].
+// The grid is at most kMaxGrid CTAs, at least 8 slabs each.
+GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K, int prec, int sms) {
+    GemmLayout L;
+    L.part = align256(size_t(M) * K * 2);
+    L.n_mtiles = int((M + kBN - 1) / kBN);
+    L.n_units = int((N + kWT * kBM - 1) / (kWT * kBM)) * L.n_mtiles;
+    L.total_slabs = (long long)L.n_units * (K / kSlabK);
+    const long long by_work = std::max<long long>(1, L.total_slabs / 8);
+    L.grid = int(std::min<long long>(std::min<long long>(sms > 0 ? sms : kMaxGrid, kMaxGrid), by_work));
+    L.counters = (prec == Q2_0_PREC_F16_SPLIT ? 2 : 1) * L.part;
+    L.partials = L.counters + align256(size_t(L.n_units) * 4);
+    L.total = L.partials + size_t(2) * L.grid * kPartialBytes;
+    return L;
+}
+
+}  // namespace
+
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int prec) {
-    (void)N;
-    const size_t part = (size_t(M) * K * 2 + 255) & ~size_t(255);
-    return prec == Q2_0_PREC_F16_SPLIT ? 2 * part : part;
+    // sized for the largest grid so the query needs no device
+    return gemm_layout(M, N, K, prec, kMaxGrid).total;
 }
 
 int gemm_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, int64_t M, int prec,
@@ -451,19 +643,23 @@ int gemm_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, i
     if (ws_bytes < gemm_workspace_bytes(M, N, K, prec) || !ws) return Q2_0_EINVAL;
     unsigned long long *err = error_word_ptr();
     if (!err) return Q2_0_ECUDA;
-    __half *xh = static_cast<__half *>(ws);
-    const size_t part = (size_t(M) * K * 2 + 255) & ~size_t(255);
-    __half *xl = split ? reinterpret_cast<__half *>(static_cast<uint8_t *>(ws) + part) : nullptr;
+    const GemmLayout L = gemm_layout(M, N, K, prec, sm_count());
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    __half *xh = reinterpret_cast<__half *>(wsb);
+    __half *xl = split ? reinterpret_cast<__half *>(wsb + L.part) : nullptr;
+    int *counters = reinterpret_cast<int *>(wsb + L.counters);
+    float *partials = reinterpret_cast<float *>(wsb + L.partials);
     const int64_t groups = M * K / 16;
     int64_t pgrid = std::min<int64_t>((groups + 255) / 256, int64_t(sm_count()) * 8);
-    gemm_prep_kernel<<<unsigned(std::max<int64_t>(pgrid, 1)), 256, 0, s>>>(x, xh, xl, groups, split);
+    gemm_prep_kernel<<<unsigned(std::max<int64_t>(pgrid, 1)), 256, 0, s>>>(x, xh, xl, groups, split,
+                                                                         counters, L.n_units);
     if (cudaGetLastError() != cudaSuccess) return Q2_0_ECUDA;
 
     GemmArgs args;
     std::memset(&args, 0, sizeof(args));
     const uint64_t row_bytes = uint64_t(K / 64) * 18;
     if (!encode_tmap_2d(&args.w_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row_bytes, uint64_t(N),
-                        row_bytes, 144, kBM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                        row_bytes, 144, kWT * kBM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_tmap_2d(&args.xh_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, uint64_t(K), uint64_t(M),
                         uint64_t(K) * 2, kSlabK, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
         return Q2_0_ECUDA;
@@ -477,9 +673,23 @@ int gemm_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, i
     args.K = int(K);
     args.split = split;
     args.err = err;
+    args.n_mtiles = L.n_mtiles;
+    args.n_units = L.n_units;
+    args.total_slabs = L.total_slabs;
+    args.counters = counters;
+    args.partials = partials;
     if (ensure_attr() != cudaSuccess) return Q2_0_ECUDA;
-    dim3 grid(unsigned((N + kBM - 1) / kBM), unsigned((M + kBN - 1) / kBN));
-    gemm_tc_kernel<<<grid, kThreads, gemm_smem_bytes(), s>>>(args);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(L.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = gemm_smem_bytes();
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel, args) != cudaSuccess) return Q2_0_ECUDA;
     return cuda_status(cudaGetLastError());
 }
 

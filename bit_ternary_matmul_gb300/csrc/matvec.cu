@@ -12,29 +12,34 @@
 // from one word, the codes of elements i = m and i = 8 + m into the two fp16
 // halves of a register; read as fp16 these are the subnormals q * 4^m * 2^-24,
 // exact. (word >> 8) with the same masks picks elements 4 + m and 12 + m. So a
-// word becomes 8 A-operand registers with one LOP3 each (+1 shift). The
+// word becomes 8 A-operand registers with one logic op each (+1 shift). The
 // per-field factor 4^m is removed by scaling the activations of field m by
 // 4^-m, and the "- 1" of (q - 1) by starting each block's accumulation at
 // -sum(activation * 4^m * 2^-24) of that block (the value all-ones codes give).
 //
 // Activations (F32) enter as fp16 hi + lo pairs: per column j, u = x * 2^s_j
 // with 2^s_j chosen so max|u| lies in [2^14, 2^15); for element e of a block,
-// v = u * 2^-2(e%4), hi = fp16(v), lo = fp16(v - hi). The B operand of an MMA
-// has 8 columns: for ncols <= 4 they are (hi of cols 0..3, lo of cols 0..3);
-// for 5..8 two MMAs use (hi of cols 0..7) and (lo of cols 0..7). A separate
-// small kernel (mv_prep) writes these fragments, in exactly the register order
-// the MMA wants, once per call; the mat-vec kernel then only loads them.
+// v = u * 2^-2(e%4), hi = fp16(v), lo = fp16(v - hi). MMA n-tile t carries
+// activation columns 4t..4t+3: its B column 2i is the hi part of column 4t+i
+// and B column 2i+1 the lo part, so the lanes that carry data are consecutive
+// (lanes 0..7 for one column) and a thread's two accumulator registers of a row
+// hold hi and lo of the same column. A small kernel (mv_prep) writes these
+// fragments once per call, in register order; the mat-vec kernel only loads them.
 //
-// Streaming. Each CTA (8 consumer warps + 1 producer warp) owns row tiles of
-// 256 rows. A pipeline stage is one 2-D TMA box of 256 rows x 144 bytes (8
-// blocks = 512 weights per row) plus the 8 blocks' activation fragments (1-D
-// bulk copy). 144-byte rows make the shared-memory words of the 8 rows of an
-// MMA group fall in distinct banks. Block pairs (36 bytes) start 4-byte
-// aligned: the odd block's words are aligned, the even block's words straddle
-// two aligned words and are rebuilt with one byte-permute.
+// Streaming. Each CTA (16 consumer warps of 16 rows + 1 producer warp) owns row
+// tiles of 256 rows. A pipeline stage is one 2-D TMA box of 256 rows x 144 bytes
+// (8 blocks = 512 weights per row) plus the 8 blocks' fragment records (1-D
+// bulk copy); as many stages as fit in shared memory. 144-byte rows make the
+// shared-memory words of the 8 rows of an MMA group fall in distinct banks.
+// Block pairs (36 bytes) start 4-byte aligned: the odd block's words are
+// aligned, the even block's words straddle two aligned words and are rebuilt
+// with one byte-permute. The consumer loop is limited by shared-memory
+// wavefronts, so the record layout is chosen for dense 16-byte fragment loads.
 //
 // Requirements of the TMA path: K % 512 == 0 (row stride a multiple of 16 B)
 // and W 16-byte aligned. Other shapes run mv_generic_kernel (CUDA cores, f32).
+#include <cuda_fp8.h>
+
 #include <algorithm>
 #include <cstring>
 #include <mutex>
@@ -43,6 +48,7 @@
 
 #include "q2_0_device.cuh"
 #include "q2_0_internal.h"
+#include "q2_0_tcgen05.cuh"
 
 namespace q2 {
 
@@ -52,17 +58,12 @@ constexpr int kTileRows = 256;
 constexpr int kChunkBlocks = 8;
 constexpr int kChunkBytes = kChunkBlocks * 18;  // 144
 constexpr int kWStageBytes = kTileRows * kChunkBytes;  // 36864
-// Record per block per n-tile, for S = lane slots that carry data (8 per column
-// for ncols <= 4, 4 per column for 5..8): B-fragment registers 0..3 of the S
-// slots (16 B each), registers 4..7 of the slots, then for each lane group c
-// the accumulator start (s[2c], s[2c+1], s[2c], s[2c+1]) (64 B). Data lanes
-// occupy consecutive slots, so their 16-byte loads are dense.
 constexpr int kPrepHeader = 64;  // float out_scale[8] (+ pad)
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
+constexpr int kPrepThreads = 512;
 // Dynamic shared memory the ring may use: the opt-in maximum less the static
 // part and the barriers.
 constexpr int kSmemBudget = 232448 - 1024 - 2 * kMaxStages * 8;
-constexpr int kPrepThreads = 512;
 
 // Timeout tags (info of Q2_0_DEVERR_TIMEOUT).
 constexpr int kTagMvFull = 101;
@@ -98,11 +99,13 @@ struct MvParams {
     unsigned long long *err;
 };
 
+// Record per block per n-tile, for S = lane slots carrying data (8 per column of
+// the tile; the tiles of ncols 5..8 both use 32): B-fragment registers 0..3 of
+// lanes 0..S-1 (16 B each), registers 4..7 of those lanes, then for each lane
+// group c the accumulator starts (hi, lo) of column 4t + c (8 B each).
 __host__ __device__ constexpr int n_tiles_for(int ncols) { return ncols <= 4 ? 1 : 2; }
-__host__ __device__ constexpr int used_slots(int ncols) {
-    return n_tiles_for(ncols) == 1 ? 8 * ncols : 4 * ncols;
-}
-__host__ __device__ constexpr int rec_bytes(int ncols) { return 32 * used_slots(ncols) + 64; }
+__host__ __device__ constexpr int used_slots(int ncols) { return ncols <= 4 ? 8 * ncols : 32; }
+__host__ __device__ constexpr int rec_bytes(int ncols) { return 32 * used_slots(ncols) + 32; }
 __host__ __device__ constexpr int rstage_bytes(int ncols) {
     return kChunkBlocks * n_tiles_for(ncols) * rec_bytes(ncols);
 }
@@ -120,24 +123,16 @@ size_t prep_bytes_for(int64_t K, int ncols) {
     return (b + 255) & ~size_t(255);
 }
 
-// ---------------------------------------------------------------------------
-// Activation preparation: grid (ncols, n_jobs), 256 threads.
-// ---------------------------------------------------------------------------
-// Lane slot of MMA lane L = 4g + c in a record. NT == 1: column groups g < 4
-// carry hi parts of columns 0..ncols-1, g >= 4 the lo parts; NT == 2: g < ncols.
-__host__ __device__ __forceinline__ int lane_slot(int nt, int lane, int ncols) {
-    const int g = lane >> 2, c = lane & 3;
-    return nt == 1 ? (((g & 3) + (g >> 2) * ncols) * 4 + c) : lane;
+
+// v * 2^e for |e| <= 252 with two exact power-of-two factors (each a normal f32).
+__device__ __forceinline__ float mul_pow2(float v, int e) {
+    const int e1 = e / 2, e2 = e - e1;
+    return v * __int_as_float((127 + e1) << 23) * __int_as_float((127 + e2) << 23);
 }
 
-// Accumulator start of MMA column n (the -sum for all-ones codes): stored at
-// both places lane group n/2 loads it from.
-__device__ __forceinline__ void put_start(uint8_t *rec, int s_used, int n, float v) {
-    float *q = reinterpret_cast<float *>(rec + 32 * s_used + (n >> 1) * 16) + (n & 1);
-    q[0] = v;
-    q[2] = v;
-}
-
+// ---------------------------------------------------------------------------
+// Activation preparation: grid (ncols, n_jobs), kPrepThreads threads.
+// ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
     return uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
 }
@@ -202,6 +197,8 @@ __global__ void __launch_bounds__(kPrepThreads) mv_prep_kernel(
     const float fscale[4] = {ldexpf(1.0f, s), ldexpf(1.0f, s - 2), ldexpf(1.0f, s - 4),
                              ldexpf(1.0f, s - 6)};
     const int lane = tid & 31;
+    const int su = used_slots(ncols), rb = rec_bytes(ncols);
+    const int t = j >> 2, jc = j & 3;  // n-tile and column within it
     for (int idx = tid; idx < nb * 4; idx += kPrepThreads) {
         const int b = idx >> 2, c = idx & 3;
         const float *xe = xj + b * 64 + c * 16;
@@ -232,40 +229,31 @@ __global__ void __launch_bounds__(kPrepThreads) mv_prep_kernel(
         base_lo += __shfl_xor_sync(grp, base_lo, 1);
         base_lo += __shfl_xor_sync(grp, base_lo, 2);
 
-        const int su = used_slots(ncols), rb = rec_bytes(ncols);
-        uint8_t *rec0 = J.prep + kPrepHeader + size_t(b) * NT * rb;
-        int lane_hi, lane_lo, slot_hi, slot_lo;
-        uint8_t *rec_hi, *rec_lo;
-        if (NT == 1) {
-            rec_hi = rec_lo = rec0;
-            lane_hi = 4 * j + c;
-            lane_lo = 4 * (4 + j) + c;
-            slot_hi = j;
-            slot_lo = 4 + j;
-        } else {
-            rec_hi = rec0;
-            rec_lo = rec0 + rb;
-            lane_hi = lane_lo = 4 * j + c;
-            slot_hi = slot_lo = j;
-        }
-        const int sh = lane_slot(NT, lane_hi, ncols), sl = lane_slot(NT, lane_lo, ncols);
-        *reinterpret_cast<uint4 *>(rec_hi + sh * 16) = make_uint4(rh[0], rh[1], rh[2], rh[3]);
-        *reinterpret_cast<uint4 *>(rec_hi + 16 * su + sh * 16) = make_uint4(rh[4], rh[5], rh[6], rh[7]);
-        *reinterpret_cast<uint4 *>(rec_lo + sl * 16) = make_uint4(rl[0], rl[1], rl[2], rl[3]);
-        *reinterpret_cast<uint4 *>(rec_lo + 16 * su + sl * 16) = make_uint4(rl[4], rl[5], rl[6], rl[7]);
-        if (c == 0) {
-            put_start(rec_hi, su, slot_hi, -base_hi);
-            put_start(rec_lo, su, slot_lo, -base_lo);
-        }
-        // Column 0's CTA also zeroes the column starts of unused columns.
-        if (j == 0 && c == 0) {
-            for (int t = 0; t < NT; ++t) {
-                uint8_t *rt = rec0 + t * rb;
-                for (int u = ncols; u < (NT == 1 ? 4 : 8); ++u) {
-                    put_start(rt, su, u, 0.0f);
-                    if (NT == 1) put_start(rt, su, 4 + u, 0.0f);
+        // B column 2*jc (hi) is lane group 2*jc, column 2*jc+1 (lo) group 2*jc+1.
+        uint8_t *rec = J.prep + kPrepHeader + (size_t(b) * NT + t) * rb;
+        const int l_hi = 4 * (2 * jc) + c, l_lo = 4 * (2 * jc + 1) + c;
+        *reinterpret_cast<uint4 *>(rec + l_hi * 16) = make_uint4(rh[0], rh[1], rh[2], rh[3]);
+        *reinterpret_cast<uint4 *>(rec + 16 * su + l_hi * 16) = make_uint4(rh[4], rh[5], rh[6], rh[7]);
+        *reinterpret_cast<uint4 *>(rec + l_lo * 16) = make_uint4(rl[0], rl[1], rl[2], rl[3]);
+        *reinterpret_cast<uint4 *>(rec + 16 * su + l_lo * 16) = make_uint4(rl[4], rl[5], rl[6], rl[7]);
+        if (c == 0)
+            *reinterpret_cast<float2 *>(rec + 32 * su + 8 * jc) = make_float2(-base_hi, -base_lo);
+        // Column 0's CTA also clears the slots and starts of columns past ncols
+        // in the last tile (the tiles of ncols 5..8 share the 32-slot layout).
+        if (j == 0) {
+            const int last_t = NT - 1;
+            uint8_t *rl_rec = J.prep + kPrepHeader + (size_t(b) * NT + last_t) * rb;
+            for (int jj = ncols - 4 * last_t; jj < 4; ++jj) {
+                if (8 * jj + 8 > su) break;
+                for (int part = 0; part < 2; ++part) {
+                    const int l = 4 * (2 * jj + part) + c;
+                    *reinterpret_cast<uint4 *>(rl_rec + l * 16) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(rl_rec + 16 * su + l * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
+            if (c == 0)
+                for (int jj = ncols - 4 * last_t; jj < 4; ++jj)
+                    *reinterpret_cast<float2 *>(rl_rec + 32 * su + 8 * jj) = make_float2(0.f, 0.f);
         }
     }
 }
@@ -283,11 +271,6 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
           "f"(c3));
 }
 
-// fp16 scale at a shared-memory address, as f32 (16-bit load + convert).
-__device__ __forceinline__ float lds_half_as_float(const uint8_t *p) {
-    return __half2float(*reinterpret_cast<const __half *>(p));
-}
-
 __device__ __forceinline__ uint32_t pick(const uint4 &a, const uint4 &b, int r) {
     switch (r) {
         case 0: return a.x;
@@ -299,6 +282,11 @@ __device__ __forceinline__ uint32_t pick(const uint4 &a, const uint4 &b, int r) 
         case 6: return b.z;
         default: return b.w;
     }
+}
+
+// fp16 scale at a shared-memory address, as f32.
+__device__ __forceinline__ float lds_half_as_float(const uint8_t *p) {
+    return __half2float(*reinterpret_cast<const __half *>(p));
 }
 
 // Code words and scales of one block pair for a thread's two rows (a, b):
@@ -327,21 +315,88 @@ __device__ __forceinline__ PairRegs load_pair(const uint8_t *row_a, const uint8_
     return r;
 }
 
-// Consumer warps per CTA for RG 16-row groups per warp (256-row tiles).
-template <int RG>
-constexpr int consumer_warps() { return kTileRows / (16 * RG); }
-template <int RG>
-constexpr int cta_threads() { return (consumer_warps<RG>() + 1) * 32; }
+// One pipeline stage (8 blocks of a thread's rows a = row_a, b = row_a + 8) as
+// straight-line code: per block pair, the B fragments (data lanes only) and
+// accumulator starts, the two code words and scales per row, then the four MMA
+// steps issued step-major across the pair's two chains, then the scaling.
+template <int NT>
+__device__ __forceinline__ void mv_stage(float (&acc)[NT][4], uint4 (&fr0)[2][NT],
+                                         uint4 (&fr1)[2][NT], const uint8_t *row_a,
+                                         const uint8_t *rs, int rec_bytes, int su, int lane, int c,
+                                         const bool (&lane_used)[NT]) {
+    const uint8_t *row_b = row_a + 8 * kChunkBytes;
+#pragma unroll
+    for (int pr = 0; pr < kChunkBlocks / 2; ++pr) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const uint8_t *rec = rs + ((2 * pr + u) * NT + t) * rec_bytes;
+                if (lane_used[t]) {  // other lanes keep their zero registers
+                    fr0[u][t] = *reinterpret_cast<const uint4 *>(rec + lane * 16);
+                    fr1[u][t] = *reinterpret_cast<const uint4 *>(rec + 16 * su + lane * 16);
+                }
+            }
+        const PairRegs cur = load_pair(row_a, row_b, pr, c);
+        uint32_t sa[2], sb[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            sa[u] = cur.wa[u] >> 8;
+            sb[u] = cur.wb[u] >> 8;
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            float2 st[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                st[u] = *reinterpret_cast<const float2 *>(rs + ((2 * pr + u) * NT + t) * rec_bytes +
+                                                          32 * su + 8 * c);
+            float cc[2][4];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                cc[u][0] = st[u].x;
+                cc[u][1] = st[u].y;
+                cc[u][2] = st[u].x;
+                cc[u][3] = st[u].y;
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t mask = 0x00030003u << (2 * m);
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    float dd[4];
+                    mma_16816(dd, cur.wa[u] & mask, cur.wb[u] & mask, sa[u] & mask, sb[u] & mask,
+                              pick(fr0[u][t], fr1[u][t], 2 * m), pick(fr0[u][t], fr1[u][t], 2 * m + 1),
+                              cc[u][0], cc[u][1], cc[u][2], cc[u][3]);
+                    cc[u][0] = dd[0];
+                    cc[u][1] = dd[1];
+                    cc[u][2] = dd[2];
+                    cc[u][3] = dd[3];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                acc[t][0] = fmaf(cur.da[u], cc[u][0], acc[t][0]);
+                acc[t][1] = fmaf(cur.da[u], cc[u][1], acc[t][1]);
+                acc[t][2] = fmaf(cur.db[u], cc[u][2], acc[t][2]);
+                acc[t][3] = fmaf(cur.db[u], cc[u][3], acc[t][3]);
+            }
+        }
+    }
+}
 
 __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// NT: MMA n-tiles (1 for ncols <= 4, 2 for 5..8); RG: 16-row groups per warp.
-template <int NT, int RG>
-__global__ void __launch_bounds__(cta_threads<RG>(), 1)
+constexpr int kConsumerWarps = kTileRows / 16;  // one 16-row MMA group per warp
+constexpr int kCtaThreads = (kConsumerWarps + 1) * 32;
+
+// NT: MMA n-tiles (1 for ncols <= 4, 2 for 5..8).
+template <int NT>
+__global__ void __launch_bounds__(kCtaThreads, 1)
     mv_tc_kernel(const __grid_constant__ MvJob single, const MvParams p) {
-    constexpr int kCW = consumer_warps<RG>();
+    constexpr int kCW = kConsumerWarps;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int kStages = p.n_stages;
     const int su = used_slots(p.ncols), kRecBytes = rec_bytes(p.ncols);
@@ -413,8 +468,8 @@ __global__ void __launch_bounds__(cta_threads<RG>(), 1)
                         prep_ready = true;
                     }
                     bulk_g2s(r_stage + stage * kRStageBytes,
-                             J->prep + kPrepHeader + size_t(ch) * kRStageBytes,
-                             kRStageBytes, &full[stage]);
+                             J->prep + kPrepHeader + size_t(ch) * kRStageBytes, kRStageBytes,
+                             &full[stage]);
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -440,13 +495,11 @@ __global__ void __launch_bounds__(cta_threads<RG>(), 1)
     // ------------------------------ consumers ------------------------------
     grid_dependency_wait();  // the epilogue reads the column scales written by prep
     const int g = lane >> 2, c = lane & 3;
-    // B lanes that carry data: NT==1 -> groups g < ncols (hi) and 4 <= g < 4+ncols (lo)
+    // Lane groups g < 2 * (columns of tile t) carry B data.
     bool lane_used[NT];
 #pragma unroll
-    for (int t = 0; t < NT; ++t)
-        lane_used[t] = (NT == 1) ? ((g & 3) < p.ncols) : (g < p.ncols);
+    for (int t = 0; t < NT; ++t) lane_used[t] = g < 2 * min(4, p.ncols - 4 * t);
 
-    const int slot = lane_slot(NT, lane, p.ncols);
     // B-fragment registers of a block pair; lanes that carry no column keep zeros.
     uint4 fr0[2][NT], fr1[2][NT];
 #pragma unroll
@@ -461,13 +514,11 @@ __global__ void __launch_bounds__(cta_threads<RG>(), 1)
         int tile;
         item_at(i, J, tile);
         const int n_chunks = J->n_chunks;
-        float acc[RG][NT][4];
+        float acc[NT][4];
 #pragma unroll
-        for (int rg = 0; rg < RG; ++rg)
+        for (int t = 0; t < NT; ++t)
 #pragma unroll
-            for (int t = 0; t < NT; ++t)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) acc[rg][t][k] = 0.0f;
+            for (int k = 0; k < 4; ++k) acc[t][k] = 0.0f;
 
         bool ok = true;
         for (int ch = 0; ch < n_chunks; ++ch) {
@@ -478,64 +529,8 @@ __global__ void __launch_bounds__(cta_threads<RG>(), 1)
                 ok = false;
                 break;
             }
-            const uint8_t *ws = w_stage + stage * kWStageBytes;
-            const uint8_t *rs = r_stage + stage * kRStageBytes;
-            // Block pairs (36 bytes per row). The words and scales of pair pr+1 are
-            // loaded before pair pr's MMAs, which are issued step-major across the
-            // pair's two accumulation chains.
-            const int ra = warp * 16 + g;
-            const uint8_t *row_a = ws + ra * kChunkBytes;
-            const uint8_t *row_b = row_a + 8 * kChunkBytes;
-            PairRegs nxt = load_pair(row_a, row_b, 0, c);
-#pragma unroll
-            for (int pr = 0; pr < kChunkBlocks / 2; ++pr) {
-                const PairRegs cur = nxt;
-                if (pr + 1 < kChunkBlocks / 2) nxt = load_pair(row_a, row_b, pr + 1, c);
-#pragma unroll
-                for (int u = 0; u < 2; ++u)
-#pragma unroll
-                    for (int t = 0; t < NT; ++t) {
-                        const uint8_t *rec = rs + ((2 * pr + u) * NT + t) * kRecBytes;
-                        if (lane_used[t]) {  // unused lanes keep their zero registers
-                            fr0[u][t] = *reinterpret_cast<const uint4 *>(rec + slot * 16);
-                            fr1[u][t] = *reinterpret_cast<const uint4 *>(rec + 16 * su + slot * 16);
-                        }
-                    }
-                uint32_t sa[2], sb[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    sa[u] = __umulhi(cur.wa[u], 0x01000000u);  // >> 8 on the FMA pipe
-                    sb[u] = __umulhi(cur.wb[u], 0x01000000u);
-                }
-#pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    float4 cc[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u)
-                        cc[u] = *reinterpret_cast<const float4 *>(
-                            rs + ((2 * pr + u) * NT + t) * kRecBytes + 32 * su + 16 * c);
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const uint32_t mask = 0x00030003u << (2 * m);
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            float dd[4];
-                            mma_16816(dd, cur.wa[u] & mask, cur.wb[u] & mask, sa[u] & mask,
-                                      sb[u] & mask, pick(fr0[u][t], fr1[u][t], 2 * m),
-                                      pick(fr0[u][t], fr1[u][t], 2 * m + 1), cc[u].x, cc[u].y,
-                                      cc[u].z, cc[u].w);
-                            cc[u] = make_float4(dd[0], dd[1], dd[2], dd[3]);
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        acc[0][t][0] = fmaf(cur.da[u], cc[u].x, acc[0][t][0]);
-                        acc[0][t][1] = fmaf(cur.da[u], cc[u].y, acc[0][t][1]);
-                        acc[0][t][2] = fmaf(cur.db[u], cc[u].z, acc[0][t][2]);
-                        acc[0][t][3] = fmaf(cur.db[u], cc[u].w, acc[0][t][3]);
-                    }
-                }
-            }
+            mv_stage<NT>(acc, fr0, fr1, w_stage + stage * kWStageBytes + (warp * 16 + g) * kChunkBytes,
+                         r_stage + stage * kRStageBytes, kRecBytes, su, lane, c, lane_used);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
             if (++stage == kStages) {
@@ -545,32 +540,524 @@ __global__ void __launch_bounds__(cta_threads<RG>(), 1)
         }
         if (!ok) break;
 
-        // ---- epilogue: combine hi + lo, undo the column scale, store ----
+        // ---- epilogue: hi + lo of column 4t + c, undo the column scale, store ----
         const float *out_scale = reinterpret_cast<const float *>(J->prep);
         const int N = J->N;
+        const int row_a = tile * kTileRows + warp * 16 + g;
+        const int row_b = row_a + 8;
 #pragma unroll
-        for (int rg = 0; rg < RG; ++rg) {
-            const int row_a = tile * kTileRows + warp * (16 * RG) + rg * 16 + g;
-            const int row_b = row_a + 8;
-            float v[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if (NT == 1)
-                    v[k] = acc[rg][0][k] + __shfl_xor_sync(0xffffffffu, acc[rg][0][k], 2);
-                else
-                    v[k] = acc[rg][0][k] + acc[rg][NT - 1][k];
+        for (int t = 0; t < NT; ++t) {
+            const int col = 4 * t + c;
+            if (col < p.ncols) {
+                const float sc = out_scale[col];
+                if (row_a < N) J->y[size_t(col) * N + row_a] = (acc[t][0] + acc[t][1]) * sc;
+                if (row_b < N) J->y[size_t(col) * N + row_b] = (acc[t][2] + acc[t][3]) * sc;
             }
-            if (NT == 1 && c >= 2) continue;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 mat-vec (ncols 1..3)
+//
+// The codes become tensor-core operands without any arithmetic: byte j of a
+// code word holds elements 4j..4j+3 at bits 0-1, 2-3, 4-5, 6-7, and read as
+// e4m3 a byte whose only set bits are 0-1 is the subnormal q * 2^-9, one whose
+// only set bits are 2-3 is q * 2^-7 (bit 2 is the top mantissa bit, bit 3 the
+// lowest exponent bit: 0, 2^-7, 2^-6, 1.5 * 2^-6). So word & 0x03030303,
+// word & 0x0C0C0C0C, (word >> 4) & 0x03030303 and (word >> 4) & 0x0C0C0C0C are
+// four registers of exact e4m3 weights, one logic op each. Four expansion
+// warps per 128-row tile store them into tensor memory (one row per TMEM lane)
+// and one thread issues tcgen05.mma kind::f8f6f4 (M = 128, N = 16, K = 32)
+// with A in TMEM and B = the activations as e4m3 pieces in shared memory.
+//
+// Activations as e4m3 pieces. Per column j, u = x * 2^s_j with max|u| in
+// [2^-2, 2^-1); element e gives v = u * 2^9 (codes at bits 0-1) or u * 2^7
+// (bits 2-3), split into kT5Pieces e4m3 values: piece p = e4m3(r_p * 2^4p),
+// r_0 = v, r_{p+1} = r_p - piece_p * 2^-4p; each rounding keeps 4 significant
+// bits, so the residual after 5 pieces is below 2^-20 |v|. Piece p of column j
+// is B row n = 5j + p. A block's MMA result per row is then C_n = sum q *
+// piece_n / (2^9 or 2^7).
+//
+// Per block accumulators. d changes every 64 weights of a row, so each block
+// gets its own 16-column TMEM accumulator; the epilogue loads it and forms,
+// per row and column,
+//   t = sum_p 2^-4p C_(5j+p) - beta_j,   acc_j += d * t,
+// where beta_j is the same sum for all-ones codes (the "- 1" of (q - 1)),
+// computed by the preparation kernel with the same f32 operations from exact
+// per-piece sums, so that all-ones blocks give exactly 0.
+//
+// Pipeline per CTA (persistent over 128-row tiles), stage = 8 blocks:
+//   warp 0      streams the stage's TMA box (144 B x 128 rows) and, by bulk
+//               copy, its B image and betas into an 8-deep shared-memory ring;
+//   warps 2-9   expand the stage's codes into one of two TMEM A buffers
+//               (warps 2-5 blocks 0-3, warps 6-9 blocks 4-7; warp w owns TMEM
+//               lanes 32 (w % 4) .. +31, i.e. those rows);
+//   warps 1, 14 issue the stage's 16 MMAs into one of two TMEM D buffers (warp
+//               1 the even stages, warp 14 the odd ones: a single issuing
+//               thread spends ~60-70 cycles per MMA and ~100 per barrier
+//               check, so two chains run side by side) and commit them to the
+//               expansion (A free) and epilogue (D full) barriers;
+//   warps 10-13 epilogue, one row per thread: D, the row's d values from the
+//               ring and the betas; they release the D buffer and the ring slot.
+// ---------------------------------------------------------------------------
+constexpr int kT5Rows = 128;
+constexpr int kT5Pieces = 5;
+constexpr int kT5MaxCols = 3;                         // 5 * 3 pieces fit N = 16
+constexpr int kT5N = 16;
+constexpr int kT5Stages = 8;
+constexpr int kT5RawBytes = kT5Rows * kChunkBytes;   // 18432
+constexpr int kT5ImgBytes = kT5N * kChunkBlocks * 64; // 8192: 16 rows x 512 K bytes, SW128
+constexpr int kT5BetaBytes = kChunkBlocks * 4 * 4;   // beta[8 blocks][4 columns] f32
+constexpr int kT5PrepHeader = 1024;                  // int col_shift[8], images 1024-aligned
+constexpr int kT5ExpWarps = 8;
+constexpr int kT5EpiWarps = 4;
+constexpr int kT5Warps = 3 + kT5ExpWarps + kT5EpiWarps;  // + producer, 2 MMA issuers
+constexpr int kT5Threads = kT5Warps * 32;
+constexpr int kT5Smem = 1024 /* alignment slack */ +
+                        kT5Stages * (kT5ImgBytes + kT5RawBytes + kT5BetaBytes) +
+                        (2 * kT5Stages + 8) * 8;
+constexpr int kTagT5Full = 111;
+constexpr int kTagT5Empty = 112;
+constexpr int kTagT5AFull = 113;
+constexpr int kTagT5DFull = 114;
+constexpr int kTagT5DEmpty = 115;
+
+size_t t5_prep_bytes(int64_t K) {
+    const size_t n_chunks = size_t(K / 512);
+    size_t b = kT5PrepHeader + n_chunks * (kT5ImgBytes + kT5BetaBytes);
+    return (b + 255) & ~size_t(255);
+}
+
+// Byte offset of element (row n, K position kc) of one stage's B image: K-major
+// rows of 128 bytes in atoms of 8 rows (1024 B); the 16-byte chunk index is
+// XOR-ed with the row within the atom (128-byte swizzle); 4 atom columns of
+// 128 K bytes (2 KB each: rows 0-7, then rows 8-15).
+__host__ __device__ constexpr int t5_img_offset(int n, int kc) {
+    return (kc >> 7) * 2048 + (n >> 3) * 1024 + (n & 7) * 128 +
+           ((((kc & 127) >> 4) ^ (n & 7)) << 4) + (kc & 15);
+}
+
+// Preparation: grid (ncols, n_jobs), kPrepThreads threads. Thread (block b,
+// word c, r) handles the 4 elements 16c + 4jj + r (jj = 0..3) of block b and
+// writes, per piece, one 32-bit word of the B image: K positions 64 (b % 8) +
+// 16c + 4r + jj (the order the expansion warps store codes in TMEM: column
+// 4c + r of a block holds elements 16c + 4jj + r in byte jj). The per-piece
+// all-ones sums are exact integers in units of 2^-18 (a piece is a multiple of
+// 2^-9, divided by 2^9 or 2^7; |sum| < 64 * 448 * 2^-7), rounded once to f32.
+__global__ void __launch_bounds__(kPrepThreads) t5_prep_kernel(
+    const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs, int ncols) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const MvPrepJob &J = jobs ? jobs[blockIdx.y] : single;
+    const int K = J.K;
+    const int j = blockIdx.x;
+    const float *xj = J.x + size_t(j) * K;
+    const int tid = threadIdx.x;
+    const int nb = K / 64;
+    const int n_chunks = K / 512;
+
+    // 1) column scale 2^s with max|x * 2^s| in [2^-2, 2^-1)
+    float m = 0.0f;
+    if ((reinterpret_cast<uintptr_t>(xj) & 15u) == 0) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(xj);
+        for (int k = tid; k < K / 4; k += kPrepThreads) {
+            const float4 f = x4[k];
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+        }
+    } else {
+        for (int k = tid; k < K; k += kPrepThreads) m = fmaxf(m, fabsf(xj[k]));
+    }
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int col = 2 * c + k;
-                if (col < p.ncols) {
-                    const float sc = out_scale[col];
-                    if (row_a < N) J->y[size_t(col) * N + row_a] = v[k] * sc;
-                    if (row_b < N) J->y[size_t(col) * N + row_b] = v[2 + k] * sc;
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ float red[kPrepThreads / 32];
+    if ((tid & 31) == 0) red[tid >> 5] = m;
+    __syncthreads();
+    float amax = red[0];
+#pragma unroll
+    for (int w = 1; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+    int s = 0;
+    if (amax > 0.0f && amax <= 3.4e38f) {
+        int e;
+        frexpf(amax, &e);  // amax = f * 2^e, f in [0.5, 1)
+        s = -e - 1;
+    }
+    int *col_shift = reinterpret_cast<int *>(J.prep);
+    if (tid == 0) col_shift[j] = s;
+
+    // 2) pieces
+    uint8_t *img = J.prep + kT5PrepHeader;
+    float *beta = reinterpret_cast<float *>(img + size_t(n_chunks) * kT5ImgBytes);
+    const int lane = tid & 31;
+    const unsigned grp = 0xFFFFu << (lane & 16);  // the block's 16 threads
+    for (int idx = tid; idx < nb * 16; idx += kPrepThreads) {
+        const int b = idx >> 4, c = (idx >> 2) & 3, r = idx & 3;
+        const float *xe = xj + b * 64 + c * 16 + r;
+        const int e_in = s + ((r & 1) ? 7 : 9);    // v = x * 2^e_in
+        const float to_int = (r & 1) ? 2048.0f : 512.0f;  // piece / (2^7 or 2^9) in 2^-18 units
+        float v[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) v[jj] = mul_pow2(xe[4 * jj], e_in);
+        uint8_t *bimg = img + size_t(b >> 3) * kT5ImgBytes;
+        const int kc = 64 * (b & 7) + 16 * c;
+        int isum[kT5Pieces];
+#pragma unroll
+        for (int p = 0; p < kT5Pieces; ++p) {
+            const float up = __int_as_float((127 + 4 * p) << 23);
+            const float down = __int_as_float((127 - 4 * p) << 23);
+            const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                make_float2(v[0] * up, v[1] * up), __NV_SATFINITE, __NV_E4M3);
+            const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                make_float2(v[2] * up, v[3] * up), __NV_SATFINITE, __NV_E4M3);
+            const float2 plo = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3)));
+            const float2 phi = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
+            v[0] -= plo.x * down;
+            v[1] -= plo.y * down;
+            v[2] -= phi.x * down;
+            v[3] -= phi.y * down;
+            isum[p] = __float2int_rn(plo.x * to_int) + __float2int_rn(plo.y * to_int) +
+                      __float2int_rn(phi.x * to_int) + __float2int_rn(phi.y * to_int);
+            *reinterpret_cast<uint32_t *>(bimg + t5_img_offset(kT5Pieces * j + p, kc) + 4 * r) =
+                uint32_t(lo) | (uint32_t(hi) << 16);
+        }
+        float base[kT5Pieces];
+#pragma unroll
+        for (int p = 0; p < kT5Pieces; ++p) {
+            int t = isum[p];
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) t += __shfl_xor_sync(grp, t, o);
+            base[p] = float(t) * 0x1p-18f;
+        }
+        if ((idx & 15) == 0) {
+            // the epilogue's combination, applied to the all-ones results
+            float t = base[4] * 0x1p-16f;
+            t = fmaf(base[3], 0x1p-12f, t);
+            t = fmaf(base[2], 0x1p-8f, t);
+            t = fmaf(base[1], 0x1p-4f, t);
+            t = t + base[0];
+            beta[size_t(b >> 3) * (kT5BetaBytes / 4) + (b & 7) * 4 + j] = t;
+        }
+    }
+}
+
+// kind::f8f6f4 instruction descriptor: D f32, A and B e4m3, both K-major, N, M.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n) {
+    return (1u << 4) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+
+// NC: activation columns (1..3).
+template <int NC>
+__global__ void __launch_bounds__(kT5Threads, 1)
+    mv_t5_kernel(const __grid_constant__ MvJob single, const MvParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *img_ring = smem;                                      // kT5Stages x 8 KB
+    uint8_t *raw_ring = img_ring + kT5Stages * kT5ImgBytes;         // kT5Stages x 18 KB
+    uint8_t *beta_ring = raw_ring + kT5Stages * kT5RawBytes;        // kT5Stages x 128 B
+    uint64_t *full = reinterpret_cast<uint64_t *>(beta_ring + kT5Stages * kT5BetaBytes);
+    uint64_t *empty = full + kT5Stages;    // arrived by the 4 epilogue warps
+    uint64_t *a_full = empty + kT5Stages;  // [2] arrived by the 8 expansion warps
+    uint64_t *a_empty = a_full + 2;        // [2] tcgen05.commit
+    uint64_t *d_full = a_empty + 2;        // [2] tcgen05.commit
+    uint64_t *d_empty = d_full + 2;        // [2] arrived by the 4 epilogue warps
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kT5Stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kT5EpiWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&a_full[i], kT5ExpWarps);
+            mbar_init(&a_empty[i], 1);
+            mbar_init(&d_full[i], 1);
+            mbar_init(&d_empty[i], kT5EpiWarps);
+        }
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&s_tmem, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    int n_items, item_base = 0;
+    if (p.jobs) {
+        item_base = p.cta_begin[blockIdx.x];
+        n_items = p.cta_begin[blockIdx.x + 1] - item_base;
+    } else {
+        n_items = blockIdx.x < unsigned(single.n_tiles)
+                      ? (single.n_tiles - 1 - int(blockIdx.x)) / int(gridDim.x) + 1
+                      : 0;
+    }
+    auto item_at = [&](int i, const MvJob *&J, int &tile) {
+        if (p.jobs) {
+            const MvItem it = p.items[item_base + i];
+            J = &p.jobs[it.job];
+            tile = it.tile;
+        } else {
+            J = &single;
+            tile = int(blockIdx.x) + i * int(gridDim.x);
+        }
+    };
+    auto stage_parity = [](int s) { return uint32_t(s / kT5Stages) & 1u; };
+
+    if (warp == 0) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            int s = 0;
+            bool ok = true, prep_ready = false;
+            for (int i = 0; i < n_items && ok; ++i) {
+                const MvJob *J;
+                int tile;
+                item_at(i, J, tile);
+                const uint8_t *img = J->prep + kT5PrepHeader;
+                const uint8_t *beta = img + size_t(J->n_chunks) * kT5ImgBytes;
+                for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+                    const int st = s % kT5Stages;
+                    if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagT5Empty) ||
+                        *(volatile int *)&s_abort) {
+                        ok = false;
+                        s_abort = 1;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[st], kT5RawBytes + kT5ImgBytes + kT5BetaBytes);
+                    tma_load_2d(raw_ring + st * kT5RawBytes, &J->tmap, ch * kChunkBytes,
+                                tile * kT5Rows, &full[st]);
+                    if (!prep_ready) {
+                        grid_dependency_wait();  // the B images come from the prep kernel
+                        prep_ready = true;
+                    }
+                    bulk_g2s(img_ring + st * kT5ImgBytes, img + size_t(ch) * kT5ImgBytes,
+                             kT5ImgBytes, &full[st]);
+                    bulk_g2s(beta_ring + st * kT5BetaBytes, beta + size_t(ch) * kT5BetaBytes,
+                             kT5BetaBytes, &full[st]);
+                }
+            }
+            if (!ok) {
+                // let copies already issued land (bounded) before the CTA exits
+                for (int k = 1; k <= kT5Stages && s - k >= 0; ++k)
+                    mbar_wait(&full[(s - k) % kT5Stages], stage_parity(s - k), p.err, kTagT5Full);
+            }
+        }
+    } else if (warp == 1 || warp == kT5Warps - 1) {
+        // ------------------------------ MMA issuers ------------------------------
+        // warp 1 issues the even stages (TMEM buffers 0), the last warp the odd
+        // ones (buffers 1): two independent issue chains. The whole warp runs
+        // the loop; the elected lane issues the MMAs and their commits.
+        constexpr uint32_t idesc = idesc_e4m3(kT5Rows, kT5N);
+        const bool leader = elect_one();
+        const int buf = warp == 1 ? 0 : 1;
+        const uint64_t desc0 = sw128_desc(smem_addr(img_ring));
+        int s = 0, last = -1;
+        bool ok = true;
+        for (int i = 0; i < n_items && ok; ++i) {
+            const MvJob *J;
+            int tile;
+            item_at(i, J, tile);
+            for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+                if ((s & 1) != buf) continue;
+                const int st = s % kT5Stages;
+                const uint32_t use = uint32_t(s >> 1) & 1u;
+                const bool got = mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
+                                 mbar_wait(&a_full[buf], use, p.err, kTagT5AFull) &&
+                                 mbar_wait(&d_empty[buf], use ^ 1u, p.err, kTagT5DEmpty) &&
+                                 !*(volatile int *)&s_abort;
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_base = tmem + buf * 128;
+                const uint32_t d_base = tmem + 256 + buf * 128;
+                // descriptor start-address field advanced by the byte offset / 16
+                const uint64_t dst = desc0 + uint64_t((st * kT5ImgBytes) >> 4);
+                if (leader) {
+#pragma unroll
+                    for (int b = 0; b < kChunkBlocks; ++b)
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk)
+                            tc_mma_f8f6f4_ta(d_base + b * kT5N, a_base + b * 16 + kk * 8,
+                                             dst + uint64_t(((b >> 1) * 2048 + (b & 1) * 64 +
+                                                             kk * 32) >> 4),
+                                             idesc, uint32_t(kk));
+                    tc_commit(&a_empty[buf]);
+                    tc_commit(&d_full[buf]);
+                }
+                __syncwarp();
+                last = s;
+            }
+        }
+        if (last >= 0)  // TMEM is freed only after the last MMAs completed
+            mbar_wait(&d_full[buf], uint32_t(last >> 1) & 1u, p.err, kTagT5DFull);
+    } else if (warp < 2 + kT5ExpWarps) {
+        // ------------------------------ expansion ------------------------------
+        // warp w: TMEM lane quarter w % 4 (rows 32 (w % 4) ..), blocks 4G .. 4G+3
+        const int G = (warp - 2) >> 2;
+        const int qd = warp & 3;
+        const int row = 32 * qd + lane;
+        const uint32_t lane_base = uint32_t(32 * qd) << 16;
+        int s = 0;
+        bool ok = true;
+        for (int i = 0; i < n_items && ok; ++i) {
+            const MvJob *J;
+            int tile;
+            item_at(i, J, tile);
+            for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+                const int st = s % kT5Stages;
+                const int buf = s & 1;
+                const bool got =
+                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
+                    mbar_wait(&a_empty[buf], (uint32_t(s >> 1) & 1u) ^ 1u, p.err, kTagT5AFull) &&
+                    !*(volatile int *)&s_abort;
+                if (!__all_sync(0xffffffffu, got)) {
+                    s_abort = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes + G * 72;
+                uint32_t u[18];
+#pragma unroll
+                for (int k = 0; k < 9; ++k) {
+                    const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * k);
+                    u[2 * k] = v.x;
+                    u[2 * k + 1] = v.y;
+                }
+                const uint32_t a_base = tmem + lane_base + buf * 128 + 4 * G * 16;
+#pragma unroll
+                for (int bi = 0; bi < 4; ++bi) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        if (bi == 0) w[c] = __byte_perm(u[c], u[c + 1], 0x5432);
+                        else if (bi == 1) w[c] = u[5 + c];
+                        else if (bi == 2) w[c] = __byte_perm(u[9 + c], u[10 + c], 0x5432);
+                        else w[c] = u[14 + c];
+                    }
+                    uint32_t a[16];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t hw = w[c] >> 4;
+                        a[4 * c + 0] = w[c] & 0x03030303u;
+                        a[4 * c + 1] = w[c] & 0x0C0C0C0Cu;
+                        a[4 * c + 2] = hw & 0x03030303u;
+                        a[4 * c + 3] = hw & 0x0C0C0C0Cu;
+                    }
+                    tmem_st16(a_base + bi * 16, a);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[buf]);
+            }
+        }
+    } else if (warp < 2 + kT5ExpWarps + kT5EpiWarps) {
+        // ------------------------------ epilogue ------------------------------
+        // warp w: TMEM lane quarter w % 4; one row per thread, all 8 blocks.
+        grid_dependency_wait();  // reads the column shifts written by prep
+        const int qd = warp & 3;
+        const int row = 32 * qd + lane;
+        const uint32_t lane_base = uint32_t(32 * qd) << 16;
+        float acc[NC];
+#pragma unroll
+        for (int j = 0; j < NC; ++j) acc[j] = 0.0f;
+        int s = 0;
+        bool ok = true;
+        for (int i = 0; i < n_items && ok; ++i) {
+            const MvJob *J;
+            int tile;
+            item_at(i, J, tile);
+            for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+                const int st = s % kT5Stages;
+                const int buf = s & 1;
+                const bool got =
+                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
+                    mbar_wait(&d_full[buf], uint32_t(s >> 1) & 1u, p.err, kTagT5DFull) &&
+                    !*(volatile int *)&s_abort;
+                if (!__all_sync(0xffffffffu, got)) {
+                    s_abort = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_base = tmem + lane_base + 256 + buf * 128;
+                const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes;
+                const float *bt = reinterpret_cast<const float *>(beta_ring + st * kT5BetaBytes);
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    float C[4][NC * 5];
+                    if (NC == 1) {
+                        uint32_t r[4][8];
+#pragma unroll
+                        for (int bi = 0; bi < 4; ++bi)
+                            tmem_ld8(d_base + (4 * hb + bi) * kT5N, r[bi]);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int bi = 0; bi < 4; ++bi)
+#pragma unroll
+                            for (int n = 0; n < 5; ++n) C[bi][n] = __uint_as_float(r[bi][n]);
+                    } else {
+                        uint32_t r[4][16];
+#pragma unroll
+                        for (int bi = 0; bi < 4; ++bi)
+                            tmem_ld16(d_base + (4 * hb + bi) * kT5N, r[bi]);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int bi = 0; bi < 4; ++bi)
+#pragma unroll
+                            for (int n = 0; n < NC * 5; ++n) C[bi][n] = __uint_as_float(r[bi][n]);
+                    }
+#pragma unroll
+                    for (int bi = 0; bi < 4; ++bi) {
+                        const int b = 4 * hb + bi;
+                        const float d = lds_half_as_float(rp + 18 * b);
+#pragma unroll
+                        for (int j = 0; j < NC; ++j) {
+                            const float *c = &C[bi][5 * j];
+                            float t = c[4] * 0x1p-16f;
+                            t = fmaf(c[3], 0x1p-12f, t);
+                            t = fmaf(c[2], 0x1p-8f, t);
+                            t = fmaf(c[1], 0x1p-4f, t);
+                            t = t + c[0];
+                            acc[j] = fmaf(d, t - bt[b * 4 + j], acc[j]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&d_empty[buf]);
+                    mbar_arrive(&empty[st]);
+                }
+                if (ch == J->n_chunks - 1) {
+                    const int *col_shift = reinterpret_cast<const int *>(J->prep);
+                    const int r = tile * kT5Rows + row;
+                    if (r < J->N)
+#pragma unroll
+                        for (int j = 0; j < NC; ++j)
+                            J->y[size_t(j) * J->N + r] = mul_pow2(acc[j], -col_shift[j]);
+#pragma unroll
+                    for (int j = 0; j < NC; ++j) acc[j] = 0.0f;
                 }
             }
         }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -620,13 +1107,26 @@ __global__ void __launch_bounds__(256) mv_generic_kernel(const uint8_t *__restri
         for (int cc = 0; cc < ncols; ++cc) y[size_t(cc) * N + row] = acc[cc];
 }
 
-// One 16-row group per consumer warp: 16 consumer warps per CTA for both
-// n-tile counts.
-constexpr int kRG1 = 1;
-constexpr int kRG2 = 1;
-
 std::mutex g_attr_mu;
 bool g_attr_done[64][2];
+bool g_t5_attr_done[64][kT5MaxCols];
+
+template <int NC>
+cudaError_t set_t5_attr() {
+    return cudaFuncSetAttribute(mv_t5_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kT5Smem);
+}
+
+cudaError_t ensure_t5_attrs(int ncols) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (dev < 64 && g_t5_attr_done[dev][ncols - 1]) return cudaSuccess;
+    e = ncols == 1 ? set_t5_attr<1>() : ncols == 2 ? set_t5_attr<2>() : set_t5_attr<3>();
+    if (e == cudaSuccess && dev < 64) g_t5_attr_done[dev][ncols - 1] = true;
+    return e;
+}
 
 cudaError_t ensure_attrs(int nt) {
     int dev = 0;
@@ -635,34 +1135,42 @@ cudaError_t ensure_attrs(int nt) {
     std::lock_guard<std::mutex> lk(g_attr_mu);
     if (dev < 64 && g_attr_done[dev][nt - 1]) return cudaSuccess;
     if (nt == 1)
-        e = cudaFuncSetAttribute(mv_tc_kernel<1, kRG1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(mv_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBudget + 2 * kMaxStages * 8);
     else
-        e = cudaFuncSetAttribute(mv_tc_kernel<2, kRG2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(mv_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemBudget + 2 * kMaxStages * 8);
     if (e == cudaSuccess && dev < 64) g_attr_done[dev][nt - 1] = true;
     return e;
 }
 
-bool make_job(MvJob &J, const uint8_t *w, const uint8_t *prep, float *y, int64_t N, int64_t K) {
+// The tcgen05 path (128-row tiles) serves ncols <= kT5MaxCols; more columns run
+// the mma.sync kernel (256-row tiles).
+bool use_t5(int ncols) { return ncols <= kT5MaxCols; }
+int tile_rows_for(int ncols) { return use_t5(ncols) ? kT5Rows : kTileRows; }
+
+bool make_job(MvJob &J, const uint8_t *w, const uint8_t *prep, float *y, int64_t N, int64_t K,
+              int rows) {
     std::memset(&J, 0, sizeof(J));
     const uint64_t row_bytes = uint64_t(K / 64) * 18;
     if (!encode_tmap_2d(&J.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row_bytes, uint64_t(N), row_bytes,
-                        kChunkBytes, kTileRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+                        kChunkBytes, rows, CU_TENSOR_MAP_SWIZZLE_NONE))
         return false;
     J.prep = prep;
     J.y = y;
     J.N = int(N);
     J.nb = int(K / 64);
     J.n_chunks = int(K / 512);
-    J.n_tiles = int((N + kTileRows - 1) / kTileRows);
+    J.n_tiles = int((N + rows - 1) / rows);
     return true;
 }
 
 cudaError_t launch_prep(const MvPrepJob &single, const MvPrepJob *jobs, int n_jobs, int ncols,
                         cudaStream_t s) {
     dim3 grid(ncols, n_jobs);
-    if (n_tiles_for(ncols) == 1)
+    if (use_t5(ncols))
+        t5_prep_kernel<<<grid, kPrepThreads, 0, s>>>(single, jobs, ncols);
+    else if (n_tiles_for(ncols) == 1)
         mv_prep_kernel<1><<<grid, kPrepThreads, 0, s>>>(single, jobs, ncols);
     else
         mv_prep_kernel<2><<<grid, kPrepThreads, 0, s>>>(single, jobs, ncols);
@@ -674,7 +1182,7 @@ cudaError_t launch_prep(const MvPrepJob &single, const MvPrepJob *jobs, int n_jo
 // producer waits for the prep grid before loading any activation fragment.
 cudaError_t launch_tc(const MvJob &single, const MvParams &prm, int grid, cudaStream_t s) {
     const int nt = n_tiles_for(prm.ncols);
-    cudaError_t e = ensure_attrs(nt);
+    cudaError_t e = use_t5(prm.ncols) ? ensure_t5_attrs(prm.ncols) : ensure_attrs(nt);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -684,14 +1192,23 @@ cudaError_t launch_tc(const MvJob &single, const MvParams &prm, int grid, cudaSt
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (nt == 1) {
-        cfg.blockDim = dim3(cta_threads<kRG1>());
+    if (use_t5(prm.ncols)) {
+        cfg.blockDim = dim3(kT5Threads);
+        cfg.dynamicSmemBytes = kT5Smem;
+        if (prm.ncols == 1)
+            e = cudaLaunchKernelEx(&cfg, mv_t5_kernel<1>, single, prm);
+        else if (prm.ncols == 2)
+            e = cudaLaunchKernelEx(&cfg, mv_t5_kernel<2>, single, prm);
+        else
+            e = cudaLaunchKernelEx(&cfg, mv_t5_kernel<3>, single, prm);
+    } else if (nt == 1) {
+        cfg.blockDim = dim3(kCtaThreads);
         cfg.dynamicSmemBytes = smem_bytes_for(prm.ncols);
-        e = cudaLaunchKernelEx(&cfg, mv_tc_kernel<1, kRG1>, single, prm);
+        e = cudaLaunchKernelEx(&cfg, mv_tc_kernel<1>, single, prm);
     } else {
-        cfg.blockDim = dim3(cta_threads<kRG2>());
+        cfg.blockDim = dim3(kCtaThreads);
         cfg.dynamicSmemBytes = smem_bytes_for(prm.ncols);
-        e = cudaLaunchKernelEx(&cfg, mv_tc_kernel<2, kRG2>, single, prm);
+        e = cudaLaunchKernelEx(&cfg, mv_tc_kernel<2>, single, prm);
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -705,7 +1222,9 @@ cudaError_t launch_generic(const uint8_t *w, const float *x, float *y, int64_t N
 
 }  // namespace
 
-size_t matvec_workspace_bytes(int64_t K, int ncols) { return prep_bytes_for(K, ncols); }
+size_t matvec_workspace_bytes(int64_t K, int ncols) {
+    return use_t5(ncols) ? t5_prep_bytes(K) : prep_bytes_for(K, ncols);
+}
 
 bool matvec_fast_path_ok(const void *w, int64_t K) {
     return K % 512 == 0 && (reinterpret_cast<uintptr_t>(w) & 15u) == 0;
@@ -714,7 +1233,7 @@ bool matvec_fast_path_ok(const void *w, int64_t K) {
 int matvec_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
                void *ws, size_t ws_bytes, cudaStream_t s) {
     if (!matvec_fast_path_ok(w, K)) return cuda_status(launch_generic(w, x, y, N, K, ncols, s));
-    if (ws_bytes < prep_bytes_for(K, ncols)) return Q2_0_EINVAL;
+    if (ws_bytes < matvec_workspace_bytes(K, ncols)) return Q2_0_EINVAL;
     unsigned long long *err = error_word_ptr();
     if (!err) return Q2_0_ECUDA;
     uint8_t *prep = static_cast<uint8_t *>(ws);
@@ -722,7 +1241,7 @@ int matvec_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K,
     cudaError_t e = launch_prep(pj, nullptr, 1, ncols, s);
     if (e != cudaSuccess) return Q2_0_ECUDA;
     MvJob J;
-    if (!make_job(J, w, prep, y, N, K)) return Q2_0_ECUDA;
+    if (!make_job(J, w, prep, y, N, K, tile_rows_for(ncols))) return Q2_0_ECUDA;
     MvParams prm{nullptr, nullptr, nullptr, ncols, n_stages_for(ncols), err};
     const int grid = std::max(1, std::min(J.n_tiles, sm_count()));
     return cuda_status(launch_tc(J, prm, grid, s));
@@ -787,7 +1306,7 @@ int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **o
         size_t total = 0;
         for (int j = 0; j < P->n_fast; ++j) {
             off[j] = total;
-            total += prep_bytes_for(descs[fast[j]].K, ncols);
+            total += matvec_workspace_bytes(descs[fast[j]].K, ncols);
         }
         std::vector<MvJob> jobs(P->n_fast);
         std::vector<MvPrepJob> pjobs(P->n_fast);
@@ -795,7 +1314,7 @@ int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **o
         for (int j = 0; j < P->n_fast && st == Q2_0_OK; ++j) {
             const q2_0_mv_desc &d = descs[fast[j]];
             if (!make_job(jobs[j], static_cast<const uint8_t *>(d.w), P->d_prep + off[j], d.y, d.N,
-                          d.K))
+                          d.K, tile_rows_for(ncols)))
                 st = Q2_0_ECUDA;
             pjobs[j] = MvPrepJob{d.x, P->d_prep + off[j], int(d.K)};
         }
@@ -806,7 +1325,8 @@ int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **o
         for (int j = 0; j < P->n_fast; ++j)
             for (int t = 0; t < jobs[j].n_tiles; ++t) {
                 items.push_back(MvItem{j, t});
-                const int rows = std::min(kTileRows, jobs[j].N - t * kTileRows);
+                const int tr = tile_rows_for(ncols);
+                const int rows = std::min(tr, jobs[j].N - t * tr);
                 cost.push_back(double(rows) * jobs[j].nb);
             }
         std::vector<int> order(items.size());

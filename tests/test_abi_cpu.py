@@ -62,7 +62,9 @@ def test_argument_validation_without_gpu(L):
     assert L.q2_0_mul_mat(p, p, p, 4, 65, 4, 0, null, 0, null) == EINVAL
     ws = L.q2_0_mul_mat_workspace_size(4, 4, 512, 0)
     assert ws >= 2 * 4 * 512 * 2
-    assert L.q2_0_mul_mat_workspace_size(4, 4, 512, 1) * 2 == ws
+    # F16 needs no lo half of X; both hold the same stream-K counters and partial tiles
+    ws16 = L.q2_0_mul_mat_workspace_size(4, 4, 512, 1)
+    assert ws16 % 256 == 0 and ws16 + 4 * 512 * 2 <= ws
     assert L.q2_0_mul_mat(p, p, p, 4, 512, 4, 0, ctypes.c_void_p(0x100000), ws - 1, null) == EINVAL
     # get_rows: n_ids == 0 is a no-op, negative is invalid
     assert L.q2_0_get_rows(p, 4, 64, p, 0, p, null) == q.Q2_0_OK
