@@ -580,26 +580,31 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
 // piece_n / (2^9 or 2^7).
 //
 // Per block accumulators. d changes every 64 weights of a row, so each block
-// gets its own 16-column TMEM accumulator; the epilogue loads it and forms,
-// per row and column,
+// gets its own accumulator columns; the epilogue loads them and forms, per
+// row and column,
 //   t = sum_p 2^-4p C_(5j+p) - beta_j,   acc_j += d * t,
 // where beta_j is the same sum for all-ones codes (the "- 1" of (q - 1)),
 // computed by the preparation kernel with the same f32 operations from exact
-// per-piece sums, so that all-ones blocks give exactly 0.
+// per-piece sums, so that all-ones blocks give exactly 0. With one column
+// (5 pieces) two blocks share a 16-column accumulator: the even block's pieces
+// are B rows 0-4 and the odd block's rows 8-12, each block's other rows zero,
+// and the odd block's MMAs accumulate onto the even block's result. With 2-3
+// columns each block has its own 16 columns.
 //
 // Pipeline per CTA (persistent over 128-row tiles), stage = 8 blocks:
-//   warp 0      streams the stage's TMA box (144 B x 128 rows) and, by bulk
+//   warp 2      streams the stage's TMA box (144 B x 128 rows) and, by bulk
 //               copy, its B image and betas into an 8-deep shared-memory ring;
-//   warps 2-9   expand the stage's codes into one of two TMEM A buffers
-//               (warps 2-5 blocks 0-3, warps 6-9 blocks 4-7; warp w owns TMEM
-//               lanes 32 (w % 4) .. +31, i.e. those rows);
-//   warps 1, 14 issue the stage's 16 MMAs into one of two TMEM D buffers (warp
-//               1 the even stages, warp 14 the odd ones: a single issuing
-//               thread spends ~60-70 cycles per MMA and ~100 per barrier
-//               check, so two chains run side by side) and commit them to the
-//               expansion (A free) and epilogue (D full) barriers;
-//   warps 10-13 epilogue, one row per thread: D, the row's d values from the
+//   warps 4-11  expand the stage's codes into a TMEM A buffer (3 buffers with
+//               one column, 2 with 2-3; warps 4-7 blocks 0-3, warps 8-11 blocks
+//               4-7; warp w owns TMEM lanes 32 (w % 4) .. +31, i.e. those rows);
+//   warp 3      issues the stage's 16 MMAs into one of two TMEM D buffers and
+//               commits them to the expansion (A free) and epilogue (D full)
+//               barriers. The whole warp runs the loop and the elected lane
+//               issues: from a lone lane each MMA cost ~70 cycles to issue;
+//   warps 12-15 epilogue, one row per thread: D, the row's d values from the
 //               ring and the betas; they release the D buffer and the ring slot.
+// The expansion of a stage waits for the MMAs that last read its A buffer, so
+// the A buffer count sets how far expansion runs ahead of the tensor core.
 // ---------------------------------------------------------------------------
 constexpr int kT5Rows = 128;
 constexpr int kT5Pieces = 5;
@@ -612,11 +617,26 @@ constexpr int kT5BetaBytes = kChunkBlocks * 4 * 4;   // beta[8 blocks][4 columns
 constexpr int kT5PrepHeader = 1024;                  // int col_shift[8], images 1024-aligned
 constexpr int kT5ExpWarps = 8;
 constexpr int kT5EpiWarps = 4;
-constexpr int kT5Warps = 3 + kT5ExpWarps + kT5EpiWarps;  // + producer, 2 MMA issuers
+// Warp roles. A warp reaches only the TMEM lanes of its quarter (warp % 4), so
+// each quarter hosts 2 expansion warps and 1 epilogue warp. Two MMA issuers
+// (even and odd stages) sit on warps 1 and 3, the producer on warp 2.
+constexpr int kT5ProdWarp = 2;
+constexpr int kT5MmaWarp = 3;    // even stages; allocates TMEM
+constexpr int kT5MmaWarp2 = 1;   // odd stages
+constexpr int kT5ExpWarp0 = 4;   // warps 4-11
+constexpr int kT5EpiWarp0 = 12;  // warps 12-15
+constexpr int kT5Warps = kT5EpiWarp0 + kT5EpiWarps;
 constexpr int kT5Threads = kT5Warps * 32;
+constexpr int kT5MaxABufs = 3;
 constexpr int kT5Smem = 1024 /* alignment slack */ +
                         kT5Stages * (kT5ImgBytes + kT5RawBytes + kT5BetaBytes) +
-                        (2 * kT5Stages + 8) * 8;
+                        (2 * kT5Stages + 2 * kT5MaxABufs + 4) * 8;
+// TMEM columns (512): A buffers of 128 (8 blocks x 16 columns of 4 e4m3), then
+// two D buffers of 64 (one column: 4 block pairs x 16) or 128 (8 blocks x 16).
+__host__ __device__ constexpr int t5_abufs(int nc) { return nc == 1 ? 3 : 2; }
+__host__ __device__ constexpr int t5_dcols(int nc) { return nc == 1 ? 64 : 128; }
+static_assert(t5_abufs(1) * 128 + 2 * t5_dcols(1) <= 512, "TMEM budget");
+static_assert(t5_abufs(2) * 128 + 2 * t5_dcols(2) <= 512, "TMEM budget");
 constexpr int kTagT5Full = 111;
 constexpr int kTagT5Empty = 112;
 constexpr int kTagT5AFull = 113;
@@ -645,7 +665,9 @@ __host__ __device__ constexpr int t5_img_offset(int n, int kc) {
 // 4c + r of a block holds elements 16c + 4jj + r in byte jj). The per-piece
 // all-ones sums are exact integers in units of 2^-18 (a piece is a multiple of
 // 2^-9, divided by 2^9 or 2^7; |sum| < 64 * 448 * 2^-7), rounded once to f32.
-__global__ void __launch_bounds__(kPrepThreads) t5_prep_kernel(
+constexpr int kT5PrepThreads = 256;
+
+__global__ void __launch_bounds__(kT5PrepThreads) t5_prep_kernel(
     const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs, int ncols) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const MvPrepJob &J = jobs ? jobs[blockIdx.y] : single;
@@ -655,26 +677,30 @@ __global__ void __launch_bounds__(kPrepThreads) t5_prep_kernel(
     const int tid = threadIdx.x;
     const int nb = K / 64;
     const int n_chunks = K / 512;
+    // grid z splits a column's 16 * nb items (one per thread, grid-stride for
+    // very long columns); the CTAs past this column's items have nothing to do
+    if (int(blockIdx.z) * kT5PrepThreads >= nb * 16) return;
 
-    // 1) column scale 2^s with max|x * 2^s| in [2^-2, 2^-1)
+    // 1) column scale 2^s with max|x * 2^s| in [2^-2, 2^-1) (each CTA of the
+    //    column reads the whole column)
     float m = 0.0f;
     if ((reinterpret_cast<uintptr_t>(xj) & 15u) == 0) {
         const float4 *x4 = reinterpret_cast<const float4 *>(xj);
-        for (int k = tid; k < K / 4; k += kPrepThreads) {
+        for (int k = tid; k < K / 4; k += kT5PrepThreads) {
             const float4 f = x4[k];
             m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
         }
     } else {
-        for (int k = tid; k < K; k += kPrepThreads) m = fmaxf(m, fabsf(xj[k]));
+        for (int k = tid; k < K; k += kT5PrepThreads) m = fmaxf(m, fabsf(xj[k]));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    __shared__ float red[kPrepThreads / 32];
+    __shared__ float red[kT5PrepThreads / 32];
     if ((tid & 31) == 0) red[tid >> 5] = m;
     __syncthreads();
     float amax = red[0];
 #pragma unroll
-    for (int w = 1; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+    for (int w = 1; w < kT5PrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
     int s = 0;
     if (amax > 0.0f && amax <= 3.4e38f) {
         int e;
@@ -682,14 +708,15 @@ __global__ void __launch_bounds__(kPrepThreads) t5_prep_kernel(
         s = -e - 1;
     }
     int *col_shift = reinterpret_cast<int *>(J.prep);
-    if (tid == 0) col_shift[j] = s;
+    if (blockIdx.z == 0 && tid == 0) col_shift[j] = s;
 
     // 2) pieces
     uint8_t *img = J.prep + kT5PrepHeader;
     float *beta = reinterpret_cast<float *>(img + size_t(n_chunks) * kT5ImgBytes);
     const int lane = tid & 31;
     const unsigned grp = 0xFFFFu << (lane & 16);  // the block's 16 threads
-    for (int idx = tid; idx < nb * 16; idx += kPrepThreads) {
+    for (int idx = int(blockIdx.z) * kT5PrepThreads + tid; idx < nb * 16;
+         idx += int(gridDim.z) * kT5PrepThreads) {
         const int b = idx >> 4, c = (idx >> 2) & 3, r = idx & 3;
         const float *xe = xj + b * 64 + c * 16 + r;
         const int e_in = s + ((r & 1) ? 7 : 9);    // v = x * 2^e_in
@@ -716,8 +743,15 @@ __global__ void __launch_bounds__(kPrepThreads) t5_prep_kernel(
             v[3] -= phi.y * down;
             isum[p] = __float2int_rn(plo.x * to_int) + __float2int_rn(plo.y * to_int) +
                       __float2int_rn(phi.x * to_int) + __float2int_rn(phi.y * to_int);
-            *reinterpret_cast<uint32_t *>(bimg + t5_img_offset(kT5Pieces * j + p, kc) + 4 * r) =
+            // one column: the block's pieces are rows 0-4 (even block) or 8-12 (odd)
+            const int n = ncols == 1 ? 8 * (b & 1) + p : kT5Pieces * j + p;
+            *reinterpret_cast<uint32_t *>(bimg + t5_img_offset(n, kc) + 4 * r) =
                 uint32_t(lo) | (uint32_t(hi) << 16);
+        }
+        if (ncols == 1) {
+            // the rows the other block of the pair reads its result from stay zero
+            for (int n = 8 * (1 - (b & 1)); n < 8 * (1 - (b & 1)) + 8; ++n)
+                *reinterpret_cast<uint32_t *>(bimg + t5_img_offset(n, kc) + 4 * r) = 0u;
         }
         float base[kT5Pieces];
 #pragma unroll
@@ -748,6 +782,8 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n) {
 template <int NC>
 __global__ void __launch_bounds__(kT5Threads, 1)
     mv_t5_kernel(const __grid_constant__ MvJob single, const MvParams p) {
+    constexpr int kABufs = t5_abufs(NC);
+    constexpr int kDCols = t5_dcols(NC);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -755,11 +791,11 @@ __global__ void __launch_bounds__(kT5Threads, 1)
     uint8_t *raw_ring = img_ring + kT5Stages * kT5ImgBytes;         // kT5Stages x 18 KB
     uint8_t *beta_ring = raw_ring + kT5Stages * kT5RawBytes;        // kT5Stages x 128 B
     uint64_t *full = reinterpret_cast<uint64_t *>(beta_ring + kT5Stages * kT5BetaBytes);
-    uint64_t *empty = full + kT5Stages;    // arrived by the 4 epilogue warps
-    uint64_t *a_full = empty + kT5Stages;  // [2] arrived by the 8 expansion warps
-    uint64_t *a_empty = a_full + 2;        // [2] tcgen05.commit
-    uint64_t *d_full = a_empty + 2;        // [2] tcgen05.commit
-    uint64_t *d_empty = d_full + 2;        // [2] arrived by the 4 epilogue warps
+    uint64_t *empty = full + kT5Stages;        // arrived by the 4 epilogue warps
+    uint64_t *a_full = empty + kT5Stages;      // [kABufs] arrived by the 8 expansion warps
+    uint64_t *a_empty = a_full + kT5MaxABufs;  // [kABufs] tcgen05.commit
+    uint64_t *d_full = a_empty + kT5MaxABufs;  // [2] tcgen05.commit
+    uint64_t *d_empty = d_full + 2;            // [2] arrived by the 4 epilogue warps
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
@@ -771,16 +807,18 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kT5EpiWarps);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kABufs; ++i) {
             mbar_init(&a_full[i], kT5ExpWarps);
             mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&d_full[i], 1);
             mbar_init(&d_empty[i], kT5EpiWarps);
         }
         s_abort = 0;
         fence_barrier_init();
     }
-    if (warp == 1) {
+    if (warp == kT5MmaWarp) {
         tmem_alloc(&s_tmem, 512);
         tmem_relinquish();
     }
@@ -809,8 +847,13 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         }
     };
     auto stage_parity = [](int s) { return uint32_t(s / kT5Stages) & 1u; };
+    // A buffer of stage s and the parity of its use; D buffer likewise
+    auto a_buf = [](int s) { return s % kABufs; };
+    auto a_use = [](int s) { return uint32_t(s / kABufs) & 1u; };
+    auto a_col = [&](int s) { return uint32_t(a_buf(s) * 128); };
+    auto d_col = [&](int s) { return uint32_t(kABufs * 128 + (s & 1) * kDCols); };
 
-    if (warp == 0) {
+    if (warp == kT5ProdWarp) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
             int s = 0;
@@ -848,14 +891,17 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     mbar_wait(&full[(s - k) % kT5Stages], stage_parity(s - k), p.err, kTagT5Full);
             }
         }
-    } else if (warp == 1 || warp == kT5Warps - 1) {
+    } else if (warp == kT5MmaWarp || warp == kT5MmaWarp2) {
         // ------------------------------ MMA issuers ------------------------------
-        // warp 1 issues the even stages (TMEM buffers 0), the last warp the odd
-        // ones (buffers 1): two independent issue chains. The whole warp runs
-        // the loop; the elected lane issues the MMAs and their commits.
+        // Each issuer's per-stage control path (barrier checks, fence, issue,
+        // commits) takes about a stage's worth of time, so two issuers take
+        // the even and the odd stages (D buffer = stage parity; consecutive
+        // uses of an A buffer are ordered through its expansion). The whole
+        // warp runs the loop (addresses and descriptors stay warp-uniform);
+        // the elected lane waits, issues the MMAs and commits them.
         constexpr uint32_t idesc = idesc_e4m3(kT5Rows, kT5N);
         const bool leader = elect_one();
-        const int buf = warp == 1 ? 0 : 1;
+        const int parity = warp == kT5MmaWarp ? 0 : 1;
         const uint64_t desc0 = sw128_desc(smem_addr(img_ring));
         int s = 0, last = -1;
         bool ok = true;
@@ -864,45 +910,52 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             int tile;
             item_at(i, J, tile);
             for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
-                if ((s & 1) != buf) continue;
+                if ((s & 1) != parity) continue;
                 const int st = s % kT5Stages;
-                const uint32_t use = uint32_t(s >> 1) & 1u;
-                const bool got = mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
-                                 mbar_wait(&a_full[buf], use, p.err, kTagT5AFull) &&
-                                 mbar_wait(&d_empty[buf], use ^ 1u, p.err, kTagT5DEmpty) &&
-                                 !*(volatile int *)&s_abort;
+                // the leader waits; the other lanes park at the shuffle
+                bool got = true;
+                if (leader)
+                    got = mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
+                          mbar_wait(&a_full[a_buf(s)], a_use(s), p.err, kTagT5AFull) &&
+                          mbar_wait(&d_empty[s & 1], (uint32_t(s >> 1) & 1u) ^ 1u, p.err,
+                                    kTagT5DEmpty) &&
+                          !*(volatile int *)&s_abort;
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     s_abort = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a_base = tmem + buf * 128;
-                const uint32_t d_base = tmem + 256 + buf * 128;
+                const uint32_t a_base = tmem + a_col(s);
+                const uint32_t d_base = tmem + d_col(s);
                 // descriptor start-address field advanced by the byte offset / 16
                 const uint64_t dst = desc0 + uint64_t((st * kT5ImgBytes) >> 4);
                 if (leader) {
 #pragma unroll
                     for (int b = 0; b < kChunkBlocks; ++b)
 #pragma unroll
-                        for (int kk = 0; kk < 2; ++kk)
-                            tc_mma_f8f6f4_ta(d_base + b * kT5N, a_base + b * 16 + kk * 8,
+                        for (int kk = 0; kk < 2; ++kk) {
+                            // one column: blocks 2i, 2i+1 share accumulator i
+                            const uint32_t dcol = NC == 1 ? (b >> 1) * kT5N : b * kT5N;
+                            const uint32_t accum = NC == 1 ? uint32_t((b & 1) | kk) : uint32_t(kk);
+                            tc_mma_f8f6f4_ta(d_base + dcol, a_base + b * 16 + kk * 8,
                                              dst + uint64_t(((b >> 1) * 2048 + (b & 1) * 64 +
                                                              kk * 32) >> 4),
-                                             idesc, uint32_t(kk));
-                    tc_commit(&a_empty[buf]);
-                    tc_commit(&d_full[buf]);
+                                             idesc, accum);
+                        }
+                    tc_commit(&a_empty[a_buf(s)]);
+                    tc_commit(&d_full[s & 1]);
                 }
                 __syncwarp();
                 last = s;
             }
         }
         if (last >= 0)  // TMEM is freed only after the last MMAs completed
-            mbar_wait(&d_full[buf], uint32_t(last >> 1) & 1u, p.err, kTagT5DFull);
-    } else if (warp < 2 + kT5ExpWarps) {
+            mbar_wait(&d_full[last & 1], uint32_t(last >> 1) & 1u, p.err, kTagT5DFull);
+    } else if (warp >= kT5ExpWarp0 && warp < kT5ExpWarp0 + kT5ExpWarps) {
         // ------------------------------ expansion ------------------------------
         // warp w: TMEM lane quarter w % 4 (rows 32 (w % 4) ..), blocks 4G .. 4G+3
-        const int G = (warp - 2) >> 2;
+        const int G = (warp - kT5ExpWarp0) >> 2;
         const int qd = warp & 3;
         const int row = 32 * qd + lane;
         const uint32_t lane_base = uint32_t(32 * qd) << 16;
@@ -914,10 +967,9 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             item_at(i, J, tile);
             for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
                 const int st = s % kT5Stages;
-                const int buf = s & 1;
                 const bool got =
                     mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
-                    mbar_wait(&a_empty[buf], (uint32_t(s >> 1) & 1u) ^ 1u, p.err, kTagT5AFull) &&
+                    mbar_wait(&a_empty[a_buf(s)], a_use(s) ^ 1u, p.err, kTagT5AFull) &&
                     !*(volatile int *)&s_abort;
                 if (!__all_sync(0xffffffffu, got)) {
                     s_abort = 1;
@@ -933,23 +985,20 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     u[2 * k] = v.x;
                     u[2 * k + 1] = v.y;
                 }
-                const uint32_t a_base = tmem + lane_base + buf * 128 + 4 * G * 16;
+                const uint32_t a_base = tmem + lane_base + a_col(s) + 4 * G * 16;
 #pragma unroll
                 for (int bi = 0; bi < 4; ++bi) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (bi == 0) w[c] = __byte_perm(u[c], u[c + 1], 0x5432);
-                        else if (bi == 1) w[c] = u[5 + c];
-                        else if (bi == 2) w[c] = __byte_perm(u[9 + c], u[10 + c], 0x5432);
-                        else w[c] = u[14 + c];
-                    }
                     uint32_t a[16];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const uint32_t hw = w[c] >> 4;
-                        a[4 * c + 0] = w[c] & 0x03030303u;
-                        a[4 * c + 1] = w[c] & 0x0C0C0C0Cu;
+                        uint32_t w;
+                        if (bi == 0) w = __byte_perm(u[c], u[c + 1], 0x5432);
+                        else if (bi == 1) w = u[5 + c];
+                        else if (bi == 2) w = __byte_perm(u[9 + c], u[10 + c], 0x5432);
+                        else w = u[14 + c];
+                        const uint32_t hw = w >> 4;
+                        a[4 * c + 0] = w & 0x03030303u;
+                        a[4 * c + 1] = w & 0x0C0C0C0Cu;
                         a[4 * c + 2] = hw & 0x03030303u;
                         a[4 * c + 3] = hw & 0x0C0C0C0Cu;
                     }
@@ -958,10 +1007,10 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[buf]);
+                if (lane == 0) mbar_arrive(&a_full[a_buf(s)]);
             }
         }
-    } else if (warp < 2 + kT5ExpWarps + kT5EpiWarps) {
+    } else if (warp >= kT5EpiWarp0) {
         // ------------------------------ epilogue ------------------------------
         // warp w: TMEM lane quarter w % 4; one row per thread, all 8 blocks.
         grid_dependency_wait();  // reads the column shifts written by prep
@@ -979,10 +1028,9 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             item_at(i, J, tile);
             for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
                 const int st = s % kT5Stages;
-                const int buf = s & 1;
                 const bool got =
                     mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
-                    mbar_wait(&d_full[buf], uint32_t(s >> 1) & 1u, p.err, kTagT5DFull) &&
+                    mbar_wait(&d_full[s & 1], uint32_t(s >> 1) & 1u, p.err, kTagT5DFull) &&
                     !*(volatile int *)&s_abort;
                 if (!__all_sync(0xffffffffu, got)) {
                     s_abort = 1;
@@ -990,22 +1038,24 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_base = tmem + lane_base + 256 + buf * 128;
+                const uint32_t d_base = tmem + lane_base + d_col(s);
                 const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes;
                 const float *bt = reinterpret_cast<const float *>(beta_ring + st * kT5BetaBytes);
 #pragma unroll
                 for (int hb = 0; hb < 2; ++hb) {
+                    // blocks 4hb .. 4hb+3: C[bi][n] = accumulator column n of block 4hb+bi
                     float C[4][NC * 5];
                     if (NC == 1) {
-                        uint32_t r[4][8];
+                        uint32_t r[2][16];
 #pragma unroll
-                        for (int bi = 0; bi < 4; ++bi)
-                            tmem_ld8(d_base + (4 * hb + bi) * kT5N, r[bi]);
+                        for (int pi = 0; pi < 2; ++pi)
+                            tmem_ld16(d_base + (2 * hb + pi) * kT5N, r[pi]);
                         tmem_wait_ld();
 #pragma unroll
                         for (int bi = 0; bi < 4; ++bi)
 #pragma unroll
-                            for (int n = 0; n < 5; ++n) C[bi][n] = __uint_as_float(r[bi][n]);
+                            for (int n = 0; n < 5; ++n)
+                                C[bi][n] = __uint_as_float(r[bi >> 1][8 * (bi & 1) + n]);
                     } else {
                         uint32_t r[4][16];
 #pragma unroll
@@ -1036,7 +1086,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&d_empty[buf]);
+                    mbar_arrive(&d_empty[s & 1]);
                     mbar_arrive(&empty[st]);
                 }
                 if (ch == J->n_chunks - 1) {
@@ -1055,7 +1105,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kT5MmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -1165,12 +1215,15 @@ bool make_job(MvJob &J, const uint8_t *w, const uint8_t *prep, float *y, int64_t
     return true;
 }
 
+// max_k: the largest K among the jobs (sets the t5 prep's grid z).
 cudaError_t launch_prep(const MvPrepJob &single, const MvPrepJob *jobs, int n_jobs, int ncols,
-                        cudaStream_t s) {
+                        int64_t max_k, cudaStream_t s) {
     dim3 grid(ncols, n_jobs);
-    if (use_t5(ncols))
-        t5_prep_kernel<<<grid, kPrepThreads, 0, s>>>(single, jobs, ncols);
-    else if (n_tiles_for(ncols) == 1)
+    if (use_t5(ncols)) {
+        const int64_t items = max_k / 64 * 16;
+        grid.z = unsigned(std::min<int64_t>((items + kT5PrepThreads - 1) / kT5PrepThreads, 65535));
+        t5_prep_kernel<<<grid, kT5PrepThreads, 0, s>>>(single, jobs, ncols);
+    } else if (n_tiles_for(ncols) == 1)
         mv_prep_kernel<1><<<grid, kPrepThreads, 0, s>>>(single, jobs, ncols);
     else
         mv_prep_kernel<2><<<grid, kPrepThreads, 0, s>>>(single, jobs, ncols);
@@ -1238,7 +1291,7 @@ int matvec_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K,
     if (!err) return Q2_0_ECUDA;
     uint8_t *prep = static_cast<uint8_t *>(ws);
     MvPrepJob pj{x, prep, int(K)};
-    cudaError_t e = launch_prep(pj, nullptr, 1, ncols, s);
+    cudaError_t e = launch_prep(pj, nullptr, 1, ncols, K, s);
     if (e != cudaSuccess) return Q2_0_ECUDA;
     MvJob J;
     if (!make_job(J, w, prep, y, N, K, tile_rows_for(ncols))) return Q2_0_ECUDA;
@@ -1257,6 +1310,7 @@ struct q2_0_mv_plan {
     int ncols = 1;
     int n_fast = 0;
     int grid = 0;
+    int64_t max_k = 0;  // largest K among the TMA-path jobs
     q2::MvJob *d_jobs = nullptr;
     q2::MvItem *d_items = nullptr;
     int *d_cta_begin = nullptr;
@@ -1317,6 +1371,7 @@ int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **o
                           d.K, tile_rows_for(ncols)))
                 st = Q2_0_ECUDA;
             pjobs[j] = MvPrepJob{d.x, P->d_prep + off[j], int(d.K)};
+            P->max_k = std::max<int64_t>(P->max_k, d.K);
         }
         // Longest-processing-time-first schedule of (job, tile) items over one CTA
         // per SM; cost of an item = rows in the tile x K.
@@ -1386,7 +1441,7 @@ int mv_plan_execute(const q2_0_mv_plan *P, cudaStream_t s) {
     if (cudaGetDevice(&cur) != cudaSuccess || cur != P->device) return Q2_0_EINVAL;
     if (P->n_fast > 0) {
         MvPrepJob none{nullptr, nullptr, 0};
-        if (launch_prep(none, P->d_prep_jobs, P->n_fast, P->ncols, s) != cudaSuccess)
+        if (launch_prep(none, P->d_prep_jobs, P->n_fast, P->ncols, P->max_k, s) != cudaSuccess)
             return Q2_0_ECUDA;
         MvJob dummy;
         std::memset(&dummy, 0, sizeof(dummy));

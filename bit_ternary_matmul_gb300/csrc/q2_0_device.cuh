@@ -69,16 +69,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete is suspended in
+// hardware until it completes or about suspend_ns pass, instead of returning
+// at once: waiting threads do not take issue slots from their neighbours.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t parity,
+                                                      uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete. Gives up after about
 // one second: records the timeout (tag identifies the wait) and returns false.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr uint32_t kWaitSuspendNs = 20000;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned long long *err,
                                           int tag) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_suspend(bar, parity, kWaitSuspendNs)) return true;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             record_error(err, Q2_0_DEVERR_TIMEOUT, tag);
             return false;
