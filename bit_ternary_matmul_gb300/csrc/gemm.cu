@@ -66,13 +66,13 @@ struct GemmArgs {
     int split;  // 1: hi + lo, 0: hi only
     int n_units, n_mtiles;  // units = (N / 256 rounded up) x (M / 128 rounded up)
     long long total_slabs;  // n_units * K / 64: the stream-K iteration space
-    int *counters;          // per unit: pieces finished (zeroed by the prepass)
     float *partials;        // 2 slots per CTA of kBN x (kWT * kBM) fp32
     unsigned long long *err;
 };
 
 // Stream-K: CTA c owns global slabs [T*c/G, T*(c+1)/G) of the unit-major slab
-// order; a unit whose slabs span several CTAs is finished by the last of them.
+// order. A unit whose slabs span several CTAs is summed afterwards by
+// gemm_reduce_kernel from the CTAs' partial tiles, in K order.
 __host__ __device__ inline long long sk_begin(int c, long long T, int G) {
     return (T * c) / G;
 }
@@ -97,12 +97,10 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
 __global__ void __launch_bounds__(256) gemm_prep_kernel(const float *__restrict__ x,
                                                         __half *__restrict__ xh,
                                                         __half *__restrict__ xl, int64_t groups,
-                                                        int split, int *counters, int n_counters) {
+                                                        int split) {
     // The GEMM kernel that follows may start its prologue and weight loads now;
-    // it waits for this grid before reading X or the counters.
+    // it waits for this grid before reading X.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_counters; i += gridDim.x * blockDim.x)
-        counters[i] = 0;
     for (int64_t gidx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; gidx < groups;
          gidx += int64_t(gridDim.x) * blockDim.x) {
         const float4 *src = reinterpret_cast<const float4 *>(x + gidx * 16);
@@ -150,6 +148,9 @@ __device__ __forceinline__ uint32_t expand_pair(uint32_t word, int t, __half2 d2
 }
 
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmArgs a) {
+    // The stream-K reduction that follows may be scheduled now; it waits for
+    // this grid to finish before it reads any partial tile.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled X tiles
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -167,7 +168,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     uint64_t *acc_empty = acc_full + 1;      // [1]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
-    int *last_flag = abort_flag + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         ok = false;
                         break;
                     }
-                    if (!prep_done) {  // X (and the counters) come from the prepass
+                    if (!prep_done) {  // X comes from the prepass
                         asm volatile("griddepcontrol.wait;" ::: "memory");
                         prep_done = true;
                     }
@@ -409,9 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const int q = warp & 3, t = (warp - 2 - kExpandWarps) >> 2;
         const uint32_t lane_addr = uint32_t(q * 32) << 16;
         const int rloc = t * kBM + q * 32 + lane;  // row within the unit
-        asm volatile("griddepcontrol.wait;" ::: "memory");  // counters zeroed by the prepass
-        // A warp whose wait timed out stops reading TMEM and writing, but keeps
-        // taking part in the epilogue barriers so that the other warps finish.
+        // A warp whose wait timed out stops reading TMEM and writing.
         bool dead = false;
         int nu = 0;
         for (long long g = g_begin; g < g_end; ++nu) {
@@ -424,17 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 const bool got = mbar_wait(acc_full, uint32_t(nu & 1), a.err, kTagGemm + 8);
                 dead = !__all_sync(0xffffffffu, got);
             }
+            if (dead) continue;
             const bool whole = kb == 0 && ke == n_slabs;
-            if (dead) {
-                if (!whole) {
-                    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-                    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-                }
-                continue;
-            }
             tc_fence_after();
             const int n = n0 + rloc;
-            // partial pieces: slot 2c for a CTA's first segment, 2c + 1 for its last
+            // partial tiles: slot 2c for a CTA's first segment, 2c + 1 for its last
             const long long ustart = (long long)u * n_slabs;
             float *mine = a.partials +
                           size_t(2 * blockIdx.x + (g_begin >= ustart ? 0 : 1)) * (kPartialBytes / 4);
@@ -459,76 +451,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);  // accumulators free for the next segment
-            if (whole) continue;
-            // Publish the piece; the CTA that completes the unit sums its pieces in
-            // K order (deterministic) and writes Y.
-            __threadfence();
-            asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-            const int c_first = sk_owner(ustart, a.total_slabs, gridDim.x);
-            const int c_last = sk_owner(ustart + n_slabs - 1, a.total_slabs, gridDim.x);
-            if (warp == 2 + kExpandWarps && lane == 0)
-                *last_flag = atomicAdd(&a.counters[u], 1) == c_last - c_first;
-            asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
-            if (!*(volatile int *)last_flag) continue;
-            __threadfence();
-            // Sum the pieces in K order, all 256 epilogue threads over the unit's
-            // tile as float4 runs of 4 rows; loads of up to 2 pieces in flight.
-            const int tid = (warp - 2 - kExpandWarps) * 32 + lane;
-            constexpr int kRowVec = kWT * kBM / 4;            // float4 per token row
-            constexpr int kTileVec = kBN * kRowVec;           // float4 per tile
-            const bool vec_y = (a.N % 4) == 0 && (reinterpret_cast<uintptr_t>(a.y) & 15u) == 0;
-            const int n_pieces = c_last - c_first + 1;
-#pragma unroll 1
-            for (int i0 = tid; i0 < kTileVec; i0 += kEpiWarps * 32 * 4) {
-                float4 acc[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int p0 = 0; p0 < n_pieces; p0 += 2) {
-                    float4 v[2][4];
-#pragma unroll
-                    for (int pp = 0; pp < 2; ++pp) {
-                        const int cp = c_first + p0 + pp;
-                        if (p0 + pp < n_pieces) {
-                            const float4 *piece = reinterpret_cast<const float4 *>(
-                                a.partials +
-                                size_t(2 * cp + (sk_begin(cp, a.total_slabs, gridDim.x) >= ustart ? 0 : 1)) *
-                                    (kPartialBytes / 4));
-#pragma unroll
-                            for (int r = 0; r < 4; ++r) {
-                                const int i = i0 + r * kEpiWarps * 32;
-                                v[pp][r] = i < kTileVec ? __ldcg(piece + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int pp = 0; pp < 2; ++pp)
-                        if (p0 + pp < n_pieces)
-#pragma unroll
-                            for (int r = 0; r < 4; ++r) {
-                                acc[r].x += v[pp][r].x;
-                                acc[r].y += v[pp][r].y;
-                                acc[r].z += v[pp][r].z;
-                                acc[r].w += v[pp][r].w;
-                            }
-                }
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int i = i0 + r * kEpiWarps * 32;
-                    if (i >= kTileVec) continue;
-                    const int m = m0 + i / kRowVec;
-                    const int nn = n0 + 4 * (i % kRowVec);
-                    if (m >= a.M) continue;
-                    float *yr = a.y + size_t(m) * a.N;
-                    if (vec_y && nn + 3 < a.N) {
-                        *reinterpret_cast<float4 *>(yr + nn) = acc[r];
-                    } else {
-                        if (nn < a.N) yr[nn] = acc[r].x;
-                        if (nn + 1 < a.N) yr[nn + 1] = acc[r].y;
-                        if (nn + 2 < a.N) yr[nn + 2] = acc[r].z;
-                        if (nn + 3 < a.N) yr[nn + 3] = acc[r].w;
-                    }
-                }
-            }
         }
     }
     tc_fence_before();
@@ -536,6 +458,74 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Stream-K reduction: the units split across CTAs, summed from the partial
+// tiles in K order (deterministic) and written to Y. grid = (kReduceSlices,
+// GEMM grid): column c of the grid takes the unit in which CTA c's range
+// begins, if that unit began in an earlier CTA's range and ends in c's (c is
+// the unit's last contributor), so each split unit is summed exactly once;
+// slice z takes 1/kReduceSlices of the unit's tile. Launched as a programmatic
+// dependent of the GEMM: it waits for the GEMM grid before reading partials.
+// ---------------------------------------------------------------------------
+constexpr int kReduceSlices = 8;
+constexpr int kReduceThreads = 256;
+
+__global__ void __launch_bounds__(kReduceThreads) gemm_reduce_kernel(
+    const float *__restrict__ partials, float *__restrict__ y, int M, int N, int n_mtiles,
+    int n_slabs, long long total_slabs) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int G = int(gridDim.y), c = int(blockIdx.y);
+    const long long gb = sk_begin(c, total_slabs, G);
+    const int u = int(gb / n_slabs);
+    const long long ustart = (long long)u * n_slabs;
+    if (gb == ustart) return;  // c begins its first unit: not a split unit's finisher
+    const int c_first = sk_owner(ustart, total_slabs, G);
+    const int c_last = sk_owner(ustart + n_slabs - 1, total_slabs, G);
+    if (c != c_last) return;
+    const int n0 = (u / n_mtiles) * (kWT * kBM);
+    const int m0 = (u % n_mtiles) * kBN;
+    constexpr int kRowVec = kWT * kBM / 4;          // float4 per token row
+    constexpr int kTileVec = kBN * kRowVec;         // float4 per tile
+    constexpr int kSliceVec = kTileVec / kReduceSlices;
+    constexpr int kPer = kSliceVec / kReduceThreads;  // float4 per thread
+    const bool vec_y = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(y) & 15u) == 0;
+    float4 acc[kPer];
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int i_base = int(blockIdx.x) * kSliceVec + int(threadIdx.x);
+    for (int cp = c_first; cp <= c_last; ++cp) {
+        const float4 *piece = reinterpret_cast<const float4 *>(
+            partials + size_t(2 * cp + (sk_begin(cp, total_slabs, G) >= ustart ? 0 : 1)) *
+                           (kPartialBytes / 4));
+        float4 v[kPer];
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) v[r] = __ldcg(piece + i_base + r * kReduceThreads);
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) {
+            acc[r].x += v[r].x;
+            acc[r].y += v[r].y;
+            acc[r].z += v[r].z;
+            acc[r].w += v[r].w;
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+        const int i = i_base + r * kReduceThreads;
+        const int m = m0 + i / kRowVec;
+        const int nn = n0 + 4 * (i % kRowVec);
+        if (m >= M) continue;
+        float *yr = y + size_t(m) * N;
+        if (vec_y && nn + 3 < N) {
+            *reinterpret_cast<float4 *>(yr + nn) = acc[r];
+        } else {
+            if (nn < N) yr[nn] = acc[r].x;
+            if (nn + 1 < N) yr[nn + 1] = acc[r].y;
+            if (nn + 2 < N) yr[nn + 2] = acc[r].z;
+            if (nn + 3 < N) yr[nn + 3] = acc[r].w;
+        }
     }
 }
 
@@ -600,7 +590,6 @@ namespace {
 
 struct GemmLayout {
     size_t part;      // bytes of X_hi (and of X_lo)
-    size_t counters;  // offset of the per-unit counters
     size_t partials;  // offset of the partial tiles
     size_t total;
     int n_units, n_mtiles, grid;
@@ -609,7 +598,7 @@ struct GemmLayout {
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// Workspace: [X_hi][X_lo (split)][unit counters][2 partial tiles per stream-K CTA].
+// Workspace: [X_hi][X_lo (split)][2 partial tiles per stream-K CTA].
 // The grid is at most kMaxGrid CTAs, at least 8 slabs each.
 GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K, int prec, int sms) {
     GemmLayout L;
@@ -619,8 +608,7 @@ GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K, int prec, int sms) {
     L.total_slabs = (long long)L.n_units * (K / kSlabK);
     const long long by_work = std::max<long long>(1, L.total_slabs / 8);
     L.grid = int(std::min<long long>(std::min<long long>(sms > 0 ? sms : kMaxGrid, kMaxGrid), by_work));
-    L.counters = (prec == Q2_0_PREC_F16_SPLIT ? 2 : 1) * L.part;
-    L.partials = L.counters + align256(size_t(L.n_units) * 4);
+    L.partials = (prec == Q2_0_PREC_F16_SPLIT ? 2 : 1) * L.part;
     L.total = L.partials + size_t(2) * L.grid * kPartialBytes;
     return L;
 }
@@ -647,12 +635,11 @@ int gemm_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, i
     uint8_t *wsb = static_cast<uint8_t *>(ws);
     __half *xh = reinterpret_cast<__half *>(wsb);
     __half *xl = split ? reinterpret_cast<__half *>(wsb + L.part) : nullptr;
-    int *counters = reinterpret_cast<int *>(wsb + L.counters);
     float *partials = reinterpret_cast<float *>(wsb + L.partials);
     const int64_t groups = M * K / 16;
     int64_t pgrid = std::min<int64_t>((groups + 255) / 256, int64_t(sm_count()) * 8);
-    gemm_prep_kernel<<<unsigned(std::max<int64_t>(pgrid, 1)), 256, 0, s>>>(x, xh, xl, groups, split,
-                                                                         counters, L.n_units);
+    gemm_prep_kernel<<<unsigned(std::max<int64_t>(pgrid, 1)), 256, 0, s>>>(x, xh, xl, groups,
+                                                                         split);
     if (cudaGetLastError() != cudaSuccess) return Q2_0_ECUDA;
 
     GemmArgs args;
@@ -676,7 +663,6 @@ int gemm_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, i
     args.n_mtiles = L.n_mtiles;
     args.n_units = L.n_units;
     args.total_slabs = L.total_slabs;
-    args.counters = counters;
     args.partials = partials;
     if (ensure_attr() != cudaSuccess) return Q2_0_ECUDA;
     cudaLaunchConfig_t cfg = {};
@@ -690,6 +676,14 @@ int gemm_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, i
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel, args) != cudaSuccess) return Q2_0_ECUDA;
+    // the stream-K reduction, as a programmatic dependent of the GEMM
+    cfg.gridDim = dim3(kReduceSlices, L.grid);
+    cfg.blockDim = dim3(kReduceThreads);
+    cfg.dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(&cfg, gemm_reduce_kernel, static_cast<const float *>(partials), y,
+                           int(M), int(N), L.n_mtiles, int(K / kSlabK), L.total_slabs) !=
+        cudaSuccess)
+        return Q2_0_ECUDA;
     return cuda_status(cudaGetLastError());
 }
 
