@@ -50,6 +50,7 @@ EXPORTS = (
     "q2_0_mul_mat_vec_ws", "q2_0_mul_mat_vec_noalloc", "q2_0_mv_plan_create", "q2_0_mv_plan_execute",
     "q2_0_mv_plan_launches", "q2_0_mv_plan_destroy", "q2_0_mul_mat_workspace_size",
     "q2_0_mul_mat", "q2_0_get_rows", "q2_0_quantize_ref", "q2_0_get_error",
+    "q2_0_mul_mat_vec_f16", "q2_0_mul_mat_f16",
 )
 
 
@@ -111,6 +112,10 @@ def lib():
             L.q2_0_mul_mat_workspace_size.restype = sz
             L.q2_0_mul_mat.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, sz, vp]
             L.q2_0_mul_mat.restype = i32
+            L.q2_0_mul_mat_vec_f16.argtypes = [vp, vp, vp, i64, i64, i32, vp]
+            L.q2_0_mul_mat_vec_f16.restype = i32
+            L.q2_0_mul_mat_f16.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+            L.q2_0_mul_mat_f16.restype = i32
             L.q2_0_get_rows.argtypes = [vp, i64, i64, vp, i64, vp, vp]
             L.q2_0_get_rows.restype = i32
             L.q2_0_quantize_ref.argtypes = [vp, vp, i64, i64, vp]
@@ -170,6 +175,21 @@ def q2_0_mul_mat_vec(w: torch.Tensor, x: torch.Tensor, N: int, K: int, ncols: in
                                 _dev(x, "x", torch.float32, ncols * K),
                                 _dev(y, "y", torch.float32, ncols * N), N, K, ncols, _stream(stream))
     _check("q2_0_mul_mat_vec", st)
+    return y
+
+
+def q2_0_mul_mat_vec_f16(w: torch.Tensor, x: torch.Tensor, N: int, K: int,
+                         ncols: int | None = None, y: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """As q2_0_mul_mat_vec with x F16 [ncols][K]."""
+    ncols = x.shape[0] if (ncols is None and x.dim() == 2) else (ncols or 1)
+    if y is None:
+        y = torch.empty((ncols, N), dtype=torch.float32, device=x.device)
+    st = lib().q2_0_mul_mat_vec_f16(_dev(w, "w", torch.uint8, packed_bytes(N, K)),
+                                    _dev(x, "x", torch.float16, ncols * K),
+                                    _dev(y, "y", torch.float32, ncols * N), N, K, ncols,
+                                    _stream(stream))
+    _check("q2_0_mul_mat_vec_f16", st)
     return y
 
 
@@ -270,6 +290,27 @@ def q2_0_mul_mat(w: torch.Tensor, x: torch.Tensor, N: int, K: int, M: int | None
                             _dev(y, "y", torch.float32, M * N), N, K, M, prec, ws_ptr, ws_bytes,
                             _stream(stream))
     _check("q2_0_mul_mat", st)
+    return y
+
+
+def q2_0_mul_mat_f16(w: torch.Tensor, x: torch.Tensor, N: int, K: int, M: int | None = None,
+                     y: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """As q2_0_mul_mat with x F16 [M][K] (exact fp16 operands; workspace size of
+    Q2_0_PREC_F16)."""
+    M = x.shape[0] if M is None else M
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_bytes = workspace.numel()
+        ws_ptr = _dev(workspace, "workspace", torch.uint8,
+                      q2_0_mul_mat_workspace_size(M, N, K, Q2_0_PREC_F16))
+    st = lib().q2_0_mul_mat_f16(_dev(w, "w", torch.uint8, packed_bytes(N, K)),
+                                _dev(x, "x", torch.float16, M * K),
+                                _dev(y, "y", torch.float32, M * N), N, K, M, ws_ptr, ws_bytes,
+                                _stream(stream))
+    _check("q2_0_mul_mat_f16", st)
     return y
 
 

@@ -142,12 +142,16 @@ int q2_0_mul_mat_vec_ws(const void *w, const float *x, float *y, int64_t N, int6
         return Q2_0_EINVAL;
     int st = check_device(nullptr);
     if (st != Q2_0_OK) return st;
-    return matvec_run(static_cast<const uint8_t *>(w), x, y, N, K, ncols, workspace,
+    return matvec_run(static_cast<const uint8_t *>(w), x, kXF32, y, N, K, ncols, workspace,
                       workspace_bytes, as_stream(stream));
 }
 
-int q2_0_mul_mat_vec(const void *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
-                     void *stream) {
+}  // extern "C"
+
+namespace {
+
+int mul_mat_vec_pool(const void *w, const void *x, int xtype, float *y, int64_t N, int64_t K,
+                     int ncols, void *stream) {
     if (!w || !x || !y || N < 1 || N > (int64_t(1) << 31) - 1 || !valid_k(K) || ncols < 1 ||
         ncols > 8)
         return Q2_0_EINVAL;
@@ -157,10 +161,47 @@ int q2_0_mul_mat_vec(const void *w, const float *x, float *y, int64_t N, int64_t
     PoolScratch ws;
     st = ws.alloc(need, as_stream(stream));
     if (st != Q2_0_OK) return st;
-    st = matvec_run(static_cast<const uint8_t *>(w), x, y, N, K, ncols, ws.ptr, need,
+    st = matvec_run(static_cast<const uint8_t *>(w), x, xtype, y, N, K, ncols, ws.ptr, need,
                     as_stream(stream));
     int st2 = ws.release();
     return st != Q2_0_OK ? st : st2;
+}
+
+int mul_mat_impl(const void *w, const void *x, int xtype, float *y, int64_t N, int64_t K,
+                 int64_t M, int prec, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!w || !x || !y || N < 1 || M < 1 || N > (int64_t(1) << 31) - 1 ||
+        M > (int64_t(1) << 31) - 1 || !valid_k(K) ||
+        (prec != Q2_0_PREC_F16_SPLIT && prec != Q2_0_PREC_F16))
+        return Q2_0_EINVAL;
+    size_t need = gemm_workspace_bytes(M, N, K, prec);
+    if (workspace && (workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return Q2_0_EINVAL;
+    int st = check_device(nullptr);
+    if (st != Q2_0_OK) return st;
+    if (workspace || need == 0)
+        return gemm_run(static_cast<const uint8_t *>(w), x, xtype, y, N, K, M, prec, workspace,
+                        workspace_bytes, as_stream(stream));
+    PoolScratch ws;
+    st = ws.alloc(need, as_stream(stream));
+    if (st != Q2_0_OK) return st;
+    st = gemm_run(static_cast<const uint8_t *>(w), x, xtype, y, N, K, M, prec, ws.ptr, need,
+                  as_stream(stream));
+    int st2 = ws.release();
+    return st != Q2_0_OK ? st : st2;
+}
+
+}  // namespace
+
+extern "C" {
+
+int q2_0_mul_mat_vec(const void *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
+                     void *stream) {
+    return mul_mat_vec_pool(w, x, kXF32, y, N, K, ncols, stream);
+}
+
+int q2_0_mul_mat_vec_f16(const void *w, const void *x, float *y, int64_t N, int64_t K, int ncols,
+                         void *stream) {
+    return mul_mat_vec_pool(w, x, kXF16, y, N, K, ncols, stream);
 }
 
 int q2_0_mv_plan_create(const q2_0_mv_desc *descs, int n_desc, int ncols, q2_0_mv_plan **plan) {
@@ -196,25 +237,12 @@ size_t q2_0_mul_mat_workspace_size(int64_t M, int64_t N, int64_t K, int prec) {
 
 int q2_0_mul_mat(const void *w, const float *x, float *y, int64_t N, int64_t K, int64_t M, int prec,
                  void *workspace, size_t workspace_bytes, void *stream) {
-    if (!w || !x || !y || N < 1 || M < 1 || N > (int64_t(1) << 31) - 1 ||
-        M > (int64_t(1) << 31) - 1 || !valid_k(K) ||
-        (prec != Q2_0_PREC_F16_SPLIT && prec != Q2_0_PREC_F16))
-        return Q2_0_EINVAL;
-    size_t need = gemm_workspace_bytes(M, N, K, prec);
-    if (workspace && (workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
-        return Q2_0_EINVAL;
-    int st = check_device(nullptr);
-    if (st != Q2_0_OK) return st;
-    if (workspace || need == 0)
-        return gemm_run(static_cast<const uint8_t *>(w), x, y, N, K, M, prec, workspace,
-                        workspace_bytes, as_stream(stream));
-    PoolScratch ws;
-    st = ws.alloc(need, as_stream(stream));
-    if (st != Q2_0_OK) return st;
-    st = gemm_run(static_cast<const uint8_t *>(w), x, y, N, K, M, prec, ws.ptr, need,
-                  as_stream(stream));
-    int st2 = ws.release();
-    return st != Q2_0_OK ? st : st2;
+    return mul_mat_impl(w, x, kXF32, y, N, K, M, prec, workspace, workspace_bytes, stream);
+}
+
+int q2_0_mul_mat_f16(const void *w, const void *x, float *y, int64_t N, int64_t K, int64_t M,
+                     void *workspace, size_t workspace_bytes, void *stream) {
+    return mul_mat_impl(w, x, kXF16, y, N, K, M, Q2_0_PREC_F16, workspace, workspace_bytes, stream);
 }
 
 int q2_0_get_rows(const void *table, int64_t n_rows, int64_t K, const int32_t *ids, int64_t n_ids,

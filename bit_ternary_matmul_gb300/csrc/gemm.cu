@@ -91,10 +91,38 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
 }
 
 // ---------------------------------------------------------------------------
-// Prepass: X f32 [M][K] -> fp16 hi (and lo) [M][K] in the permuted K order.
-// One thread per 16-element word group.
+// Prepass: X [M][K] (F32, or F16 whose values are already exact fp16) -> fp16
+// hi (and lo) [M][K] in the permuted K order. One thread per 16-element word
+// group; X 16-byte aligned.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) gemm_prep_kernel(const float *__restrict__ x,
+__device__ __forceinline__ void load16(const float *p, float (&v)[16]) {
+    const float4 *src = reinterpret_cast<const float4 *>(p);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 f = src[q];
+        v[4 * q] = f.x;
+        v[4 * q + 1] = f.y;
+        v[4 * q + 2] = f.z;
+        v[4 * q + 3] = f.w;
+    }
+}
+__device__ __forceinline__ void load16(const __half *p, float (&v)[16]) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(p);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const uint4 u = src[q];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+            v[8 * q + 2 * k] = f.x;
+            v[8 * q + 2 * k + 1] = f.y;
+        }
+    }
+}
+
+template <typename XT>
+__global__ void __launch_bounds__(256) gemm_prep_kernel(const XT *__restrict__ x,
                                                         __half *__restrict__ xh,
                                                         __half *__restrict__ xl, int64_t groups,
                                                         int split) {
@@ -103,16 +131,8 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const float *__restrict_
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int64_t gidx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; gidx < groups;
          gidx += int64_t(gridDim.x) * blockDim.x) {
-        const float4 *src = reinterpret_cast<const float4 *>(x + gidx * 16);
         float v[16];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 f = src[q];
-            v[4 * q] = f.x;
-            v[4 * q + 1] = f.y;
-            v[4 * q + 2] = f.z;
-            v[4 * q + 3] = f.w;
-        }
+        load16(x + gidx * 16, v);
         uint32_t hw[8], lw[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
@@ -533,8 +553,12 @@ __global__ void __launch_bounds__(kReduceThreads) gemm_reduce_kernel(
 // Generic GEMM (any K % 64 == 0, any alignment): CUDA cores, f32.
 // Block of 32 x 8 threads computes Y[m0..m0+8) x [n0..n0+32).
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ float ld_x(const float *p) { return *p; }
+__device__ __forceinline__ float ld_x(const __half *p) { return __half2float(*p); }
+
+template <typename XT>
 __global__ void __launch_bounds__(256) gemm_generic_kernel(const uint8_t *__restrict__ w,
-                                                           const float *__restrict__ x,
+                                                           const XT *__restrict__ x,
                                                            float *__restrict__ y, int M, int N,
                                                            int K) {
     const int n = blockIdx.x * 32 + threadIdx.x;
@@ -550,9 +574,10 @@ __global__ void __launch_bounds__(256) gemm_generic_kernel(const uint8_t *__rest
             const uint8_t *pw = blk + 2 + 4 * wi;
             const uint32_t word = uint32_t(pw[0]) | (uint32_t(pw[1]) << 8) |
                                   (uint32_t(pw[2]) << 16) | (uint32_t(pw[3]) << 24);
-            const float *xe = x + size_t(m) * K + b * 64 + wi * 16;
+            const XT *xe = x + size_t(m) * K + b * 64 + wi * 16;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) s = fmaf(float(int((word >> (2 * i)) & 3u) - 1), xe[i], s);
+            for (int i = 0; i < 16; ++i)
+                s = fmaf(float(int((word >> (2 * i)) & 3u) - 1), ld_x(xe + i), s);
         }
         acc = fmaf(d, s, acc);
     }
@@ -579,7 +604,7 @@ cudaError_t ensure_attr() {
     return e;
 }
 
-bool tc_path_ok(const void *w, const float *x, int64_t K) {
+bool tc_path_ok(const void *w, const void *x, int64_t K) {
     return K % 512 == 0 && (reinterpret_cast<uintptr_t>(w) & 15u) == 0 &&
            (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
 }
@@ -620,14 +645,20 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int prec) {
     return gemm_layout(M, N, K, prec, kMaxGrid).total;
 }
 
-int gemm_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, int64_t M, int prec,
-             void *ws, size_t ws_bytes, cudaStream_t s) {
+int gemm_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, int64_t K,
+             int64_t M, int prec, void *ws, size_t ws_bytes, cudaStream_t s) {
     if (!tc_path_ok(w, x, K)) {
         dim3 grid(unsigned((N + 31) / 32), unsigned((M + 7) / 8));
-        gemm_generic_kernel<<<grid, dim3(32, 8), 0, s>>>(w, x, y, int(M), int(N), int(K));
+        if (xtype == kXF16)
+            gemm_generic_kernel<__half><<<grid, dim3(32, 8), 0, s>>>(
+                w, static_cast<const __half *>(x), y, int(M), int(N), int(K));
+        else
+            gemm_generic_kernel<float><<<grid, dim3(32, 8), 0, s>>>(
+                w, static_cast<const float *>(x), y, int(M), int(N), int(K));
         return cuda_status(cudaGetLastError());
     }
-    const int split = prec == Q2_0_PREC_F16_SPLIT ? 1 : 0;
+    // F16 activations are exact fp16 operands: no lo part
+    const int split = (prec == Q2_0_PREC_F16_SPLIT && xtype == kXF32) ? 1 : 0;
     if (ws_bytes < gemm_workspace_bytes(M, N, K, prec) || !ws) return Q2_0_EINVAL;
     unsigned long long *err = error_word_ptr();
     if (!err) return Q2_0_ECUDA;
@@ -638,8 +669,13 @@ int gemm_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, i
     float *partials = reinterpret_cast<float *>(wsb + L.partials);
     const int64_t groups = M * K / 16;
     int64_t pgrid = std::min<int64_t>((groups + 255) / 256, int64_t(sm_count()) * 8);
-    gemm_prep_kernel<<<unsigned(std::max<int64_t>(pgrid, 1)), 256, 0, s>>>(x, xh, xl, groups,
-                                                                         split);
+    const unsigned pg = unsigned(std::max<int64_t>(pgrid, 1));
+    if (xtype == kXF16)
+        gemm_prep_kernel<__half><<<pg, 256, 0, s>>>(static_cast<const __half *>(x), xh, xl, groups,
+                                                    split);
+    else
+        gemm_prep_kernel<float><<<pg, 256, 0, s>>>(static_cast<const float *>(x), xh, xl, groups,
+                                                   split);
     if (cudaGetLastError() != cudaSuccess) return Q2_0_ECUDA;
 
     GemmArgs args;

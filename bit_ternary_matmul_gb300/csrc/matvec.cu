@@ -38,6 +38,8 @@
 //
 // Requirements of the TMA path: K % 512 == 0 (row stride a multiple of 16 B)
 // and W 16-byte aligned. Other shapes run mv_generic_kernel (CUDA cores, f32).
+// Activations are F32 or F16 (the prep kernels and the generic kernel read
+// either; F16 values are converted exactly).
 #include <cuda_fp8.h>
 
 #include <algorithm>
@@ -70,7 +72,7 @@ constexpr int kTagMvFull = 101;
 constexpr int kTagMvEmpty = 102;
 
 struct MvPrepJob {
-    const float *x;  // [ncols][K]
+    const void *x;   // [ncols][K], F32 or F16 (the prep kernel's template argument)
     uint8_t *prep;   // prepared fragments
     int K;
 };
@@ -130,6 +132,10 @@ __device__ __forceinline__ float mul_pow2(float v, int e) {
     return v * __int_as_float((127 + e1) << 23) * __int_as_float((127 + e2) << 23);
 }
 
+// Activation element load: F32 as is, F16 (IEEE binary16) converted exactly.
+__device__ __forceinline__ float ld_x(const float *p) { return *p; }
+__device__ __forceinline__ float ld_x(const __half *p) { return __half2float(*p); }
+
 // ---------------------------------------------------------------------------
 // Activation preparation: grid (ncols, n_jobs), kPrepThreads threads.
 // ---------------------------------------------------------------------------
@@ -137,7 +143,7 @@ __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
     return uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
 }
 
-template <int NT>
+template <int NT, typename XT>
 __global__ void __launch_bounds__(kPrepThreads) mv_prep_kernel(
     const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs, int ncols) {
     // The mat-vec kernel that follows may start its prologue (barrier set-up,
@@ -146,7 +152,7 @@ __global__ void __launch_bounds__(kPrepThreads) mv_prep_kernel(
     const MvPrepJob &J = jobs ? jobs[blockIdx.y] : single;
     const int K = J.K;
     const int j = blockIdx.x;  // activation column
-    const float *xj = J.x + size_t(j) * K;
+    const XT *xj = static_cast<const XT *>(J.x) + size_t(j) * K;
     const int tid = threadIdx.x;
     const int nb = K / 64;
 
@@ -155,7 +161,7 @@ __global__ void __launch_bounds__(kPrepThreads) mv_prep_kernel(
     float first[16];
     float m = 0.0f;
     if (tid < nb * 4) {
-        if ((reinterpret_cast<uintptr_t>(xj) & 15u) == 0) {
+        if (sizeof(XT) == 4 && (reinterpret_cast<uintptr_t>(xj) & 15u) == 0) {
             const float4 *src = reinterpret_cast<const float4 *>(xj + tid * 16);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
@@ -167,14 +173,14 @@ __global__ void __launch_bounds__(kPrepThreads) mv_prep_kernel(
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) first[i] = xj[tid * 16 + i];
+            for (int i = 0; i < 16; ++i) first[i] = ld_x(xj + tid * 16 + i);
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(first[i]));
     }
     for (int k = (kPrepThreads + tid) * 16; k < K; k += kPrepThreads * 16)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(xj[k + i]));
+        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(ld_x(xj + k + i)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     __shared__ float red[kPrepThreads / 32];
@@ -201,12 +207,12 @@ __global__ void __launch_bounds__(kPrepThreads) mv_prep_kernel(
     const int t = j >> 2, jc = j & 3;  // n-tile and column within it
     for (int idx = tid; idx < nb * 4; idx += kPrepThreads) {
         const int b = idx >> 2, c = idx & 3;
-        const float *xe = xj + b * 64 + c * 16;
+        const XT *xe = xj + b * 64 + c * 16;
         __half hi[16], lo[16];
         float base_hi = 0.0f, base_lo = 0.0f;  // sum over the block of part * 4^m * 2^-24
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const float xv = idx == tid ? first[i] : xe[i];
+            const float xv = idx == tid ? first[i] : ld_x(xe + i);
             const float v = xv * fscale[i & 3];
             hi[i] = __float2half_rn(v);
             lo[i] = __float2half_rn(v - __half2float(hi[i]));
@@ -667,13 +673,14 @@ __host__ __device__ constexpr int t5_img_offset(int n, int kc) {
 // 2^-9, divided by 2^9 or 2^7; |sum| < 64 * 448 * 2^-7), rounded once to f32.
 constexpr int kT5PrepThreads = 256;
 
+template <typename XT>
 __global__ void __launch_bounds__(kT5PrepThreads) t5_prep_kernel(
     const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs, int ncols) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const MvPrepJob &J = jobs ? jobs[blockIdx.y] : single;
     const int K = J.K;
     const int j = blockIdx.x;
-    const float *xj = J.x + size_t(j) * K;
+    const XT *xj = static_cast<const XT *>(J.x) + size_t(j) * K;
     const int tid = threadIdx.x;
     const int nb = K / 64;
     const int n_chunks = K / 512;
@@ -684,14 +691,14 @@ __global__ void __launch_bounds__(kT5PrepThreads) t5_prep_kernel(
     // 1) column scale 2^s with max|x * 2^s| in [2^-2, 2^-1) (each CTA of the
     //    column reads the whole column)
     float m = 0.0f;
-    if ((reinterpret_cast<uintptr_t>(xj) & 15u) == 0) {
+    if (sizeof(XT) == 4 && (reinterpret_cast<uintptr_t>(xj) & 15u) == 0) {
         const float4 *x4 = reinterpret_cast<const float4 *>(xj);
         for (int k = tid; k < K / 4; k += kT5PrepThreads) {
             const float4 f = x4[k];
             m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
         }
     } else {
-        for (int k = tid; k < K; k += kT5PrepThreads) m = fmaxf(m, fabsf(xj[k]));
+        for (int k = tid; k < K; k += kT5PrepThreads) m = fmaxf(m, fabsf(ld_x(xj + k)));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -718,12 +725,12 @@ __global__ void __launch_bounds__(kT5PrepThreads) t5_prep_kernel(
     for (int idx = int(blockIdx.z) * kT5PrepThreads + tid; idx < nb * 16;
          idx += int(gridDim.z) * kT5PrepThreads) {
         const int b = idx >> 4, c = (idx >> 2) & 3, r = idx & 3;
-        const float *xe = xj + b * 64 + c * 16 + r;
+        const XT *xe = xj + b * 64 + c * 16 + r;
         const int e_in = s + ((r & 1) ? 7 : 9);    // v = x * 2^e_in
         const float to_int = (r & 1) ? 2048.0f : 512.0f;  // piece / (2^7 or 2^9) in 2^-18 units
         float v[4];
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) v[jj] = mul_pow2(xe[4 * jj], e_in);
+        for (int jj = 0; jj < 4; ++jj) v[jj] = mul_pow2(ld_x(xe + 4 * jj), e_in);
         uint8_t *bimg = img + size_t(b >> 3) * kT5ImgBytes;
         const int kc = 64 * (b & 7) + 16 * c;
         int isum[kT5Pieces];
@@ -1115,8 +1122,9 @@ __global__ void __launch_bounds__(kT5Threads, 1)
 // Generic mat-vec (any K % 64 == 0, any alignment): one warp per row, f32 on
 // CUDA cores, block-wise: s = sum (q - 1) * x over the block, then acc += d*s.
 // ---------------------------------------------------------------------------
+template <typename XT>
 __global__ void __launch_bounds__(256) mv_generic_kernel(const uint8_t *__restrict__ w,
-                                                         const float *__restrict__ x,
+                                                         const XT *__restrict__ x,
                                                          float *__restrict__ y, int N, int K,
                                                          int ncols) {
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -1142,7 +1150,7 @@ __global__ void __launch_bounds__(256) mv_generic_kernel(const uint8_t *__restri
                 const int k = b * 64 + wi * 16 + i;
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc)
-                    if (cc < ncols) s[cc] = fmaf(q1, x[size_t(cc) * K + k], s[cc]);
+                    if (cc < ncols) s[cc] = fmaf(q1, ld_x(x + size_t(cc) * K + k), s[cc]);
             }
         }
 #pragma unroll
@@ -1216,18 +1224,25 @@ bool make_job(MvJob &J, const uint8_t *w, const uint8_t *prep, float *y, int64_t
 }
 
 // max_k: the largest K among the jobs (sets the t5 prep's grid z).
-cudaError_t launch_prep(const MvPrepJob &single, const MvPrepJob *jobs, int n_jobs, int ncols,
-                        int64_t max_k, cudaStream_t s) {
+template <typename XT>
+cudaError_t launch_prep_t(const MvPrepJob &single, const MvPrepJob *jobs, int n_jobs, int ncols,
+                          int64_t max_k, cudaStream_t s) {
     dim3 grid(ncols, n_jobs);
     if (use_t5(ncols)) {
         const int64_t items = max_k / 64 * 16;
         grid.z = unsigned(std::min<int64_t>((items + kT5PrepThreads - 1) / kT5PrepThreads, 65535));
-        t5_prep_kernel<<<grid, kT5PrepThreads, 0, s>>>(single, jobs, ncols);
+        t5_prep_kernel<XT><<<grid, kT5PrepThreads, 0, s>>>(single, jobs, ncols);
     } else if (n_tiles_for(ncols) == 1)
-        mv_prep_kernel<1><<<grid, kPrepThreads, 0, s>>>(single, jobs, ncols);
+        mv_prep_kernel<1, XT><<<grid, kPrepThreads, 0, s>>>(single, jobs, ncols);
     else
-        mv_prep_kernel<2><<<grid, kPrepThreads, 0, s>>>(single, jobs, ncols);
+        mv_prep_kernel<2, XT><<<grid, kPrepThreads, 0, s>>>(single, jobs, ncols);
     return cudaGetLastError();
+}
+
+cudaError_t launch_prep(const MvPrepJob &single, const MvPrepJob *jobs, int n_jobs, int ncols,
+                        int64_t max_k, int xtype, cudaStream_t s) {
+    return xtype == kXF16 ? launch_prep_t<__half>(single, jobs, n_jobs, ncols, max_k, s)
+                          : launch_prep_t<float>(single, jobs, n_jobs, ncols, max_k, s);
 }
 
 // The tensor-core kernel is launched as a programmatic dependent of the prep
@@ -1267,9 +1282,15 @@ cudaError_t launch_tc(const MvJob &single, const MvParams &prm, int grid, cudaSt
     return cudaGetLastError();
 }
 
-cudaError_t launch_generic(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K,
-                           int ncols, cudaStream_t s) {
-    mv_generic_kernel<<<unsigned((N + 7) / 8), 256, 0, s>>>(w, x, y, int(N), int(K), ncols);
+cudaError_t launch_generic(const uint8_t *w, const void *x, int xtype, float *y, int64_t N,
+                           int64_t K, int ncols, cudaStream_t s) {
+    const unsigned grid = unsigned((N + 7) / 8);
+    if (xtype == kXF16)
+        mv_generic_kernel<__half><<<grid, 256, 0, s>>>(w, static_cast<const __half *>(x), y,
+                                                       int(N), int(K), ncols);
+    else
+        mv_generic_kernel<float><<<grid, 256, 0, s>>>(w, static_cast<const float *>(x), y,
+                                                      int(N), int(K), ncols);
     return cudaGetLastError();
 }
 
@@ -1283,15 +1304,16 @@ bool matvec_fast_path_ok(const void *w, int64_t K) {
     return K % 512 == 0 && (reinterpret_cast<uintptr_t>(w) & 15u) == 0;
 }
 
-int matvec_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
-               void *ws, size_t ws_bytes, cudaStream_t s) {
-    if (!matvec_fast_path_ok(w, K)) return cuda_status(launch_generic(w, x, y, N, K, ncols, s));
+int matvec_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, int64_t K,
+               int ncols, void *ws, size_t ws_bytes, cudaStream_t s) {
+    if (!matvec_fast_path_ok(w, K))
+        return cuda_status(launch_generic(w, x, xtype, y, N, K, ncols, s));
     if (ws_bytes < matvec_workspace_bytes(K, ncols)) return Q2_0_EINVAL;
     unsigned long long *err = error_word_ptr();
     if (!err) return Q2_0_ECUDA;
     uint8_t *prep = static_cast<uint8_t *>(ws);
     MvPrepJob pj{x, prep, int(K)};
-    cudaError_t e = launch_prep(pj, nullptr, 1, ncols, K, s);
+    cudaError_t e = launch_prep(pj, nullptr, 1, ncols, K, xtype, s);
     if (e != cudaSuccess) return Q2_0_ECUDA;
     MvJob J;
     if (!make_job(J, w, prep, y, N, K, tile_rows_for(ncols))) return Q2_0_ECUDA;
@@ -1441,7 +1463,8 @@ int mv_plan_execute(const q2_0_mv_plan *P, cudaStream_t s) {
     if (cudaGetDevice(&cur) != cudaSuccess || cur != P->device) return Q2_0_EINVAL;
     if (P->n_fast > 0) {
         MvPrepJob none{nullptr, nullptr, 0};
-        if (launch_prep(none, P->d_prep_jobs, P->n_fast, P->ncols, P->max_k, s) != cudaSuccess)
+        if (launch_prep(none, P->d_prep_jobs, P->n_fast, P->ncols, P->max_k, kXF32, s) !=
+            cudaSuccess)
             return Q2_0_ECUDA;
         MvJob dummy;
         std::memset(&dummy, 0, sizeof(dummy));
@@ -1450,7 +1473,8 @@ int mv_plan_execute(const q2_0_mv_plan *P, cudaStream_t s) {
         if (launch_tc(dummy, prm, P->grid, s) != cudaSuccess) return Q2_0_ECUDA;
     }
     for (const q2_0_mv_desc &d : P->generic)
-        if (launch_generic(static_cast<const uint8_t *>(d.w), d.x, d.y, d.N, d.K, P->ncols, s) !=
+        if (launch_generic(static_cast<const uint8_t *>(d.w), d.x, kXF32, d.y, d.N, d.K, P->ncols,
+                           s) !=
             cudaSuccess)
             return Q2_0_ECUDA;
     return Q2_0_OK;

@@ -60,6 +60,6 @@ extern "C" int q2_0_mul_mat_vec_noalloc(const void *w, const float *x, float *y,
     void *scratch = nullptr;
     st = q2::scratch_for_current_device(&scratch);
     if (st != Q2_0_OK) return st;
-    return q2::matvec_run(static_cast<const uint8_t *>(w), x, y, N, K, ncols, scratch,
+    return q2::matvec_run(static_cast<const uint8_t *>(w), x, q2::kXF32, y, N, K, ncols, scratch,
                           q2::kNoAllocScratchBytes, reinterpret_cast<cudaStream_t>(stream));
 }

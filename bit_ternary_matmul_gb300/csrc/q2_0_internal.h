@@ -38,11 +38,15 @@ cudaError_t launch_get_rows(const uint8_t *table, int64_t n_rows, int64_t K, con
 cudaError_t launch_quantize(const float *src, uint8_t *dst, int64_t nrows, int64_t K,
                             cudaStream_t s);
 
-// mat-vec
+// activation element types
+constexpr int kXF32 = 0;
+constexpr int kXF16 = 1;
+
+// mat-vec (x is F32 or F16 by xtype)
 size_t matvec_workspace_bytes(int64_t K, int ncols);
 bool matvec_fast_path_ok(const void *w, int64_t K);
-int matvec_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
-               void *ws, size_t ws_bytes, cudaStream_t s);
+int matvec_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, int64_t K,
+               int ncols, void *ws, size_t ws_bytes, cudaStream_t s);
 
 // batched mat-vec plans (opaque to the C ABI)
 int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **plan);
@@ -50,9 +54,9 @@ int mv_plan_execute(const q2_0_mv_plan *plan, cudaStream_t s);
 int mv_plan_launches(const q2_0_mv_plan *plan);
 void mv_plan_destroy(q2_0_mv_plan *plan);
 
-// GEMM
+// GEMM (x is F32 or F16 by xtype; F16 runs the single-operand precision)
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int prec);
-int gemm_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, int64_t M, int prec,
-             void *ws, size_t ws_bytes, cudaStream_t s);
+int gemm_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, int64_t K,
+             int64_t M, int prec, void *ws, size_t ws_bytes, cudaStream_t s);
 
 }  // namespace q2

@@ -91,6 +91,17 @@ int q2_0_device_check(void);
 int q2_0_mul_mat_vec(const void *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
                      void *stream);
 
+/*
+ * q2_0_mul_mat_vec_f16 — q2_0_mul_mat_vec with F16 (IEEE binary16)
+ * activations x [ncols][K], any alignment; y F32. The pages' WebGPU port
+ * supports F32 activations only and lists F16 ones as missing ("WebGPU: add
+ * Q2_0 support", limitations paragraph); this is that variant. Each fp16
+ * value is used exactly, so the F32 error bound applies with x read as the
+ * exact fp16 values. Scratch as q2_0_mul_mat_vec (default memory pool).
+ */
+int q2_0_mul_mat_vec_f16(const void *w, const void *x, float *y, int64_t N, int64_t K, int ncols,
+                         void *stream);
+
 /* Scratch bytes q2_0_mul_mat_vec_ws needs for (K, ncols); 0 on bad arguments. */
 size_t q2_0_mul_mat_vec_workspace_size(int64_t K, int ncols);
 
@@ -166,6 +177,18 @@ void q2_0_mv_plan_destroy(q2_0_mv_plan *plan);
 size_t q2_0_mul_mat_workspace_size(int64_t M, int64_t N, int64_t K, int prec);
 int q2_0_mul_mat(const void *w, const float *x, float *y, int64_t N, int64_t K, int64_t M, int prec,
                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * q2_0_mul_mat_f16 — q2_0_mul_mat with F16 activations x [M][K] (the missing
+ * F16 path of the same limitations paragraph). fp16 x is already an exact fp16
+ * tensor-core operand, so one product per weight suffices and the bound is
+ * |y - exact| <= 1e-5 * sum_k |W[n][k] X[m][k]| + 1e-7 with X the fp16 values.
+ * workspace: at least q2_0_mul_mat_workspace_size(M, N, K, Q2_0_PREC_F16)
+ * bytes, 256-byte aligned, or NULL for the default memory pool. Fast path:
+ * K % 512 == 0, w and x 16-byte aligned; otherwise a CUDA-core kernel.
+ */
+int q2_0_mul_mat_f16(const void *w, const void *x, float *y, int64_t N, int64_t K, int64_t M,
+                     void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * q2_0_get_rows — gather rows of a Q2_0 table into F32, bit-exact.

@@ -50,6 +50,11 @@ def test_argument_validation_without_gpu(L):
     assert L.q2_0_mul_mat_vec(p, p, p, 4, 64, 0, null) == EINVAL
     assert L.q2_0_mul_mat_vec(p, p, p, 4, 64, 9, null) == EINVAL
     assert L.q2_0_mul_mat_vec(p, p, p, 0, 64, 1, null) == EINVAL
+    assert L.q2_0_mul_mat_vec_f16(null, p, p, 4, 64, 1, null) == EINVAL
+    assert L.q2_0_mul_mat_vec_f16(p, p, p, 4, 100, 1, null) == EINVAL
+    assert L.q2_0_mul_mat_vec_f16(p, p, p, 4, 64, 9, null) == EINVAL
+    assert L.q2_0_mul_mat_f16(p, p, p, 4, 65, 4, null, 0, null) == EINVAL
+    assert L.q2_0_mul_mat_f16(p, null, p, 4, 64, 4, null, 0, null) == EINVAL
     # mat-vec with workspace: too small, misaligned
     need = L.q2_0_mul_mat_vec_workspace_size(512, 1)
     assert need > 0 and need % 256 == 0

@@ -362,3 +362,51 @@ def test_gemm_prefill_shapes_sampled(dev, N, K, M, prec):
     tol = TOL_SPLIT if prec == q.Q2_0_PREC_F16_SPLIT else TOL_F16
     _assert_close(got, yo, acc, tol, f"GEMM {N}x{K} M={M} prec={prec}")
     _no_device_error()
+
+
+# ---------------------------------------------------------------------------
+# F16 activations (the missing path of the WebGPU port's limitations paragraph)
+# ---------------------------------------------------------------------------
+F16_MV_CASES = [(2048, 2048, 1), (300, 2048, 2), (257, 1536, 3), (1000, 6144, 4),
+                (513, 4096, 8), (33, 576, 1), (130, 1088, 8)]
+
+
+@pytest.mark.parametrize("N,K,ncols", F16_MV_CASES)
+def test_matvec_f16_parity(dev, N, K, ncols):
+    g = synth.rng(2101, N, K, ncols)
+    w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    x16 = synth.activations(g, ncols, K, 0.001, 30.0).astype(np.float16)
+    y = q.q2_0_mul_mat_vec_f16(_to(dev, w), _to(dev, x16), N, K, ncols).cpu().numpy()
+    # the oracle gets the exact values of the fp16 activations
+    yo, acc = oracle.matmul(w, N, K, x16.astype(np.float32))
+    _assert_close(y, yo, acc, TOL_SPLIT, f"mat-vec f16 {N}x{K} ncols={ncols}")
+    _no_device_error()
+
+
+@pytest.mark.parametrize("N,K,M", [(128, 512, 128), (300, 1024, 70), (17, 64, 5),
+                                   (130, 2048, 257), (40, 576, 9)])
+def test_gemm_f16_parity_small(dev, N, K, M):
+    g = synth.rng(3101, N, K, M)
+    w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    x16 = synth.activations(g, M, K, synth.PREFILL_OUTLIER_FRAC,
+                            synth.PREFILL_OUTLIER).astype(np.float16)
+    y = q.q2_0_mul_mat_f16(_to(dev, w), _to(dev, x16), N, K, M).cpu().numpy()
+    yo, acc = oracle.matmul(w, N, K, x16.astype(np.float32))
+    _assert_close(y, yo, acc, TOL_SPLIT, f"GEMM f16 {N}x{K} M={M}")
+    _no_device_error()
+
+
+@pytest.mark.parametrize("N,K,M", [(6144, 2048, 512), (2048, 6144, 512)])
+def test_gemm_f16_prefill_sampled(dev, N, K, M):
+    g = synth.rng(3103, N, K, M)
+    w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    x16 = synth.activations(g, M, K, synth.PREFILL_OUTLIER_FRAC,
+                            synth.PREFILL_OUTLIER).astype(np.float16)
+    ws = torch.empty(q.q2_0_mul_mat_workspace_size(M, N, K, q.Q2_0_PREC_F16), dtype=torch.uint8,
+                     device=dev)
+    y = q.q2_0_mul_mat_f16(_to(dev, w), _to(dev, x16), N, K, M, workspace=ws)
+    rows = np.unique(np.concatenate([[0, 127, 128, N - 1], g.integers(0, N, 60)]))
+    yo, acc = oracle.matmul(w, N, K, x16.astype(np.float32), rows=rows)
+    got = y[:, torch.from_numpy(rows).to(dev)].cpu().numpy()
+    _assert_close(got, yo, acc, TOL_SPLIT, f"GEMM f16 {N}x{K} M={M}")
+    _no_device_error()
