@@ -380,6 +380,10 @@ def run_ours(args):
     e2e_val = reduce_sum(dist, e2e["value"], dev) if dist else e2e["value"]
     e2e["value"] = e2e_val
 
+    extras = None
+    if args.only == "all" and not args.no_extras:
+        extras = measure_extras(torch, q, stream, dev)
+
     code, info = q.q2_0_get_error(stream)
     if code != 0:
         raise SystemExit(f"device error word {code} (info {info}) after timing")
@@ -429,12 +433,77 @@ def run_ours(args):
             "roofline": dominant, "roofline_other": other,
             "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "clocks": clk, "cpu_baseline": cpu, "impl": "ours",
+            "extras": extras,
         }
         print(json.dumps(line), flush=True)
     if plan is not None:
         plan.close()
     if dist is not None:
         dist.destroy_process_group()
+
+
+def measure_extras(torch, q, stream, dev, reps: int = 20):
+    """Side measurements outside the step, each a CUDA-graph replay timed with
+    events on the launching stream:
+      - the 151936 x 4096 output-head mat-vec (ncols 1), with F32 and with F16
+        activations (175 MB of packed weights, above L2);
+      - the M = 512 prefill GEMMs with F16 activations (q2_0_mul_mat_f16).
+    Returns the GB/s and TFLOP/s figures."""
+    g = synth.rng(SEED + 7)
+    N, K = VOCAB, 4096
+    w = torch.from_numpy(synth.packed_matrix(g, N, K, *synth.DECODE_SCALE,
+                                             synth.DECODE_FRAC_CODE3)).to(dev)
+    x = torch.from_numpy(synth.activations(g, 1, K)).to(dev)
+    x16 = x.half()
+    y = torch.empty((1, N), dtype=torch.float32, device=dev)
+    head_bytes = w.numel()
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(gr, stream=stream):
+                fn()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            gr.replay()
+            a.record(stream)
+            for _ in range(reps):
+                gr.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps  # ms
+
+    ms32 = timed(lambda: q.q2_0_mul_mat_vec(w, x, N, K, 1, y=y, stream=stream))
+    ms16 = timed(lambda: q.q2_0_mul_mat_vec_f16(w, x16, N, K, 1, y=y, stream=stream))
+    del w
+    gm = []
+    for name, Ng, Kg, wg, xg in gemm_inputs():
+        ws = torch.empty(q.q2_0_mul_mat_workspace_size(PREFILL_M, Ng, Kg, q.Q2_0_PREC_F16),
+                         dtype=torch.uint8, device=dev)
+        gm.append((torch.from_numpy(wg).to(dev), torch.from_numpy(xg).to(dev).half(),
+                   torch.empty((PREFILL_M, Ng), dtype=torch.float32, device=dev), Ng, Kg, ws))
+    flops = sum(2.0 * PREFILL_M * Ng * Kg for _, _, _, Ng, Kg, _ in gm)
+
+    def gemms():
+        for wg, xg, yg, Ng, Kg, ws in gm:
+            q.q2_0_mul_mat_f16(wg, xg, Ng, Kg, PREFILL_M, y=yg, workspace=ws, stream=stream)
+
+    msg = timed(gemms)
+    return {
+        "head_matvec_151936x4096": {"bytes": head_bytes,
+                                    "f32_gbs": round(head_bytes / (ms32 * 1e-3) / 1e9, 1),
+                                    "f16_gbs": round(head_bytes / (ms16 * 1e-3) / 1e9, 1),
+                                    "f32_us": round(ms32 * 1e3, 2), "f16_us": round(ms16 * 1e3, 2)},
+        "gemm_f16_m512": {"tflops": round(flops / (msg * 1e-3) / 1e12, 2),
+                          "us": round(msg * 1e3, 2),
+                          "shapes": [[PREFILL_M, Ng, Kg] for _, _, _, Ng, Kg, _ in gm]},
+        "timing": "CUDA-graph replay, CUDA events on the launching stream, outside the step",
+    }
 
 
 def measure_e2e(args, torch, stream, plan, h_xall, d_xall, d_yall, dec_bytes):
@@ -549,6 +618,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the side measurements (head mat-vec F32/F16, F16 GEMM)")
     ap.add_argument("--only", choices=["all", "decode", "gemm", "get_rows"], default="all",
                     help="run one part of the step (for profiling); the JSON line is the "
                          "benchmark only with the default 'all'")

@@ -79,6 +79,10 @@ def lib():
             L.qo_float_to_half_rn_array.argtypes = [f32p, ctypes.POINTER(ctypes.c_uint16), i64]
             L.qo_num_threads.restype = ctypes.c_int
             L.qo_set_num_threads.argtypes = [ctypes.c_int]
+            L.qo_decode_block_g128.argtypes = [u8p, f64p]
+            L.qo_matmul_rows_g128.argtypes = [u8p, i64, i64, f32p, i64, i64p, i64, f64p, f64p]
+            L.qo_get_rows_g128.argtypes = [u8p, i64, i64, i32p, i64, f32p]
+            L.qo_get_rows_g128.restype = i64
             L.qo_weights_per_block.restype = ctypes.c_int
             L.qo_bytes_per_block.restype = ctypes.c_int
             _lib = L
@@ -188,6 +192,47 @@ def get_rows(table, n_rows: int, K: int, ids):
     out = np.zeros((ii.size, K), dtype=np.float32)
     bad = lib().qo_get_rows(_p(tb, ctypes.c_uint8), n_rows, K, _p(ii, ctypes.c_int32),
                             ii.size, _p(out, ctypes.c_float))
+    return out, int(bad)
+
+
+# ---- group-128 blocks (34 bytes per 128 weights) ------------------------------
+def decode_block_g128(block) -> np.ndarray:
+    b = _u8(block)
+    assert b.size == 34
+    out = np.empty(128, dtype=np.float64)
+    lib().qo_decode_block_g128(_p(b, ctypes.c_uint8), _p(out, ctypes.c_double))
+    return out
+
+
+def matmul_g128(w, N: int, K: int, x, rows=None):
+    """As matmul for an N x K group-128 matrix (K % 128 == 0)."""
+    wb = _u8(w)
+    xx = np.ascontiguousarray(x, dtype=np.float32)
+    if xx.ndim == 1:
+        xx = xx[None, :]
+    assert xx.shape[1] == K and K % 128 == 0
+    assert wb.size >= N * (K // 128) * 34
+    ncols = xx.shape[0]
+    if rows is None:
+        nr, rp = N, None
+    else:
+        rr = np.ascontiguousarray(rows, dtype=np.int64)
+        assert rr.size == 0 or (rr.min() >= 0 and rr.max() < N)
+        nr, rp = rr.size, _p(rr, ctypes.c_int64)
+    y = np.empty((ncols, nr), dtype=np.float64)
+    acc = np.empty((ncols, nr), dtype=np.float64)
+    lib().qo_matmul_rows_g128(_p(wb, ctypes.c_uint8), N, K, _p(xx, ctypes.c_float), ncols, rp,
+                              nr, _p(y, ctypes.c_double), _p(acc, ctypes.c_double))
+    return y, acc
+
+
+def get_rows_g128(table, n_rows: int, K: int, ids):
+    """As get_rows for a group-128 table."""
+    tb = _u8(table)
+    ii = np.ascontiguousarray(ids, dtype=np.int32)
+    out = np.zeros((ii.size, K), dtype=np.float32)
+    bad = lib().qo_get_rows_g128(_p(tb, ctypes.c_uint8), n_rows, K, _p(ii, ctypes.c_int32),
+                                 ii.size, _p(out, ctypes.c_float))
     return out, int(bad)
 
 

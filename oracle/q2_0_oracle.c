@@ -260,6 +260,74 @@ void qo_quantize_rows(const float *src, int64_t nrows, int64_t K, uint8_t *dst) 
                               dst + (r * nb + b) * QO_BYTES_PER_BLOCK);
 }
 
+/* ---------------------------------------------------------------------------
+ * Group-128 blocks. [AISV] "Šest procent, o která se vedl spor": the packing the
+ * format's authors use for their own models has 128 weights per block, 34 bytes
+ * (2.125 bits per weight); its closing section: files named Q2_0.gguf without
+ * the _g64 suffix are that older packing. The pages give only the size. Reading
+ * (parity unpinned by the pages beyond the size): the group-64 layout extended
+ * to 128 weights — fp16 scale at +0, then eight little-endian 32-bit words;
+ * element 16w+i is bits 2i..2i+1 of word w; code q decodes to (q - 1) * d.
+ * ------------------------------------------------------------------------- */
+#define QO_G128_WEIGHTS 128
+#define QO_G128_BYTES 34
+
+void qo_decode_block_g128(const uint8_t *blk, double *out) {
+    double d = qo_half_to_double(qo_block_scale_bits(blk));
+    for (int e = 0; e < QO_G128_WEIGHTS; ++e) {
+        int w = e / 16, i = e % 16;
+        uint32_t word = qo_word_le(blk + 2 + 4 * w);
+        out[e] = (double)((int)((word >> (2 * i)) & 3u) - 1) * d;
+    }
+}
+
+/* As qo_matmul_rows for an N x K group-128 matrix (K % 128 == 0). */
+void qo_matmul_rows_g128(const uint8_t *w, int64_t N, int64_t K, const float *x, int64_t ncols,
+                         const int64_t *rows, int64_t n_rows, double *y, double *acc) {
+    int64_t nr = rows ? n_rows : N;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t j = 0; j < nr; ++j) {
+        int64_t n = rows ? rows[j] : j;
+        double wrow[QO_G128_WEIGHTS];
+        int64_t nb = K / QO_G128_WEIGHTS;
+        for (int64_t c = 0; c < ncols; ++c) {
+            double s = 0.0, a = 0.0;
+            const float *xc = x + c * K;
+            for (int64_t b = 0; b < nb; ++b) {
+                qo_decode_block_g128(w + (n * nb + b) * QO_G128_BYTES, wrow);
+                for (int e = 0; e < QO_G128_WEIGHTS; ++e) {
+                    double t = wrow[e] * (double)xc[b * QO_G128_WEIGHTS + e];
+                    s += t;
+                    a += fabs(t);
+                }
+            }
+            y[c * nr + j] = s;
+            if (acc) acc[c * nr + j] = a;
+        }
+    }
+}
+
+/* As qo_get_rows for a group-128 table. */
+int64_t qo_get_rows_g128(const uint8_t *table, int64_t n_rows, int64_t K, const int32_t *ids,
+                         int64_t n_ids, float *out) {
+    int64_t bad = 0;
+    int64_t nb = K / QO_G128_WEIGHTS;
+    for (int64_t r = 0; r < n_ids; ++r) {
+        int64_t id = ids[r];
+        if (id < 0 || id >= n_rows) {
+            ++bad;
+            continue;
+        }
+        double blk[QO_G128_WEIGHTS];
+        for (int64_t b = 0; b < nb; ++b) {
+            qo_decode_block_g128(table + (id * nb + b) * QO_G128_BYTES, blk);
+            for (int e = 0; e < QO_G128_WEIGHTS; ++e)
+                out[r * K + b * QO_G128_WEIGHTS + e] = (float)blk[e];
+        }
+    }
+    return bad;
+}
+
 /* Packed size of an N x K matrix at a given group size, from the layout: one
  * fp16 scale (2 bytes) plus group/4 bytes of 2-bit codes per group. [AISV]
  * "Šest procent…": 34 bytes per 128 weights vs 18 per 64. */

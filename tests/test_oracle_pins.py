@@ -340,3 +340,100 @@ def test_quantizer_idempotent_and_edges(oracle_mod):
     blk = np.zeros(64, np.float32)
     blk[7] = np.float32(1 + 2.0 ** -11)
     assert oracle_mod.block_scale_bits(oracle_mod.quantize(blk, 1, 64)) == 0x3C00
+
+
+# ---------------------------------------------------------------------------
+# Group-128 blocks (34 bytes per 128 weights)
+# ---------------------------------------------------------------------------
+def _golden_blocks_g128():
+    out = []
+    with open(os.path.join(GOLDEN, "decode_blocks_g128.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            dhex, qhex, exp = [t.strip() for t in line.split("|")]
+            d = int(dhex, 16)
+            blk = bytes([d & 0xFF, d >> 8]) + bytes.fromhex(qhex)
+            assert len(blk) == 34
+            toks = exp.split()
+            if toks[0] == "fill":
+                vals = [float(toks[1])] * 128
+                for t in toks[2:]:
+                    e, v = t.split(":")
+                    vals[int(e)] = float(v)
+            elif toks[0] == "cycle":
+                cyc = [float(t) for t in toks[1:5]]
+                vals = [cyc[e % 4] for e in range(128)]
+            else:
+                raise ValueError(line)
+            out.append((blk, np.array(vals, dtype=np.float64)))
+    return out
+
+
+def test_decode_golden_blocks_g128(oracle_mod):
+    cases = _golden_blocks_g128()
+    assert len(cases) >= 8
+    for blk, exp in cases:
+        got = oracle_mod.decode_block_g128(np.frombuffer(blk, dtype=np.uint8))
+        assert np.array_equal(got, exp), (blk.hex(), got, exp)
+        assert np.array_equal(np.signbit(got), np.signbit(exp)), blk.hex()
+
+
+def _g128_matrix(g, N, K):
+    """Random group-128 matrix bytes: fp16 scales in [0.01, 3), codes 0..3."""
+    nb = K // 128
+    d = g.uniform(0.01, 3.0, size=(N, nb)).astype(np.float16).view(np.uint16)
+    blk = np.zeros((N, nb, 34), dtype=np.uint8)
+    blk[:, :, 0] = d & 0xFF
+    blk[:, :, 1] = d >> 8
+    blk[:, :, 2:] = g.integers(0, 256, size=(N, nb, 32), dtype=np.uint8)
+    return blk.reshape(-1)
+
+
+def test_g128_halves_decode_as_group64_blocks(oracle_mod):
+    """Each half of a group-128 block reads like a group-64 block with the same scale
+    (the word rule runs over words 0-3 and 4-7): decode both ways."""
+    g = np.random.default_rng(128)
+    for _ in range(200):
+        b = _g128_matrix(g, 1, 128)
+        got = oracle_mod.decode_block_g128(b)
+        lo = np.concatenate([b[:2], b[2:18]])
+        hi = np.concatenate([b[:2], b[18:34]])
+        ref = np.concatenate([oracle_mod.decode_block(lo), oracle_mod.decode_block(hi)])
+        assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("N,K,ncols", [(1, 128, 1), (3, 256, 2), (2, 384, 3)])
+def test_matmul_g128_exact_rational(oracle_mod, N, K, ncols):
+    g = np.random.default_rng(N * 1000 + K + ncols)
+    w = _g128_matrix(g, N, K)
+    x = synth.activations(g, ncols, K, 0.05, 30.0)
+    y, acc = oracle_mod.matmul_g128(w, N, K, x)
+    for c in range(ncols):
+        for n in range(N):
+            row = np.concatenate([oracle_mod.decode_block_g128(w[(n * (K // 128) + b) * 34:
+                                                                 (n * (K // 128) + b + 1) * 34])
+                                  for b in range(K // 128)])
+            ex = _exact_dot(row, x[c])
+            exa = sum((abs(Fraction(float(a)) * Fraction(float(v))) for a, v in zip(row, x[c])),
+                      Fraction(0))
+            bound = K * 2.0 ** -52 * float(exa)
+            assert abs(Fraction(y[c, n]) - ex) <= Fraction(bound)
+            assert abs(Fraction(acc[c, n]) - exa) <= Fraction(bound)
+
+
+def test_g128_closed_forms_and_get_rows(oracle_mod):
+    N, K = 3, 256
+    d = np.float16(0.75).view(np.uint16)
+    for q, level in [(0, -0.75), (1, 0.0), (2, 0.75), (3, 1.5)]:
+        byte = q | (q << 2) | (q << 4) | (q << 6)
+        blk = np.array([d & 0xFF, d >> 8] + [byte] * 32, dtype=np.uint8)
+        w = np.tile(blk, N * (K // 128))
+        x = np.random.default_rng(q).standard_normal((2, K)).astype(np.float32)
+        y, _ = oracle_mod.matmul_g128(w, N, K, x)
+        ref = level * x.astype(np.float64).sum(axis=1)
+        assert np.allclose(y, ref[:, None], rtol=1e-14, atol=1e-14)
+        out, bad = oracle_mod.get_rows_g128(w, N, K, np.array([2, 0, 5], dtype=np.int32))
+        assert bad == 1
+        assert np.all(out[:2] == np.float32(level)) and np.all(out[2] == 0)
