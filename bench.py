@@ -447,7 +447,9 @@ def measure_extras(torch, q, stream, dev, reps: int = 20):
     events on the launching stream:
       - the 151936 x 4096 output-head mat-vec (ncols 1), with F32 and with F16
         activations (175 MB of packed weights, above L2);
-      - the M = 512 prefill GEMMs with F16 activations (q2_0_mul_mat_f16).
+      - the M = 512 prefill GEMMs with F16 activations (q2_0_mul_mat_f16);
+      - the group-128 packing of the head-sized matrix: exact repack to the
+        64-weight layout (bytes read + written) and the direct mat-vec.
     Returns the GB/s and TFLOP/s figures."""
     g = synth.rng(SEED + 7)
     N, K = VOCAB, 4096
@@ -494,6 +496,14 @@ def measure_extras(torch, q, stream, dev, reps: int = 20):
             q.q2_0_mul_mat_f16(wg, xg, Ng, Kg, PREFILL_M, y=yg, workspace=ws, stream=stream)
 
     msg = timed(gemms)
+    del gm
+    # group-128 packing: the exact repack to the 64-weight layout, and the direct
+    # CUDA-core mat-vec, on the head-sized matrix
+    w128 = torch.from_numpy(synth.packed_matrix_g128(g, N, K, *synth.DECODE_SCALE)).to(dev)
+    w64 = torch.empty(q.packed_bytes(N, K), dtype=torch.uint8, device=dev)
+    ms_rp = timed(lambda: q.q2_0_g128_to_g64(w128, N, K, dst=w64, stream=stream))
+    ms_g = timed(lambda: q.q2_0_g128_mul_mat_vec(w128, x, N, K, 1, y=y, stream=stream))
+    rp_bytes = w128.numel() + w64.numel()
     return {
         "head_matvec_151936x4096": {"bytes": head_bytes,
                                     "f32_gbs": round(head_bytes / (ms32 * 1e-3) / 1e9, 1),
@@ -502,6 +512,10 @@ def measure_extras(torch, q, stream, dev, reps: int = 20):
         "gemm_f16_m512": {"tflops": round(flops / (msg * 1e-3) / 1e12, 2),
                           "us": round(msg * 1e3, 2),
                           "shapes": [[PREFILL_M, Ng, Kg] for _, _, _, Ng, Kg, _ in gm]},
+        "g128_151936x4096": {"repack_gbs": round(rp_bytes / (ms_rp * 1e-3) / 1e9, 1),
+                             "repack_bytes": rp_bytes,
+                             "direct_matvec_gbs": round(w128.numel() / (ms_g * 1e-3) / 1e9, 1),
+                             "direct_matvec_us": round(ms_g * 1e3, 2)},
         "timing": "CUDA-graph replay, CUDA events on the launching stream, outside the step",
     }
 

@@ -51,6 +51,7 @@ EXPORTS = (
     "q2_0_mv_plan_launches", "q2_0_mv_plan_destroy", "q2_0_mul_mat_workspace_size",
     "q2_0_mul_mat", "q2_0_get_rows", "q2_0_quantize_ref", "q2_0_get_error",
     "q2_0_mul_mat_vec_f16", "q2_0_mul_mat_f16",
+    "q2_0_g128_to_g64", "q2_0_g128_get_rows", "q2_0_g128_mul_mat_vec",
 )
 
 
@@ -116,6 +117,12 @@ def lib():
             L.q2_0_mul_mat_vec_f16.restype = i32
             L.q2_0_mul_mat_f16.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
             L.q2_0_mul_mat_f16.restype = i32
+            L.q2_0_g128_to_g64.argtypes = [vp, vp, i64, i64, vp]
+            L.q2_0_g128_to_g64.restype = i32
+            L.q2_0_g128_get_rows.argtypes = [vp, i64, i64, vp, i64, vp, vp]
+            L.q2_0_g128_get_rows.restype = i32
+            L.q2_0_g128_mul_mat_vec.argtypes = [vp, vp, vp, i64, i64, i32, vp]
+            L.q2_0_g128_mul_mat_vec.restype = i32
             L.q2_0_get_rows.argtypes = [vp, i64, i64, vp, i64, vp, vp]
             L.q2_0_get_rows.restype = i32
             L.q2_0_quantize_ref.argtypes = [vp, vp, i64, i64, vp]
@@ -348,3 +355,48 @@ def q2_0_get_error(stream=None):
     if code < 0:
         raise Q2Error("q2_0_get_error", Q2_0_ECUDA)
     return code, info.value
+
+
+# ---- group-128 packing (34-byte blocks of 128 weights) ---------------------------
+def packed_bytes_g128(N: int, K: int) -> int:
+    return N * (K // 128) * 34
+
+
+def q2_0_g128_to_g64(src: torch.Tensor, nrows: int, K: int, dst: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """Exact repack of a group-128 matrix into the 64-weight layout (uint8)."""
+    if dst is None:
+        dst = torch.empty(packed_bytes(nrows, K), dtype=torch.uint8, device=src.device)
+    st = lib().q2_0_g128_to_g64(_dev(src, "src", torch.uint8, packed_bytes_g128(nrows, K)),
+                               _dev(dst, "dst", torch.uint8, packed_bytes(nrows, K)), nrows, K,
+                               _stream(stream))
+    _check("q2_0_g128_to_g64", st)
+    return dst
+
+
+def q2_0_g128_get_rows(table: torch.Tensor, n_rows: int, K: int, ids: torch.Tensor,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    n_ids = ids.numel()
+    if out is None:
+        out = torch.empty((n_ids, K), dtype=torch.float32, device=ids.device)
+    if n_ids == 0:
+        return out
+    st = lib().q2_0_g128_get_rows(_dev(table, "table", torch.uint8, packed_bytes_g128(n_rows, K)),
+                                 n_rows, K, _dev(ids, "ids", torch.int32, n_ids), n_ids,
+                                 _dev(out, "out", torch.float32, n_ids * K), _stream(stream))
+    _check("q2_0_g128_get_rows", st)
+    return out
+
+
+def q2_0_g128_mul_mat_vec(w: torch.Tensor, x: torch.Tensor, N: int, K: int,
+                         ncols: int | None = None, y: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    ncols = x.shape[0] if (ncols is None and x.dim() == 2) else (ncols or 1)
+    if y is None:
+        y = torch.empty((ncols, N), dtype=torch.float32, device=x.device)
+    st = lib().q2_0_g128_mul_mat_vec(_dev(w, "w", torch.uint8, packed_bytes_g128(N, K)),
+                                    _dev(x, "x", torch.float32, ncols * K),
+                                    _dev(y, "y", torch.float32, ncols * N), N, K, ncols,
+                                    _stream(stream))
+    _check("q2_0_g128_mul_mat_vec", st)
+    return y

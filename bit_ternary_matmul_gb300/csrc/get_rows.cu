@@ -19,14 +19,18 @@ namespace q2 {
 
 namespace {
 
-template <bool kVec4>
+// kGroup: weights per block (64: 18-byte blocks; 128: the 34-byte group-128
+// packing, whose 32 code bytes follow the same byte rule).
+template <bool kVec4, int kGroup>
 __global__ void __launch_bounds__(256) get_rows_kernel(const uint8_t *__restrict__ table,
                                                        int64_t n_rows, int64_t K,
                                                        const int32_t *__restrict__ ids,
                                                        int64_t n_ids, float *__restrict__ out,
                                                        unsigned long long *err) {
+    constexpr int kCodeBytes = kGroup / 4;
+    constexpr int kBlockBytes = 2 + kCodeBytes;
     const int64_t q4_per_row = K / 4;  // float4 per output row
-    const int64_t nb = K / 64;
+    const int64_t nb = K / kGroup;
     const int64_t total = n_ids * q4_per_row;
     for (int64_t t = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; t < total;
          t += int64_t(gridDim.x) * blockDim.x) {
@@ -37,9 +41,9 @@ __global__ void __launch_bounds__(256) get_rows_kernel(const uint8_t *__restrict
             if (j == 0) record_error(err, Q2_0_DEVERR_BAD_ID, r);
             continue;
         }
-        const int64_t b = j >> 4;         // block within the row
-        const int byte_in_codes = j & 15;  // code byte = elements 4*(j%16) .. +3
-        const uint8_t *blk = table + (id * nb + b) * 18;
+        const int64_t b = j / kCodeBytes;                  // block within the row
+        const int byte_in_codes = int(j % kCodeBytes);     // elements 4*byte .. +3
+        const uint8_t *blk = table + (id * nb + b) * kBlockBytes;
         const uint32_t dbits = uint32_t(__ldg(blk)) | (uint32_t(__ldg(blk + 1)) << 8);
         const uint32_t codes = __ldg(blk + 2 + byte_in_codes);
         const float d = half_bits_to_float(dbits);
@@ -64,7 +68,8 @@ __global__ void __launch_bounds__(256) get_rows_kernel(const uint8_t *__restrict
 }  // namespace
 
 cudaError_t launch_get_rows(const uint8_t *table, int64_t n_rows, int64_t K, const int32_t *ids,
-                            int64_t n_ids, float *out, unsigned long long *err, cudaStream_t s) {
+                            int64_t n_ids, float *out, unsigned long long *err, cudaStream_t s,
+                            int group) {
     const int64_t total = n_ids * (K / 4);
     int64_t blocks = (total + 255) / 256;
     const int64_t cap = int64_t(sm_count()) * 16;
@@ -72,12 +77,19 @@ cudaError_t launch_get_rows(const uint8_t *table, int64_t n_rows, int64_t K, con
     if (blocks < 1) blocks = 1;
     // Rows are K*4 bytes (a multiple of 256), so every row is 16-byte aligned
     // when `out` is; otherwise the same kernel stores scalars.
-    if ((reinterpret_cast<uintptr_t>(out) & 15u) == 0)
-        get_rows_kernel<true><<<unsigned(blocks), 256, 0, s>>>(table, n_rows, K, ids, n_ids, out,
-                                                               err);
-    else
-        get_rows_kernel<false><<<unsigned(blocks), 256, 0, s>>>(table, n_rows, K, ids, n_ids, out,
-                                                                err);
+    const bool vec = (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+    const unsigned g = unsigned(blocks);
+    if (group == 128) {
+        if (vec)
+            get_rows_kernel<true, 128><<<g, 256, 0, s>>>(table, n_rows, K, ids, n_ids, out, err);
+        else
+            get_rows_kernel<false, 128><<<g, 256, 0, s>>>(table, n_rows, K, ids, n_ids, out, err);
+    } else {
+        if (vec)
+            get_rows_kernel<true, 64><<<g, 256, 0, s>>>(table, n_rows, K, ids, n_ids, out, err);
+        else
+            get_rows_kernel<false, 64><<<g, 256, 0, s>>>(table, n_rows, K, ids, n_ids, out, err);
+    }
     return cudaGetLastError();
 }
 

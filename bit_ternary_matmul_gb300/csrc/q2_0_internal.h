@@ -32,8 +32,10 @@ bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *bas
                     CUtensorMapSwizzle swizzle);
 
 // ---- kernels' host launchers -------------------------------------------------
+// group: 64 (18-byte blocks) or 128 (34-byte blocks)
 cudaError_t launch_get_rows(const uint8_t *table, int64_t n_rows, int64_t K, const int32_t *ids,
-                            int64_t n_ids, float *out, unsigned long long *err, cudaStream_t s);
+                            int64_t n_ids, float *out, unsigned long long *err, cudaStream_t s,
+                            int group = 64);
 
 cudaError_t launch_quantize(const float *src, uint8_t *dst, int64_t nrows, int64_t K,
                             cudaStream_t s);

@@ -204,6 +204,32 @@ int q2_0_get_rows(const void *table, int64_t n_rows, int64_t K, const int32_t *i
                   float *out, void *stream);
 
 /*
+ * Group-128 Q2_0: 34-byte blocks of 128 weights (fp16 d, then eight
+ * little-endian words of sixteen 2-bit codes; element 16w+i in bits 2i..2i+1
+ * of word w; code q -> (q - 1) * d). Source: "Llama.cpp umí dvoubitový Q2_0 i
+ * na kartách NVIDIA" (aisvetem.cz), "Šest procent, o která se vedl spor" (34
+ * bytes per 128 weights) and its closing section (Q2_0.gguf files without the
+ * _g64 suffix use this packing). The pages fix only the size; the word layout
+ * is the 64-weight block's, extended. K % 128 == 0 for all three calls.
+ *
+ * q2_0_g128_to_g64 — exact repack: src is an nrows x K group-128 matrix
+ * (nrows*K/128*34 bytes), dst (nrows*K/64*18 bytes, written) the same matrix in
+ * the 64-weight layout: block i becomes blocks 2i and 2i+1 with i's scale and
+ * its code bytes 0..15 and 16..31. Every q2_0_* call then applies to dst.
+ */
+int q2_0_g128_to_g64(const void *src, void *dst, int64_t nrows, int64_t K, void *stream);
+
+/* q2_0_g128_get_rows — as q2_0_get_rows over a group-128 table, bit-exact. */
+int q2_0_g128_get_rows(const void *table, int64_t n_rows, int64_t K, const int32_t *ids,
+                      int64_t n_ids, float *out, void *stream);
+
+/* q2_0_g128_mul_mat_vec — as q2_0_mul_mat_vec over a group-128 matrix, on CUDA
+ * cores (for callers that keep the 128-weight packing; the repack plus
+ * q2_0_mul_mat_vec is the fast route). Same error bound; no scratch. */
+int q2_0_g128_mul_mat_vec(const void *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
+                         void *stream);
+
+/*
  * q2_0_quantize_ref — the reference quantizer, bit-exact.
  * Source: "Llama.cpp umí dvoubitový Q2_0 i na kartách NVIDIA" (aisvetem.cz),
  * section "Na běžný model to není": the block's largest |w| is the scale and

@@ -64,6 +64,21 @@ def packed_matrix(g: np.random.Generator, N: int, K: int, scale_lo: float, scale
     return out.reshape(-1)
 
 
+def packed_matrix_g128(g: np.random.Generator, N: int, K: int, scale_lo: float,
+                       scale_hi: float) -> np.ndarray:
+    """Raw bytes of an N x K matrix in the group-128 packing: N * K/128 blocks of
+    34 bytes, a 2-byte fp16 scale (fp16 of U[scale_lo, scale_hi]) then 32 code
+    bytes whose four 2-bit fields are iid uniform over {0, 1, 2}."""
+    assert K % 128 == 0
+    nb = N * (K // 128)
+    out = np.empty((nb, 34), dtype=np.uint8)
+    d = fp16_bits(g.uniform(scale_lo, scale_hi, size=nb).astype(np.float32))
+    out[:, 0] = (d & 0xFF).astype(np.uint8)
+    out[:, 1] = (d >> 8).astype(np.uint8)
+    out[:, 2:] = _TERNARY_BYTES[g.integers(0, 81, size=(nb, 32), dtype=np.uint8)]
+    return out.reshape(-1)
+
+
 def activations(g: np.random.Generator, rows: int, K: int, frac_outlier: float = 0.0,
                 outlier: float = 30.0) -> np.ndarray:
     """f32 [rows][K] ~ N(0,1); a fraction of entries at seeded positions = ±outlier."""

@@ -55,6 +55,13 @@ def test_argument_validation_without_gpu(L):
     assert L.q2_0_mul_mat_vec_f16(p, p, p, 4, 64, 9, null) == EINVAL
     assert L.q2_0_mul_mat_f16(p, p, p, 4, 65, 4, null, 0, null) == EINVAL
     assert L.q2_0_mul_mat_f16(p, null, p, 4, 64, 4, null, 0, null) == EINVAL
+    # group-128: K must be a multiple of 128
+    assert L.q2_0_g128_to_g64(p, p, 4, 64, null) == EINVAL
+    assert L.q2_0_g128_to_g64(null, p, 4, 128, null) == EINVAL
+    assert L.q2_0_g128_get_rows(p, 4, 192, p, 3, p, null) == EINVAL
+    assert L.q2_0_g128_get_rows(p, 4, 128, p, 0, p, null) == q.Q2_0_OK
+    assert L.q2_0_g128_mul_mat_vec(p, p, p, 4, 128, 9, null) == EINVAL
+    assert L.q2_0_g128_mul_mat_vec(p, p, p, 0, 128, 1, null) == EINVAL
     # mat-vec with workspace: too small, misaligned
     need = L.q2_0_mul_mat_vec_workspace_size(512, 1)
     assert need > 0 and need % 256 == 0

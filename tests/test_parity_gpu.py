@@ -410,3 +410,72 @@ def test_gemm_f16_prefill_sampled(dev, N, K, M):
     got = y[:, torch.from_numpy(rows).to(dev)].cpu().numpy()
     _assert_close(got, yo, acc, TOL_SPLIT, f"GEMM f16 {N}x{K} M={M}")
     _no_device_error()
+
+
+# ---------------------------------------------------------------------------
+# Group-128 packing (34-byte blocks)
+# ---------------------------------------------------------------------------
+def _g128_matrix(g, N, K, lo=0.005, hi=0.05, frac_code3=0.01):
+    """Seeded group-128 bytes: the same draw as the 64-weight generator, laid out
+    as 34-byte blocks (scale, then 32 code bytes)."""
+    nb = K // 128
+    d = g.uniform(lo, hi, size=(N, nb)).astype(np.float16).view(np.uint16)
+    codes = g.integers(0, 3, size=(N, nb, 128), dtype=np.uint8)
+    codes[g.random((N, nb, 128)) < frac_code3] = 3
+    q = codes.reshape(N, nb, 32, 4)
+    byte = (q[..., 0] | (q[..., 1] << 2) | (q[..., 2] << 4) | (q[..., 3] << 6)).astype(np.uint8)
+    blk = np.zeros((N, nb, 34), dtype=np.uint8)
+    blk[:, :, 0] = d & 0xFF
+    blk[:, :, 1] = d >> 8
+    blk[:, :, 2:] = byte
+    return blk.reshape(-1)
+
+
+def test_g128_get_rows_bit_exact(dev):
+    g = synth.rng(4101)
+    n_rows, K = 3000, 4096
+    table = _g128_matrix(g, n_rows, K)
+    tb = table.reshape(n_rows, K // 128, 34)
+    tb[0, 0, :2] = [0x00, 0x80]        # d = -0: signed zeros
+    tb[1, 1, :2] = [0x01, 0x00]        # subnormal d
+    tb[2, 2, 2:] = 0xFF                # all code 3
+    ids = np.concatenate([[0, 1, 2, 2999], g.integers(0, n_rows, 508)]).astype(np.int32)
+    got = q.q2_0_g128_get_rows(_to(dev, table), n_rows, K, _to(dev, ids)).cpu().numpy()
+    ref, bad = oracle.get_rows_g128(table, n_rows, K, ids)
+    assert bad == 0
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    _no_device_error()
+
+
+def test_g128_repack_then_fast_paths(dev):
+    """The repacked matrix decodes to the same weights, and the fast mat-vec and
+    GEMM on it match the group-128 oracle."""
+    g = synth.rng(4102)
+    N, K = 777, 2048
+    w128 = _g128_matrix(g, N, K)
+    w64 = q.q2_0_g128_to_g64(_to(dev, w128), N, K).cpu().numpy()
+    rows = np.arange(N, dtype=np.int32)
+    dec128, _ = oracle.get_rows_g128(w128, N, K, rows)
+    assert np.array_equal(oracle.dequantize(w64, N, K).astype(np.float32).view(np.uint32),
+                          dec128.view(np.uint32))
+    for ncols in (1, 2, 5):
+        x = synth.activations(g, ncols, K, 0.001, 30.0)
+        y = q.q2_0_mul_mat_vec(_to(dev, w64), _to(dev, x), N, K, ncols).cpu().numpy()
+        yo, acc = oracle.matmul_g128(w128, N, K, x)
+        _assert_close(y, yo, acc, TOL_SPLIT, f"repacked mat-vec ncols={ncols}")
+    x = synth.activations(g, 64, K, synth.PREFILL_OUTLIER_FRAC, synth.PREFILL_OUTLIER)
+    y = q.q2_0_mul_mat(_to(dev, w64), _to(dev, x), N, K, 64).cpu().numpy()
+    yo, acc = oracle.matmul_g128(w128, N, K, x)
+    _assert_close(y, yo, acc, TOL_SPLIT, "repacked GEMM")
+    _no_device_error()
+
+
+@pytest.mark.parametrize("N,K,ncols", [(300, 1024, 1), (129, 2048, 3), (64, 128, 8), (5, 896, 2)])
+def test_g128_matvec_direct(dev, N, K, ncols):
+    g = synth.rng(4103, N, K, ncols)
+    w = _g128_matrix(g, N, K)
+    x = synth.activations(g, ncols, K, 0.001, 30.0)
+    y = q.q2_0_g128_mul_mat_vec(_to(dev, w), _to(dev, x), N, K, ncols).cpu().numpy()
+    yo, acc = oracle.matmul_g128(w, N, K, x)
+    _assert_close(y, yo, acc, TOL_SPLIT, f"g128 mat-vec {N}x{K} ncols={ncols}")
+    _no_device_error()
