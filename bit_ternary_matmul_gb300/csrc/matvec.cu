@@ -40,6 +40,7 @@
 // and W 16-byte aligned. Other shapes run mv_generic_kernel (CUDA cores, f32).
 // Activations are F32 or F16 (the prep kernels and the generic kernel read
 // either; F16 values are converted exactly).
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include <algorithm>
@@ -873,7 +874,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                 const uint8_t *beta = img + size_t(J->n_chunks) * kT5ImgBytes;
                 for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
                     const int st = s % kT5Stages;
-                    if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagT5Empty) ||
+                    if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagT5Empty, true) ||
                         *(volatile int *)&s_abort) {
                         ok = false;
                         s_abort = 1;
@@ -1119,6 +1120,478 @@ __global__ void __launch_bounds__(kT5Threads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// tcgen05 mat-vec on packed fp4 (ncols = 1)
+//
+// The codes are exact e2m1 values without arithmetic as well: e2m1 is sign,
+// two exponent bits, one mantissa bit, and a nibble whose only set bits are
+// the low two (exponent bit 0, mantissa) reads as 0, 0.5, 1, 1.5 = q / 2. With
+// each code at bits 2i of a word, word & 0x33333333 holds the even elements
+// 0, 2, .., 14 as eight packed e2m1 values and (word >> 2) & 0x33333333 the odd
+// ones: 16 weights per shift and two logic ops, half the register traffic of
+// the e4m3 form. tcgen05.mma kind::mxf4 takes K = 64 (a whole block) per
+// instruction with A in TMEM; its per-32-element ue8m0 scales are all 1.0
+// (0x7F), so it multiplies the e2m1 values as they are.
+//
+// The activations are 12 e2m1 pieces: u = x * 2^s with max|u| in [1, 2),
+// v = 2u (so that A * B = q * u), piece p = e2m1(r_p * 4^p), r_0 = v,
+// r_{p+1} = r_p - piece_p * 4^-p; each rounding leaves at most a quarter of
+// the magnitude, so after 12 pieces the residual is below 2^-25 max|v|.
+// Piece p is B row p; the epilogue forms t = sum_p 4^-p C_p - beta and
+// acc += d * t, beta computed by the prep kernel from exact per-piece sums
+// with the same f32 operations. Pipeline and warp roles as the e4m3 kernel;
+// per 8-block stage the A buffer is 64 TMEM columns and the D buffer 128.
+// ---------------------------------------------------------------------------
+constexpr int kT4Pieces = 12;
+constexpr int kT4ImgBytes = kT5N * kChunkBlocks * 32;  // 4096: 16 rows x 256 bytes (512 e2m1)
+constexpr int kT4BetaBytes = kChunkBlocks * 4;         // beta[8 blocks] f32
+constexpr int kT4ABufs = 3;
+constexpr int kT4ACol = 256;                           // A buffers at 256 + 64 i
+constexpr int kT4ScaleCol = 448;                       // scales A 448..451, B 452..455
+constexpr int kT4Smem = 1024 /* alignment slack */ +
+                        kT5Stages * (kT4ImgBytes + kT5RawBytes + kT4BetaBytes) +
+                        (2 * kT5Stages + 2 * kT5MaxABufs + 8) * 8;
+
+size_t t4_prep_bytes(int64_t K) {
+    const size_t n_chunks = size_t(K / 512);
+    size_t b = kT5PrepHeader + n_chunks * (kT4ImgBytes + kT4BetaBytes);
+    return (b + 255) & ~size_t(255);
+}
+
+// kind::mxf4 instruction descriptor: A and B e2m1 (1), N, scales ue8m0, M.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int m, int n) {
+    return (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (1u << 23) |
+           (uint32_t(m >> 4) << 24);
+}
+
+// Preparation: grid (1, n_jobs, z), kT5PrepThreads threads. Item (block b,
+// word c, parity h): the 8 elements 16c + 2j + h (j = 0..7) of block b, one
+// 32-bit word of the B image per piece (K positions 64 (b % 8) + 16c + 8h + j,
+// nibble j). Per-piece all-ones sums are exact integers in units of 1/4.
+template <typename XT>
+__global__ void __launch_bounds__(kT5PrepThreads) t4_prep_kernel(
+    const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const MvPrepJob &J = jobs ? jobs[blockIdx.y] : single;
+    const int K = J.K;
+    const XT *xj = static_cast<const XT *>(J.x);
+    const int tid = threadIdx.x;
+    const int nb = K / 64;
+    const int n_chunks = K / 512;
+    if (int(blockIdx.z) * kT5PrepThreads >= nb * 8) return;
+
+    // 1) column scale 2^s with max|x * 2^s| in [1, 2)
+    float m = 0.0f;
+    if (sizeof(XT) == 4 && (reinterpret_cast<uintptr_t>(xj) & 15u) == 0) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(xj);
+        for (int k = tid; k < K / 4; k += kT5PrepThreads) {
+            const float4 f = x4[k];
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+        }
+    } else {
+        for (int k = tid; k < K; k += kT5PrepThreads) m = fmaxf(m, fabsf(ld_x(xj + k)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ float red[kT5PrepThreads / 32];
+    if ((tid & 31) == 0) red[tid >> 5] = m;
+    __syncthreads();
+    float amax = red[0];
+#pragma unroll
+    for (int w = 1; w < kT5PrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+    int s = 0;
+    if (amax > 0.0f && amax <= 3.4e38f) {
+        int e;
+        frexpf(amax, &e);  // amax = f * 2^e, f in [0.5, 1)
+        s = 1 - e;
+    }
+    int *col_shift = reinterpret_cast<int *>(J.prep);
+    if (blockIdx.z == 0 && tid == 0) col_shift[0] = s;
+
+    // 2) pieces
+    uint8_t *img = J.prep + kT5PrepHeader;
+    float *beta = reinterpret_cast<float *>(img + size_t(n_chunks) * kT4ImgBytes);
+    const int lane = tid & 31;
+    const unsigned grp = 0xFFu << (lane & 24);  // the block's 8 threads
+    for (int idx = int(blockIdx.z) * kT5PrepThreads + tid; idx < nb * 8;
+         idx += int(gridDim.z) * kT5PrepThreads) {
+        const int b = idx >> 3, c = (idx >> 1) & 3, h = idx & 1;
+        const XT *xe = xj + b * 64 + c * 16 + h;
+        float v[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) v[jj] = mul_pow2(ld_x(xe + 2 * jj), s + 1);  // v = 2u
+        uint8_t *bimg = img + size_t(b >> 3) * kT4ImgBytes;
+        const int kbyte = 32 * (b & 7) + 8 * c + 4 * h;  // byte of K position 64(b%8)+16c+8h
+        int isum[kT4Pieces];
+#pragma unroll
+        for (int p = 0; p < kT4Pieces; ++p) {
+            const float up = __int_as_float((127 + 2 * p) << 23);
+            const float down = __int_as_float((127 - 2 * p) << 23);
+            uint32_t word = 0;
+            int acc2 = 0;  // sum of 2 * piece (exact small integers)
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) {
+                const __nv_fp4x2_storage_t pc = __nv_cvt_float2_to_fp4x2(
+                    make_float2(v[2 * q2] * up, v[2 * q2 + 1] * up), __NV_E2M1, cudaRoundNearest);
+                const float2 pv =
+                    __half22float2(__half2(__nv_cvt_fp4x2_to_halfraw2(pc, __NV_E2M1)));
+                v[2 * q2] -= pv.x * down;
+                v[2 * q2 + 1] -= pv.y * down;
+                acc2 += __float2int_rn(2.0f * pv.x) + __float2int_rn(2.0f * pv.y);
+                word |= uint32_t(pc) << (8 * q2);
+            }
+            isum[p] = acc2;
+            *reinterpret_cast<uint32_t *>(bimg + t5_img_offset(p, kbyte)) = word;
+        }
+        // rows 12..15 of the image stay zero
+        if (h == 0)
+            for (int n = kT4Pieces; n < kT5N; ++n)
+                *reinterpret_cast<uint2 *>(bimg + t5_img_offset(n, kbyte)) = make_uint2(0u, 0u);
+        float base[kT4Pieces];
+#pragma unroll
+        for (int p = 0; p < kT4Pieces; ++p) {
+            int t = isum[p];
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) t += __shfl_xor_sync(grp, t, o);
+            base[p] = float(t) * 0.25f;  // sum of piece * (value of code 1 = 1/2)
+        }
+        if ((idx & 7) == 0) {
+            float t = base[kT4Pieces - 1] * __int_as_float((127 - 2 * (kT4Pieces - 1)) << 23);
+#pragma unroll
+            for (int p = kT4Pieces - 2; p >= 1; --p)
+                t = fmaf(base[p], __int_as_float((127 - 2 * p) << 23), t);
+            t = t + base[0];
+            beta[size_t(b >> 3) * (kT4BetaBytes / 4) + (b & 7)] = t;
+        }
+    }
+}
+
+// Warp roles of the fp4 kernel. A warp reaches only the TMEM lanes of its
+// quarter (warp % 4, which is also its SM sub-partition):
+//   warp 2       producer;
+//   warps 3, 1   MMA issuers of the even / odd stages (warp 3 allocates TMEM);
+//   warps 4-7    expansion, one per lane quarter, all 8 blocks of a stage;
+//   warps 8-15   epilogue, two per quarter (blocks 4G .. 4G+3).
+constexpr int kT4ProdWarp = 2;
+constexpr int kT4MmaWarp = 3;
+constexpr int kT4MmaWarp2 = 1;
+constexpr int kT4ExpWarp0 = 4;
+constexpr int kT4ExpWarps = 4;
+constexpr int kT4EpiWarp0 = 8;
+constexpr int kT4EpiWarps = 8;
+constexpr int kT4Threads = 16 * 32;
+
+__global__ void __launch_bounds__(kT4Threads, 1)
+    mv_t4_kernel(const __grid_constant__ MvJob single, const MvParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *img_ring = smem;                                      // kT5Stages x 4 KB
+    uint8_t *raw_ring = img_ring + kT5Stages * kT4ImgBytes;         // kT5Stages x 18 KB
+    uint8_t *beta_ring = raw_ring + kT5Stages * kT5RawBytes;        // kT5Stages x 32 B
+    uint64_t *full = reinterpret_cast<uint64_t *>(beta_ring + kT5Stages * kT4BetaBytes);
+    uint64_t *empty = full + kT5Stages;
+    uint64_t *a_full = empty + kT5Stages;
+    uint64_t *a_empty = a_full + kT5MaxABufs;
+    uint64_t *d_full = a_empty + kT5MaxABufs;
+    uint64_t *d_empty = d_full + 2;
+    uint64_t *drain = d_empty + 2;  // [2] one per MMA issuer: its final commit
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    __shared__ float s_part[kT5Rows];  // the second epilogue half's row sums at a tile end
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kT5Stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kT4EpiWarps);
+        }
+        for (int i = 0; i < kT4ABufs; ++i) {
+            mbar_init(&a_full[i], kT4ExpWarps);
+            mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&d_full[i], 1);
+            mbar_init(&d_empty[i], kT4EpiWarps);
+        }
+        for (int i = 0; i < 2; ++i) mbar_init(&drain[i], 1);
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kT4MmaWarp) {
+        tmem_alloc(&s_tmem, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    int n_items, item_base = 0;
+    if (p.jobs) {
+        item_base = p.cta_begin[blockIdx.x];
+        n_items = p.cta_begin[blockIdx.x + 1] - item_base;
+    } else {
+        n_items = blockIdx.x < unsigned(single.n_tiles)
+                      ? (single.n_tiles - 1 - int(blockIdx.x)) / int(gridDim.x) + 1
+                      : 0;
+    }
+    auto item_at = [&](int i, const MvJob *&J, int &tile) {
+        if (p.jobs) {
+            const MvItem it = p.items[item_base + i];
+            J = &p.jobs[it.job];
+            tile = it.tile;
+        } else {
+            J = &single;
+            tile = int(blockIdx.x) + i * int(gridDim.x);
+        }
+    };
+    auto stage_parity = [](int s) { return uint32_t(s / kT5Stages) & 1u; };
+    auto a_buf = [](int s) { return s % kT4ABufs; };
+    auto a_use = [](int s) { return uint32_t(s / kT4ABufs) & 1u; };
+    auto a_col = [](int s) { return uint32_t(kT4ACol + (s % kT4ABufs) * 64); };
+    auto d_col = [](int s) { return uint32_t((s & 1) * 128); };
+
+    if (warp == kT4ProdWarp) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            int s = 0, last = -1;
+            bool ok = true, prep_ready = false;
+            for (int i = 0; i < n_items && ok; ++i) {
+                const MvJob *J;
+                int tile;
+                item_at(i, J, tile);
+                const uint8_t *img = J->prep + kT5PrepHeader;
+                const uint8_t *beta = img + size_t(J->n_chunks) * kT4ImgBytes;
+                for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+                    const int st = s % kT5Stages;
+                    if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagT5Empty, true) ||
+                        *(volatile int *)&s_abort) {
+                        ok = false;
+                        s_abort = 1;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[st], kT5RawBytes + kT4ImgBytes + kT4BetaBytes);
+                    tma_load_2d(raw_ring + st * kT5RawBytes, &J->tmap, ch * kChunkBytes,
+                                tile * kT5Rows, &full[st]);
+                    if (!prep_ready) {
+                        grid_dependency_wait();  // the B images come from the prep kernel
+                        prep_ready = true;
+                    }
+                    bulk_g2s(img_ring + st * kT4ImgBytes, img + size_t(ch) * kT4ImgBytes,
+                             kT4ImgBytes, &full[st]);
+                    bulk_g2s(beta_ring + st * kT4BetaBytes, beta + size_t(ch) * kT4BetaBytes,
+                             kT4BetaBytes, &full[st]);
+                    last = s;
+                }
+            }
+            if (!ok) {
+                // let the copies in flight land (bounded) before the CTA exits
+                for (int t = last; t >= 0 && t > last - kT5Stages; --t)
+                    mbar_wait(&full[t % kT5Stages], stage_parity(t), p.err, kTagT5Full);
+            }
+        }
+    } else if (warp == kT4MmaWarp || warp == kT4MmaWarp2) {
+        // ------------------------------ MMA issuers ------------------------------
+        // even / odd stages; the whole warp runs the loop, the elected lane waits,
+        // issues (one K = 64 MMA per block) and commits
+        constexpr uint32_t idesc = idesc_mxf4(kT5Rows, kT5N);
+        const bool leader = elect_one();
+        const int mine = warp == kT4MmaWarp ? 0 : 1;
+        const uint64_t desc0 = sw128_desc(smem_addr(img_ring));
+        const uint32_t sfa = tmem + kT4ScaleCol, sfb = tmem + kT4ScaleCol + 4;
+        int s = 0, last = -1;
+        bool ok = true;
+        for (int i = 0; i < n_items && ok; ++i) {
+            const MvJob *J;
+            int tile;
+            item_at(i, J, tile);
+            for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+                if ((s & 1) != mine) continue;
+                const int st = s % kT5Stages;
+                bool got = true;
+                if (leader)
+                    got = mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
+                          mbar_wait(&a_full[a_buf(s)], a_use(s), p.err, kTagT5AFull) &&
+                          mbar_wait(&d_empty[s & 1], (uint32_t(s >> 1) & 1u) ^ 1u, p.err,
+                                    kTagT5DEmpty) &&
+                          !*(volatile int *)&s_abort;
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_base = tmem + a_col(s);
+                const uint32_t d_base = tmem + d_col(s);
+                const uint64_t dst = desc0 + uint64_t((st * kT4ImgBytes) >> 4);
+                if (leader) {
+#pragma unroll
+                    for (int b = 0; b < kChunkBlocks; ++b)
+                        tc_mma_mxf4_ta(d_base + b * kT5N, a_base + b * 8,
+                                       dst + uint64_t(((b >> 2) * 2048 + (b & 3) * 32) >> 4), idesc,
+                                       sfa, sfb, 0u);
+                    tc_commit(&a_empty[a_buf(s)]);
+                    tc_commit(&d_full[s & 1]);
+                }
+                __syncwarp();
+                last = s;
+            }
+        }
+        // TMEM is freed only after this issuer's MMAs completed: one more commit
+        // tracks all of them
+        if (last >= 0) {
+            if (leader) tc_commit(&drain[mine]);
+            __syncwarp();
+            if (leader) mbar_wait(&drain[mine], 0u, p.err, kTagT5DFull);
+            __syncwarp();
+        }
+    } else if (warp >= kT4ExpWarp0 && warp < kT4ExpWarp0 + kT4ExpWarps) {
+        // ------------------------------ expansion ------------------------------
+        // warp w: TMEM lane quarter w % 4 (rows 32 (w % 4) ..), all 8 blocks
+        const int qd = warp & 3;
+        const int row = 32 * qd + lane;
+        const uint32_t lane_base = uint32_t(32 * qd) << 16;
+        {  // scale factors 1.0 (ue8m0 127) for this quarter's lanes
+            const uint32_t one = 0x7F7F7F7Fu;
+            tmem_st4(tmem + lane_base + kT4ScaleCol, one, one, one, one);
+            tmem_st4(tmem + lane_base + kT4ScaleCol + 4, one, one, one, one);
+        }
+        int s = 0;
+        bool ok = true;
+        for (int i = 0; i < n_items && ok; ++i) {
+            const MvJob *J;
+            int tile;
+            item_at(i, J, tile);
+            for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+                const int st = s % kT5Stages;
+                const bool got =
+                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
+                    mbar_wait(&a_empty[a_buf(s)], a_use(s) ^ 1u, p.err, kTagT5AFull) &&
+                    !*(volatile int *)&s_abort;
+                if (!__all_sync(0xffffffffu, got)) {
+                    s_abort = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int G = 0; G < 2; ++G) {
+                    const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes + G * 72;
+                    uint32_t u[18];
+#pragma unroll
+                    for (int k = 0; k < 9; ++k) {
+                        const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * k);
+                        u[2 * k] = v.x;
+                        u[2 * k + 1] = v.y;
+                    }
+                    uint32_t a[32];
+#pragma unroll
+                    for (int bi = 0; bi < 4; ++bi) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t w;
+                            if (bi == 0) w = __byte_perm(u[c], u[c + 1], 0x5432);
+                            else if (bi == 1) w = u[5 + c];
+                            else if (bi == 2) w = __byte_perm(u[9 + c], u[10 + c], 0x5432);
+                            else w = u[14 + c];
+                            a[8 * bi + 2 * c + 0] = w & 0x33333333u;
+                            a[8 * bi + 2 * c + 1] = (w >> 2) & 0x33333333u;
+                        }
+                    }
+                    tmem_st32(tmem + lane_base + a_col(s) + 32 * G, a);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[a_buf(s)]);
+            }
+        }
+    } else if (warp >= kT4EpiWarp0 && warp < kT4EpiWarp0 + kT4EpiWarps) {
+        // ------------------------------ epilogue ------------------------------
+        // warp w: TMEM lane quarter w % 4, blocks 4G .. 4G+3 of each stage. A warp
+        // whose wait fails (or that sees the abort flag) turns dead: it skips all
+        // TMEM and barrier-wait work but still takes part in the tile-end named
+        // barriers, which every epilogue warp meets the same number of times.
+        grid_dependency_wait();  // reads the column shift written by prep
+        const int G = (warp - kT4EpiWarp0) >> 2;
+        const int qd = warp & 3;
+        const int row = 32 * qd + lane;
+        const uint32_t lane_base = uint32_t(32 * qd) << 16;
+        float acc = 0.0f;
+        bool dead = false;
+        int s = 0;
+        for (int i = 0; i < n_items; ++i) {
+            const MvJob *J;
+            int tile;
+            item_at(i, J, tile);
+            for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+                const int st = s % kT5Stages;
+                if (!dead) {
+                    const bool got =
+                        !*(volatile int *)&s_abort &&
+                        mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
+                        mbar_wait(&d_full[s & 1], uint32_t(s >> 1) & 1u, p.err, kTagT5DFull);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        s_abort = 1;
+                        dead = true;
+                    }
+                }
+                if (!dead) {
+                    tc_fence_after();
+                    const uint32_t d_base = tmem + lane_base + d_col(s) + 4 * G * kT5N;
+                    uint32_t r[4][16];
+#pragma unroll
+                    for (int bi = 0; bi < 4; ++bi) tmem_ld16(d_base + bi * kT5N, r[bi]);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&d_empty[s & 1]);  // D is in registers
+                    const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes;
+                    const float *bt =
+                        reinterpret_cast<const float *>(beta_ring + st * kT4BetaBytes);
+#pragma unroll
+                    for (int bi = 0; bi < 4; ++bi) {
+                        const int b = 4 * G + bi;
+                        float t = __uint_as_float(r[bi][kT4Pieces - 1]) *
+                                  __int_as_float((127 - 2 * (kT4Pieces - 1)) << 23);
+#pragma unroll
+                        for (int pp = kT4Pieces - 2; pp >= 1; --pp)
+                            t = fmaf(__uint_as_float(r[bi][pp]),
+                                     __int_as_float((127 - 2 * pp) << 23), t);
+                        t = t + __uint_as_float(r[bi][0]);
+                        const float d = lds_half_as_float(rp + 18 * b);
+                        acc = fmaf(d, t - bt[b], acc);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[st]);
+                }
+                if (ch == J->n_chunks - 1) {
+                    // combine the two halves' row sums (named barrier of the 8 epilogue warps)
+                    if (G == 1) s_part[row] = acc;
+                    asm volatile("bar.sync 1, %0;" ::"n"(kT4EpiWarps * 32) : "memory");
+                    if (G == 0 && !dead) {
+                        const int *col_shift = reinterpret_cast<const int *>(J->prep);
+                        const int rr = tile * kT5Rows + row;
+                        if (rr < J->N) J->y[rr] = mul_pow2(acc + s_part[row], -col_shift[0]);
+                    }
+                    asm volatile("bar.sync 1, %0;" ::"n"(kT4EpiWarps * 32) : "memory");
+                    acc = 0.0f;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kT4MmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Generic mat-vec (any K % 64 == 0, any alignment): one warp per row, f32 on
 // CUDA cores, block-wise: s = sum (q - 1) * x over the block, then acc += d*s.
 // ---------------------------------------------------------------------------
@@ -1175,6 +1648,19 @@ cudaError_t set_t5_attr() {
                                 kT5Smem);
 }
 
+bool g_t4_attr_done[64];
+
+cudaError_t ensure_t4_attr() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (dev < 64 && g_t4_attr_done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(mv_t4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kT4Smem);
+    if (e == cudaSuccess && dev < 64) g_t4_attr_done[dev] = true;
+    return e;
+}
+
 cudaError_t ensure_t5_attrs(int ncols) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1202,8 +1688,9 @@ cudaError_t ensure_attrs(int nt) {
     return e;
 }
 
-// The tcgen05 path (128-row tiles) serves ncols <= kT5MaxCols; more columns run
-// the mma.sync kernel (256-row tiles).
+// ncols = 1 runs the fp4 tcgen05 kernel, ncols 2-3 the e4m3 one (both 128-row
+// tiles); more columns run the mma.sync kernel (256-row tiles).
+bool use_t4(int ncols) { return ncols == 1; }
 bool use_t5(int ncols) { return ncols <= kT5MaxCols; }
 int tile_rows_for(int ncols) { return use_t5(ncols) ? kT5Rows : kTileRows; }
 
@@ -1228,7 +1715,11 @@ template <typename XT>
 cudaError_t launch_prep_t(const MvPrepJob &single, const MvPrepJob *jobs, int n_jobs, int ncols,
                           int64_t max_k, cudaStream_t s) {
     dim3 grid(ncols, n_jobs);
-    if (use_t5(ncols)) {
+    if (use_t4(ncols)) {
+        const int64_t items = max_k / 64 * 8;
+        grid.z = unsigned(std::min<int64_t>((items + kT5PrepThreads - 1) / kT5PrepThreads, 65535));
+        t4_prep_kernel<XT><<<grid, kT5PrepThreads, 0, s>>>(single, jobs);
+    } else if (use_t5(ncols)) {
         const int64_t items = max_k / 64 * 16;
         grid.z = unsigned(std::min<int64_t>((items + kT5PrepThreads - 1) / kT5PrepThreads, 65535));
         t5_prep_kernel<XT><<<grid, kT5PrepThreads, 0, s>>>(single, jobs, ncols);
@@ -1250,7 +1741,9 @@ cudaError_t launch_prep(const MvPrepJob &single, const MvPrepJob *jobs, int n_jo
 // producer waits for the prep grid before loading any activation fragment.
 cudaError_t launch_tc(const MvJob &single, const MvParams &prm, int grid, cudaStream_t s) {
     const int nt = n_tiles_for(prm.ncols);
-    cudaError_t e = use_t5(prm.ncols) ? ensure_t5_attrs(prm.ncols) : ensure_attrs(nt);
+    cudaError_t e = use_t4(prm.ncols)   ? ensure_t4_attr()
+                    : use_t5(prm.ncols) ? ensure_t5_attrs(prm.ncols)
+                                        : ensure_attrs(nt);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -1260,7 +1753,11 @@ cudaError_t launch_tc(const MvJob &single, const MvParams &prm, int grid, cudaSt
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (use_t5(prm.ncols)) {
+    if (use_t4(prm.ncols)) {
+        cfg.blockDim = dim3(kT4Threads);
+        cfg.dynamicSmemBytes = kT4Smem;
+        e = cudaLaunchKernelEx(&cfg, mv_t4_kernel, single, prm);
+    } else if (use_t5(prm.ncols)) {
         cfg.blockDim = dim3(kT5Threads);
         cfg.dynamicSmemBytes = kT5Smem;
         if (prm.ncols == 1)
@@ -1297,7 +1794,8 @@ cudaError_t launch_generic(const uint8_t *w, const void *x, int xtype, float *y,
 }  // namespace
 
 size_t matvec_workspace_bytes(int64_t K, int ncols) {
-    return use_t5(ncols) ? t5_prep_bytes(K) : prep_bytes_for(K, ncols);
+    return use_t4(ncols) ? t4_prep_bytes(K) : use_t5(ncols) ? t5_prep_bytes(K)
+                                                            : prep_bytes_for(K, ncols);
 }
 
 bool matvec_fast_path_ok(const void *w, int64_t K) {

@@ -17,8 +17,9 @@
 namespace q2 {
 namespace {
 
-// Q2_0_NOALLOC_SCRATCH_BYTES (1 MiB): enough for K up to 64,000 at ncols <= 3,
-// 63,488 at ncols = 4 and 31,744 at ncols 5..8 (the scratch grows with K and ncols).
+// Q2_0_NOALLOC_SCRATCH_BYTES (1 MiB): enough for K up to 129,536 at ncols = 1,
+// 64,000 at ncols 2..3, 63,488 at ncols = 4 and 31,744 at ncols 5..8 (the scratch
+// grows with K and ncols).
 constexpr size_t kNoAllocScratchBytes = Q2_0_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) uint8_t g_mv_noalloc_scratch[kNoAllocScratchBytes];

@@ -87,15 +87,26 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t pa
 
 // Wait for the phase with the given parity to complete. Gives up after about
 // one second: records the timeout (tag identifies the wait) and returns false.
+// Between checks the thread backs off for a few tens of nanoseconds, so that a
+// waiting warp takes few issue slots from the warps that share its SM
+// sub-partition while still waking within ~100 cycles; sleep = true suspends
+// in hardware instead (up to a few hundred cycles of wake-up), for waits with
+// slack such as a producer ahead of a deep ring.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kWaitSuspendNs = 20000;
+constexpr uint32_t kWaitBackoffNs = 32;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned long long *err,
-                                          int tag) {
+                                          int tag, bool sleep = false) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait_suspend(bar, parity, kWaitSuspendNs)) return true;
+        if (sleep) {
+            if (mbar_try_wait_suspend(bar, parity, kWaitSuspendNs)) return true;
+        } else {
+            __nanosleep(kWaitBackoffNs);
+            if (mbar_try_wait(bar, parity)) return true;
+        }
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             record_error(err, Q2_0_DEVERR_TIMEOUT, tag);
             return false;
