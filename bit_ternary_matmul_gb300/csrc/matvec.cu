@@ -459,7 +459,8 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
                 const MvJob *J;
                 int tile;
                 item_at(i, J, tile);
-                for (int ch = 0; ch < J->n_chunks; ++ch) {
+                const int nch = J->n_chunks;
+                for (int ch = 0; ch < nch; ++ch) {
                     if (!mbar_wait(&empty[stage], ph ^ 1u, p.err, kTagMvEmpty) ||
                         *(volatile int *)&s_abort) {
                         ok = false;
@@ -606,8 +607,10 @@ __global__ void __launch_bounds__(kCtaThreads, 1)
 //               4-7; warp w owns TMEM lanes 32 (w % 4) .. +31, i.e. those rows);
 //   warp 3      issues the stage's 16 MMAs into one of two TMEM D buffers and
 //               commits them to the expansion (A free) and epilogue (D full)
-//               barriers. The whole warp runs the loop and the elected lane
-//               issues: from a lone lane each MMA cost ~70 cycles to issue;
+//               barriers. The whole warp runs the loop and waits, and the
+//               elected lane issues: from a lone lane each MMA cost ~70 cycles
+//               to issue, and a warp diverged around the waits took ~200 cycles
+//               to reconverge;
 //   warps 12-15 epilogue, one row per thread: D, the row's d values from the
 //               ring and the betas; they release the D buffer and the ring slot.
 // The expansion of a stage waits for the MMAs that last read its A buffer, so
@@ -872,7 +875,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                 item_at(i, J, tile);
                 const uint8_t *img = J->prep + kT5PrepHeader;
                 const uint8_t *beta = img + size_t(J->n_chunks) * kT5ImgBytes;
-                for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+                const int nch = J->n_chunks;
+                for (int ch = 0; ch < nch; ++ch, ++s) {
                     const int st = s % kT5Stages;
                     if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagT5Empty, true) ||
                         *(volatile int *)&s_abort) {
@@ -905,8 +909,9 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         // commits) takes about a stage's worth of time, so two issuers take
         // the even and the odd stages (D buffer = stage parity; consecutive
         // uses of an A buffer are ordered through its expansion). The whole
-        // warp runs the loop (addresses and descriptors stay warp-uniform);
-        // the elected lane waits, issues the MMAs and commits them.
+        // warp runs the loop and waits (addresses and descriptors stay
+        // warp-uniform, and the warp stays converged); the elected lane issues
+        // the MMAs and commits them.
         constexpr uint32_t idesc = idesc_e4m3(kT5Rows, kT5N);
         const bool leader = elect_one();
         const int parity = warp == kT5MmaWarp ? 0 : 1;
@@ -917,17 +922,16 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             const MvJob *J;
             int tile;
             item_at(i, J, tile);
-            for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+            const int nch = J->n_chunks;
+            for (int ch = 0; ch < nch; ++ch, ++s) {
                 if ((s & 1) != parity) continue;
                 const int st = s % kT5Stages;
-                // the leader waits; the other lanes park at the shuffle
-                bool got = true;
-                if (leader)
-                    got = mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
-                          mbar_wait(&a_full[a_buf(s)], a_use(s), p.err, kTagT5AFull) &&
-                          mbar_wait(&d_empty[s & 1], (uint32_t(s >> 1) & 1u) ^ 1u, p.err,
-                                    kTagT5DEmpty) &&
-                          !*(volatile int *)&s_abort;
+                const bool got =
+                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
+                    mbar_wait(&a_full[a_buf(s)], a_use(s), p.err, kTagT5AFull) &&
+                    mbar_wait(&d_empty[s & 1], (uint32_t(s >> 1) & 1u) ^ 1u, p.err,
+                              kTagT5DEmpty) &&
+                    !*(volatile int *)&s_abort;
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     s_abort = 1;
@@ -973,7 +977,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             const MvJob *J;
             int tile;
             item_at(i, J, tile);
-            for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+            const int nch = J->n_chunks;
+            for (int ch = 0; ch < nch; ++ch, ++s) {
                 const int st = s % kT5Stages;
                 const bool got =
                     mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
@@ -1034,7 +1039,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             const MvJob *J;
             int tile;
             item_at(i, J, tile);
-            for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+            const int nch = J->n_chunks;
+            for (int ch = 0; ch < nch; ++ch, ++s) {
                 const int st = s % kT5Stages;
                 const bool got =
                     mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
@@ -1097,7 +1103,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     mbar_arrive(&d_empty[s & 1]);
                     mbar_arrive(&empty[st]);
                 }
-                if (ch == J->n_chunks - 1) {
+                if (ch == nch - 1) {
                     const int *col_shift = reinterpret_cast<const int *>(J->prep);
                     const int r = tile * kT5Rows + row;
                     if (r < J->N)
@@ -1364,7 +1370,8 @@ __global__ void __launch_bounds__(kT4Threads, 1)
                 item_at(i, J, tile);
                 const uint8_t *img = J->prep + kT5PrepHeader;
                 const uint8_t *beta = img + size_t(J->n_chunks) * kT4ImgBytes;
-                for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+                const int nch = J->n_chunks;
+                for (int ch = 0; ch < nch; ++ch, ++s) {
                     const int st = s % kT5Stages;
                     if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagT5Empty, true) ||
                         *(volatile int *)&s_abort) {
@@ -1394,8 +1401,8 @@ __global__ void __launch_bounds__(kT4Threads, 1)
         }
     } else if (warp == kT4MmaWarp || warp == kT4MmaWarp2) {
         // ------------------------------ MMA issuers ------------------------------
-        // even / odd stages; the whole warp runs the loop, the elected lane waits,
-        // issues (one K = 64 MMA per block) and commits
+        // even / odd stages; the whole warp runs the loop and waits (so it stays
+        // converged), the elected lane issues (one K = 64 MMA per block) and commits
         constexpr uint32_t idesc = idesc_mxf4(kT5Rows, kT5N);
         const bool leader = elect_one();
         const int mine = warp == kT4MmaWarp ? 0 : 1;
@@ -1407,16 +1414,16 @@ __global__ void __launch_bounds__(kT4Threads, 1)
             const MvJob *J;
             int tile;
             item_at(i, J, tile);
-            for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+            const int nch = J->n_chunks;
+            for (int ch = 0; ch < nch; ++ch, ++s) {
                 if ((s & 1) != mine) continue;
                 const int st = s % kT5Stages;
-                bool got = true;
-                if (leader)
-                    got = mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
-                          mbar_wait(&a_full[a_buf(s)], a_use(s), p.err, kTagT5AFull) &&
-                          mbar_wait(&d_empty[s & 1], (uint32_t(s >> 1) & 1u) ^ 1u, p.err,
-                                    kTagT5DEmpty) &&
-                          !*(volatile int *)&s_abort;
+                const bool got =
+                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
+                    mbar_wait(&a_full[a_buf(s)], a_use(s), p.err, kTagT5AFull) &&
+                    mbar_wait(&d_empty[s & 1], (uint32_t(s >> 1) & 1u) ^ 1u, p.err,
+                              kTagT5DEmpty) &&
+                    !*(volatile int *)&s_abort;
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     s_abort = 1;
@@ -1464,7 +1471,8 @@ __global__ void __launch_bounds__(kT4Threads, 1)
             const MvJob *J;
             int tile;
             item_at(i, J, tile);
-            for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+            const int nch = J->n_chunks;
+            for (int ch = 0; ch < nch; ++ch, ++s) {
                 const int st = s % kT5Stages;
                 const bool got =
                     mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
@@ -1526,7 +1534,8 @@ __global__ void __launch_bounds__(kT4Threads, 1)
             const MvJob *J;
             int tile;
             item_at(i, J, tile);
-            for (int ch = 0; ch < J->n_chunks; ++ch, ++s) {
+            const int nch = J->n_chunks;
+            for (int ch = 0; ch < nch; ++ch, ++s) {
                 const int st = s % kT5Stages;
                 if (!dead) {
                     const bool got =
@@ -1567,7 +1576,7 @@ __global__ void __launch_bounds__(kT4Threads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&empty[st]);
                 }
-                if (ch == J->n_chunks - 1) {
+                if (ch == nch - 1) {
                     // combine the two halves' row sums (named barrier of the 8 epilogue warps)
                     if (G == 1) s_part[row] = acc;
                     asm volatile("bar.sync 1, %0;" ::"n"(kT4EpiWarps * 32) : "memory");
