@@ -97,6 +97,7 @@ struct MvParams {
     const MvJob *jobs;        // nullptr: the single job passed by value
     const MvItem *items;      // per-CTA work lists (schedule), when jobs != nullptr
     const int *cta_begin;     // [gridDim.x + 1]
+    const int *cta_stages;    // [gridDim.x] stages (512-column chunks) per CTA, plan only
     int ncols;
     int n_stages;             // pipeline depth (n_stages_for(ncols))
     unsigned long long *err;
@@ -150,6 +151,10 @@ __global__ void __launch_bounds__(kPrepThreads) mv_prep_kernel(
     // The mat-vec kernel that follows may start its prologue (barrier set-up,
     // weight loads) now; it waits for this grid before reading the fragments.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Launched as a programmatic dependent of the kernel before it on the stream
+    // (a mat-vec that may still read this buffer, or the producer of x): wait
+    // for that grid before reading x or writing the prep buffer.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const MvPrepJob &J = jobs ? jobs[blockIdx.y] : single;
     const int K = J.K;
     const int j = blockIdx.x;  // activation column
@@ -403,6 +408,9 @@ constexpr int kCtaThreads = (kConsumerWarps + 1) * 32;
 template <int NT>
 __global__ void __launch_bounds__(kCtaThreads, 1)
     mv_tc_kernel(const __grid_constant__ MvJob single, const MvParams p) {
+    // The next prep launch on the stream may become resident now; it waits for
+    // this grid before it touches any buffer this kernel reads.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int kCW = kConsumerWarps;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int kStages = p.n_stages;
@@ -681,6 +689,10 @@ template <typename XT>
 __global__ void __launch_bounds__(kT5PrepThreads) t5_prep_kernel(
     const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs, int ncols) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Launched as a programmatic dependent of the kernel before it on the stream
+    // (a mat-vec that may still read this buffer, or the producer of x): wait
+    // for that grid before reading x or writing the prep buffer.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const MvPrepJob &J = jobs ? jobs[blockIdx.y] : single;
     const int K = J.K;
     const int j = blockIdx.x;
@@ -793,6 +805,9 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n) {
 template <int NC>
 __global__ void __launch_bounds__(kT5Threads, 1)
     mv_t5_kernel(const __grid_constant__ MvJob single, const MvParams p) {
+    // The next prep launch on the stream may become resident now; it waits for
+    // this grid before it touches any buffer this kernel reads.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int kABufs = t5_abufs(NC);
     constexpr int kDCols = t5_dcols(NC);
     extern __shared__ uint8_t smem_raw[];
@@ -1153,9 +1168,13 @@ constexpr int kT4BetaBytes = kChunkBlocks * 4;         // beta[8 blocks] f32
 constexpr int kT4ABufs = 3;
 constexpr int kT4ACol = 256;                           // A buffers at 256 + 64 i
 constexpr int kT4ScaleCol = 448;                       // scales A 448..451, B 452..455
+// mbarriers: full / empty per stage, a_full / a_empty per A buffer, d_full /
+// d_empty per D buffer, a drain per MMA issuer, part_full / part_empty per
+// tile-end buffer
+constexpr int kT4Barriers = 2 * kT5Stages + 2 * kT4ABufs + 2 * 2 + 2 + 2 * 2;
 constexpr int kT4Smem = 1024 /* alignment slack */ +
                         kT5Stages * (kT4ImgBytes + kT5RawBytes + kT4BetaBytes) +
-                        (2 * kT5Stages + 2 * kT5MaxABufs + 8) * 8;
+                        kT4Barriers * 8;
 
 size_t t4_prep_bytes(int64_t K) {
     const size_t n_chunks = size_t(K / 512);
@@ -1177,6 +1196,10 @@ template <typename XT>
 __global__ void __launch_bounds__(kT5PrepThreads) t4_prep_kernel(
     const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Launched as a programmatic dependent of the kernel before it on the stream
+    // (a mat-vec that may still read this buffer, or the producer of x): wait
+    // for that grid before reading x or writing the prep buffer.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const MvPrepJob &J = jobs ? jobs[blockIdx.y] : single;
     const int K = J.K;
     const XT *xj = static_cast<const XT *>(J.x);
@@ -1271,6 +1294,19 @@ __global__ void __launch_bounds__(kT5PrepThreads) t4_prep_kernel(
     }
 }
 
+// Where the epilogue writes the tile a ring stage belongs to; the producer fills
+// one per slot before the slot's barrier arrive.
+struct T4StageMeta {
+    float *y;
+    const int *col_shift;  // the job's column shift (written by the prep kernel)
+    int row0;              // first row of the tile
+    int n_rows;            // rows of the matrix
+    int flags;             // kT4FirstOfTile | kT4LastOfTile
+    int pad;
+};
+constexpr int kT4FirstOfTile = 1;
+constexpr int kT4LastOfTile = 2;
+
 // Warp roles of the fp4 kernel. A warp reaches only the TMEM lanes of its
 // quarter (warp % 4, which is also its SM sub-partition):
 //   warp 2       producer;
@@ -1288,6 +1324,9 @@ constexpr int kT4Threads = 16 * 32;
 
 __global__ void __launch_bounds__(kT4Threads, 1)
     mv_t4_kernel(const __grid_constant__ MvJob single, const MvParams p) {
+    // The next prep launch on the stream may become resident now; it waits for
+    // this grid before it touches any buffer this kernel reads.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
@@ -1300,10 +1339,15 @@ __global__ void __launch_bounds__(kT4Threads, 1)
     uint64_t *a_empty = a_full + kT5MaxABufs;
     uint64_t *d_full = a_empty + kT5MaxABufs;
     uint64_t *d_empty = d_full + 2;
-    uint64_t *drain = d_empty + 2;  // [2] one per MMA issuer: its final commit
+    uint64_t *drain = d_empty + 2;      // [2] one per MMA issuer: its final commit
+    uint64_t *part_full = drain + 2;    // [2] tile-end row sums of the epilogue half G = 1
+    uint64_t *part_empty = part_full + 2;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
-    __shared__ float s_part[kT5Rows];  // the second epilogue half's row sums at a tile end
+    __shared__ float s_part[2][kT5Rows];  // the epilogue half G = 1's row sums at a tile end
+    // per ring slot, written by the producer before the slot's barrier arrive:
+    // where the epilogue writes the tile that the stage belongs to
+    __shared__ T4StageMeta s_meta[kT5Stages];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1321,7 +1365,11 @@ __global__ void __launch_bounds__(kT4Threads, 1)
             mbar_init(&d_full[i], 1);
             mbar_init(&d_empty[i], kT4EpiWarps);
         }
-        for (int i = 0; i < 2; ++i) mbar_init(&drain[i], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&drain[i], 1);
+            mbar_init(&part_full[i], kT4EpiWarps / 2);
+            mbar_init(&part_empty[i], kT4EpiWarps / 2);
+        }
         s_abort = 0;
         fence_barrier_init();
     }
@@ -1353,6 +1401,8 @@ __global__ void __launch_bounds__(kT4Threads, 1)
             tile = int(blockIdx.x) + i * int(gridDim.x);
         }
     };
+    // stages of this CTA (every role but the producer runs a flat stage loop)
+    const int n_stages = p.jobs ? p.cta_stages[blockIdx.x] : n_items * single.n_chunks;
     auto stage_parity = [](int s) { return uint32_t(s / kT5Stages) & 1u; };
     auto a_buf = [](int s) { return s % kT4ABufs; };
     auto a_use = [](int s) { return uint32_t(s / kT4ABufs) & 1u; };
@@ -1379,6 +1429,12 @@ __global__ void __launch_bounds__(kT4Threads, 1)
                         s_abort = 1;
                         break;
                     }
+                    T4StageMeta &m = s_meta[st];
+                    m.y = J->y;
+                    m.col_shift = reinterpret_cast<const int *>(J->prep);
+                    m.row0 = tile * kT5Rows;
+                    m.n_rows = J->N;
+                    m.flags = (ch == 0 ? kT4FirstOfTile : 0) | (ch == nch - 1 ? kT4LastOfTile : 0);
                     mbar_arrive_expect_tx(&full[st], kT5RawBytes + kT4ImgBytes + kT4BetaBytes);
                     tma_load_2d(raw_ring + st * kT5RawBytes, &J->tmap, ch * kChunkBytes,
                                 tile * kT5Rows, &full[st]);
@@ -1408,15 +1464,9 @@ __global__ void __launch_bounds__(kT4Threads, 1)
         const int mine = warp == kT4MmaWarp ? 0 : 1;
         const uint64_t desc0 = sw128_desc(smem_addr(img_ring));
         const uint32_t sfa = tmem + kT4ScaleCol, sfb = tmem + kT4ScaleCol + 4;
-        int s = 0, last = -1;
-        bool ok = true;
-        for (int i = 0; i < n_items && ok; ++i) {
-            const MvJob *J;
-            int tile;
-            item_at(i, J, tile);
-            const int nch = J->n_chunks;
-            for (int ch = 0; ch < nch; ++ch, ++s) {
-                if ((s & 1) != mine) continue;
+        int last = -1;
+        {
+            for (int s = mine; s < n_stages; s += 2) {
                 const int st = s % kT5Stages;
                 const bool got =
                     mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
@@ -1425,7 +1475,6 @@ __global__ void __launch_bounds__(kT4Threads, 1)
                               kTagT5DEmpty) &&
                     !*(volatile int *)&s_abort;
                 if (!__all_sync(0xffffffffu, got)) {
-                    ok = false;
                     s_abort = 1;
                     break;
                 }
@@ -1465,14 +1514,8 @@ __global__ void __launch_bounds__(kT4Threads, 1)
             tmem_st4(tmem + lane_base + kT4ScaleCol, one, one, one, one);
             tmem_st4(tmem + lane_base + kT4ScaleCol + 4, one, one, one, one);
         }
-        int s = 0;
-        bool ok = true;
-        for (int i = 0; i < n_items && ok; ++i) {
-            const MvJob *J;
-            int tile;
-            item_at(i, J, tile);
-            const int nch = J->n_chunks;
-            for (int ch = 0; ch < nch; ++ch, ++s) {
+        {
+            for (int s = 0; s < n_stages; ++s) {
                 const int st = s % kT5Stages;
                 const bool got =
                     mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
@@ -1480,7 +1523,6 @@ __global__ void __launch_bounds__(kT4Threads, 1)
                     !*(volatile int *)&s_abort;
                 if (!__all_sync(0xffffffffu, got)) {
                     s_abort = 1;
-                    ok = false;
                     break;
                 }
                 tc_fence_after();
@@ -1518,76 +1560,79 @@ __global__ void __launch_bounds__(kT4Threads, 1)
         }
     } else if (warp >= kT4EpiWarp0 && warp < kT4EpiWarp0 + kT4EpiWarps) {
         // ------------------------------ epilogue ------------------------------
-        // warp w: TMEM lane quarter w % 4, blocks 4G .. 4G+3 of each stage. A warp
-        // whose wait fails (or that sees the abort flag) turns dead: it skips all
-        // TMEM and barrier-wait work but still takes part in the tile-end named
-        // barriers, which every epilogue warp meets the same number of times.
+        // warp w: TMEM lane quarter w % 4, blocks 4G .. 4G+3 of each stage. At a
+        // tile end the half G = 1 hands its row sums to G = 0 through a
+        // double-buffered shared array (part_full / part_empty), and G = 0
+        // writes y. Every wait is bounded; a warp whose wait fails leaves the loop.
         grid_dependency_wait();  // reads the column shift written by prep
         const int G = (warp - kT4EpiWarp0) >> 2;
         const int qd = warp & 3;
         const int row = 32 * qd + lane;
         const uint32_t lane_base = uint32_t(32 * qd) << 16;
         float acc = 0.0f;
-        bool dead = false;
-        int s = 0;
-        for (int i = 0; i < n_items; ++i) {
-            const MvJob *J;
-            int tile;
-            item_at(i, J, tile);
-            const int nch = J->n_chunks;
-            for (int ch = 0; ch < nch; ++ch, ++s) {
-                const int st = s % kT5Stages;
-                if (!dead) {
-                    const bool got =
-                        !*(volatile int *)&s_abort &&
-                        mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
-                        mbar_wait(&d_full[s & 1], uint32_t(s >> 1) & 1u, p.err, kTagT5DFull);
-                    if (!__all_sync(0xffffffffu, got)) {
+        int shift = 0, tiles = 0;
+        for (int s = 0; s < n_stages; ++s) {
+            const int st = s % kT5Stages;
+            const bool got = !*(volatile int *)&s_abort &&
+                             mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
+                             mbar_wait(&d_full[s & 1], uint32_t(s >> 1) & 1u, p.err, kTagT5DFull);
+            if (!__all_sync(0xffffffffu, got)) {
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const T4StageMeta m = s_meta[st];  // the slot is rewritten once empty[st] completes
+            // the tile's column shift, loaded early: it is first used at the tile end
+            if (G == 0 && (m.flags & kT4FirstOfTile)) shift = *m.col_shift;
+            const uint32_t d_base = tmem + lane_base + d_col(s) + 4 * G * kT5N;
+            uint32_t r[4][16];
+#pragma unroll
+            for (int bi = 0; bi < 4; ++bi) tmem_ld16(d_base + bi * kT5N, r[bi]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&d_empty[s & 1]);  // D is in registers
+            const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes;
+            const float *bt = reinterpret_cast<const float *>(beta_ring + st * kT4BetaBytes);
+#pragma unroll
+            for (int bi = 0; bi < 4; ++bi) {
+                const int b = 4 * G + bi;
+                float t = __uint_as_float(r[bi][kT4Pieces - 1]) *
+                          __int_as_float((127 - 2 * (kT4Pieces - 1)) << 23);
+#pragma unroll
+                for (int pp = kT4Pieces - 2; pp >= 1; --pp)
+                    t = fmaf(__uint_as_float(r[bi][pp]), __int_as_float((127 - 2 * pp) << 23), t);
+                t = t + __uint_as_float(r[bi][0]);
+                const float d = lds_half_as_float(rp + 18 * b);
+                acc = fmaf(d, t - bt[b], acc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+            if (m.flags & kT4LastOfTile) {
+                const int buf = tiles & 1;
+                const uint32_t use = uint32_t(tiles >> 1) & 1u;
+                if (G == 1) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(&part_empty[buf], use ^ 1u, p.err,
+                                                           kTagT5DEmpty))) {
                         s_abort = 1;
-                        dead = true;
+                        break;
                     }
-                }
-                if (!dead) {
-                    tc_fence_after();
-                    const uint32_t d_base = tmem + lane_base + d_col(s) + 4 * G * kT5N;
-                    uint32_t r[4][16];
-#pragma unroll
-                    for (int bi = 0; bi < 4; ++bi) tmem_ld16(d_base + bi * kT5N, r[bi]);
-                    tmem_wait_ld();
-                    tc_fence_before();
+                    s_part[buf][row] = acc;
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&d_empty[s & 1]);  // D is in registers
-                    const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes;
-                    const float *bt =
-                        reinterpret_cast<const float *>(beta_ring + st * kT4BetaBytes);
-#pragma unroll
-                    for (int bi = 0; bi < 4; ++bi) {
-                        const int b = 4 * G + bi;
-                        float t = __uint_as_float(r[bi][kT4Pieces - 1]) *
-                                  __int_as_float((127 - 2 * (kT4Pieces - 1)) << 23);
-#pragma unroll
-                        for (int pp = kT4Pieces - 2; pp >= 1; --pp)
-                            t = fmaf(__uint_as_float(r[bi][pp]),
-                                     __int_as_float((127 - 2 * pp) << 23), t);
-                        t = t + __uint_as_float(r[bi][0]);
-                        const float d = lds_half_as_float(rp + 18 * b);
-                        acc = fmaf(d, t - bt[b], acc);
+                    if (lane == 0) mbar_arrive(&part_full[buf]);
+                } else {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(&part_full[buf], use, p.err, kTagT5DFull))) {
+                        s_abort = 1;
+                        break;
                     }
+                    const int rr = m.row0 + row;
+                    if (rr < m.n_rows) m.y[rr] = mul_pow2(acc + s_part[buf][row], -shift);
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[st]);
+                    if (lane == 0) mbar_arrive(&part_empty[buf]);
                 }
-                if (ch == nch - 1) {
-                    // combine the two halves' row sums (named barrier of the 8 epilogue warps)
-                    if (G == 1) s_part[row] = acc;
-                    asm volatile("bar.sync 1, %0;" ::"n"(kT4EpiWarps * 32) : "memory");
-                    if (G == 0 && !dead) {
-                        const int *col_shift = reinterpret_cast<const int *>(J->prep);
-                        const int rr = tile * kT5Rows + row;
-                        if (rr < J->N) J->y[rr] = mul_pow2(acc + s_part[row], -col_shift[0]);
-                    }
-                    asm volatile("bar.sync 1, %0;" ::"n"(kT4EpiWarps * 32) : "memory");
-                    acc = 0.0f;
-                }
+                acc = 0.0f;
+                ++tiles;
             }
         }
     }
@@ -1721,22 +1766,36 @@ bool make_job(MvJob &J, const uint8_t *w, const uint8_t *prep, float *y, int64_t
 
 // max_k: the largest K among the jobs (sets the t5 prep's grid z).
 template <typename XT>
+// The prep kernels are launched as programmatic dependents of whatever precedes
+// them on the stream: their launch overlaps that kernel's tail, and they wait
+// for it (griddepcontrol.wait) before reading x or writing their buffers.
 cudaError_t launch_prep_t(const MvPrepJob &single, const MvPrepJob *jobs, int n_jobs, int ncols,
                           int64_t max_k, cudaStream_t s) {
-    dim3 grid(ncols, n_jobs);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(ncols, n_jobs);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (use_t4(ncols)) {
         const int64_t items = max_k / 64 * 8;
-        grid.z = unsigned(std::min<int64_t>((items + kT5PrepThreads - 1) / kT5PrepThreads, 65535));
-        t4_prep_kernel<XT><<<grid, kT5PrepThreads, 0, s>>>(single, jobs);
-    } else if (use_t5(ncols)) {
+        cfg.gridDim.z =
+            unsigned(std::min<int64_t>((items + kT5PrepThreads - 1) / kT5PrepThreads, 65535));
+        cfg.blockDim = dim3(kT5PrepThreads);
+        return cudaLaunchKernelEx(&cfg, t4_prep_kernel<XT>, single, jobs);
+    }
+    if (use_t5(ncols)) {
         const int64_t items = max_k / 64 * 16;
-        grid.z = unsigned(std::min<int64_t>((items + kT5PrepThreads - 1) / kT5PrepThreads, 65535));
-        t5_prep_kernel<XT><<<grid, kT5PrepThreads, 0, s>>>(single, jobs, ncols);
-    } else if (n_tiles_for(ncols) == 1)
-        mv_prep_kernel<1, XT><<<grid, kPrepThreads, 0, s>>>(single, jobs, ncols);
-    else
-        mv_prep_kernel<2, XT><<<grid, kPrepThreads, 0, s>>>(single, jobs, ncols);
-    return cudaGetLastError();
+        cfg.gridDim.z =
+            unsigned(std::min<int64_t>((items + kT5PrepThreads - 1) / kT5PrepThreads, 65535));
+        cfg.blockDim = dim3(kT5PrepThreads);
+        return cudaLaunchKernelEx(&cfg, t5_prep_kernel<XT>, single, jobs, ncols);
+    }
+    cfg.blockDim = dim3(kPrepThreads);
+    if (n_tiles_for(ncols) == 1) return cudaLaunchKernelEx(&cfg, mv_prep_kernel<1, XT>, single, jobs, ncols);
+    return cudaLaunchKernelEx(&cfg, mv_prep_kernel<2, XT>, single, jobs, ncols);
 }
 
 cudaError_t launch_prep(const MvPrepJob &single, const MvPrepJob *jobs, int n_jobs, int ncols,
@@ -1824,7 +1883,7 @@ int matvec_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, 
     if (e != cudaSuccess) return Q2_0_ECUDA;
     MvJob J;
     if (!make_job(J, w, prep, y, N, K, tile_rows_for(ncols))) return Q2_0_ECUDA;
-    MvParams prm{nullptr, nullptr, nullptr, ncols, n_stages_for(ncols), err};
+    MvParams prm{nullptr, nullptr, nullptr, nullptr, ncols, n_stages_for(ncols), err};
     const int grid = std::max(1, std::min(J.n_tiles, sm_count()));
     return cuda_status(launch_tc(J, prm, grid, s));
 }
@@ -1843,6 +1902,7 @@ struct q2_0_mv_plan {
     q2::MvJob *d_jobs = nullptr;
     q2::MvItem *d_items = nullptr;
     int *d_cta_begin = nullptr;
+    int *d_cta_stages = nullptr;  // [grid] stages (512-column chunks) per CTA
     q2::MvPrepJob *d_prep_jobs = nullptr;
     uint8_t *d_prep = nullptr;
     unsigned long long *err = nullptr;
@@ -1859,6 +1919,7 @@ void mv_plan_destroy(q2_0_mv_plan *plan) {
     cudaFree(plan->d_jobs);
     cudaFree(plan->d_items);
     cudaFree(plan->d_cta_begin);
+    cudaFree(plan->d_cta_stages);
     cudaFree(plan->d_prep_jobs);
     cudaFree(plan->d_prep);
     cudaSetDevice(cur);
@@ -1902,37 +1963,74 @@ int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **o
             pjobs[j] = MvPrepJob{d.x, P->d_prep + off[j], int(d.K)};
             P->max_k = std::max<int64_t>(P->max_k, d.K);
         }
-        // Longest-processing-time-first schedule of (job, tile) items over one CTA
-        // per SM; cost of an item = rows in the tile x K.
+        // Schedule of (job, tile) items over one CTA per SM. A tile costs its
+        // stage count (K / 512): the pipeline takes the same time per stage
+        // whatever the tile's valid rows. Longest-processing-time-first, then
+        // moves and swaps between the most and the least loaded CTA while they
+        // lower the larger of the two loads; each CTA then takes its items in
+        // (job, tile) order, so consecutive items share a tensor map and
+        // activation images.
         std::vector<MvItem> items;
-        std::vector<double> cost;
+        std::vector<int> cost;
         for (int j = 0; j < P->n_fast; ++j)
             for (int t = 0; t < jobs[j].n_tiles; ++t) {
                 items.push_back(MvItem{j, t});
-                const int tr = tile_rows_for(ncols);
-                const int rows = std::min(tr, jobs[j].N - t * tr);
-                cost.push_back(double(rows) * jobs[j].nb);
+                cost.push_back(jobs[j].n_chunks);
             }
         std::vector<int> order(items.size());
         for (size_t k = 0; k < order.size(); ++k) order[k] = int(k);
         std::stable_sort(order.begin(), order.end(),
                          [&](int a, int b) { return cost[a] > cost[b]; });
         const int grid = std::max(1, std::min<int>(sm_count(), int(items.size())));
-        using Load = std::pair<double, int>;
+        using Load = std::pair<int64_t, int>;
         std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-        for (int c = 0; c < grid; ++c) heap.push(Load(0.0, c));
-        std::vector<std::vector<MvItem>> per_cta(grid);
+        for (int c = 0; c < grid; ++c) heap.push(Load(0, c));
+        std::vector<std::vector<int>> per_cta(grid);  // item indices
+        std::vector<int64_t> load(grid, 0);
         for (int k : order) {
             Load l = heap.top();
             heap.pop();
-            per_cta[l.second].push_back(items[k]);
-            heap.push(Load(l.first + cost[k], l.second));
+            per_cta[l.second].push_back(k);
+            load[l.second] += cost[k];
+            heap.push(Load(load[l.second], l.second));
+        }
+        for (int iter = 0; iter < 4 * int(items.size()) && grid > 1; ++iter) {
+            const int hi = int(std::max_element(load.begin(), load.end()) - load.begin());
+            const int lo = int(std::min_element(load.begin(), load.end()) - load.begin());
+            const int64_t gap = load[hi] - load[lo];
+            // moving cost d from hi to lo lowers the larger of the two loads by
+            // min(d, gap - d): take the move or swap that lowers it most
+            int64_t best = 0, gain = 0;
+            int bi = -1, bj = -1;
+            for (int a = 0; a < int(per_cta[hi].size()); ++a) {
+                const int64_t ca = cost[per_cta[hi][a]];
+                if (std::min(ca, gap - ca) > gain) { gain = std::min(ca, gap - ca); best = ca; bi = a; bj = -1; }
+                for (int b = 0; b < int(per_cta[lo].size()); ++b) {
+                    const int64_t d = ca - cost[per_cta[lo][b]];
+                    if (std::min(d, gap - d) > gain) { gain = std::min(d, gap - d); best = d; bi = a; bj = b; }
+                }
+            }
+            if (bi < 0) break;
+            const int ka = per_cta[hi][bi];
+            per_cta[hi].erase(per_cta[hi].begin() + bi);
+            per_cta[lo].push_back(ka);
+            if (bj >= 0) {
+                const int kb = per_cta[lo][bj];
+                per_cta[lo].erase(per_cta[lo].begin() + bj);
+                per_cta[hi].push_back(kb);
+            }
+            load[hi] -= best;
+            load[lo] += best;
         }
         std::vector<MvItem> flat;
-        std::vector<int> begin(grid + 1, 0);
+        std::vector<int> begin(grid + 1, 0), stages(grid, 0);
         for (int c = 0; c < grid; ++c) {
+            std::sort(per_cta[c].begin(), per_cta[c].end());  // items are built in (job, tile) order
             begin[c] = int(flat.size());
-            flat.insert(flat.end(), per_cta[c].begin(), per_cta[c].end());
+            for (int k : per_cta[c]) {
+                flat.push_back(items[k]);
+                stages[c] += jobs[items[k].job].n_chunks;
+            }
         }
         begin[grid] = int(flat.size());
         P->grid = grid;
@@ -1940,6 +2038,7 @@ int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **o
             (cudaMalloc(&P->d_jobs, sizeof(MvJob) * jobs.size()) != cudaSuccess ||
              cudaMalloc(&P->d_items, sizeof(MvItem) * flat.size()) != cudaSuccess ||
              cudaMalloc(&P->d_cta_begin, sizeof(int) * begin.size()) != cudaSuccess ||
+             cudaMalloc(&P->d_cta_stages, sizeof(int) * stages.size()) != cudaSuccess ||
              cudaMalloc(&P->d_prep_jobs, sizeof(MvPrepJob) * pjobs.size()) != cudaSuccess))
             st = Q2_0_ECUDA;
         if (st == Q2_0_OK &&
@@ -1948,6 +2047,8 @@ int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **o
              cudaMemcpy(P->d_items, flat.data(), sizeof(MvItem) * flat.size(),
                         cudaMemcpyHostToDevice) != cudaSuccess ||
              cudaMemcpy(P->d_cta_begin, begin.data(), sizeof(int) * begin.size(),
+                        cudaMemcpyHostToDevice) != cudaSuccess ||
+             cudaMemcpy(P->d_cta_stages, stages.data(), sizeof(int) * stages.size(),
                         cudaMemcpyHostToDevice) != cudaSuccess ||
              cudaMemcpy(P->d_prep_jobs, pjobs.data(), sizeof(MvPrepJob) * pjobs.size(),
                         cudaMemcpyHostToDevice) != cudaSuccess))
@@ -1975,7 +2076,8 @@ int mv_plan_execute(const q2_0_mv_plan *P, cudaStream_t s) {
             return Q2_0_ECUDA;
         MvJob dummy;
         std::memset(&dummy, 0, sizeof(dummy));
-        MvParams prm{P->d_jobs, P->d_items, P->d_cta_begin, P->ncols, n_stages_for(P->ncols),
+        MvParams prm{P->d_jobs, P->d_items, P->d_cta_begin, P->d_cta_stages, P->ncols,
+                     n_stages_for(P->ncols),
                      P->err};
         if (launch_tc(dummy, prm, P->grid, s) != cudaSuccess) return Q2_0_ECUDA;
     }
