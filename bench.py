@@ -382,7 +382,7 @@ def run_ours(args):
 
     extras = None
     if args.only == "all" and not args.no_extras:
-        extras = measure_extras(torch, q, stream, dev)
+        extras = measure_extras(torch, q, stream, dev, peaks["hbm_gbs"])
 
     code, info = q.q2_0_get_error(stream)
     if code != 0:
@@ -442,14 +442,20 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def measure_extras(torch, q, stream, dev, reps: int = 20):
+def measure_extras(torch, q, stream, dev, hbm_peak: float, reps: int = 20):
     """Side measurements outside the step, each a CUDA-graph replay timed with
     events on the launching stream:
       - the 151936 x 4096 output-head mat-vec (ncols 1), with F32 and with F16
         activations (175 MB of packed weights, above L2);
       - the M = 512 prefill GEMMs with F16 activations (q2_0_mul_mat_f16);
       - the group-128 packing of the head-sized matrix: exact repack to the
-        64-weight layout (bytes read + written) and the direct mat-vec.
+        64-weight layout (bytes read + written) and the direct mat-vec;
+      - the 8B-class decode step (253 matrices with the 151936 x 4096 head,
+        2,128,527,360 packed bytes, ncols 1) as one plan;
+      - the 8B-class prefill GEMMs at M = 2048 (4096x4096, 12288x4096,
+        4096x12288), split fp16 hi+lo.
+    The 8B-class weights and activations are drawn on the device
+    (synth.packed_matrix_device: the decode-step distribution, other bytes).
     Returns the GB/s and TFLOP/s figures."""
     g = synth.rng(SEED + 7)
     N, K = VOCAB, 4096
@@ -505,7 +511,54 @@ def measure_extras(torch, q, stream, dev, reps: int = 20):
     ms_rp = timed(lambda: q.q2_0_g128_to_g64(w128, N, K, dst=w64, stream=stream))
     ms_g = timed(lambda: q.q2_0_g128_mul_mat_vec(w128, x, N, K, 1, y=y, stream=stream))
     rp_bytes = w128.numel() + w64.numel()
+    g128_bytes = w128.numel()
+    del w128, w64
+
+    # 8B-class decode step, one plan over its 253 matrices
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(SEED + 8)
+    ents8 = []
+    for _, m in synth.decode_step_8b(with_head=True):
+        w8 = synth.packed_matrix_device(torch, gen, m.N, m.K, *synth.DECODE_SCALE,
+                                        synth.DECODE_FRAC_CODE3, dev)
+        x8 = torch.randn((1, m.K), generator=gen, device=dev)
+        ents8.append((w8, x8, torch.empty((1, m.N), dtype=torch.float32, device=dev), m.N, m.K))
+    bytes8 = sum(e[0].numel() for e in ents8)
+    plan8 = q.MvPlan(ents8, 1)
+    ms8 = timed(lambda: plan8.execute(stream))
+    plan8.close()
+    del ents8
+
+    # 8B-class prefill GEMMs at M = 2048
+    M2 = 2048
+    g2 = []
+    for Ng, Kg in [(4096, 4096), (12288, 4096), (4096, 12288)]:
+        wg = synth.packed_matrix_device(torch, gen, Ng, Kg, *synth.DECODE_SCALE,
+                                        synth.DECODE_FRAC_CODE3, dev)
+        xg = torch.randn((M2, Kg), generator=gen, device=dev)
+        out = torch.rand((M2, Kg), generator=gen, device=dev) < synth.PREFILL_OUTLIER_FRAC
+        sign = torch.where(torch.rand((M2, Kg), generator=gen, device=dev) < 0.5, -1.0, 1.0)
+        xg = torch.where(out, sign * synth.PREFILL_OUTLIER, xg)
+        ws = torch.empty(q.q2_0_mul_mat_workspace_size(M2, Ng, Kg, q.Q2_0_PREC_F16_SPLIT),
+                         dtype=torch.uint8, device=dev)
+        g2.append((wg, xg, torch.empty((M2, Ng), dtype=torch.float32, device=dev), Ng, Kg, ws))
+    flops2 = sum(2.0 * M2 * Ng * Kg for _, _, _, Ng, Kg, _ in g2)
+
+    def gemms2():
+        for wg, xg, yg, Ng, Kg, ws in g2:
+            q.q2_0_mul_mat(wg, xg, Ng, Kg, M2, prec=q.Q2_0_PREC_F16_SPLIT, y=yg, workspace=ws,
+                           stream=stream)
+
+    ms2 = timed(gemms2)
+    del g2
     return {
+        "decode_8b_step_ncols1": {"bytes": bytes8, "us": round(ms8 * 1e3, 2),
+                                  "gbs": round(bytes8 / (ms8 * 1e-3) / 1e9, 1),
+                                  "hbm_frac": round(bytes8 / (ms8 * 1e-3) / 1e9 / hbm_peak, 4),
+                                  "matrices": 253},
+        "gemm_split_m2048_8b": {"tflops": round(flops2 / (ms2 * 1e-3) / 1e12, 2),
+                                "us": round(ms2 * 1e3, 2),
+                                "shapes": [[M2, 4096, 4096], [M2, 12288, 4096], [M2, 4096, 12288]]},
         "head_matvec_151936x4096": {"bytes": head_bytes,
                                     "f32_gbs": round(head_bytes / (ms32 * 1e-3) / 1e9, 1),
                                     "f16_gbs": round(head_bytes / (ms16 * 1e-3) / 1e9, 1),
@@ -515,7 +568,7 @@ def measure_extras(torch, q, stream, dev, reps: int = 20):
                           "shapes": gemm_shapes},
         "g128_151936x4096": {"repack_gbs": round(rp_bytes / (ms_rp * 1e-3) / 1e9, 1),
                              "repack_bytes": rp_bytes,
-                             "direct_matvec_gbs": round(w128.numel() / (ms_g * 1e-3) / 1e9, 1),
+                             "direct_matvec_gbs": round(g128_bytes / (ms_g * 1e-3) / 1e9, 1),
                              "direct_matvec_us": round(ms_g * 1e3, 2)},
         "timing": "CUDA-graph replay, CUDA events on the launching stream, outside the step",
     }

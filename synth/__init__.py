@@ -64,6 +64,30 @@ def packed_matrix(g: np.random.Generator, N: int, K: int, scale_lo: float, scale
     return out.reshape(-1)
 
 
+def packed_matrix_device(torch, gen, N: int, K: int, scale_lo: float, scale_hi: float,
+                         frac_code3: float, device):
+    """The recipe of ``packed_matrix`` drawn on the GPU with a seeded
+    ``torch.Generator`` (for timing large workloads whose host generation would
+    take minutes; the bytes differ from the host stream, the distribution is the
+    same). Returns a uint8 device tensor of N * K/64 * 18 bytes."""
+    assert K % BLOCK_WEIGHTS == 0
+    nb = N * (K // BLOCK_WEIGHTS)
+    table = torch.from_numpy(_TERNARY_BYTES).to(device)
+    d = (torch.rand(nb, generator=gen, device=device) * (scale_hi - scale_lo) + scale_lo).half()
+    codes = table[torch.randint(0, 81, (nb, 16), generator=gen, device=device)]
+    if frac_code3 > 0.0:
+        field = torch.randint(0, 4, (nb, 16), generator=gen, device=device, dtype=torch.uint8)
+        hit = torch.rand((nb, 16), generator=gen, device=device) < 4.0 * frac_code3
+        # each code byte carries four fields: hitting a byte with probability 4f
+        # and one field in it sets a fraction f of all fields to 3
+        codes = torch.where(hit, codes | (torch.tensor(3, dtype=torch.uint8, device=device)
+                                          << (2 * field)), codes)
+    out = torch.empty((nb, BLOCK_BYTES), dtype=torch.uint8, device=device)
+    out[:, 0:2] = d.view(torch.uint8).view(nb, 2)
+    out[:, 2:] = codes
+    return out.reshape(-1)
+
+
 def packed_matrix_g128(g: np.random.Generator, N: int, K: int, scale_lo: float,
                        scale_hi: float) -> np.ndarray:
     """Raw bytes of an N x K matrix in the group-128 packing: N * K/128 blocks of
