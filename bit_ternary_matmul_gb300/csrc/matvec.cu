@@ -1169,9 +1169,8 @@ constexpr int kT4ABufs = 3;
 constexpr int kT4ACol = 256;                           // A buffers at 256 + 64 i
 constexpr int kT4ScaleCol = 448;                       // scales A 448..451, B 452..455
 // mbarriers: full / empty per stage, a_full / a_empty per A buffer, d_full /
-// d_empty per D buffer, a drain per MMA issuer, part_full / part_empty per
-// tile-end buffer
-constexpr int kT4Barriers = 2 * kT5Stages + 2 * kT4ABufs + 2 * 2 + 2 + 2 * 2;
+// d_empty per D buffer, a drain per MMA issuer
+constexpr int kT4Barriers = 2 * kT5Stages + 2 * kT4ABufs + 2 * 2 + 2;
 constexpr int kT4Smem = 1024 /* alignment slack */ +
                         kT5Stages * (kT4ImgBytes + kT5RawBytes + kT4BetaBytes) +
                         kT4Barriers * 8;
@@ -1312,15 +1311,17 @@ constexpr int kT4LastOfTile = 2;
 //   warp 2       producer;
 //   warps 3, 1   MMA issuers of the even / odd stages (warp 3 allocates TMEM);
 //   warps 4-7    expansion, one per lane quarter, all 8 blocks of a stage;
-//   warps 8-15   epilogue, two per quarter (blocks 4G .. 4G+3).
+//   warps 8-11   epilogue, one per lane quarter, all 8 blocks of a stage.
+// Measured: more warps per sub-partition (two expansion or two epilogue warps
+// per quarter) lengthened the stage period; 12 warps gave the shortest.
 constexpr int kT4ProdWarp = 2;
 constexpr int kT4MmaWarp = 3;
 constexpr int kT4MmaWarp2 = 1;
 constexpr int kT4ExpWarp0 = 4;
 constexpr int kT4ExpWarps = 4;
 constexpr int kT4EpiWarp0 = 8;
-constexpr int kT4EpiWarps = 8;
-constexpr int kT4Threads = 16 * 32;
+constexpr int kT4EpiWarps = 4;
+constexpr int kT4Threads = 12 * 32;
 
 __global__ void __launch_bounds__(kT4Threads, 1)
     mv_t4_kernel(const __grid_constant__ MvJob single, const MvParams p) {
@@ -1339,12 +1340,9 @@ __global__ void __launch_bounds__(kT4Threads, 1)
     uint64_t *a_empty = a_full + kT5MaxABufs;
     uint64_t *d_full = a_empty + kT5MaxABufs;
     uint64_t *d_empty = d_full + 2;
-    uint64_t *drain = d_empty + 2;      // [2] one per MMA issuer: its final commit
-    uint64_t *part_full = drain + 2;    // [2] tile-end row sums of the epilogue half G = 1
-    uint64_t *part_empty = part_full + 2;
+    uint64_t *drain = d_empty + 2;  // [2] one per MMA issuer: its final commit
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
-    __shared__ float s_part[2][kT5Rows];  // the epilogue half G = 1's row sums at a tile end
     // per ring slot, written by the producer before the slot's barrier arrive:
     // where the epilogue writes the tile that the stage belongs to
     __shared__ T4StageMeta s_meta[kT5Stages];
@@ -1365,11 +1363,7 @@ __global__ void __launch_bounds__(kT4Threads, 1)
             mbar_init(&d_full[i], 1);
             mbar_init(&d_empty[i], kT4EpiWarps);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&drain[i], 1);
-            mbar_init(&part_full[i], kT4EpiWarps / 2);
-            mbar_init(&part_empty[i], kT4EpiWarps / 2);
-        }
+        for (int i = 0; i < 2; ++i) mbar_init(&drain[i], 1);
         s_abort = 0;
         fence_barrier_init();
     }
@@ -1560,17 +1554,15 @@ __global__ void __launch_bounds__(kT4Threads, 1)
         }
     } else if (warp >= kT4EpiWarp0 && warp < kT4EpiWarp0 + kT4EpiWarps) {
         // ------------------------------ epilogue ------------------------------
-        // warp w: TMEM lane quarter w % 4, blocks 4G .. 4G+3 of each stage. At a
-        // tile end the half G = 1 hands its row sums to G = 0 through a
-        // double-buffered shared array (part_full / part_empty), and G = 0
-        // writes y. Every wait is bounded; a warp whose wait fails leaves the loop.
+        // warp w: TMEM lane quarter w % 4, all 8 blocks of each stage; it writes y
+        // at the tile's last stage. Every wait is bounded; a warp whose wait
+        // fails leaves the loop.
         grid_dependency_wait();  // reads the column shift written by prep
-        const int G = (warp - kT4EpiWarp0) >> 2;
         const int qd = warp & 3;
         const int row = 32 * qd + lane;
         const uint32_t lane_base = uint32_t(32 * qd) << 16;
         float acc = 0.0f;
-        int shift = 0, tiles = 0;
+        int shift = 0;
         for (int s = 0; s < n_stages; ++s) {
             const int st = s % kT5Stages;
             const bool got = !*(volatile int *)&s_abort &&
@@ -1581,58 +1573,35 @@ __global__ void __launch_bounds__(kT4Threads, 1)
                 break;
             }
             tc_fence_after();
-            const T4StageMeta m = s_meta[st];  // the slot is rewritten once empty[st] completes
-            // the tile's column shift, loaded early: it is first used at the tile end
-            if (G == 0 && (m.flags & kT4FirstOfTile)) shift = *m.col_shift;
-            const uint32_t d_base = tmem + lane_base + d_col(s) + 4 * G * kT5N;
-            uint32_t r[4][16];
+            const T4StageMeta m = s_meta[st];
+            if (m.flags & kT4FirstOfTile) shift = *m.col_shift;
+            const uint32_t d_base = tmem + lane_base + d_col(s);
+            uint32_t r[8][16];
 #pragma unroll
-            for (int bi = 0; bi < 4; ++bi) tmem_ld16(d_base + bi * kT5N, r[bi]);
+            for (int bi = 0; bi < 8; ++bi) tmem_ld16(d_base + bi * kT5N, r[bi]);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&d_empty[s & 1]);  // D is in registers
+            if (lane == 0) mbar_arrive(&d_empty[s & 1]);
             const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes;
             const float *bt = reinterpret_cast<const float *>(beta_ring + st * kT4BetaBytes);
 #pragma unroll
-            for (int bi = 0; bi < 4; ++bi) {
-                const int b = 4 * G + bi;
-                float t = __uint_as_float(r[bi][kT4Pieces - 1]) *
+            for (int b = 0; b < 8; ++b) {
+                float t = __uint_as_float(r[b][kT4Pieces - 1]) *
                           __int_as_float((127 - 2 * (kT4Pieces - 1)) << 23);
 #pragma unroll
                 for (int pp = kT4Pieces - 2; pp >= 1; --pp)
-                    t = fmaf(__uint_as_float(r[bi][pp]), __int_as_float((127 - 2 * pp) << 23), t);
-                t = t + __uint_as_float(r[bi][0]);
+                    t = fmaf(__uint_as_float(r[b][pp]), __int_as_float((127 - 2 * pp) << 23), t);
+                t = t + __uint_as_float(r[b][0]);
                 const float d = lds_half_as_float(rp + 18 * b);
                 acc = fmaf(d, t - bt[b], acc);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
             if (m.flags & kT4LastOfTile) {
-                const int buf = tiles & 1;
-                const uint32_t use = uint32_t(tiles >> 1) & 1u;
-                if (G == 1) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(&part_empty[buf], use ^ 1u, p.err,
-                                                           kTagT5DEmpty))) {
-                        s_abort = 1;
-                        break;
-                    }
-                    s_part[buf][row] = acc;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&part_full[buf]);
-                } else {
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait(&part_full[buf], use, p.err, kTagT5DFull))) {
-                        s_abort = 1;
-                        break;
-                    }
-                    const int rr = m.row0 + row;
-                    if (rr < m.n_rows) m.y[rr] = mul_pow2(acc + s_part[buf][row], -shift);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&part_empty[buf]);
-                }
+                const int rr = m.row0 + row;
+                if (rr < m.n_rows) m.y[rr] = mul_pow2(acc, -shift);
                 acc = 0.0f;
-                ++tiles;
             }
         }
     }
