@@ -633,16 +633,18 @@ constexpr int kT5RawBytes = kT5Rows * kChunkBytes;   // 18432
 constexpr int kT5ImgBytes = kT5N * kChunkBlocks * 64; // 8192: 16 rows x 512 K bytes, SW128
 constexpr int kT5BetaBytes = kChunkBlocks * 4 * 4;   // beta[8 blocks][4 columns] f32
 constexpr int kT5PrepHeader = 1024;                  // int col_shift[8], images 1024-aligned
-constexpr int kT5ExpWarps = 8;
+constexpr int kT5ExpWarps = 4;
 constexpr int kT5EpiWarps = 4;
 // Warp roles. A warp reaches only the TMEM lanes of its quarter (warp % 4), so
-// each quarter hosts 2 expansion warps and 1 epilogue warp. Two MMA issuers
-// (even and odd stages) sit on warps 1 and 3, the producer on warp 2.
+// each quarter hosts 1 expansion warp and 1 epilogue warp (12 warps in all: a
+// second expansion warp per quarter measured slower at ncols 2 and no faster
+// at 3). Two MMA issuers (even and odd stages) sit on warps 1 and 3, the
+// producer on warp 2.
 constexpr int kT5ProdWarp = 2;
 constexpr int kT5MmaWarp = 3;    // even stages; allocates TMEM
 constexpr int kT5MmaWarp2 = 1;   // odd stages
-constexpr int kT5ExpWarp0 = 4;   // warps 4-11
-constexpr int kT5EpiWarp0 = 12;  // warps 12-15
+constexpr int kT5ExpWarp0 = 4;   // warps 4-7
+constexpr int kT5EpiWarp0 = 8;   // warps 8-11
 constexpr int kT5Warps = kT5EpiWarp0 + kT5EpiWarps;
 constexpr int kT5Threads = kT5Warps * 32;
 constexpr int kT5MaxABufs = 3;
@@ -981,8 +983,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             mbar_wait(&d_full[last & 1], uint32_t(last >> 1) & 1u, p.err, kTagT5DFull);
     } else if (warp >= kT5ExpWarp0 && warp < kT5ExpWarp0 + kT5ExpWarps) {
         // ------------------------------ expansion ------------------------------
-        // warp w: TMEM lane quarter w % 4 (rows 32 (w % 4) ..), blocks 4G .. 4G+3
-        const int G = (warp - kT5ExpWarp0) >> 2;
+        // warp w: TMEM lane quarter w % 4 (rows 32 (w % 4) ..), all 8 blocks
         const int qd = warp & 3;
         const int row = 32 * qd + lane;
         const uint32_t lane_base = uint32_t(32 * qd) << 16;
@@ -1005,32 +1006,35 @@ __global__ void __launch_bounds__(kT5Threads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes + G * 72;
-                uint32_t u[18];
 #pragma unroll
-                for (int k = 0; k < 9; ++k) {
-                    const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * k);
-                    u[2 * k] = v.x;
-                    u[2 * k + 1] = v.y;
-                }
-                const uint32_t a_base = tmem + lane_base + a_col(s) + 4 * G * 16;
+                for (int G = 0; G < 2; ++G) {
+                    const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes + G * 72;
+                    uint32_t u[18];
 #pragma unroll
-                for (int bi = 0; bi < 4; ++bi) {
-                    uint32_t a[16];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t w;
-                        if (bi == 0) w = __byte_perm(u[c], u[c + 1], 0x5432);
-                        else if (bi == 1) w = u[5 + c];
-                        else if (bi == 2) w = __byte_perm(u[9 + c], u[10 + c], 0x5432);
-                        else w = u[14 + c];
-                        const uint32_t hw = w >> 4;
-                        a[4 * c + 0] = w & 0x03030303u;
-                        a[4 * c + 1] = w & 0x0C0C0C0Cu;
-                        a[4 * c + 2] = hw & 0x03030303u;
-                        a[4 * c + 3] = hw & 0x0C0C0C0Cu;
+                    for (int k = 0; k < 9; ++k) {
+                        const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * k);
+                        u[2 * k] = v.x;
+                        u[2 * k + 1] = v.y;
                     }
-                    tmem_st16(a_base + bi * 16, a);
+                    const uint32_t a_base = tmem + lane_base + a_col(s) + 4 * G * 16;
+#pragma unroll
+                    for (int bi = 0; bi < 4; ++bi) {
+                        uint32_t a[16];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t w;
+                            if (bi == 0) w = __byte_perm(u[c], u[c + 1], 0x5432);
+                            else if (bi == 1) w = u[5 + c];
+                            else if (bi == 2) w = __byte_perm(u[9 + c], u[10 + c], 0x5432);
+                            else w = u[14 + c];
+                            const uint32_t hw = w >> 4;
+                            a[4 * c + 0] = w & 0x03030303u;
+                            a[4 * c + 1] = w & 0x0C0C0C0Cu;
+                            a[4 * c + 2] = hw & 0x03030303u;
+                            a[4 * c + 3] = hw & 0x0C0C0C0Cu;
+                        }
+                        tmem_st16(a_base + bi * 16, a);
+                    }
                 }
                 tmem_wait_st();
                 tc_fence_before();
