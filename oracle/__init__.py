@@ -70,6 +70,9 @@ def lib():
             L.qo_dequantize_rows.argtypes = [u8p, i64, i64, i64, f64p]
             L.qo_matmul_rows.argtypes = [u8p, i64, i64, f32p, i64, i64p, i64, f64p, f64p]
             L.qo_get_rows.argtypes = [u8p, i64, i64, i32p, i64, f32p]
+            L.qo_matmul_id.argtypes = [u8p, i64, i64, i64, f32p, i64, i32p, i64, i64, i64p, i64,
+                                       f64p, f64p]
+            L.qo_matmul_id.restype = i64
             L.qo_get_rows.restype = i64
             L.qo_quantize_block.argtypes = [f32p, u8p]
             L.qo_quantize_rows.argtypes = [f32p, i64, i64, u8p]
@@ -183,6 +186,37 @@ def matmul(w, N: int, K: int, x, rows=None):
     lib().qo_matmul_rows(_p(wb, ctypes.c_uint8), N, K, _p(xx, ctypes.c_float), ncols,
                          rp, nr, _p(y, ctypes.c_double), _p(acc, ctypes.c_double))
     return y, acc
+
+
+def matmul_id(w, n_expert: int, N: int, K: int, x, ids, rows=None):
+    """Expert mat-vec: (y, acc, n_bad), y and acc fp64 [n_tokens][n_used][nr].
+
+    w: n_expert matrices of N x K, one after another. ids: int [n_tokens][n_used].
+    x: f32 [n_tokens][n_x][K] with n_x = 1 (shared by the token's experts) or
+    n_used. Slots with an id outside [0, n_expert) are counted in n_bad and
+    their rows of y and acc are NaN.
+    """
+    wb = _u8(w)
+    ii = np.ascontiguousarray(ids, dtype=np.int32)
+    assert ii.ndim == 2
+    n_tokens, n_used = ii.shape
+    xx = np.ascontiguousarray(x, dtype=np.float32)
+    assert xx.ndim == 3 and xx.shape[0] == n_tokens and xx.shape[2] == K and K % 64 == 0
+    n_x = xx.shape[1]
+    assert n_x in (1, n_used)
+    assert wb.size >= n_expert * N * (K // 64) * 18
+    if rows is None:
+        nr, rp = N, None
+    else:
+        rr = np.ascontiguousarray(rows, dtype=np.int64)
+        assert rr.size == 0 or (rr.min() >= 0 and rr.max() < N)
+        nr, rp = rr.size, _p(rr, ctypes.c_int64)
+    y = np.full((n_tokens, n_used, nr), np.nan, dtype=np.float64)
+    acc = np.full((n_tokens, n_used, nr), np.nan, dtype=np.float64)
+    bad = lib().qo_matmul_id(_p(wb, ctypes.c_uint8), n_expert, N, K, _p(xx, ctypes.c_float), n_x,
+                             _p(ii, ctypes.c_int32), n_used, n_tokens, rp, nr,
+                             _p(y, ctypes.c_double), _p(acc, ctypes.c_double))
+    return y, acc, int(bad)
 
 
 def get_rows(table, n_rows: int, K: int, ids):

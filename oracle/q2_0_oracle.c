@@ -188,6 +188,39 @@ void qo_matmul_rows(const uint8_t *w, int64_t N, int64_t K, const float *x, int6
 }
 
 /* ---------------------------------------------------------------------------
+ * Expert mat-vec (ggml mul_mat_id). [WGPU] limitations paragraph: the port
+ * leaves out MUL_MAT_ID, the expert-routed matmul of mixture-of-experts layers.
+ * as holds n_expert matrices of N x K one after another; ids is
+ * [n_tokens][n_used]; x is [n_tokens][n_x][K] with n_x = 1 (one vector per
+ * token, shared by its experts) or n_x = n_used (one vector per slot).
+ *   y[t][i][j] = sum_k W_{ids[t][i]}[rows[j]][k] * x[t][n_x == 1 ? 0 : i][k]
+ * in fp64, with acc = sum |W x| likewise; y and acc are [n_tokens*n_used][nr].
+ * Each slot is the plain matmul above on the selected matrix. Returns the
+ * number of ids outside [0, n_expert); their y and acc rows are left untouched.
+ * ------------------------------------------------------------------------- */
+int64_t qo_matmul_id(const uint8_t *as, int64_t n_expert, int64_t N, int64_t K, const float *x,
+                     int64_t n_x, const int32_t *ids, int64_t n_used, int64_t n_tokens,
+                     const int64_t *rows, int64_t n_rows, double *y, double *acc) {
+    int64_t bad = 0;
+    int64_t nr = rows ? n_rows : N;
+    size_t expert_bytes = (size_t)N * (size_t)(K / QO_WEIGHTS_PER_BLOCK) * QO_BYTES_PER_BLOCK;
+    for (int64_t t = 0; t < n_tokens; ++t) {
+        for (int64_t i = 0; i < n_used; ++i) {
+            int64_t v = t * n_used + i;
+            int64_t e = ids[v];
+            if (e < 0 || e >= n_expert) {
+                ++bad;
+                continue;
+            }
+            const float *xv = x + (t * n_x + (n_x == 1 ? 0 : i)) * K;
+            qo_matmul_rows(as + (size_t)e * expert_bytes, N, K, xv, 1, rows, n_rows, y + v * nr,
+                           acc ? acc + v * nr : NULL);
+        }
+    }
+    return bad;
+}
+
+/* ---------------------------------------------------------------------------
  * get_rows. [WGPU] shader paragraph: the get-rows shader copies rows of a Q2_0
  * tensor out and writes 64 floats per block. out[r][k] = W[ids[r]][k] as f32;
  * (q-1)*d is exact in fp64 and representable in f32, so the cast is exact and

@@ -437,3 +437,81 @@ def test_g128_closed_forms_and_get_rows(oracle_mod):
         out, bad = oracle_mod.get_rows_g128(w, N, K, np.array([2, 0, 5], dtype=np.int32))
         assert bad == 1
         assert np.all(out[:2] == np.float32(level)) and np.all(out[2] == 0)
+
+
+# ---------------------------------------------------------------------------
+# Expert mat-vec (mul_mat_id): each slot is the plain matmul of the selected
+# expert ([WGPU] limitations paragraph names MUL_MAT_ID as the missing op)
+# ---------------------------------------------------------------------------
+def _experts(g, n_expert, N, K):
+    return np.concatenate([synth.packed_matrix(g, N, K, 0.01, 3.0, 0.05) for _ in range(n_expert)])
+
+
+def test_matmul_id_exact_rational(oracle_mod):
+    g = np.random.default_rng(71)
+    n_expert, N, K, n_tokens, n_used = 3, 2, 128, 2, 2
+    w = _experts(g, n_expert, N, K)
+    x = synth.activations(g, n_tokens * n_used, K, 0.05, 30.0).reshape(n_tokens, n_used, K)
+    ids = np.array([[2, 0], [1, 2]], dtype=np.int32)
+    y, acc, bad = oracle_mod.matmul_id(w, n_expert, N, K, x, ids)
+    assert bad == 0
+    eb = N * (K // 64) * 18
+    for t in range(n_tokens):
+        for i in range(n_used):
+            W = oracle_mod.dequantize(w[ids[t, i] * eb:(ids[t, i] + 1) * eb], N, K)
+            for n in range(N):
+                ex = _exact_dot(W[n], x[t, i])
+                exa = sum((abs(Fraction(float(a)) * Fraction(float(b))) for a, b in zip(W[n], x[t, i])),
+                          Fraction(0))
+                bound = K * 2.0 ** -52 * float(exa)
+                assert abs(Fraction(y[t, i, n]) - ex) <= Fraction(bound), (t, i, n)
+                assert abs(Fraction(acc[t, i, n]) - exa) <= Fraction(bound), (t, i, n)
+
+
+def test_matmul_id_single_expert_is_matmul(oracle_mod):
+    """One expert and every id 0: each slot equals the (pinned) plain matmul."""
+    g = np.random.default_rng(72)
+    N, K, n_tokens, n_used = 5, 256, 3, 2
+    w = synth.packed_matrix(g, N, K, 0.005, 0.05, 0.01)
+    x = synth.activations(g, n_tokens * n_used, K).reshape(n_tokens, n_used, K)
+    y, acc, bad = oracle_mod.matmul_id(w, 1, N, K, x, np.zeros((n_tokens, n_used), np.int32))
+    assert bad == 0
+    ref, refa = oracle_mod.matmul(w, N, K, x.reshape(-1, K))
+    assert np.array_equal(y.reshape(-1, N), ref) and np.array_equal(acc.reshape(-1, N), refa)
+
+
+def test_matmul_id_expert_permutation_and_broadcast(oracle_mod):
+    """Relabelling the experts (with the ids relabelled alike) changes nothing;
+    one shared vector per token equals that vector repeated per slot; listed
+    rows give the same numbers."""
+    g = np.random.default_rng(73)
+    n_expert, N, K, n_tokens, n_used = 6, 7, 192, 4, 3
+    w = _experts(g, n_expert, N, K)
+    eb = N * (K // 64) * 18
+    x1 = synth.activations(g, n_tokens, K).reshape(n_tokens, 1, K)
+    ids = g.integers(0, n_expert, size=(n_tokens, n_used)).astype(np.int32)
+    y, acc, _ = oracle_mod.matmul_id(w, n_expert, N, K, x1, ids)
+    perm = g.permutation(n_expert)            # new slot of expert e is perm[e]
+    wp = np.empty_like(w)
+    for e in range(n_expert):
+        wp[perm[e] * eb:(perm[e] + 1) * eb] = w[e * eb:(e + 1) * eb]
+    yp, accp, _ = oracle_mod.matmul_id(wp, n_expert, N, K, x1, perm[ids].astype(np.int32))
+    assert np.array_equal(y, yp) and np.array_equal(acc, accp)
+    xr = np.repeat(x1, n_used, axis=1)
+    yr, accr, _ = oracle_mod.matmul_id(w, n_expert, N, K, xr, ids)
+    assert np.array_equal(y, yr) and np.array_equal(acc, accr)
+    rows = np.array([6, 0, 3])
+    ys, _, _ = oracle_mod.matmul_id(w, n_expert, N, K, x1, ids, rows=rows)
+    assert np.array_equal(ys, y[:, :, rows])
+
+
+def test_matmul_id_bad_ids(oracle_mod):
+    g = np.random.default_rng(74)
+    n_expert, N, K = 2, 3, 64
+    w = _experts(g, n_expert, N, K)
+    x = synth.activations(g, 2, K).reshape(2, 1, K)
+    ids = np.array([[0, 2], [-1, 1]], dtype=np.int32)
+    y, acc, bad = oracle_mod.matmul_id(w, n_expert, N, K, x, ids)
+    assert bad == 2
+    assert np.isnan(y[0, 1]).all() and np.isnan(y[1, 0]).all()
+    assert not np.isnan(y[0, 0]).any() and not np.isnan(y[1, 1]).any()
