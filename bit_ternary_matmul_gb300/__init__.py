@@ -52,6 +52,7 @@ EXPORTS = (
     "q2_0_mul_mat", "q2_0_get_rows", "q2_0_quantize_ref", "q2_0_get_error",
     "q2_0_mul_mat_vec_f16", "q2_0_mul_mat_f16",
     "q2_0_g128_to_g64", "q2_0_g128_get_rows", "q2_0_g128_mul_mat_vec",
+    "q2_0_mul_mat_id_workspace_size", "q2_0_mul_mat_id",
 )
 
 
@@ -125,6 +126,10 @@ def lib():
             L.q2_0_g128_mul_mat_vec.restype = i32
             L.q2_0_get_rows.argtypes = [vp, i64, i64, vp, i64, vp, vp]
             L.q2_0_get_rows.restype = i32
+            L.q2_0_mul_mat_id_workspace_size.argtypes = [i64, i64, i64]
+            L.q2_0_mul_mat_id_workspace_size.restype = sz
+            L.q2_0_mul_mat_id.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, i64, vp, vp, sz, vp]
+            L.q2_0_mul_mat_id.restype = i32
             L.q2_0_quantize_ref.argtypes = [vp, vp, i64, i64, vp]
             L.q2_0_quantize_ref.restype = i32
             L.q2_0_get_error.argtypes = [vp, ctypes.POINTER(i64)]
@@ -334,6 +339,38 @@ def q2_0_get_rows(table: torch.Tensor, n_rows: int, K: int, ids: torch.Tensor,
                              _dev(out, "out", torch.float32, n_ids * K), _stream(stream))
     _check("q2_0_get_rows", st)
     return out
+
+
+def q2_0_mul_mat_id_workspace_size(K: int, n_tokens: int, n_x: int) -> int:
+    return int(lib().q2_0_mul_mat_id_workspace_size(K, n_tokens, n_x))
+
+
+def q2_0_mul_mat_id(w: torch.Tensor, n_expert: int, N: int, K: int, x: torch.Tensor,
+                    ids: torch.Tensor, y: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Expert mat-vec: y[t][i] = W_{ids[t][i]} x[t][i or 0].
+
+    w: n_expert packed N x K matrices, one after another; x: f32 [n_tokens][n_x][K]
+    (n_x = 1 or n_used; a 2-D x is n_x = 1); ids: int32 [n_tokens][n_used];
+    y: f32 [n_tokens][n_used][N].
+    """
+    n_tokens, n_used = ids.shape
+    n_x = 1 if x.dim() == 2 else x.shape[1]
+    if y is None:
+        y = torch.empty((n_tokens, n_used, N), dtype=torch.float32, device=ids.device)
+    if n_tokens == 0:
+        return y
+    need = q2_0_mul_mat_id_workspace_size(K, n_tokens, n_x)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=ids.device)
+    wsp = _dev(workspace, "workspace", torch.uint8, need) if need > 0 else None
+    st = lib().q2_0_mul_mat_id(_dev(w, "w", torch.uint8, n_expert * packed_bytes(N, K)), n_expert,
+                               N, K, _dev(x, "x", torch.float32, n_tokens * n_x * K), n_x,
+                               _dev(ids, "ids", torch.int32, n_tokens * n_used), n_used, n_tokens,
+                               _dev(y, "y", torch.float32, n_tokens * n_used * N), wsp,
+                               need if need > 0 else 0, _stream(stream))
+    _check("q2_0_mul_mat_id", st)
+    return y
 
 
 def q2_0_quantize_ref(src: torch.Tensor, nrows: int, K: int, dst: torch.Tensor | None = None,

@@ -245,6 +245,36 @@ int q2_0_mul_mat_f16(const void *w, const void *x, float *y, int64_t N, int64_t 
     return mul_mat_impl(w, x, kXF16, y, N, K, M, Q2_0_PREC_F16, workspace, workspace_bytes, stream);
 }
 
+// Expert mat-vec shapes: n_expert * N rows must fit a tensor-map coordinate,
+// and the activation vectors a grid dimension.
+static bool valid_moe(int64_t n_expert, int64_t N, int64_t K, int64_t n_x, int64_t n_used,
+                      int64_t n_tokens) {
+    return n_expert >= 1 && N >= 1 && valid_k(K) && n_used >= 1 && n_tokens >= 0 &&
+           (n_x == 1 || n_x == n_used) && n_expert * N <= (int64_t(1) << 31) - 1 &&
+           n_tokens * n_x <= 65535 && n_tokens * n_used <= 65535;
+}
+
+size_t q2_0_mul_mat_id_workspace_size(int64_t K, int64_t n_tokens, int64_t n_x) {
+    if (!valid_k(K) || n_tokens < 0 || n_x < 1) return 0;
+    return matvec_moe_workspace_bytes(K, n_tokens * n_x);
+}
+
+int q2_0_mul_mat_id(const void *w, int64_t n_expert, int64_t N, int64_t K, const float *x,
+                    int64_t n_x, const int32_t *ids, int64_t n_used, int64_t n_tokens, float *y,
+                    void *workspace, size_t workspace_bytes, void *stream) {
+    if (!valid_moe(n_expert, N, K, n_x, n_used, n_tokens)) return Q2_0_EINVAL;
+    if (n_tokens == 0) return Q2_0_OK;
+    if (!w || !x || !ids || !y) return Q2_0_EINVAL;
+    const size_t need = matvec_moe_workspace_bytes(K, n_tokens * n_x);
+    if (matvec_fast_path_ok(w, K) &&
+        (workspace_bytes < need || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+        return Q2_0_EINVAL;
+    int st = check_device(nullptr);
+    if (st != Q2_0_OK) return st;
+    return matvec_moe_run(static_cast<const uint8_t *>(w), n_expert, N, K, x, n_x, ids, n_used,
+                          n_tokens, y, workspace, workspace_bytes, as_stream(stream));
+}
+
 int q2_0_get_rows(const void *table, int64_t n_rows, int64_t K, const int32_t *ids, int64_t n_ids,
                   float *out, void *stream) {
     if (n_ids < 0 || n_rows < 1 || !valid_k(K)) return Q2_0_EINVAL;

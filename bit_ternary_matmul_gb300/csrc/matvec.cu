@@ -76,6 +76,10 @@ struct MvPrepJob {
     const void *x;   // [ncols][K], F32 or F16 (the prep kernel's template argument)
     uint8_t *prep;   // prepared fragments
     int K;
+    // fp4 prep only, launched without a job list: grid row j prepares the vector
+    // at x + j * x_stride into prep + j * prep_stride (bytes)
+    long long x_stride;
+    long long prep_stride;
 };
 
 struct MvJob {  // 64-byte aligned through its CUtensorMap member
@@ -93,6 +97,18 @@ struct MvItem {
     int tile;
 };
 
+// Expert mat-vec (mul_mat_id) on the fp4 kernel: the single job's tensor map
+// spans all experts' rows; output vector v = t * n_used + i takes expert
+// ids[v]. ids == nullptr for every other launch.
+struct MvMoe {
+    const int32_t *ids;     // [n_vec]
+    int n_vec;              // n_tokens * n_used
+    int n_used;
+    int n_x;                // activation vectors per token: 1 (shared) or n_used
+    int n_expert;
+    long long prep_stride;  // bytes between consecutive activation vectors' prep
+};
+
 struct MvParams {
     const MvJob *jobs;        // nullptr: the single job passed by value
     const MvItem *items;      // per-CTA work lists (schedule), when jobs != nullptr
@@ -101,6 +117,7 @@ struct MvParams {
     int ncols;
     int n_stages;             // pipeline depth (n_stages_for(ncols))
     unsigned long long *err;
+    MvMoe moe;
 };
 
 // Record per block per n-tile, for S = lane slots carrying data (8 per column of
@@ -1203,7 +1220,11 @@ __global__ void __launch_bounds__(kT5PrepThreads) t4_prep_kernel(
     // (a mat-vec that may still read this buffer, or the producer of x): wait
     // for that grid before reading x or writing the prep buffer.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const MvPrepJob &J = jobs ? jobs[blockIdx.y] : single;
+    MvPrepJob J = jobs ? jobs[blockIdx.y] : single;
+    if (!jobs) {  // a strided batch of vectors, one per grid row
+        J.x = static_cast<const uint8_t *>(single.x) + size_t(blockIdx.y) * single.x_stride;
+        J.prep = single.prep + size_t(blockIdx.y) * single.prep_stride;
+    }
     const int K = J.K;
     const XT *xj = static_cast<const XT *>(J.x);
     const int tid = threadIdx.x;
@@ -1300,7 +1321,7 @@ __global__ void __launch_bounds__(kT5PrepThreads) t4_prep_kernel(
 // Where the epilogue writes the tile a ring stage belongs to; the producer fills
 // one per slot before the slot's barrier arrive.
 struct T4StageMeta {
-    float *y;
+    float *y;              // nullptr: the tile is not written (an expert id out of range)
     const int *col_shift;  // the job's column shift (written by the prep kernel)
     int row0;              // first row of the tile
     int n_rows;            // rows of the matrix
@@ -1385,9 +1406,10 @@ __global__ void __launch_bounds__(kT4Threads, 1)
         item_base = p.cta_begin[blockIdx.x];
         n_items = p.cta_begin[blockIdx.x + 1] - item_base;
     } else {
-        n_items = blockIdx.x < unsigned(single.n_tiles)
-                      ? (single.n_tiles - 1 - int(blockIdx.x)) / int(gridDim.x) + 1
-                      : 0;
+        // one matrix: its tiles; expert mat-vec: (output vector, tile) pairs
+        const int total = p.moe.ids ? p.moe.n_vec * single.n_tiles : single.n_tiles;
+        n_items = blockIdx.x < unsigned(total) ? (total - 1 - int(blockIdx.x)) / int(gridDim.x) + 1
+                                               : 0;
     }
     auto item_at = [&](int i, const MvJob *&J, int &tile) {
         if (p.jobs) {
@@ -1416,7 +1438,27 @@ __global__ void __launch_bounds__(kT4Threads, 1)
                 const MvJob *J;
                 int tile;
                 item_at(i, J, tile);
-                const uint8_t *img = J->prep + kT5PrepHeader;
+                const uint8_t *prep = J->prep;
+                float *y_out = J->y;
+                int row_base = 0;  // first tensor-map row of the matrix
+                if (p.moe.ids) {
+                    // item = (output vector v, tile): expert ids[v], that expert's
+                    // rows of the stacked tensor map, the vector's prep and y
+                    const int v = tile / J->n_tiles;
+                    tile -= v * J->n_tiles;
+                    int e = p.moe.ids[v];
+                    if (e < 0 || e >= p.moe.n_expert) {
+                        if (tile == 0) record_error(p.err, Q2_0_DEVERR_BAD_ID, v);
+                        e = 0;            // stream a valid matrix, write nothing
+                        y_out = nullptr;
+                    } else {
+                        y_out += size_t(v) * J->N;
+                    }
+                    row_base = e * J->N;
+                    const int xv = p.moe.n_x == 1 ? v / p.moe.n_used : v;
+                    prep += size_t(xv) * p.moe.prep_stride;
+                }
+                const uint8_t *img = prep + kT5PrepHeader;
                 const uint8_t *beta = img + size_t(J->n_chunks) * kT4ImgBytes;
                 const int nch = J->n_chunks;
                 for (int ch = 0; ch < nch; ++ch, ++s) {
@@ -1428,14 +1470,14 @@ __global__ void __launch_bounds__(kT4Threads, 1)
                         break;
                     }
                     T4StageMeta &m = s_meta[st];
-                    m.y = J->y;
-                    m.col_shift = reinterpret_cast<const int *>(J->prep);
+                    m.y = y_out;
+                    m.col_shift = reinterpret_cast<const int *>(prep);
                     m.row0 = tile * kT5Rows;
                     m.n_rows = J->N;
                     m.flags = (ch == 0 ? kT4FirstOfTile : 0) | (ch == nch - 1 ? kT4LastOfTile : 0);
                     mbar_arrive_expect_tx(&full[st], kT5RawBytes + kT4ImgBytes + kT4BetaBytes);
                     tma_load_2d(raw_ring + st * kT5RawBytes, &J->tmap, ch * kChunkBytes,
-                                tile * kT5Rows, &full[st]);
+                                row_base + tile * kT5Rows, &full[st]);
                     if (!prep_ready) {
                         grid_dependency_wait();  // the B images come from the prep kernel
                         prep_ready = true;
@@ -1604,7 +1646,7 @@ __global__ void __launch_bounds__(kT4Threads, 1)
             if (lane == 0) mbar_arrive(&empty[st]);
             if (m.flags & kT4LastOfTile) {
                 const int rr = m.row0 + row;
-                if (rr < m.n_rows) m.y[rr] = mul_pow2(acc, -shift);
+                if (m.y && rr < m.n_rows) m.y[rr] = mul_pow2(acc, -shift);
                 acc = 0.0f;
             }
         }
@@ -1663,6 +1705,44 @@ __global__ void __launch_bounds__(256) mv_generic_kernel(const uint8_t *__restri
     }
     if (lane == 0)
         for (int cc = 0; cc < ncols; ++cc) y[size_t(cc) * N + row] = acc[cc];
+}
+
+// Generic expert mat-vec (any K % 64 == 0, any alignment): grid (rows / 8,
+// output vectors); one warp per row of the vector's expert, as above.
+__global__ void __launch_bounds__(256) moe_generic_kernel(
+    const uint8_t *__restrict__ w, const float *__restrict__ x, const int32_t *__restrict__ ids,
+    float *__restrict__ y, int N, int K, int n_expert, int n_used, int n_x,
+    unsigned long long *err) {
+    const int v = blockIdx.y;
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int e = ids[v];
+    if (e < 0 || e >= n_expert) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) record_error(err, Q2_0_DEVERR_BAD_ID, v);
+        return;
+    }
+    if (row >= N) return;
+    const int nb = K / 64;
+    const float *xv = x + size_t(n_x == 1 ? v / n_used : v) * K;
+    const uint8_t *wr = w + (size_t(e) * N + row) * nb * 18;
+    float acc = 0.0f;
+    for (int b = lane; b < nb; b += 32) {
+        const uint8_t *blk = wr + size_t(b) * 18;
+        const float d = half_bits_to_float(uint32_t(blk[0]) | (uint32_t(blk[1]) << 8));
+        float sum = 0.0f;
+        for (int wi = 0; wi < 4; ++wi) {
+            const uint8_t *pw = blk + 2 + 4 * wi;
+            const uint32_t word = uint32_t(pw[0]) | (uint32_t(pw[1]) << 8) |
+                                  (uint32_t(pw[2]) << 16) | (uint32_t(pw[3]) << 24);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                sum = fmaf(float(int((word >> (2 * i)) & 3u) - 1), xv[b * 64 + wi * 16 + i], sum);
+        }
+        acc = fmaf(d, sum, acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) y[size_t(v) * N + row] = acc;
 }
 
 std::mutex g_attr_mu;
@@ -1858,6 +1938,41 @@ int matvec_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, 
     if (!make_job(J, w, prep, y, N, K, tile_rows_for(ncols))) return Q2_0_ECUDA;
     MvParams prm{nullptr, nullptr, nullptr, nullptr, ncols, n_stages_for(ncols), err};
     const int grid = std::max(1, std::min(J.n_tiles, sm_count()));
+    return cuda_status(launch_tc(J, prm, grid, s));
+}
+
+size_t matvec_moe_workspace_bytes(int64_t K, int64_t n_xvec) {
+    return K % 512 == 0 ? size_t(n_xvec) * t4_prep_bytes(K) : 0;
+}
+
+int matvec_moe_run(const uint8_t *w, int64_t n_expert, int64_t N, int64_t K, const float *x,
+                   int64_t n_x, const int32_t *ids, int64_t n_used, int64_t n_tokens, float *y,
+                   void *ws, size_t ws_bytes, cudaStream_t s) {
+    unsigned long long *err = error_word_ptr();
+    if (!err) return Q2_0_ECUDA;
+    const int64_t n_vec = n_tokens * n_used;
+    if (!matvec_fast_path_ok(w, K)) {
+        dim3 grid(unsigned((N + 7) / 8), unsigned(n_vec));
+        moe_generic_kernel<<<grid, 256, 0, s>>>(w, x, ids, y, int(N), int(K), int(n_expert),
+                                                int(n_used), int(n_x), err);
+        return cuda_status(cudaGetLastError());
+    }
+    const int64_t n_xvec = n_tokens * n_x;
+    if (ws_bytes < matvec_moe_workspace_bytes(K, n_xvec)) return Q2_0_EINVAL;
+    uint8_t *prep = static_cast<uint8_t *>(ws);
+    const long long stride = (long long)t4_prep_bytes(K);
+    // one fp4 prep region per activation vector
+    MvPrepJob pj{x, prep, int(K), (long long)K * 4, stride};
+    if (launch_prep(pj, nullptr, int(n_xvec), 1, K, kXF32, s) != cudaSuccess) return Q2_0_ECUDA;
+    // the tensor map spans all experts' rows; the kernel picks expert ids[v]
+    MvJob J;
+    if (!make_job(J, w, prep, y, n_expert * N, K, kT5Rows)) return Q2_0_ECUDA;
+    J.N = int(N);
+    J.n_tiles = int((N + kT5Rows - 1) / kT5Rows);
+    MvParams prm{nullptr, nullptr, nullptr, nullptr, 1, n_stages_for(1), err,
+                 MvMoe{ids, int(n_vec), int(n_used), int(n_x), int(n_expert), stride}};
+    const int64_t items = n_vec * J.n_tiles;
+    const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items, sm_count())));
     return cuda_status(launch_tc(J, prm, grid, s));
 }
 

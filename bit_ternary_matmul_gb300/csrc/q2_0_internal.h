@@ -50,6 +50,12 @@ bool matvec_fast_path_ok(const void *w, int64_t K);
 int matvec_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, int64_t K,
                int ncols, void *ws, size_t ws_bytes, cudaStream_t s);
 
+// expert mat-vec (mul_mat_id), F32 x: one fp4 prep region per activation vector
+size_t matvec_moe_workspace_bytes(int64_t K, int64_t n_xvec);
+int matvec_moe_run(const uint8_t *w, int64_t n_expert, int64_t N, int64_t K, const float *x,
+                   int64_t n_x, const int32_t *ids, int64_t n_used, int64_t n_tokens, float *y,
+                   void *ws, size_t ws_bytes, cudaStream_t s);
+
 // batched mat-vec plans (opaque to the C ABI)
 int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **plan);
 int mv_plan_execute(const q2_0_mv_plan *plan, cudaStream_t s);

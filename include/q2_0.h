@@ -56,7 +56,7 @@ typedef enum q2_0_status {
 
 /* Device error codes (first error wins until cleared). */
 #define Q2_0_DEVERR_NONE 0
-#define Q2_0_DEVERR_BAD_ID 1  /* get_rows: ids[info] outside [0, n_rows) */
+#define Q2_0_DEVERR_BAD_ID 1  /* get_rows / mul_mat_id: ids[info] out of range */
 #define Q2_0_DEVERR_TIMEOUT 2 /* a pipeline wait gave up; info = kernel tag */
 
 /* GEMM activation precision. F32 activations are used by the tensor cores as
@@ -190,6 +190,31 @@ int q2_0_mul_mat(const void *w, const float *x, float *y, int64_t N, int64_t K, 
  */
 int q2_0_mul_mat_f16(const void *w, const void *x, float *y, int64_t N, int64_t K, int64_t M,
                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * q2_0_mul_mat_id — expert mat-vec of a mixture-of-experts layer (ggml
+ * mul_mat_id; the limitations paragraph of "WebGPU: add Q2_0 support" names
+ * MUL_MAT_ID as not ported).
+ *   w    n_expert Q2_0 matrices of N x K, one after another (expert e starts
+ *        at byte e * N * K/64 * 18).
+ *   x    F32 [n_tokens][n_x][K]: n_x = 1 (one vector per token, shared by its
+ *        experts) or n_x = n_used (one vector per slot).
+ *   ids  int32 [n_tokens][n_used], expert of each slot.
+ *   y    F32 [n_tokens][n_used][N]:
+ *        y[t][i][n] = sum_k W_{ids[t][i]}[n][k] * x[t][n_x == 1 ? 0 : i][k].
+ * Bound: |y - exact| <= 1e-5 * sum_k |W x| + 1e-7, as q2_0_mul_mat_vec.
+ * workspace: at least q2_0_mul_mat_id_workspace_size(K, n_tokens, n_x) bytes,
+ * 256-byte aligned (the size is 0, and NULL allowed, off the fast path).
+ * Fast path: K % 512 == 0 and w 16-byte aligned; otherwise a CUDA-core kernel.
+ * Limits: n_expert * N < 2^31, n_tokens * n_used and n_tokens * n_x <= 65535.
+ * An id outside [0, n_expert) leaves its slot's output unwritten and records
+ * Q2_0_DEVERR_BAD_ID with info = the slot index t * n_used + i.
+ * n_tokens == 0 is a no-op. All pointers are device memory owned by the caller.
+ */
+size_t q2_0_mul_mat_id_workspace_size(int64_t K, int64_t n_tokens, int64_t n_x);
+int q2_0_mul_mat_id(const void *w, int64_t n_expert, int64_t N, int64_t K, const float *x,
+                    int64_t n_x, const int32_t *ids, int64_t n_used, int64_t n_tokens, float *y,
+                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * q2_0_get_rows — gather rows of a Q2_0 table into F32, bit-exact.

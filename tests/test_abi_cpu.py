@@ -62,6 +62,23 @@ def test_argument_validation_without_gpu(L):
     assert L.q2_0_g128_get_rows(p, 4, 128, p, 0, p, null) == q.Q2_0_OK
     assert L.q2_0_g128_mul_mat_vec(p, p, p, 4, 128, 9, null) == EINVAL
     assert L.q2_0_g128_mul_mat_vec(p, p, p, 0, 128, 1, null) == EINVAL
+    # expert mat-vec: shapes, n_x, limits, workspace; n_tokens == 0 is a no-op
+    ids = ctypes.c_void_p(0x2000)
+    assert L.q2_0_mul_mat_id(p, 4, 8, 512, p, 1, ids, 2, 0, p, null, 0, null) == q.Q2_0_OK
+    assert L.q2_0_mul_mat_id(p, 4, 8, 500, p, 1, ids, 2, 1, p, null, 0, null) == EINVAL  # K % 64
+    assert L.q2_0_mul_mat_id(p, 0, 8, 512, p, 1, ids, 2, 1, p, null, 0, null) == EINVAL  # no expert
+    assert L.q2_0_mul_mat_id(p, 4, 8, 512, p, 3, ids, 2, 1, p, null, 0, null) == EINVAL  # n_x
+    assert L.q2_0_mul_mat_id(p, 4, 8, 512, p, 1, null, 2, 1, p, null, 0, null) == EINVAL  # ids
+    assert L.q2_0_mul_mat_id(p, 1 << 20, 1 << 12, 512, p, 1, ids, 2, 1, p, null, 0,
+                             null) == EINVAL  # n_expert * N >= 2^31
+    assert L.q2_0_mul_mat_id(p, 4, 8, 512, p, 1, ids, 2, 40000, p, null, 0, null) == EINVAL
+    need = L.q2_0_mul_mat_id_workspace_size(512, 3, 2)
+    assert need == 2 * 3 * L.q2_0_mul_mat_vec_workspace_size(512, 1)
+    assert L.q2_0_mul_mat_id_workspace_size(576, 3, 2) == 0  # off the fast path: no scratch
+    assert L.q2_0_mul_mat_id(p, 4, 8, 512, p, 2, ids, 2, 3, p, ctypes.c_void_p(0x100000), need - 1,
+                             null) == EINVAL
+    assert L.q2_0_mul_mat_id(p, 4, 8, 512, p, 2, ids, 2, 3, p, ctypes.c_void_p(0x100010), need,
+                             null) == EINVAL  # workspace not 256-byte aligned
     # mat-vec with workspace: too small, misaligned
     need = L.q2_0_mul_mat_vec_workspace_size(512, 1)
     assert need > 0 and need % 256 == 0

@@ -479,3 +479,87 @@ def test_g128_matvec_direct(dev, N, K, ncols):
     yo, acc = oracle.matmul_g128(w, N, K, x)
     _assert_close(y, yo, acc, TOL_SPLIT, f"g128 mat-vec {N}x{K} ncols={ncols}")
     _no_device_error()
+
+
+# ---------------------------------------------------------------------------
+# Expert mat-vec (mul_mat_id; the limitations paragraph of the WebGPU port
+# names MUL_MAT_ID as missing)
+# ---------------------------------------------------------------------------
+def _experts(g, n_expert, N, K):
+    return np.concatenate([synth.packed_matrix(g, N, K, *synth.DECODE_SCALE,
+                                               synth.DECODE_FRAC_CODE3) for _ in range(n_expert)])
+
+
+@pytest.mark.parametrize("n_expert,N,K,n_tokens,n_used,n_x", [
+    (4, 300, 1024, 3, 2, 1),     # ragged N: the last tile runs into the next expert's rows
+    (4, 300, 1024, 3, 2, 2),     # one vector per slot
+    (6, 128, 512, 5, 3, 1),      # one tile per expert
+    (3, 97, 768, 2, 2, 2),       # K % 512 != 0: the CUDA-core kernel
+    (1, 640, 2048, 4, 1, 1),     # a single expert
+])
+def test_mul_mat_id_parity(dev, n_expert, N, K, n_tokens, n_used, n_x):
+    g = synth.rng(4101, n_expert, N, K, n_tokens, n_used, n_x)
+    w = _experts(g, n_expert, N, K)
+    x = synth.activations(g, n_tokens * n_x, K).reshape(n_tokens, n_x, K)
+    ids = g.integers(0, n_expert, size=(n_tokens, n_used)).astype(np.int32)
+    y = q.q2_0_mul_mat_id(_to(dev, w), n_expert, N, K, _to(dev, x), _to(dev, ids)).cpu().numpy()
+    yo, acc, bad = oracle.matmul_id(w, n_expert, N, K, x, ids)
+    assert bad == 0
+    _assert_close(y.reshape(-1, N), yo.reshape(-1, N), acc.reshape(-1, N), TOL_SPLIT,
+                  f"mul_mat_id {n_expert}x{N}x{K} tokens={n_tokens} used={n_used} n_x={n_x}")
+    _no_device_error()
+
+
+def test_mul_mat_id_moe_decode_sampled(dev):
+    """A 128-expert layer of hidden 2048 (expert FFN 768), 8 experts per token:
+    gate-shaped experts 768 x 2048 at 1 and 16 tokens, sampled rows."""
+    n_expert, N, K, n_used = 128, 768, 2048, 8
+    g = synth.rng(4102)
+    w = _experts(g, n_expert, N, K)
+    wd = _to(dev, w)
+    for n_tokens in (1, 16):
+        x = synth.activations(g, n_tokens, K).reshape(n_tokens, 1, K)
+        ids = np.stack([g.permutation(n_expert)[:n_used] for _ in range(n_tokens)]).astype(np.int32)
+        y = q.q2_0_mul_mat_id(wd, n_expert, N, K, _to(dev, x), _to(dev, ids)).cpu().numpy()
+        rows = np.unique(np.concatenate([[0, 127, 128, N - 1], g.integers(0, N, 20)]))
+        yo, acc, bad = oracle.matmul_id(w, n_expert, N, K, x, ids, rows=rows)
+        assert bad == 0
+        _assert_close(y[:, :, rows].reshape(-1, rows.size), yo.reshape(-1, rows.size),
+                      acc.reshape(-1, rows.size), TOL_SPLIT, f"MoE decode tokens={n_tokens}")
+    _no_device_error()
+
+
+@pytest.mark.parametrize("K", [1024, 768])
+def test_mul_mat_id_bad_ids(dev, K):
+    """Out-of-range ids leave their slots unwritten and record BAD_ID; the other
+    slots are correct."""
+    n_expert, N, n_tokens, n_used = 3, 200, 2, 2
+    g = synth.rng(4103, K)
+    w = _experts(g, n_expert, N, K)
+    x = synth.activations(g, n_tokens, K).reshape(n_tokens, 1, K)
+    ids = np.array([[1, 3], [-2, 0]], dtype=np.int32)
+    y = torch.full((n_tokens, n_used, N), 7.0, device=dev)
+    q.q2_0_mul_mat_id(_to(dev, w), n_expert, N, K, _to(dev, x), _to(dev, ids), y=y)
+    code, info = q.q2_0_get_error()
+    assert code == q.Q2_0_DEVERR_BAD_ID and info in (1, 2)
+    yh = y.cpu().numpy()
+    assert np.all(yh[0, 1] == 7.0) and np.all(yh[1, 0] == 7.0)
+    yo, acc, bad = oracle.matmul_id(w, n_expert, N, K, x, ids)
+    assert bad == 2
+    for t, i in ((0, 0), (1, 1)):
+        _assert_close(yh[t, i][None], yo[t, i][None], acc[t, i][None], TOL_SPLIT, "good slots")
+
+
+def test_mul_mat_id_unaligned_weights(dev):
+    """Weights at an odd byte offset take the CUDA-core kernel."""
+    n_expert, N, K = 2, 64, 512
+    g = synth.rng(4104)
+    w = _experts(g, n_expert, N, K)
+    buf = torch.empty(w.size + 3, dtype=torch.uint8, device=dev)
+    buf[3:] = _to(dev, w)
+    x = synth.activations(g, 2, K).reshape(2, 1, K)
+    ids = np.array([[1], [0]], dtype=np.int32)
+    y = q.q2_0_mul_mat_id(buf[3:], n_expert, N, K, _to(dev, x), _to(dev, ids)).cpu().numpy()
+    yo, acc, _ = oracle.matmul_id(w, n_expert, N, K, x, ids)
+    _assert_close(y.reshape(-1, N), yo.reshape(-1, N), acc.reshape(-1, N), TOL_SPLIT, "unaligned")
+    _no_device_error()
