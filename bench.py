@@ -453,7 +453,9 @@ def measure_extras(torch, q, stream, dev, hbm_peak: float, reps: int = 20):
       - the 8B-class decode step (253 matrices with the 151936 x 4096 head,
         2,128,527,360 packed bytes, ncols 1) as one plan;
       - the 8B-class prefill GEMMs at M = 2048 (4096x4096, 12288x4096,
-        4096x12288), split fp16 hi+lo.
+        4096x12288), split fp16 hi+lo;
+      - the expert mat-vec (q2_0_mul_mat_id) of one 128-expert layer with
+        768 x 2048 experts, 8 experts per token, at 1 and 64 tokens.
     The 8B-class weights and activations are drawn on the device
     (synth.packed_matrix_device: the decode-step distribution, other bytes).
     Returns the GB/s and TFLOP/s figures."""
@@ -551,7 +553,29 @@ def measure_extras(torch, q, stream, dev, hbm_peak: float, reps: int = 20):
 
     ms2 = timed(gemms2)
     del g2
+
+    # expert mat-vec: 128 experts of 768 x 2048, 8 per token
+    n_exp, Ne, Ke, n_used = 128, 768, 2048, 8
+    we = synth.packed_matrix_device(torch, gen, n_exp * Ne, Ke, *synth.DECODE_SCALE,
+                                    synth.DECODE_FRAC_CODE3, dev)
+    moe = {}
+    for n_tok in (1, 64):
+        xe = torch.randn((n_tok, 1, Ke), generator=gen, device=dev)
+        ide = torch.stack([torch.randperm(n_exp, generator=gen, device=dev)[:n_used]
+                           for _ in range(n_tok)]).to(torch.int32)
+        ye = torch.empty((n_tok, n_used, Ne), dtype=torch.float32, device=dev)
+        wse = torch.empty(max(1, q.q2_0_mul_mat_id_workspace_size(Ke, n_tok, 1)),
+                          dtype=torch.uint8, device=dev)
+        mse = timed(lambda: q.q2_0_mul_mat_id(we, n_exp, Ne, Ke, xe, ide, y=ye, workspace=wse,
+                                              stream=stream))
+        slot_bytes = n_tok * n_used * q.packed_bytes(Ne, Ke)
+        distinct = int(torch.unique(ide).numel()) * q.packed_bytes(Ne, Ke)
+        moe[f"tokens_{n_tok}"] = {"us": round(mse * 1e3, 2),
+                                  "slot_weight_gbs": round(slot_bytes / (mse * 1e-3) / 1e9, 1),
+                                  "distinct_expert_gbs": round(distinct / (mse * 1e-3) / 1e9, 1)}
+    del we
     return {
+        "moe_mul_mat_id_128x768x2048_top8": moe,
         "decode_8b_step_ncols1": {"bytes": bytes8, "us": round(ms8 * 1e3, 2),
                                   "gbs": round(bytes8 / (ms8 * 1e-3) / 1e9, 1),
                                   "hbm_frac": round(bytes8 / (ms8 * 1e-3) / 1e9 / hbm_peak, 4),
