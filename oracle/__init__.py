@@ -73,6 +73,10 @@ def lib():
             L.qo_matmul_id.argtypes = [u8p, i64, i64, i64, f32p, i64, i32p, i64, i64, i64p, i64,
                                        f64p, f64p]
             L.qo_matmul_id.restype = i64
+            L.qo_soa_bytes.argtypes = [i64, i64]
+            L.qo_soa_bytes.restype = i64
+            L.qo_raw_to_soa.argtypes = [u8p, i64, i64, u8p]
+            L.qo_soa_to_raw.argtypes = [u8p, i64, i64, u8p]
             L.qo_get_rows.restype = i64
             L.qo_quantize_block.argtypes = [f32p, u8p]
             L.qo_quantize_rows.argtypes = [f32p, i64, i64, u8p]
@@ -217,6 +221,33 @@ def matmul_id(w, n_expert: int, N: int, K: int, x, ids, rows=None):
                              _p(ii, ctypes.c_int32), n_used, n_tokens, rp, nr,
                              _p(y, ctypes.c_double), _p(acc, ctypes.c_double))
     return y, acc, int(bad)
+
+
+def soa_bytes(N: int, K: int) -> int:
+    """Bytes of the split layout: 16 code bytes per block, then (256-byte
+    aligned) a 2-byte scale per block."""
+    return int(lib().qo_soa_bytes(N, K))
+
+
+def raw_to_soa(w, N: int, K: int) -> np.ndarray:
+    wb = _u8(w)
+    assert wb.size >= N * (K // 64) * 18
+    out = np.zeros(soa_bytes(N, K), dtype=np.uint8)
+    lib().qo_raw_to_soa(_p(wb, ctypes.c_uint8), N, K, _p(out, ctypes.c_uint8))
+    return out
+
+
+def soa_to_raw(soa, N: int, K: int) -> np.ndarray:
+    sb = _u8(soa)
+    assert sb.size >= soa_bytes(N, K)
+    out = np.empty(N * (K // 64) * 18, dtype=np.uint8)
+    lib().qo_soa_to_raw(_p(sb, ctypes.c_uint8), N, K, _p(out, ctypes.c_uint8))
+    return out
+
+
+def matmul_soa(soa, N: int, K: int, x, rows=None):
+    """matmul of a matrix stored in the split layout (back to blocks, then dot)."""
+    return matmul(soa_to_raw(soa, N, K), N, K, x, rows)
 
 
 def get_rows(table, n_rows: int, K: int, ids):

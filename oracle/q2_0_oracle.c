@@ -221,6 +221,49 @@ int64_t qo_matmul_id(const uint8_t *as, int64_t n_expert, int64_t N, int64_t K, 
 }
 
 /* ---------------------------------------------------------------------------
+ * Split (structure-of-arrays) layout. [KOPI] "Why the weight has to stay
+ * quantized" splits a block format's scales from its quants into separate
+ * arrays when loading; for Q2_0 that gives, for an N x K matrix with
+ * nb = K/64 blocks per row:
+ *   qs[n][b][16]  the 16 code bytes of block (n, b), row-major;
+ *   d[n][b]       its 2-byte little-endian fp16 scale, row-major;
+ * with d starting qs_bytes_padded = round_up(N*nb*16, 256) bytes after qs.
+ * The split moves bytes only; soa_to_raw is its inverse.
+ * ------------------------------------------------------------------------- */
+int64_t qo_soa_bytes(int64_t N, int64_t K) {
+    int64_t nb = K / QO_WEIGHTS_PER_BLOCK;
+    int64_t qs = (N * nb * 16 + 255) / 256 * 256;
+    int64_t d = (N * nb * 2 + 255) / 256 * 256;
+    return qs + d;
+}
+
+void qo_raw_to_soa(const uint8_t *w, int64_t N, int64_t K, uint8_t *soa) {
+    int64_t nb = K / QO_WEIGHTS_PER_BLOCK;
+    int64_t nblk = N * nb;
+    uint8_t *qs = soa;
+    uint8_t *d = soa + (nblk * 16 + 255) / 256 * 256;
+    for (int64_t i = 0; i < nblk; ++i) {
+        const uint8_t *blk = w + i * QO_BYTES_PER_BLOCK;
+        d[2 * i] = blk[0];
+        d[2 * i + 1] = blk[1];
+        memcpy(qs + 16 * i, blk + 2, 16);
+    }
+}
+
+void qo_soa_to_raw(const uint8_t *soa, int64_t N, int64_t K, uint8_t *w) {
+    int64_t nb = K / QO_WEIGHTS_PER_BLOCK;
+    int64_t nblk = N * nb;
+    const uint8_t *qs = soa;
+    const uint8_t *d = soa + (nblk * 16 + 255) / 256 * 256;
+    for (int64_t i = 0; i < nblk; ++i) {
+        uint8_t *blk = w + i * QO_BYTES_PER_BLOCK;
+        blk[0] = d[2 * i];
+        blk[1] = d[2 * i + 1];
+        memcpy(blk + 2, qs + 16 * i, 16);
+    }
+}
+
+/* ---------------------------------------------------------------------------
  * get_rows. [WGPU] shader paragraph: the get-rows shader copies rows of a Q2_0
  * tensor out and writes 64 floats per block. out[r][k] = W[ids[r]][k] as f32;
  * (q-1)*d is exact in fp64 and representable in f32, so the cast is exact and

@@ -515,3 +515,51 @@ def test_matmul_id_bad_ids(oracle_mod):
     assert bad == 2
     assert np.isnan(y[0, 1]).all() and np.isnan(y[1, 0]).all()
     assert not np.isnan(y[0, 0]).any() and not np.isnan(y[1, 1]).any()
+
+
+# ---------------------------------------------------------------------------
+# Split layout (scales and codes in separate arrays; [KOPI] "Why the weight has
+# to stay quantized" splits a block format's scales from its quants)
+# ---------------------------------------------------------------------------
+def test_soa_hand_built(oracle_mod):
+    """Two blocks with every byte distinct, laid out by hand."""
+    blk0 = np.arange(1, 19, dtype=np.uint8)            # d = 0x0201, codes 3..18
+    blk1 = np.arange(101, 119, dtype=np.uint8)         # d = 0x6665, codes 103..118
+    soa = oracle_mod.raw_to_soa(np.concatenate([blk0, blk1]), 1, 128)
+    expect = np.zeros(512, dtype=np.uint8)
+    expect[0:16] = np.arange(3, 19)
+    expect[16:32] = np.arange(103, 119)
+    expect[256:260] = [1, 2, 101, 102]
+    assert oracle_mod.soa_bytes(1, 128) == 512
+    assert np.array_equal(soa, expect)
+
+
+def test_soa_round_trip_and_sizes(oracle_mod):
+    g = np.random.default_rng(81)
+    for N, K in [(1, 64), (7, 192), (33, 512), (300, 1024)]:
+        w = synth.packed_matrix(g, N, K, 0.005, 0.05, 0.01)
+        soa = oracle_mod.raw_to_soa(w, N, K)
+        nblk = N * (K // 64)
+        assert soa.size == -(-16 * nblk // 256) * 256 + -(-2 * nblk // 256) * 256
+        assert np.array_equal(oracle_mod.soa_to_raw(soa, N, K), w)
+        x = synth.activations(g, 2, K)
+        assert np.array_equal(oracle_mod.matmul_soa(soa, N, K, x)[0], oracle_mod.matmul(w, N, K, x)[0])
+
+
+def test_soa_element_decode(oracle_mod):
+    """Element e of block (n, b) read from the split arrays (code byte e // 4,
+    field e % 4; scale from d[]) equals the pinned block decode."""
+    g = np.random.default_rng(82)
+    N, K = 5, 256
+    nb = K // 64
+    w = synth.packed_matrix(g, N, K, 0.01, 3.0, 0.1)
+    soa = oracle_mod.raw_to_soa(w, N, K)
+    d_off = -(-16 * N * nb // 256) * 256
+    for n in range(N):
+        for b in range(nb):
+            i = n * nb + b
+            ref = oracle_mod.decode_block(w[18 * i:18 * i + 18])
+            d = oracle_mod.half_to_double(int(soa[d_off + 2 * i]) | (int(soa[d_off + 2 * i + 1]) << 8))
+            for e in range(64):
+                q = (int(soa[16 * i + e // 4]) >> (2 * (e % 4))) & 3
+                assert (q - 1) * d == ref[e]
