@@ -447,6 +447,8 @@ def measure_extras(torch, q, stream, dev, hbm_peak: float, reps: int = 20):
     events on the launching stream:
       - the 151936 x 4096 output-head mat-vec (ncols 1), with F32 and with F16
         activations (175 MB of packed weights, above L2);
+      - the same head mat-vec on the split layout (codes and scales in
+        separate arrays), against the 18-byte layout, and the split itself;
       - the M = 512 prefill GEMMs with F16 activations (q2_0_mul_mat_f16);
       - the group-128 packing of the head-sized matrix: exact repack to the
         64-weight layout (bytes read + written) and the direct mat-vec;
@@ -490,7 +492,12 @@ def measure_extras(torch, q, stream, dev, hbm_peak: float, reps: int = 20):
 
     ms32 = timed(lambda: q.q2_0_mul_mat_vec(w, x, N, K, 1, y=y, stream=stream))
     ms16 = timed(lambda: q.q2_0_mul_mat_vec_f16(w, x16, N, K, 1, y=y, stream=stream))
-    del w
+    # the same head in the split layout (codes and scales apart), and the split itself
+    split = q.q2_0_split_layout(w, N, K)
+    ms_sp = timed(lambda: q.q2_0_mul_mat_vec_split(split, x, N, K, 1, y=y, stream=stream))
+    ms_mk = timed(lambda: q.q2_0_split_layout(w, N, K, dst=split, stream=stream))
+    split_bytes = split.numel()
+    del w, split
     gm = []
     for name, Ng, Kg, wg, xg in gemm_inputs():
         ws = torch.empty(q.q2_0_mul_mat_workspace_size(PREFILL_M, Ng, Kg, q.Q2_0_PREC_F16),
@@ -583,6 +590,12 @@ def measure_extras(torch, q, stream, dev, hbm_peak: float, reps: int = 20):
         "gemm_split_m2048_8b": {"tflops": round(flops2 / (ms2 * 1e-3) / 1e12, 2),
                                 "us": round(ms2 * 1e3, 2),
                                 "shapes": [[M2, 4096, 4096], [M2, 12288, 4096], [M2, 4096, 12288]]},
+        "head_matvec_split_layout_151936x4096": {
+            "split_bytes": split_bytes, "us": round(ms_sp * 1e3, 2),
+            "gbs": round(head_bytes / (ms_sp * 1e-3) / 1e9, 1),
+            "vs_18_byte_layout": round(ms32 / ms_sp, 3),
+            "split_layout_us": round(ms_mk * 1e3, 2),
+            "split_layout_gbs": round((head_bytes + split_bytes) / (ms_mk * 1e-3) / 1e9, 1)},
         "head_matvec_151936x4096": {"bytes": head_bytes,
                                     "f32_gbs": round(head_bytes / (ms32 * 1e-3) / 1e9, 1),
                                     "f16_gbs": round(head_bytes / (ms16 * 1e-3) / 1e9, 1),

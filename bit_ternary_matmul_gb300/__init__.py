@@ -53,6 +53,7 @@ EXPORTS = (
     "q2_0_mul_mat_vec_f16", "q2_0_mul_mat_f16",
     "q2_0_g128_to_g64", "q2_0_g128_get_rows", "q2_0_g128_mul_mat_vec",
     "q2_0_mul_mat_id_workspace_size", "q2_0_mul_mat_id",
+    "q2_0_split_bytes", "q2_0_split_layout", "q2_0_join_layout", "q2_0_mul_mat_vec_split",
 )
 
 
@@ -130,6 +131,14 @@ def lib():
             L.q2_0_mul_mat_id_workspace_size.restype = sz
             L.q2_0_mul_mat_id.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, i64, vp, vp, sz, vp]
             L.q2_0_mul_mat_id.restype = i32
+            L.q2_0_split_bytes.argtypes = [i64, i64]
+            L.q2_0_split_bytes.restype = sz
+            L.q2_0_split_layout.argtypes = [vp, vp, i64, i64, vp]
+            L.q2_0_split_layout.restype = i32
+            L.q2_0_join_layout.argtypes = [vp, vp, i64, i64, vp]
+            L.q2_0_join_layout.restype = i32
+            L.q2_0_mul_mat_vec_split.argtypes = [vp, vp, vp, i64, i64, i32, vp]
+            L.q2_0_mul_mat_vec_split.restype = i32
             L.q2_0_quantize_ref.argtypes = [vp, vp, i64, i64, vp]
             L.q2_0_quantize_ref.restype = i32
             L.q2_0_get_error.argtypes = [vp, ctypes.POINTER(i64)]
@@ -370,6 +379,46 @@ def q2_0_mul_mat_id(w: torch.Tensor, n_expert: int, N: int, K: int, x: torch.Ten
                                _dev(y, "y", torch.float32, n_tokens * n_used * N), wsp,
                                need if need > 0 else 0, _stream(stream))
     _check("q2_0_mul_mat_id", st)
+    return y
+
+
+def q2_0_split_bytes(N: int, K: int) -> int:
+    return int(lib().q2_0_split_bytes(N, K))
+
+
+def q2_0_split_layout(w: torch.Tensor, N: int, K: int, dst: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """18-byte blocks -> split layout (codes, then 256-byte aligned fp16 scales)."""
+    nbytes = q2_0_split_bytes(N, K)
+    if dst is None:
+        dst = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
+    st = lib().q2_0_split_layout(_dev(w, "w", torch.uint8, packed_bytes(N, K)),
+                                 _dev(dst, "dst", torch.uint8, nbytes), N, K, _stream(stream))
+    _check("q2_0_split_layout", st)
+    return dst
+
+
+def q2_0_join_layout(src: torch.Tensor, N: int, K: int, w: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """Split layout -> 18-byte blocks."""
+    if w is None:
+        w = torch.empty(packed_bytes(N, K), dtype=torch.uint8, device=src.device)
+    st = lib().q2_0_join_layout(_dev(src, "src", torch.uint8, q2_0_split_bytes(N, K)),
+                                _dev(w, "w", torch.uint8, packed_bytes(N, K)), N, K, _stream(stream))
+    _check("q2_0_join_layout", st)
+    return w
+
+
+def q2_0_mul_mat_vec_split(w: torch.Tensor, x: torch.Tensor, N: int, K: int, ncols: int = 1,
+                           y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[c][n] = sum_k W[n][k] x[c][k] with W in the split layout."""
+    if y is None:
+        y = torch.empty((ncols, N), dtype=torch.float32, device=x.device)
+    st = lib().q2_0_mul_mat_vec_split(_dev(w, "w", torch.uint8, q2_0_split_bytes(N, K)),
+                                      _dev(x, "x", torch.float32, ncols * K),
+                                      _dev(y, "y", torch.float32, ncols * N), N, K, ncols,
+                                      _stream(stream))
+    _check("q2_0_mul_mat_vec_split", st)
     return y
 
 

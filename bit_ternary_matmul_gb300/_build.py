@@ -12,7 +12,8 @@ LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libq2_0.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "get_rows.cu", "quantize.cu", "matvec.cu", "gemm.cu", "noalloc.cu", "g128.cu"]
+SOURCES = ["api.cu", "get_rows.cu", "quantize.cu", "matvec.cu", "gemm.cu", "noalloc.cu", "g128.cu",
+           "soa.cu"]
 HEADERS = ["q2_0_device.cuh", "q2_0_internal.h", "q2_0_tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -245,6 +245,44 @@ int q2_0_mul_mat_f16(const void *w, const void *x, float *y, int64_t N, int64_t 
     return mul_mat_impl(w, x, kXF16, y, N, K, M, Q2_0_PREC_F16, workspace, workspace_bytes, stream);
 }
 
+size_t q2_0_split_bytes(int64_t N, int64_t K) {
+    if (N < 1 || N > (int64_t(1) << 31) - 1 || !valid_k(K)) return 0;
+    return soa_bytes(N, K);
+}
+
+int q2_0_split_layout(const void *w, void *dst, int64_t N, int64_t K, void *stream) {
+    if (!w || !dst || N < 1 || N > (int64_t(1) << 31) - 1 || !valid_k(K)) return Q2_0_EINVAL;
+    int st = check_device(nullptr);
+    if (st != Q2_0_OK) return st;
+    return cuda_status(launch_soa_move(static_cast<const uint8_t *>(w), static_cast<uint8_t *>(dst),
+                                       N, K, true, as_stream(stream)));
+}
+
+int q2_0_join_layout(const void *src, void *w, int64_t N, int64_t K, void *stream) {
+    if (!src || !w || N < 1 || N > (int64_t(1) << 31) - 1 || !valid_k(K)) return Q2_0_EINVAL;
+    int st = check_device(nullptr);
+    if (st != Q2_0_OK) return st;
+    return cuda_status(launch_soa_move(static_cast<const uint8_t *>(src), static_cast<uint8_t *>(w),
+                                       N, K, false, as_stream(stream)));
+}
+
+int q2_0_mul_mat_vec_split(const void *w, const float *x, float *y, int64_t N, int64_t K,
+                           int ncols, void *stream) {
+    if (!w || !x || !y || N < 1 || N > (int64_t(1) << 31) - 1 || !valid_k(K) || ncols < 1 ||
+        ncols > 8)
+        return Q2_0_EINVAL;
+    int st = check_device(nullptr);
+    if (st != Q2_0_OK) return st;
+    const size_t need = ncols == 1 ? matvec_workspace_bytes(K, 1) : 0;
+    PoolScratch ws;
+    st = ws.alloc(need, as_stream(stream));
+    if (st != Q2_0_OK) return st;
+    st = matvec_split_run(static_cast<const uint8_t *>(w), x, y, N, K, ncols, ws.ptr, need,
+                          as_stream(stream));
+    int st2 = ws.release();
+    return st != Q2_0_OK ? st : st2;
+}
+
 // Expert mat-vec shapes: n_expert * N rows must fit a tensor-map coordinate,
 // and the activation vectors a grid dimension.
 static bool valid_moe(int64_t n_expert, int64_t N, int64_t K, int64_t n_x, int64_t n_used,

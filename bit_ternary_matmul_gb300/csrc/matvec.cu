@@ -90,6 +90,7 @@ struct MvJob {  // 64-byte aligned through its CUtensorMap member
     int nb;        // K / 64
     int n_chunks;  // K / 512
     int n_tiles;   // ceil(N / 256)
+    CUtensorMap tmap_d;  // split layout only: fp16 scales [N][K/64], box {16, 128}
 };
 
 struct MvItem {
@@ -118,6 +119,7 @@ struct MvParams {
     int n_stages;             // pipeline depth (n_stages_for(ncols))
     unsigned long long *err;
     MvMoe moe;
+    int split;                // fp4 kernel only: 1 = the split layout (codes and scales apart)
 };
 
 // Record per block per n-tile, for S = lane slots carrying data (8 per column of
@@ -1339,6 +1341,8 @@ constexpr int kT4LastOfTile = 2;
 //   warps 8-11   epilogue, one per lane quarter, all 8 blocks of a stage.
 // Measured: more warps per sub-partition (two expansion or two epilogue warps
 // per quarter) lengthened the stage period; 12 warps gave the shortest.
+constexpr int kT4SplitCodeBytes = kT5Rows * 128;  // 16 KB of codes, then 2 KB of scales
+static_assert(kT4SplitCodeBytes + kT5Rows * 16 == kT5RawBytes, "split stage = block stage bytes");
 constexpr int kT4ProdWarp = 2;
 constexpr int kT4MmaWarp = 3;
 constexpr int kT4MmaWarp2 = 1;
@@ -1348,6 +1352,11 @@ constexpr int kT4EpiWarp0 = 8;
 constexpr int kT4EpiWarps = 4;
 constexpr int kT4Threads = 12 * 32;
 
+// kSplit: the weights are in the split layout (codes [N][K/64][16], scales
+// [N][K/64]); the stage's code box is 128 bytes x 128 rows with 128-byte swizzle
+// and its scale box 16 bytes x 128 rows, together the same 18 KB as the block
+// box of the 18-byte layout.
+template <bool kSplit>
 __global__ void __launch_bounds__(kT4Threads, 1)
     mv_t4_kernel(const __grid_constant__ MvJob single, const MvParams p) {
     // The next prep launch on the stream may become resident now; it waits for
@@ -1476,8 +1485,15 @@ __global__ void __launch_bounds__(kT4Threads, 1)
                     m.n_rows = J->N;
                     m.flags = (ch == 0 ? kT4FirstOfTile : 0) | (ch == nch - 1 ? kT4LastOfTile : 0);
                     mbar_arrive_expect_tx(&full[st], kT5RawBytes + kT4ImgBytes + kT4BetaBytes);
-                    tma_load_2d(raw_ring + st * kT5RawBytes, &J->tmap, ch * kChunkBytes,
-                                row_base + tile * kT5Rows, &full[st]);
+                    if (kSplit) {
+                        tma_load_2d(raw_ring + st * kT5RawBytes, &J->tmap, ch * 128,
+                                    row_base + tile * kT5Rows, &full[st]);
+                        tma_load_2d(raw_ring + st * kT5RawBytes + kT4SplitCodeBytes, &J->tmap_d,
+                                    ch * 16, row_base + tile * kT5Rows, &full[st]);
+                    } else {
+                        tma_load_2d(raw_ring + st * kT5RawBytes, &J->tmap, ch * kChunkBytes,
+                                    row_base + tile * kT5Rows, &full[st]);
+                    }
                     if (!prep_ready) {
                         grid_dependency_wait();  // the B images come from the prep kernel
                         prep_ready = true;
@@ -1568,26 +1584,44 @@ __global__ void __launch_bounds__(kT4Threads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int G = 0; G < 2; ++G) {
-                    const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes + G * 72;
-                    uint32_t u[18];
-#pragma unroll
-                    for (int k = 0; k < 9; ++k) {
-                        const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * k);
-                        u[2 * k] = v.x;
-                        u[2 * k + 1] = v.y;
-                    }
                     uint32_t a[32];
+                    if (kSplit) {
+                        // block 4G+bi is 16-byte chunk 4G+bi of the row, stored at
+                        // chunk (4G+bi) ^ (row % 8) by the 128-byte swizzle
+                        const uint8_t *rp = raw_ring + st * kT5RawBytes + row * 128;
 #pragma unroll
-                    for (int bi = 0; bi < 4; ++bi) {
+                        for (int bi = 0; bi < 4; ++bi) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(
+                                rp + (((4 * G + bi) ^ (row & 7)) << 4));
+                            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint32_t w;
-                            if (bi == 0) w = __byte_perm(u[c], u[c + 1], 0x5432);
-                            else if (bi == 1) w = u[5 + c];
-                            else if (bi == 2) w = __byte_perm(u[9 + c], u[10 + c], 0x5432);
-                            else w = u[14 + c];
-                            a[8 * bi + 2 * c + 0] = w & 0x33333333u;
-                            a[8 * bi + 2 * c + 1] = (w >> 2) & 0x33333333u;
+                            for (int c = 0; c < 4; ++c) {
+                                a[8 * bi + 2 * c + 0] = wv[c] & 0x33333333u;
+                                a[8 * bi + 2 * c + 1] = (wv[c] >> 2) & 0x33333333u;
+                            }
+                        }
+                    } else {
+                        const uint8_t *rp =
+                            raw_ring + st * kT5RawBytes + row * kChunkBytes + G * 72;
+                        uint32_t u[18];
+#pragma unroll
+                        for (int k = 0; k < 9; ++k) {
+                            const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * k);
+                            u[2 * k] = v.x;
+                            u[2 * k + 1] = v.y;
+                        }
+#pragma unroll
+                        for (int bi = 0; bi < 4; ++bi) {
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                uint32_t w;
+                                if (bi == 0) w = __byte_perm(u[c], u[c + 1], 0x5432);
+                                else if (bi == 1) w = u[5 + c];
+                                else if (bi == 2) w = __byte_perm(u[9 + c], u[10 + c], 0x5432);
+                                else w = u[14 + c];
+                                a[8 * bi + 2 * c + 0] = w & 0x33333333u;
+                                a[8 * bi + 2 * c + 1] = (w >> 2) & 0x33333333u;
+                            }
                         }
                     }
                     tmem_st32(tmem + lane_base + a_col(s) + 32 * G, a);
@@ -1639,7 +1673,10 @@ __global__ void __launch_bounds__(kT4Threads, 1)
                 for (int pp = kT4Pieces - 2; pp >= 1; --pp)
                     t = fmaf(__uint_as_float(r[b][pp]), __int_as_float((127 - 2 * pp) << 23), t);
                 t = t + __uint_as_float(r[b][0]);
-                const float d = lds_half_as_float(rp + 18 * b);
+                const float d =
+                    kSplit ? lds_half_as_float(raw_ring + st * kT5RawBytes + kT4SplitCodeBytes +
+                                               row * 16 + 2 * b)
+                           : lds_half_as_float(rp + 18 * b);
                 acc = fmaf(d, t - bt[b], acc);
             }
             __syncwarp();
@@ -1763,7 +1800,11 @@ cudaError_t ensure_t4_attr() {
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(g_attr_mu);
     if (dev < 64 && g_t4_attr_done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(mv_t4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kT4Smem);
+    e = cudaFuncSetAttribute(mv_t4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kT4Smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mv_t4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kT4Smem);
     if (e == cudaSuccess && dev < 64) g_t4_attr_done[dev] = true;
     return e;
 }
@@ -1877,7 +1918,8 @@ cudaError_t launch_tc(const MvJob &single, const MvParams &prm, int grid, cudaSt
     if (use_t4(prm.ncols)) {
         cfg.blockDim = dim3(kT4Threads);
         cfg.dynamicSmemBytes = kT4Smem;
-        e = cudaLaunchKernelEx(&cfg, mv_t4_kernel, single, prm);
+        e = prm.split ? cudaLaunchKernelEx(&cfg, mv_t4_kernel<true>, single, prm)
+                      : cudaLaunchKernelEx(&cfg, mv_t4_kernel<false>, single, prm);
     } else if (use_t5(prm.ncols)) {
         cfg.blockDim = dim3(kT5Threads);
         cfg.dynamicSmemBytes = kT5Smem;
@@ -1937,6 +1979,38 @@ int matvec_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, 
     MvJob J;
     if (!make_job(J, w, prep, y, N, K, tile_rows_for(ncols))) return Q2_0_ECUDA;
     MvParams prm{nullptr, nullptr, nullptr, nullptr, ncols, n_stages_for(ncols), err};
+    const int grid = std::max(1, std::min(J.n_tiles, sm_count()));
+    return cuda_status(launch_tc(J, prm, grid, s));
+}
+
+int matvec_split_run(const uint8_t *soa, const float *x, float *y, int64_t N, int64_t K,
+                     int ncols, void *ws, size_t ws_bytes, cudaStream_t s) {
+    const uint8_t *dsc = soa + soa_qs_bytes(N, K);
+    if (ncols != 1 || !matvec_fast_path_ok(soa, K))
+        return cuda_status(launch_soa_generic(soa, x, y, N, K, ncols, s));
+    if (ws_bytes < t4_prep_bytes(K)) return Q2_0_EINVAL;
+    unsigned long long *err = error_word_ptr();
+    if (!err) return Q2_0_ECUDA;
+    uint8_t *prep = static_cast<uint8_t *>(ws);
+    MvPrepJob pj{x, prep, int(K)};
+    if (launch_prep(pj, nullptr, 1, 1, K, kXF32, s) != cudaSuccess) return Q2_0_ECUDA;
+    MvJob J;
+    std::memset(&J, 0, sizeof(J));
+    const uint64_t nb = uint64_t(K / 64);
+    // codes: 128 bytes (8 blocks) x 128 rows per box, 128-byte swizzle;
+    // scales: 16 bytes x 128 rows per box
+    if (!encode_tmap_2d(&J.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, soa, nb * 16, uint64_t(N), nb * 16,
+                        128, kT5Rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap_2d(&J.tmap_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, dsc, nb * 2, uint64_t(N), nb * 2,
+                        16, kT5Rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return Q2_0_ECUDA;
+    J.prep = prep;
+    J.y = y;
+    J.N = int(N);
+    J.nb = int(nb);
+    J.n_chunks = int(K / 512);
+    J.n_tiles = int((N + kT5Rows - 1) / kT5Rows);
+    MvParams prm{nullptr, nullptr, nullptr, nullptr, 1, n_stages_for(1), err, MvMoe{}, 1};
     const int grid = std::max(1, std::min(J.n_tiles, sm_count()));
     return cuda_status(launch_tc(J, prm, grid, s));
 }

@@ -50,6 +50,18 @@ bool matvec_fast_path_ok(const void *w, int64_t K);
 int matvec_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, int64_t K,
                int ncols, void *ws, size_t ws_bytes, cudaStream_t s);
 
+// split layout: codes [N][K/64][16], then (256-byte aligned) fp16 scales [N][K/64]
+size_t soa_qs_bytes(int64_t N, int64_t K);
+size_t soa_bytes(int64_t N, int64_t K);
+cudaError_t launch_soa_move(const uint8_t *src, uint8_t *dst, int64_t N, int64_t K, bool to_soa,
+                            cudaStream_t s);
+cudaError_t launch_soa_generic(const uint8_t *soa, const float *x, float *y, int64_t N, int64_t K,
+                               int ncols, cudaStream_t s);
+// mat-vec on the split layout: ncols 1 with K % 512 == 0 on the fp4 kernel
+// (scratch: matvec_workspace_bytes(K, 1)); other shapes on CUDA cores
+int matvec_split_run(const uint8_t *soa, const float *x, float *y, int64_t N, int64_t K,
+                     int ncols, void *ws, size_t ws_bytes, cudaStream_t s);
+
 // expert mat-vec (mul_mat_id), F32 x: one fp4 prep region per activation vector
 size_t matvec_moe_workspace_bytes(int64_t K, int64_t n_xvec);
 int matvec_moe_run(const uint8_t *w, int64_t n_expert, int64_t N, int64_t K, const float *x,

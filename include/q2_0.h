@@ -192,6 +192,33 @@ int q2_0_mul_mat_f16(const void *w, const void *x, float *y, int64_t N, int64_t 
                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Split layout — scales and codes in separate arrays, as the loader in
+ * "kopitiam_runtime::gpu_offload" (section "Why the weight has to stay
+ * quantized") splits a block format's scales from its quants. For an N x K
+ * Q2_0 matrix with nb = K/64 blocks per row, the split buffer holds
+ *   qs[n][b][16]  the 16 code bytes of block (n, b), row-major, then, from
+ *                 byte round_up(N * nb * 16, 256),
+ *   d[n][b]       its fp16 scale (2 bytes, little-endian), row-major;
+ * q2_0_split_bytes(N, K) bytes in all. The code and scale rules are the
+ * 18-byte block's. The split is a load-time option; q2_0_mul_mat_vec_split
+ * computes what q2_0_mul_mat_vec computes on the 18-byte layout.
+ *   q2_0_split_layout  18-byte blocks w -> split buffer dst (bit-exact move).
+ *   q2_0_join_layout   split buffer src -> 18-byte blocks w (its inverse).
+ *   q2_0_mul_mat_vec_split  y = W x with W in the split layout; same bound as
+ *       q2_0_mul_mat_vec. Fast path (fp4 tensor cores): ncols 1, K % 512 == 0,
+ *       the buffer 16-byte aligned; otherwise a CUDA-core kernel. Scratch is
+ *       stream-ordered, from the default memory pool.
+ * Returns 0 from q2_0_split_bytes and Q2_0_EINVAL from the others for N < 1,
+ * N >= 2^31 or K not a positive multiple of 64. Device pointers, owned by the
+ * caller.
+ */
+size_t q2_0_split_bytes(int64_t N, int64_t K);
+int q2_0_split_layout(const void *w, void *dst, int64_t N, int64_t K, void *stream);
+int q2_0_join_layout(const void *src, void *w, int64_t N, int64_t K, void *stream);
+int q2_0_mul_mat_vec_split(const void *w, const float *x, float *y, int64_t N, int64_t K,
+                           int ncols, void *stream);
+
+/*
  * q2_0_mul_mat_id — expert mat-vec of a mixture-of-experts layer (ggml
  * mul_mat_id; the limitations paragraph of "WebGPU: add Q2_0 support" names
  * MUL_MAT_ID as not ported).

@@ -79,6 +79,14 @@ def test_argument_validation_without_gpu(L):
                              null) == EINVAL
     assert L.q2_0_mul_mat_id(p, 4, 8, 512, p, 2, ids, 2, 3, p, ctypes.c_void_p(0x100010), need,
                              null) == EINVAL  # workspace not 256-byte aligned
+    # split layout: sizes and argument checks
+    assert L.q2_0_split_bytes(1, 128) == 512
+    assert L.q2_0_split_bytes(300, 1024) == 76800 + 9728
+    assert L.q2_0_split_bytes(0, 128) == 0 and L.q2_0_split_bytes(4, 100) == 0
+    assert L.q2_0_split_layout(null, p, 4, 64, null) == EINVAL
+    assert L.q2_0_join_layout(p, p, 4, 96, null) == EINVAL
+    assert L.q2_0_mul_mat_vec_split(p, p, p, 4, 64, 9, null) == EINVAL
+    assert L.q2_0_mul_mat_vec_split(p, p, p, 0, 64, 1, null) == EINVAL
     # mat-vec with workspace: too small, misaligned
     need = L.q2_0_mul_mat_vec_workspace_size(512, 1)
     assert need > 0 and need % 256 == 0

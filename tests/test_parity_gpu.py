@@ -563,3 +563,56 @@ def test_mul_mat_id_unaligned_weights(dev):
     yo, acc, _ = oracle.matmul_id(w, n_expert, N, K, x, ids)
     _assert_close(y.reshape(-1, N), yo.reshape(-1, N), acc.reshape(-1, N), TOL_SPLIT, "unaligned")
     _no_device_error()
+
+
+# ---------------------------------------------------------------------------
+# Split layout (codes and scales in separate arrays)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("N,K", [(1, 64), (300, 1024), (129, 576), (2048, 2048)])
+def test_split_layout_bit_exact_and_round_trip(dev, N, K):
+    g = synth.rng(5101, N, K)
+    w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    ref = oracle.raw_to_soa(w, N, K)
+    dst = torch.full((q.q2_0_split_bytes(N, K),), 0xAB, dtype=torch.uint8, device=dev)
+    q.q2_0_split_layout(_to(dev, w), N, K, dst=dst)
+    got = dst.cpu().numpy()
+    # the padding between and after the arrays is not written; compare the arrays
+    nblk = N * (K // 64)
+    d_off = -(-16 * nblk // 256) * 256
+    assert np.array_equal(got[:16 * nblk], ref[:16 * nblk])
+    assert np.array_equal(got[d_off:d_off + 2 * nblk], ref[d_off:d_off + 2 * nblk])
+    back = q.q2_0_join_layout(dst, N, K).cpu().numpy()
+    assert np.array_equal(back, w)
+
+
+@pytest.mark.parametrize("N,K,ncols", [(300, 2048, 1), (2048, 6144, 1), (1000, 512, 1),
+                                       (129, 576, 1), (257, 1024, 3), (64, 2048, 8)])
+def test_matvec_split_parity(dev, N, K, ncols):
+    g = synth.rng(5102, N, K, ncols)
+    w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    x = synth.activations(g, ncols, K)
+    soa = q.q2_0_split_layout(_to(dev, w), N, K)
+    y = q.q2_0_mul_mat_vec_split(soa, _to(dev, x), N, K, ncols).cpu().numpy()
+    yo, acc = oracle.matmul_soa(oracle.raw_to_soa(w, N, K), N, K, x)
+    _assert_close(y, yo, acc, TOL_SPLIT, f"split mat-vec {N}x{K} ncols={ncols}")
+    _no_device_error()
+
+
+def test_matvec_split_head_sampled_and_unaligned(dev):
+    """The 151936 x 4096 head in the split layout (sampled rows), and the same
+    buffer at an 8-byte offset, which takes the CUDA-core kernel."""
+    N, K = 151936, 4096
+    g = synth.rng(5103)
+    w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    x = synth.activations(g, 1, K)
+    soa = q.q2_0_split_layout(_to(dev, w), N, K)
+    y = q.q2_0_mul_mat_vec_split(soa, _to(dev, x), N, K).cpu().numpy()
+    rows = np.unique(np.concatenate([[0, 127, 128, N - 1], g.integers(0, N, 60)]))
+    yo, acc = oracle.matmul(w, N, K, x, rows=rows)
+    _assert_close(y[:, rows], yo, acc, TOL_SPLIT, "split head")
+    nb = q.q2_0_split_bytes(N, K)
+    buf = torch.empty(nb + 8, dtype=torch.uint8, device=dev)
+    buf[8:] = soa
+    y2 = q.q2_0_mul_mat_vec_split(buf[8:], _to(dev, x), N, K).cpu().numpy()
+    _assert_close(y2[:, rows], yo, acc, TOL_SPLIT, "split head, unaligned")
+    _no_device_error()
