@@ -1343,6 +1343,7 @@ constexpr int kT4LastOfTile = 2;
 // per quarter) lengthened the stage period; 12 warps gave the shortest.
 constexpr int kT4SplitCodeBytes = kT5Rows * 128;  // 16 KB of codes, then 2 KB of scales
 static_assert(kT4SplitCodeBytes + kT5Rows * 16 == kT5RawBytes, "split stage = block stage bytes");
+static_assert(kT4Pieces == 12, "the epilogue loads pieces 0-7 and 8-11");
 constexpr int kT4ProdWarp = 2;
 constexpr int kT4MmaWarp = 3;
 constexpr int kT4MmaWarp2 = 1;
@@ -1356,8 +1357,11 @@ constexpr int kT4Threads = 12 * 32;
 // [N][K/64]); the stage's code box is 128 bytes x 128 rows with 128-byte swizzle
 // and its scale box 16 bytes x 128 rows, together the same 18 KB as the block
 // box of the 18-byte layout.
+// At most 128 registers a thread (384 x 128 = 48K of the SM's 64K), so a CTA of
+// the next prep kernel (256 threads x 64 registers) can be resident beside it
+// and the programmatic launch overlaps the two.
 template <bool kSplit>
-__global__ void __launch_bounds__(kT4Threads, 1)
+__global__ void __maxnreg__(128)
     mv_t4_kernel(const __grid_constant__ MvJob single, const MvParams p) {
     // The next prep launch on the stream may become resident now; it waits for
     // this grid before it touches any buffer this kernel reads.
@@ -1656,9 +1660,13 @@ __global__ void __launch_bounds__(kT4Threads, 1)
             const T4StageMeta m = s_meta[st];
             if (m.flags & kT4FirstOfTile) shift = *m.col_shift;
             const uint32_t d_base = tmem + lane_base + d_col(s);
-            uint32_t r[8][16];
+            // pieces 0-7 and 8-11 of each block (columns 12-15 hold zeros)
+            uint32_t r[8][8], r2[8][4];
 #pragma unroll
-            for (int bi = 0; bi < 8; ++bi) tmem_ld16(d_base + bi * kT5N, r[bi]);
+            for (int bi = 0; bi < 8; ++bi) {
+                tmem_ld8(d_base + bi * kT5N, r[bi]);
+                tmem_ld4(d_base + bi * kT5N + 8, r2[bi]);
+            }
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -1667,12 +1675,12 @@ __global__ void __launch_bounds__(kT4Threads, 1)
             const float *bt = reinterpret_cast<const float *>(beta_ring + st * kT4BetaBytes);
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
-                float t = __uint_as_float(r[b][kT4Pieces - 1]) *
-                          __int_as_float((127 - 2 * (kT4Pieces - 1)) << 23);
+                auto piece = [&](int pp) { return __uint_as_float(pp < 8 ? r[b][pp] : r2[b][pp - 8]); };
+                float t = piece(kT4Pieces - 1) * __int_as_float((127 - 2 * (kT4Pieces - 1)) << 23);
 #pragma unroll
                 for (int pp = kT4Pieces - 2; pp >= 1; --pp)
-                    t = fmaf(__uint_as_float(r[b][pp]), __int_as_float((127 - 2 * pp) << 23), t);
-                t = t + __uint_as_float(r[b][0]);
+                    t = fmaf(piece(pp), __int_as_float((127 - 2 * pp) << 23), t);
+                t = t + piece(0);
                 const float d =
                     kSplit ? lds_half_as_float(raw_ring + st * kT5RawBytes + kT4SplitCodeBytes +
                                                row * 16 + 2 * b)
