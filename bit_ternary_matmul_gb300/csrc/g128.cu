@@ -9,7 +9,7 @@
 // then eight little-endian words, element 16w+i in bits 2i..2i+1 of word w,
 // code q -> (q - 1) * d.
 //
-// On this GPU the fast kernels are built around 18-byte blocks (TMA boxes of
+// On GB300 the fast kernels are built around 18-byte blocks (TMA boxes of
 // 144-byte rows). A group-128 matrix is therefore repacked once, exactly, into
 // the 64-weight layout (each block becomes two blocks with the same scale, 36
 // bytes instead of 34), after which every fast path applies. get_rows reads the

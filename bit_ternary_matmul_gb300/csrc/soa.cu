@@ -10,8 +10,8 @@
 // The split is a byte move; the code and scale rules are those of the 18-byte
 // block ("WebGPU: add Q2_0 support", format paragraph).
 //
-// On this GPU the split gives 128-byte code rows per 8 blocks, a width the
-// tensor-memory copy engine can swizzle, so the fp4 mat-vec reads them with
+// On GB300 the split gives 128-byte code rows per 8 blocks, a width the TMA
+// engine can swizzle, so the fp4 mat-vec reads them with
 // conflict-free 16-byte shared-memory loads and no byte shuffles
 // (mv_t4_kernel<true>). This file holds the layout kernels and the CUDA-core
 // mat-vec used off that fast path.
