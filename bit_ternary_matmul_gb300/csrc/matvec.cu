@@ -1171,23 +1171,37 @@ __global__ void __launch_bounds__(kT5Threads, 1)
 // the low two (exponent bit 0, mantissa) reads as 0, 0.5, 1, 1.5 = q / 2. With
 // each code at bits 2i of a word, word & 0x33333333 holds the even elements
 // 0, 2, .., 14 as eight packed e2m1 values and (word >> 2) & 0x33333333 the odd
-// ones: 16 weights per shift and two logic ops, half the register traffic of
-// the e4m3 form. tcgen05.mma kind::mxf4 takes K = 64 (a whole block) per
-// instruction with A in TMEM; its per-32-element ue8m0 scales are all 1.0
-// (0x7F), so it multiplies the e2m1 values as they are.
+// ones: 16 weights per shift and two logic ops. tcgen05.mma kind::mxf4 takes
+// K = 64 (a whole block) per instruction with A in TMEM; its per-32-element
+// ue8m0 scales are all 1.0 (0x7F), so it multiplies the e2m1 values as they are.
 //
-// The activations are 12 e2m1 pieces: u = x * 2^s with max|u| in [1, 2),
-// v = 2u (so that A * B = q * u), piece p = e2m1(r_p * 4^p), r_0 = v,
-// r_{p+1} = r_p - piece_p * 4^-p; each rounding leaves at most a quarter of
-// the magnitude, so after 12 pieces the residual is below 2^-25 max|v|.
-// Piece p is B row p; the epilogue forms t = sum_p 4^-p C_p - beta and
-// acc += d * t, beta computed by the prep kernel from exact per-piece sums
-// with the same f32 operations. Pipeline and warp roles as the e4m3 kernel;
-// per 8-block stage the A buffer is 64 TMEM columns and the D buffer 128.
+// Activations, block by block. For block b of the vector (64 elements) with
+// M_b = max |x| over the block, M_b = f * 2^e (f in [0.5, 1)), the prep kernel
+// forms v = x * 2^(2 - e) (max |v| in [2, 4)) and splits it into 16 e2m1 pieces:
+// piece p = e2m1(r_p * 4^p), r_0 = v, r_(p+1) = r_p - piece_p * 4^-p. Every
+// subtraction is exact, the scaled residual after the first piece stays within
+// [-2, 2], and |r_16| <= 2^-32, so each element keeps its value to 2^-33 of its
+// own block's maximum (not of the whole vector's). Piece p is B row p.
+//
+// The "- 1" of (q - 1) without cancellation. With A = q / 2 the MMA gives, per
+// row and piece, C_p = sum_k (q_k / 2) piece_pk, an exact f32 (multiples of 1/4
+// below 2^9). The prep kernel computes the same sums for all-ones codes,
+// B_p = sum_k piece_pk / 2, and stores them combined in three groups,
+//   H = sum_{p<6} 4^-p B_p,  M = sum_{6<=p<12} 4^-p B_p,  L = sum_{p>=12} 4^-p B_p,
+// each of which spans fewer than 24 bits and is therefore exact in f32. The
+// epilogue forms the same three groups of C (also exact) and subtracts group by
+// group, so the element of a zero weight cancels exactly however large it is;
+// the one rounding left, (H_C - H) + (M_C - M) + (L_C - L), is relative to the
+// sum over the nonzero weights. The block's contribution is d * t * 2^(e - 1).
+// Per stage the 8 block contributions are summed in f32 and the stage sums are
+// added with a compensated (two-sum) accumulation, so the accumulated rounding
+// does not grow with K.
 // ---------------------------------------------------------------------------
-constexpr int kT4Pieces = 12;
+constexpr int kT4Pieces = 16;
 constexpr int kT4ImgBytes = kT5N * kChunkBlocks * 32;  // 4096: 16 rows x 256 bytes (512 e2m1)
-constexpr int kT4BetaBytes = kChunkBlocks * 4;         // beta[8 blocks] f32
+// per block of a stage: float {2^(e - 1), H, M, L}
+constexpr int kT4BlockRec = 4;
+constexpr int kT4BetaBytes = kChunkBlocks * kT4BlockRec * 4;  // 128
 constexpr int kT4ABufs = 3;
 constexpr int kT4ACol = 256;                           // A buffers at 256 + 64 i
 constexpr int kT4ScaleCol = 448;                       // scales A 448..451, B 452..455
@@ -1197,6 +1211,7 @@ constexpr int kT4Barriers = 2 * kT5Stages + 2 * kT4ABufs + 2 * 2 + 2;
 constexpr int kT4Smem = 1024 /* alignment slack */ +
                         kT5Stages * (kT4ImgBytes + kT5RawBytes + kT4BetaBytes) +
                         kT4Barriers * 8;
+static_assert(kT4Pieces == kT5N, "one B row per piece");
 
 size_t t4_prep_bytes(int64_t K) {
     const size_t n_chunks = size_t(K / 512);
@@ -1210,10 +1225,17 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int m, int n) {
            (uint32_t(m >> 4) << 24);
 }
 
+// 2^k as a float for k in [-149, 127] (subnormal below -126).
+__device__ __forceinline__ float pow2f(int k) {
+    return k >= -126 ? __int_as_float((127 + k) << 23) : __int_as_float(1 << (149 + k));
+}
+
 // Preparation: grid (1, n_jobs, z), kT5PrepThreads threads. Item (block b,
 // word c, parity h): the 8 elements 16c + 2j + h (j = 0..7) of block b, one
 // 32-bit word of the B image per piece (K positions 64 (b % 8) + 16c + 8h + j,
-// nibble j). Per-piece all-ones sums are exact integers in units of 1/4.
+// nibble j). The 8 items of a block are 8 consecutive lanes: they share the
+// block maximum and sum the all-ones groups H, M, L by shuffles (every partial
+// sum is exact).
 template <typename XT>
 __global__ void __launch_bounds__(kT5PrepThreads) t4_prep_kernel(
     const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs) {
@@ -1229,54 +1251,36 @@ __global__ void __launch_bounds__(kT5PrepThreads) t4_prep_kernel(
     }
     const int K = J.K;
     const XT *xj = static_cast<const XT *>(J.x);
-    const int tid = threadIdx.x;
     const int nb = K / 64;
     const int n_chunks = K / 512;
-    if (int(blockIdx.z) * kT5PrepThreads >= nb * 8) return;
-
-    // 1) column scale 2^s with max|x * 2^s| in [1, 2)
-    float m = 0.0f;
-    if (sizeof(XT) == 4 && (reinterpret_cast<uintptr_t>(xj) & 15u) == 0) {
-        const float4 *x4 = reinterpret_cast<const float4 *>(xj);
-        for (int k = tid; k < K / 4; k += kT5PrepThreads) {
-            const float4 f = x4[k];
-            m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
-        }
-    } else {
-        for (int k = tid; k < K; k += kT5PrepThreads) m = fmaxf(m, fabsf(ld_x(xj + k)));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    __shared__ float red[kT5PrepThreads / 32];
-    if ((tid & 31) == 0) red[tid >> 5] = m;
-    __syncthreads();
-    float amax = red[0];
-#pragma unroll
-    for (int w = 1; w < kT5PrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
-    int s = 0;
-    if (amax > 0.0f && amax <= 3.4e38f) {
-        int e;
-        frexpf(amax, &e);  // amax = f * 2^e, f in [0.5, 1)
-        s = 1 - e;
-    }
-    int *col_shift = reinterpret_cast<int *>(J.prep);
-    if (blockIdx.z == 0 && tid == 0) col_shift[0] = s;
-
-    // 2) pieces
     uint8_t *img = J.prep + kT5PrepHeader;
-    float *beta = reinterpret_cast<float *>(img + size_t(n_chunks) * kT4ImgBytes);
-    const int lane = tid & 31;
+    float *brec = reinterpret_cast<float *>(img + size_t(n_chunks) * kT4ImgBytes);
+    const int lane = threadIdx.x & 31;
     const unsigned grp = 0xFFu << (lane & 24);  // the block's 8 threads
-    for (int idx = int(blockIdx.z) * kT5PrepThreads + tid; idx < nb * 8;
+    // 8 items per block and nb blocks: whole warps share a block range, so the
+    // shuffles below always run with all 8 lanes of a block present
+    for (int idx = int(blockIdx.z) * kT5PrepThreads + int(threadIdx.x); idx < nb * 8;
          idx += int(gridDim.z) * kT5PrepThreads) {
         const int b = idx >> 3, c = (idx >> 1) & 3, h = idx & 1;
         const XT *xe = xj + b * 64 + c * 16 + h;
         float v[8];
+        float m = 0.0f;
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) v[jj] = mul_pow2(ld_x(xe + 2 * jj), s + 1);  // v = 2u
+        for (int jj = 0; jj < 8; ++jj) {
+            v[jj] = ld_x(xe + 2 * jj);
+            m = fmaxf(m, fabsf(v[jj]));
+        }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(grp, m, o));
+        // v = x * 2^(2 - e), max |v| over the block in [2, 4); all-zero (or
+        // non-finite) blocks keep e = 0
+        int e = 0;
+        if (m > 0.0f && m <= 3.402823466e38f) frexpf(m, &e);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) v[jj] = mul_pow2(v[jj], 2 - e);
         uint8_t *bimg = img + size_t(b >> 3) * kT4ImgBytes;
         const int kbyte = 32 * (b & 7) + 8 * c + 4 * h;  // byte of K position 64(b%8)+16c+8h
-        int isum[kT4Pieces];
+        float grp_sum[3] = {0.0f, 0.0f, 0.0f};  // this item's share of H, M, L
 #pragma unroll
         for (int p = 0; p < kT4Pieces; ++p) {
             const float up = __int_as_float((127 + 2 * p) << 23);
@@ -1294,29 +1298,18 @@ __global__ void __launch_bounds__(kT5PrepThreads) t4_prep_kernel(
                 acc2 += __float2int_rn(2.0f * pv.x) + __float2int_rn(2.0f * pv.y);
                 word |= uint32_t(pc) << (8 * q2);
             }
-            isum[p] = acc2;
             *reinterpret_cast<uint32_t *>(bimg + t5_img_offset(p, kbyte)) = word;
+            // sum of piece / 2 = acc2 / 4, weighted by 4^-p, into its group
+            const int gi = p < 6 ? 0 : p < 12 ? 1 : 2;
+            grp_sum[gi] = fmaf(float(acc2) * 0.25f, down, grp_sum[gi]);
         }
-        // rows 12..15 of the image stay zero
-        if (h == 0)
-            for (int n = kT4Pieces; n < kT5N; ++n)
-                *reinterpret_cast<uint2 *>(bimg + t5_img_offset(n, kbyte)) = make_uint2(0u, 0u);
-        float base[kT4Pieces];
 #pragma unroll
-        for (int p = 0; p < kT4Pieces; ++p) {
-            int t = isum[p];
+        for (int gi = 0; gi < 3; ++gi)
 #pragma unroll
-            for (int o = 1; o < 8; o <<= 1) t += __shfl_xor_sync(grp, t, o);
-            base[p] = float(t) * 0.25f;  // sum of piece * (value of code 1 = 1/2)
-        }
-        if ((idx & 7) == 0) {
-            float t = base[kT4Pieces - 1] * __int_as_float((127 - 2 * (kT4Pieces - 1)) << 23);
-#pragma unroll
-            for (int p = kT4Pieces - 2; p >= 1; --p)
-                t = fmaf(base[p], __int_as_float((127 - 2 * p) << 23), t);
-            t = t + base[0];
-            beta[size_t(b >> 3) * (kT4BetaBytes / 4) + (b & 7)] = t;
-        }
+            for (int o = 1; o < 8; o <<= 1) grp_sum[gi] += __shfl_xor_sync(grp, grp_sum[gi], o);
+        if ((idx & 7) == 0)
+            *reinterpret_cast<float4 *>(brec + size_t(b) * kT4BlockRec) =
+                make_float4(pow2f(e - 1), grp_sum[0], grp_sum[1], grp_sum[2]);
     }
 }
 
@@ -1324,7 +1317,6 @@ __global__ void __launch_bounds__(kT5PrepThreads) t4_prep_kernel(
 // one per slot before the slot's barrier arrive.
 struct T4StageMeta {
     float *y;              // nullptr: the tile is not written (an expert id out of range)
-    const int *col_shift;  // the job's column shift (written by the prep kernel)
     int row0;              // first row of the tile
     int n_rows;            // rows of the matrix
     int flags;             // kT4FirstOfTile | kT4LastOfTile
@@ -1343,7 +1335,6 @@ constexpr int kT4LastOfTile = 2;
 // per quarter) lengthened the stage period; 12 warps gave the shortest.
 constexpr int kT4SplitCodeBytes = kT5Rows * 128;  // 16 KB of codes, then 2 KB of scales
 static_assert(kT4SplitCodeBytes + kT5Rows * 16 == kT5RawBytes, "split stage = block stage bytes");
-static_assert(kT4Pieces == 12, "the epilogue loads pieces 0-7 and 8-11");
 constexpr int kT4ProdWarp = 2;
 constexpr int kT4MmaWarp = 3;
 constexpr int kT4MmaWarp2 = 1;
@@ -1484,7 +1475,6 @@ __global__ void __maxnreg__(128)
                     }
                     T4StageMeta &m = s_meta[st];
                     m.y = y_out;
-                    m.col_shift = reinterpret_cast<const int *>(prep);
                     m.row0 = tile * kT5Rows;
                     m.n_rows = J->N;
                     m.flags = (ch == 0 ? kT4FirstOfTile : 0) | (ch == nch - 1 ? kT4LastOfTile : 0);
@@ -1641,12 +1631,10 @@ __global__ void __maxnreg__(128)
         // warp w: TMEM lane quarter w % 4, all 8 blocks of each stage; it writes y
         // at the tile's last stage. Every wait is bounded; a warp whose wait
         // fails leaves the loop.
-        grid_dependency_wait();  // reads the column shift written by prep
         const int qd = warp & 3;
         const int row = 32 * qd + lane;
         const uint32_t lane_base = uint32_t(32 * qd) << 16;
-        float acc = 0.0f;
-        int shift = 0;
+        float acc = 0.0f, comp = 0.0f;  // compensated sum of the stage sums
         for (int s = 0; s < n_stages; ++s) {
             const int st = s % kT5Stages;
             const bool got = !*(volatile int *)&s_abort &&
@@ -1658,41 +1646,57 @@ __global__ void __maxnreg__(128)
             }
             tc_fence_after();
             const T4StageMeta m = s_meta[st];
-            if (m.flags & kT4FirstOfTile) shift = *m.col_shift;
             const uint32_t d_base = tmem + lane_base + d_col(s);
-            // pieces 0-7 and 8-11 of each block (columns 12-15 hold zeros)
-            uint32_t r[8][8], r2[8][4];
-#pragma unroll
-            for (int bi = 0; bi < 8; ++bi) {
-                tmem_ld8(d_base + bi * kT5N, r[bi]);
-                tmem_ld4(d_base + bi * kT5N + 8, r2[bi]);
-            }
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&d_empty[s & 1]);
             const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes;
-            const float *bt = reinterpret_cast<const float *>(beta_ring + st * kT4BetaBytes);
+            const float4 *brec = reinterpret_cast<const float4 *>(beta_ring + st * kT4BetaBytes);
+            float stage_sum = 0.0f;
+            // blocks 4 hb .. 4 hb + 3: their 16 pieces each (64 registers)
 #pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                auto piece = [&](int pp) { return __uint_as_float(pp < 8 ? r[b][pp] : r2[b][pp - 8]); };
-                float t = piece(kT4Pieces - 1) * __int_as_float((127 - 2 * (kT4Pieces - 1)) << 23);
+            for (int hb = 0; hb < 2; ++hb) {
+                uint32_t r[4][16];
 #pragma unroll
-                for (int pp = kT4Pieces - 2; pp >= 1; --pp)
-                    t = fmaf(piece(pp), __int_as_float((127 - 2 * pp) << 23), t);
-                t = t + piece(0);
-                const float d =
-                    kSplit ? lds_half_as_float(raw_ring + st * kT5RawBytes + kT4SplitCodeBytes +
-                                               row * 16 + 2 * b)
-                           : lds_half_as_float(rp + 18 * b);
-                acc = fmaf(d, t - bt[b], acc);
+                for (int bi = 0; bi < 4; ++bi) tmem_ld16(d_base + (4 * hb + bi) * kT5N, r[bi]);
+                tmem_wait_ld();
+                if (hb == 1) {  // the stage's accumulators are all in registers
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&d_empty[s & 1]);
+                }
+#pragma unroll
+                for (int bi = 0; bi < 4; ++bi) {
+                    const int b = 4 * hb + bi;
+                    auto C = [&](int pp) { return __uint_as_float(r[bi][pp]); };
+                    // the three exact groups of sum_p 4^-p C_p
+                    float gh = C(5) * 0x1p-10f, gm = C(11) * 0x1p-22f, gl = C(15) * 0x1p-30f;
+#pragma unroll
+                    for (int pp = 4; pp >= 0; --pp) gh = fmaf(C(pp), __int_as_float((127 - 2 * pp) << 23), gh);
+#pragma unroll
+                    for (int pp = 10; pp >= 6; --pp) gm = fmaf(C(pp), __int_as_float((127 - 2 * pp) << 23), gm);
+#pragma unroll
+                    for (int pp = 14; pp >= 12; --pp) gl = fmaf(C(pp), __int_as_float((127 - 2 * pp) << 23), gl);
+                    const float4 br = brec[b];  // {2^(e - 1), H, M, L}
+                    const float t = ((gh - br.y) + (gm - br.z)) + (gl - br.w);
+                    const float d =
+                        kSplit ? lds_half_as_float(raw_ring + st * kT5RawBytes + kT4SplitCodeBytes +
+                                                   row * 16 + 2 * b)
+                               : lds_half_as_float(rp + 18 * b);
+                    stage_sum = fmaf(d, t * br.x, stage_sum);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
+            // acc + comp += stage_sum (two-sum: the rounding error is kept)
+            {
+                const float sum = acc + stage_sum;
+                const float bb = sum - acc;
+                comp += (acc - (sum - bb)) + (stage_sum - bb);
+                acc = sum;
+            }
             if (m.flags & kT4LastOfTile) {
                 const int rr = m.row0 + row;
-                if (m.y && rr < m.n_rows) m.y[rr] = mul_pow2(acc, -shift);
+                if (m.y && rr < m.n_rows) m.y[rr] = acc + comp;
                 acc = 0.0f;
+                comp = 0.0f;
             }
         }
     }

@@ -9,6 +9,7 @@ import torch
 import bit_ternary_matmul_gb300 as q
 import oracle
 import synth
+import wide_range as wr
 
 pytestmark = pytest.mark.gpu
 
@@ -615,4 +616,145 @@ def test_matvec_split_head_sampled_and_unaligned(dev):
     buf[8:] = soa
     y2 = q.q2_0_mul_mat_vec_split(buf[8:], _to(dev, x), N, K).cpu().numpy()
     _assert_close(y2[:, rows], yo, acc, TOL_SPLIT, "split head, unaligned")
+    _no_device_error()
+
+
+# ---------------------------------------------------------------------------
+# Wide dynamic range inside one activation vector. The tolerance is relative to
+# sum|w*x|, so a small element must keep its own relative precision even when
+# it shares a vector (or a block of 64) with an element 10^5 times larger, and
+# an element whose weight is zero (code 1) must contribute exactly nothing,
+# however large it is. The inputs come from tests/wide_range.py.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("ncols", [1, 2, 4, 8])
+@pytest.mark.parametrize("kind", wr.WIDE_KINDS)
+def test_matvec_wide_range(dev, kind, ncols):
+    g = synth.rng(2202, wr.WIDE_KINDS.index(kind), ncols)
+    N, K = 260, 2048
+    w, x = wr.wide_range_case(kind, g, N, K, ncols)
+    y = q.q2_0_mul_mat_vec(_to(dev, w), _to(dev, x), N, K, ncols).cpu().numpy()
+    yo, acc = oracle.matmul(w, N, K, x)
+    _assert_close(y, yo, acc, TOL_SPLIT, f"mat-vec {kind} ncols={ncols}")
+    _no_device_error()
+
+
+@pytest.mark.parametrize("ncols", [1, 3, 8])
+def test_plan_wide_range(dev, ncols):
+    g = synth.rng(2203, ncols)
+    ents, host = [], []
+    for i, (N, K) in enumerate([(300, 2048), (129, 6144), (1000, 1024)]):
+        w, x = wr.wide_range_case(wr.WIDE_KINDS[i % len(wr.WIDE_KINDS)], g, N, K, ncols)
+        ents.append((_to(dev, w), _to(dev, x), torch.empty((ncols, N), device=dev), N, K))
+        host.append((w, x))
+    plan = q.MvPlan(ents, ncols)
+    plan.execute()
+    torch.cuda.synchronize()
+    for (w, x), (_, _, yd, N, K) in zip(host, ents):
+        yo, acc = oracle.matmul(w, N, K, x)
+        _assert_close(yd.cpu().numpy(), yo, acc, TOL_SPLIT, f"plan wide {N}x{K} ncols={ncols}")
+    plan.close()
+    _no_device_error()
+
+
+@pytest.mark.parametrize("kind", wr.WIDE_KINDS)
+def test_mul_mat_id_wide_range(dev, kind):
+    n_expert, N, K, n_tokens, n_used = 3, 200, 1024, 2, 2
+    g = synth.rng(2204, wr.WIDE_KINDS.index(kind))
+    ws, xs = zip(*[wr.wide_range_case(kind, g, N, K, n_tokens) for _ in range(n_expert)])
+    w = np.concatenate(ws)
+    x = xs[0].reshape(n_tokens, 1, K)
+    ids = np.array([[0, 2], [1, 0]], dtype=np.int32)
+    y = q.q2_0_mul_mat_id(_to(dev, w), n_expert, N, K, _to(dev, x), _to(dev, ids)).cpu().numpy()
+    yo, acc, bad = oracle.matmul_id(w, n_expert, N, K, x, ids)
+    assert bad == 0
+    _assert_close(y.reshape(-1, N), yo.reshape(-1, N), acc.reshape(-1, N), TOL_SPLIT,
+                  f"mul_mat_id {kind}")
+    _no_device_error()
+
+
+@pytest.mark.parametrize("kind", wr.WIDE_KINDS)
+def test_matvec_split_wide_range(dev, kind):
+    g = synth.rng(2205, wr.WIDE_KINDS.index(kind))
+    N, K = 300, 2048
+    w, x = wr.wide_range_case(kind, g, N, K, 1)
+    soa = q.q2_0_split_layout(_to(dev, w), N, K)
+    y = q.q2_0_mul_mat_vec_split(soa, _to(dev, x), N, K, 1).cpu().numpy()
+    yo, acc = oracle.matmul(w, N, K, x)
+    _assert_close(y, yo, acc, TOL_SPLIT, f"split mat-vec {kind}")
+    _no_device_error()
+
+
+@pytest.mark.parametrize("ncols", [1, 4])
+def test_matvec_f16_wide_range(dev, ncols):
+    g = synth.rng(2206, ncols)
+    N, K = 260, 2048
+    w, x = wr.wide_range_case("const_outliers", g, N, K, ncols)
+    x16 = x.astype(np.float16)
+    y = q.q2_0_mul_mat_vec_f16(_to(dev, w), _to(dev, x16), N, K, ncols).cpu().numpy()
+    yo, acc = oracle.matmul(w, N, K, x16.astype(np.float32))
+    _assert_close(y, yo, acc, TOL_SPLIT, f"mat-vec f16 wide ncols={ncols}")
+    _no_device_error()
+
+
+# ---------------------------------------------------------------------------
+# GEMM: edge blocks, activations far from 1 (tiny, huge) and wide range
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("prec", [q.Q2_0_PREC_F16_SPLIT, q.Q2_0_PREC_F16])
+def test_gemm_edge_blocks(dev, prec):
+    """Rows seeded with the edge blocks (d = +-0, subnormal d, all code 3, all
+    code 1, d = 65504 with codes 0..2): all finite in f32."""
+    g = synth.rng(3201, prec)
+    N, K, M = 300, 2048, 70
+    w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    edges = synth.edge_blocks()
+    wv = w.reshape(N, K // 64, 18)
+    for r in range(0, N, 3):
+        wv[r, r % (K // 64)] = edges[r % len(edges)]
+        wv[r, (r + 7) % (K // 64)] = edges[(r + 1) % len(edges)]
+    x = synth.activations(g, M, K, synth.PREFILL_OUTLIER_FRAC, synth.PREFILL_OUTLIER)
+    y = q.q2_0_mul_mat(_to(dev, w), _to(dev, x), N, K, M, prec).cpu().numpy()
+    yo, acc = oracle.matmul(w, N, K, x)
+    tol = TOL_SPLIT if prec == q.Q2_0_PREC_F16_SPLIT else TOL_F16
+    _assert_close(y, yo, acc, tol, f"GEMM edge blocks prec={prec}")
+    _no_device_error()
+
+
+@pytest.mark.parametrize("prec", [q.Q2_0_PREC_F16_SPLIT, q.Q2_0_PREC_F16])
+@pytest.mark.parametrize("scale", [1e-4, 1e-6, 1e-30, 1e5, 1e30])
+def test_gemm_activation_magnitude(dev, prec, scale):
+    """Activations scaled far below fp16's normal range and far above its
+    largest value: the result keeps the stated tolerance."""
+    g = synth.rng(3202, prec, int(np.log10(scale)) + 40)
+    N, K, M = 260, 2048, 40
+    w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    x = (synth.activations(g, M, K, synth.PREFILL_OUTLIER_FRAC, synth.PREFILL_OUTLIER)
+         * np.float32(scale)).astype(np.float32)
+    y = q.q2_0_mul_mat(_to(dev, w), _to(dev, x), N, K, M, prec).cpu().numpy()
+    yo, acc = oracle.matmul(w, N, K, x)
+    tol = TOL_SPLIT if prec == q.Q2_0_PREC_F16_SPLIT else TOL_F16
+    _assert_close(y, yo, acc, tol, f"GEMM x*{scale:g} prec={prec}")
+    _no_device_error()
+
+
+@pytest.mark.parametrize("kind", wr.WIDE_KINDS)
+def test_gemm_wide_range(dev, kind):
+    g = synth.rng(3203, wr.WIDE_KINDS.index(kind))
+    N, K, M = 260, 2048, 24
+    w, x = wr.wide_range_case(kind, g, N, K, M)
+    y = q.q2_0_mul_mat(_to(dev, w), _to(dev, x), N, K, M).cpu().numpy()
+    yo, acc = oracle.matmul(w, N, K, x)
+    _assert_close(y, yo, acc, TOL_SPLIT, f"GEMM {kind}")
+    _no_device_error()
+
+
+@pytest.mark.parametrize("ncols", [1, 4])
+@pytest.mark.parametrize("scale", [1e-30, 1e30])
+def test_matvec_activation_magnitude(dev, ncols, scale):
+    g = synth.rng(2207, ncols, int(np.log10(scale)) + 40)
+    N, K = 260, 2048
+    w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    x = (synth.activations(g, ncols, K, 0.001, 30.0) * np.float32(scale)).astype(np.float32)
+    y = q.q2_0_mul_mat_vec(_to(dev, w), _to(dev, x), N, K, ncols).cpu().numpy()
+    yo, acc = oracle.matmul(w, N, K, x)
+    _assert_close(y, yo, acc, TOL_SPLIT, f"mat-vec x*{scale:g} ncols={ncols}")
     _no_device_error()
