@@ -17,7 +17,7 @@
 namespace q2 {
 namespace {
 
-// Q2_0_NOALLOC_SCRATCH_BYTES (1 MiB): enough for K up to 129,536 at ncols = 1,
+// Q2_0_NOALLOC_SCRATCH_BYTES (1 MiB): enough for K up to 126,976 at ncols = 1,
 // 64,000 at ncols 2..3, 63,488 at ncols = 4 and 31,744 at ncols 5..8 (the scratch
 // grows with K and ncols).
 constexpr size_t kNoAllocScratchBytes = Q2_0_NOALLOC_SCRATCH_BYTES;

@@ -124,7 +124,7 @@ int q2_0_mul_mat_vec_ws(const void *w, const float *x, float *y, int64_t N, int6
  *   that every GPU which loads the library holds until the process exits.
  *   Limit: if q2_0_mul_mat_vec_workspace_size(K, ncols) exceeds
  *   Q2_0_NOALLOC_SCRATCH_BYTES the call returns Q2_0_ENOSPACE (1 MiB covers K up
- *   to 129,536 for ncols = 1, 64,000 for ncols 2..3, 63,488 for ncols = 4 and 31,744
+ *   to 126,976 for ncols = 1, 64,000 for ncols 2..3, 63,488 for ncols = 4 and 31,744
  *   for ncols 5..8).
  *   Set-up: the first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
