@@ -67,6 +67,7 @@ struct GemmArgs {
     int n_units, n_mtiles;  // units = (N / 256 rounded up) x (M / 128 rounded up)
     long long total_slabs;  // n_units * K / 64: the stream-K iteration space
     float *partials;        // 2 slots per CTA of kBN x (kWT * kBM) fp32
+    const int *row_shift;   // [M]: X row m entered the MMA as X * 2^row_shift[m]
     unsigned long long *err;
 };
 
@@ -92,8 +93,13 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
 
 // ---------------------------------------------------------------------------
 // Prepass: X [M][K] (F32, or F16 whose values are already exact fp16) -> fp16
-// hi (and lo) [M][K] in the permuted K order. One thread per 16-element word
-// group; X 16-byte aligned.
+// hi (and lo) [M][K] in the permuted K order, each row scaled by a power of
+// two first. Row m with M_m = max |x| = f * 2^e (f in [0.5, 1)) is multiplied
+// by 2^s, s = 15 - e, so that its largest element lies in [2^14, 2^15): hi
+// never overflows fp16, and the lo parts of small elements stay above fp16's
+// subnormal range down to 2^-29 of the row maximum. F16 rows are only scaled
+// up (s >= 0), which keeps them exact. The scaling is exact and undone on the
+// f32 result (y = acc * 2^-s). One warp per row; X 16-byte aligned.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void load16(const float *p, float (&v)[16]) {
     const float4 *src = reinterpret_cast<const float4 *>(p);
@@ -121,33 +127,64 @@ __device__ __forceinline__ void load16(const __half *p, float (&v)[16]) {
     }
 }
 
+// v * 2^e for |e| <= 252 with two exact power-of-two factors (each a normal f32).
+__device__ __forceinline__ float mul_pow2(float v, int e) {
+    const int e1 = e / 2, e2 = e - e1;
+    return v * __int_as_float((127 + e1) << 23) * __int_as_float((127 + e2) << 23);
+}
+
+constexpr int kPrepRowsPerCta = 8;
+
 template <typename XT>
-__global__ void __launch_bounds__(256) gemm_prep_kernel(const XT *__restrict__ x,
-                                                        __half *__restrict__ xh,
-                                                        __half *__restrict__ xl, int64_t groups,
-                                                        int split) {
+__global__ void __launch_bounds__(kPrepRowsPerCta * 32) gemm_prep_kernel(
+    const XT *__restrict__ x, __half *__restrict__ xh, __half *__restrict__ xl,
+    int *__restrict__ row_shift, int M, int K, int split) {
     // The GEMM kernel that follows may start its prologue and weight loads now;
     // it waits for this grid before reading X.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    for (int64_t gidx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; gidx < groups;
-         gidx += int64_t(gridDim.x) * blockDim.x) {
+    const int m = blockIdx.x * kPrepRowsPerCta + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (m >= M) return;
+    const XT *xr = x + size_t(m) * K;
+    const int groups = K / 16;
+    float amax = 0.0f;
+    for (int gi = lane; gi < groups; gi += 32) {
         float v[16];
-        load16(x + gidx * 16, v);
+        load16(xr + gi * 16, v);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) amax = fmaxf(amax, fabsf(v[t]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int sh = 0;
+    if (amax > 0.0f && amax <= 3.402823466e38f) {
+        int e;
+        frexpf(amax, &e);
+        sh = 15 - e;
+        if (sizeof(XT) == 2 && sh < 0) sh = 0;
+    }
+    if (lane == 0) row_shift[m] = sh;
+    __half *hr = xh + size_t(m) * K;
+    __half *lr = split ? xl + size_t(m) * K : nullptr;
+    for (int gi = lane; gi < groups; gi += 32) {
+        float v[16];
+        load16(xr + gi * 16, v);
         uint32_t hw[8], lw[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-            const __half h0 = __float2half_rn(v[t]);
-            const __half h1 = __float2half_rn(v[t + 8]);
+            const float a0 = mul_pow2(v[t], sh), a1 = mul_pow2(v[t + 8], sh);
+            const __half h0 = __float2half_rn(a0);
+            const __half h1 = __float2half_rn(a1);
             hw[t] = uint32_t(__half_as_ushort(h0)) | (uint32_t(__half_as_ushort(h1)) << 16);
-            const __half l0 = __float2half_rn(v[t] - __half2float(h0));
-            const __half l1 = __float2half_rn(v[t + 8] - __half2float(h1));
+            const __half l0 = __float2half_rn(a0 - __half2float(h0));
+            const __half l1 = __float2half_rn(a1 - __half2float(h1));
             lw[t] = uint32_t(__half_as_ushort(l0)) | (uint32_t(__half_as_ushort(l1)) << 16);
         }
-        uint4 *dh = reinterpret_cast<uint4 *>(xh + gidx * 16);
+        uint4 *dh = reinterpret_cast<uint4 *>(hr + gi * 16);
         dh[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         dh[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
         if (split) {
-            uint4 *dl = reinterpret_cast<uint4 *>(xl + gidx * 16);
+            uint4 *dl = reinterpret_cast<uint4 *>(lr + gi * 16);
             dl[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             dl[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
         }
@@ -426,6 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         }
     } else {
         // ------------------------------- epilogue -------------------------------
+        // the row exponents come from the prepass (the producer waits for it
+        // before loading X; the epilogue waits too before reading them)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         const int q = warp & 3, t = (warp - 2 - kExpandWarps) >> 2;
         const uint32_t lane_addr = uint32_t(q * 32) << 16;
         const int rloc = t * kBM + q * 32 + lane;  // row within the unit
@@ -459,7 +499,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             const int m = m0 + cb + j;
-                            if (m < a.M) a.y[size_t(m) * a.N + n] = __uint_as_float(v[j]);
+                            if (m < a.M)
+                                a.y[size_t(m) * a.N + n] =
+                                    mul_pow2(__uint_as_float(v[j]), -a.row_shift[m]);
                         }
                     }
                 } else {
@@ -494,8 +536,8 @@ constexpr int kReduceSlices = 8;
 constexpr int kReduceThreads = 256;
 
 __global__ void __launch_bounds__(kReduceThreads) gemm_reduce_kernel(
-    const float *__restrict__ partials, float *__restrict__ y, int M, int N, int n_mtiles,
-    int n_slabs, long long total_slabs) {
+    const float *__restrict__ partials, const int *__restrict__ row_shift, float *__restrict__ y,
+    int M, int N, int n_mtiles, int n_slabs, long long total_slabs) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int G = int(gridDim.y), c = int(blockIdx.y);
     const long long gb = sk_begin(c, total_slabs, G);
@@ -538,6 +580,11 @@ __global__ void __launch_bounds__(kReduceThreads) gemm_reduce_kernel(
         const int nn = n0 + 4 * (i % kRowVec);
         if (m >= M) continue;
         float *yr = y + size_t(m) * N;
+        const int sh = -row_shift[m];
+        acc[r].x = mul_pow2(acc[r].x, sh);
+        acc[r].y = mul_pow2(acc[r].y, sh);
+        acc[r].z = mul_pow2(acc[r].z, sh);
+        acc[r].w = mul_pow2(acc[r].w, sh);
         if (vec_y && nn + 3 < N) {
             *reinterpret_cast<float4 *>(yr + nn) = acc[r];
         } else {
@@ -616,6 +663,7 @@ namespace {
 struct GemmLayout {
     size_t part;      // bytes of X_hi (and of X_lo)
     size_t partials;  // offset of the partial tiles
+    size_t shifts;    // offset of the per-row exponents (int [M])
     size_t total;
     int n_units, n_mtiles, grid;
     long long total_slabs;
@@ -623,7 +671,7 @@ struct GemmLayout {
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// Workspace: [X_hi][X_lo (split)][2 partial tiles per stream-K CTA].
+// Workspace: [X_hi][X_lo (split)][2 partial tiles per stream-K CTA][row exponents].
 // The grid is at most kMaxGrid CTAs, at least 8 slabs each.
 GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K, int prec, int sms) {
     GemmLayout L;
@@ -634,7 +682,8 @@ GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K, int prec, int sms) {
     const long long by_work = std::max<long long>(1, L.total_slabs / 8);
     L.grid = int(std::min<long long>(std::min<long long>(sms > 0 ? sms : kMaxGrid, kMaxGrid), by_work));
     L.partials = (prec == Q2_0_PREC_F16_SPLIT ? 2 : 1) * L.part;
-    L.total = L.partials + size_t(2) * L.grid * kPartialBytes;
+    L.shifts = L.partials + size_t(2) * L.grid * kPartialBytes;
+    L.total = L.shifts + align256(size_t(M) * 4);
     return L;
 }
 
@@ -667,15 +716,14 @@ int gemm_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, in
     __half *xh = reinterpret_cast<__half *>(wsb);
     __half *xl = split ? reinterpret_cast<__half *>(wsb + L.part) : nullptr;
     float *partials = reinterpret_cast<float *>(wsb + L.partials);
-    const int64_t groups = M * K / 16;
-    int64_t pgrid = std::min<int64_t>((groups + 255) / 256, int64_t(sm_count()) * 8);
-    const unsigned pg = unsigned(std::max<int64_t>(pgrid, 1));
+    int *row_shift = reinterpret_cast<int *>(wsb + L.shifts);
+    const unsigned pg = unsigned((M + kPrepRowsPerCta - 1) / kPrepRowsPerCta);
     if (xtype == kXF16)
-        gemm_prep_kernel<__half><<<pg, 256, 0, s>>>(static_cast<const __half *>(x), xh, xl, groups,
-                                                    split);
+        gemm_prep_kernel<__half><<<pg, kPrepRowsPerCta * 32, 0, s>>>(
+            static_cast<const __half *>(x), xh, xl, row_shift, int(M), int(K), split);
     else
-        gemm_prep_kernel<float><<<pg, 256, 0, s>>>(static_cast<const float *>(x), xh, xl, groups,
-                                                   split);
+        gemm_prep_kernel<float><<<pg, kPrepRowsPerCta * 32, 0, s>>>(
+            static_cast<const float *>(x), xh, xl, row_shift, int(M), int(K), split);
     if (cudaGetLastError() != cudaSuccess) return Q2_0_ECUDA;
 
     GemmArgs args;
@@ -700,6 +748,7 @@ int gemm_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, in
     args.n_units = L.n_units;
     args.total_slabs = L.total_slabs;
     args.partials = partials;
+    args.row_shift = row_shift;
     if (ensure_attr() != cudaSuccess) return Q2_0_ECUDA;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -716,8 +765,9 @@ int gemm_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, in
     cfg.gridDim = dim3(kReduceSlices, L.grid);
     cfg.blockDim = dim3(kReduceThreads);
     cfg.dynamicSmemBytes = 0;
-    if (cudaLaunchKernelEx(&cfg, gemm_reduce_kernel, static_cast<const float *>(partials), y,
-                           int(M), int(N), L.n_mtiles, int(K / kSlabK), L.total_slabs) !=
+    if (cudaLaunchKernelEx(&cfg, gemm_reduce_kernel, static_cast<const float *>(partials),
+                           static_cast<const int *>(row_shift), y, int(M), int(N), L.n_mtiles,
+                           int(K / kSlabK), L.total_slabs) !=
         cudaSuccess)
         return Q2_0_ECUDA;
     return cuda_status(cudaGetLastError());

@@ -4,42 +4,30 @@
 // PR 30914), mat-vec kernel excerpt: four threads share a 64-weight block, each
 // owning one 32-bit word of 16 codes; codes are shifted out of the word two
 // bits at a time, (q - 1) multiplies the activation, and the scale d is applied
-// once per block sum. This file keeps that structure — a thread owns word c of
-// a block, d is applied once per block — but does the multiply-accumulate on
-// the tensor cores (mma.sync m16n8k16, fp16 in, fp32 accumulate):
+// once per block sum. This file keeps the per-word decode and the single
+// application of d per block, and moves the multiply-accumulate onto the
+// 5th-generation tensor cores (tcgen05.mma, accumulators in tensor memory):
 //
-// Decode without shifts. For field m (0..3) the mask 0x00030003 << 2m picks,
-// from one word, the codes of elements i = m and i = 8 + m into the two fp16
-// halves of a register; read as fp16 these are the subnormals q * 4^m * 2^-24,
-// exact. (word >> 8) with the same masks picks elements 4 + m and 12 + m. So a
-// word becomes 8 A-operand registers with one logic op each (+1 shift). The
-// per-field factor 4^m is removed by scaling the activations of field m by
-// 4^-m, and the "- 1" of (q - 1) by starting each block's accumulation at
-// -sum(activation * 4^m * 2^-24) of that block (the value all-ones codes give).
+//   ncols = 1     mv_t4_kernel: codes as packed e2m1 (q / 2, two logic ops per
+//                 16 weights), activations as 16 block-scaled e2m1 pieces,
+//                 kind::mxf4 with K = 64 = one block per MMA; the "- 1" is an
+//                 exact per-block correction (see the fp4 section);
+//   ncols 2..8    mv_s8_kernel<NC>: codes as signed e4m3 (q - 1, one byte-permute
+//                 lookup per 4 weights), activations as 5 block-scaled e4m3
+//                 pieces per column, kind::f8f6f4 with K = 32;
+//   other shapes  mv_generic_kernel: CUDA cores, f32 (K % 512 != 0 or W not
+//                 16-byte aligned).
 //
-// Activations (F32) enter as fp16 hi + lo pairs: per column j, u = x * 2^s_j
-// with 2^s_j chosen so max|u| lies in [2^14, 2^15); for element e of a block,
-// v = u * 2^-2(e%4), hi = fp16(v), lo = fp16(v - hi). MMA n-tile t carries
-// activation columns 4t..4t+3: its B column 2i is the hi part of column 4t+i
-// and B column 2i+1 the lo part, so the lanes that carry data are consecutive
-// (lanes 0..7 for one column) and a thread's two accumulator registers of a row
-// hold hi and lo of the same column. A small kernel (mv_prep) writes these
-// fragments once per call, in register order; the mat-vec kernel only loads them.
-//
-// Streaming. Each CTA (16 consumer warps of 16 rows + 1 producer warp) owns row
-// tiles of 256 rows. A pipeline stage is one 2-D TMA box of 256 rows x 144 bytes
-// (8 blocks = 512 weights per row) plus the 8 blocks' fragment records (1-D
-// bulk copy); as many stages as fit in shared memory. 144-byte rows make the
-// shared-memory words of the 8 rows of an MMA group fall in distinct banks.
-// Block pairs (36 bytes) start 4-byte aligned: the odd block's words are
-// aligned, the even block's words straddle two aligned words and are rebuilt
-// with one byte-permute. The consumer loop is limited by shared-memory
-// wavefronts, so the record layout is chosen for dense 16-byte fragment loads.
-//
-// Requirements of the TMA path: K % 512 == 0 (row stride a multiple of 16 B)
-// and W 16-byte aligned. Other shapes run mv_generic_kernel (CUDA cores, f32).
-// Activations are F32 or F16 (the prep kernels and the generic kernel read
-// either; F16 values are converted exactly).
+// Both tensor-core kernels are persistent, one CTA of 12 warps per SM, over
+// 128-row tiles of one matrix or of a plan's many matrices; a pipeline stage is
+// one 2-D TMA box of 128 rows x 144 bytes (8 blocks = 512 weights per row) plus
+// the stage's activation image (bulk copy), in an 8-deep shared-memory ring.
+// Warp 2 streams the stages, warps 3 and 1 issue the MMAs of the even and odd
+// stages, warps 4-7 expand the codes of a stage into tensor memory (one warp
+// per 32-lane quarter: a warp reaches only the lanes of its quarter) and warps
+// 8-11 combine the accumulators, apply d and write y. Activations are F32 or
+// F16 (the prep kernels and the generic kernel read either; F16 values are
+// converted exactly).
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
@@ -57,24 +45,27 @@ namespace q2 {
 
 namespace {
 
-constexpr int kTileRows = 256;
-constexpr int kChunkBlocks = 8;
-constexpr int kChunkBytes = kChunkBlocks * 18;  // 144
-constexpr int kWStageBytes = kTileRows * kChunkBytes;  // 36864
-constexpr int kPrepHeader = 64;  // float out_scale[8] (+ pad)
-constexpr int kMaxStages = 12;
-constexpr int kPrepThreads = 512;
-// Dynamic shared memory the ring may use: the opt-in maximum less the static
-// part and the barriers.
-constexpr int kSmemBudget = 232448 - 1024 - 2 * kMaxStages * 8;
-
-// Timeout tags (info of Q2_0_DEVERR_TIMEOUT).
-constexpr int kTagMvFull = 101;
-constexpr int kTagMvEmpty = 102;
+constexpr int kChunkBlocks = 8;                  // blocks per stage
+constexpr int kChunkBytes = kChunkBlocks * 18;   // 144 bytes of a row per stage
+constexpr int kTcRows = 128;                     // rows per tile (MMA M)
+constexpr int kRawBytes = kTcRows * kChunkBytes; // 18432: one stage's TMA box
+constexpr int kPrepHeader = 1024;                // activation images start 1024-aligned
+constexpr int kPrepThreads = 256;
+constexpr int kTcThreads = 12 * 32;
+// Warp roles of both tensor-core kernels (see the file comment).
+constexpr int kProdWarp = 2;
+constexpr int kMmaWarp = 3;    // even stages; allocates TMEM
+constexpr int kMmaWarp2 = 1;   // odd stages
+constexpr int kExpWarp0 = 4;   // warps 4-7
+constexpr int kExpWarps = 4;
+constexpr int kEpiWarp0 = 8;   // warps 8-11
+constexpr int kEpiWarps = 4;
+// Dynamic shared memory a CTA may use: the opt-in maximum less the static part.
+constexpr int kSmemOptIn = 232448;
 
 struct MvPrepJob {
     const void *x;   // [ncols][K], F32 or F16 (the prep kernel's template argument)
-    uint8_t *prep;   // prepared fragments
+    uint8_t *prep;   // prepared activation images
     int K;
     // fp4 prep only, launched without a job list: grid row j prepares the vector
     // at x + j * x_stride into prep + j * prep_stride (bytes)
@@ -83,13 +74,13 @@ struct MvPrepJob {
 };
 
 struct MvJob {  // 64-byte aligned through its CUtensorMap member
-    CUtensorMap tmap;  // W as uint8 [N][K/64*18], box {144, 256}
+    CUtensorMap tmap;  // W as uint8 [N][K/64*18], box {144, 128}
     const uint8_t *prep;
     float *y;
     int N;
     int nb;        // K / 64
     int n_chunks;  // K / 512
-    int n_tiles;   // ceil(N / 256)
+    int n_tiles;   // ceil(N / 128)
     CUtensorMap tmap_d;  // split layout only: fp16 scales [N][K/64], box {16, 128}
 };
 
@@ -116,36 +107,21 @@ struct MvParams {
     const int *cta_begin;     // [gridDim.x + 1]
     const int *cta_stages;    // [gridDim.x] stages (512-column chunks) per CTA, plan only
     int ncols;
-    int n_stages;             // pipeline depth (n_stages_for(ncols))
     unsigned long long *err;
     MvMoe moe;
     int split;                // fp4 kernel only: 1 = the split layout (codes and scales apart)
 };
 
-// Record per block per n-tile, for S = lane slots carrying data (8 per column of
-// the tile; the tiles of ncols 5..8 both use 32): B-fragment registers 0..3 of
-// lanes 0..S-1 (16 B each), registers 4..7 of those lanes, then for each lane
-// group c the accumulator starts (hi, lo) of column 4t + c (8 B each).
-__host__ __device__ constexpr int n_tiles_for(int ncols) { return ncols <= 4 ? 1 : 2; }
-__host__ __device__ constexpr int used_slots(int ncols) { return ncols <= 4 ? 8 * ncols : 32; }
-__host__ __device__ constexpr int rec_bytes(int ncols) { return 32 * used_slots(ncols) + 32; }
-__host__ __device__ constexpr int rstage_bytes(int ncols) {
-    return kChunkBlocks * n_tiles_for(ncols) * rec_bytes(ncols);
-}
-constexpr int n_stages_for(int ncols) {
-    return kSmemBudget / (kWStageBytes + rstage_bytes(ncols)) < kMaxStages
-               ? kSmemBudget / (kWStageBytes + rstage_bytes(ncols))
-               : kMaxStages;
-}
-constexpr int smem_bytes_for(int ncols) {
-    return n_stages_for(ncols) * (kWStageBytes + rstage_bytes(ncols)) + 2 * kMaxStages * 8;
-}
-
-size_t prep_bytes_for(int64_t K, int ncols) {
-    size_t b = kPrepHeader + size_t(K / 64) * n_tiles_for(ncols) * rec_bytes(ncols);
-    return (b + 255) & ~size_t(255);
-}
-
+// Where the epilogue writes the tile a ring stage belongs to; the producer fills
+// one per slot before the slot's barrier arrive.
+struct StageMeta {
+    float *y;              // nullptr: the tile is not written (an expert id out of range)
+    int row0;              // first row of the tile
+    int n_rows;            // rows of the matrix (also the column stride of y)
+    int flags;             // kLastOfTile
+    int pad;
+};
+constexpr int kLastOfTile = 2;
 
 // v * 2^e for |e| <= 252 with two exact power-of-two factors (each a normal f32).
 __device__ __forceinline__ float mul_pow2(float v, int e) {
@@ -153,1014 +129,43 @@ __device__ __forceinline__ float mul_pow2(float v, int e) {
     return v * __int_as_float((127 + e1) << 23) * __int_as_float((127 + e2) << 23);
 }
 
+// 2^k as a float for k <= 127: subnormal below -126, zero below -149.
+__device__ __forceinline__ float pow2f(int k) {
+    return k >= -126 ? __int_as_float((127 + k) << 23)
+                     : k >= -149 ? __int_as_float(1 << (149 + k)) : 0.0f;
+}
+
 // Activation element load: F32 as is, F16 (IEEE binary16) converted exactly.
 __device__ __forceinline__ float ld_x(const float *p) { return *p; }
 __device__ __forceinline__ float ld_x(const __half *p) { return __half2float(*p); }
-
-// ---------------------------------------------------------------------------
-// Activation preparation: grid (ncols, n_jobs), kPrepThreads threads.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
-    return uint32_t(__half_as_ushort(lo)) | (uint32_t(__half_as_ushort(hi)) << 16);
-}
-
-template <int NT, typename XT>
-__global__ void __launch_bounds__(kPrepThreads) mv_prep_kernel(
-    const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs, int ncols) {
-    // The mat-vec kernel that follows may start its prologue (barrier set-up,
-    // weight loads) now; it waits for this grid before reading the fragments.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // Launched as a programmatic dependent of the kernel before it on the stream
-    // (a mat-vec that may still read this buffer, or the producer of x): wait
-    // for that grid before reading x or writing the prep buffer.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const MvPrepJob &J = jobs ? jobs[blockIdx.y] : single;
-    const int K = J.K;
-    const int j = blockIdx.x;  // activation column
-    const XT *xj = static_cast<const XT *>(J.x) + size_t(j) * K;
-    const int tid = threadIdx.x;
-    const int nb = K / 64;
-
-    // 1) column scale 2^s with max|x * 2^s| in [2^14, 2^15). The thread's first
-    //    16-element group stays in registers for step 2.
-    float first[16];
-    float m = 0.0f;
-    if (tid < nb * 4) {
-        if (sizeof(XT) == 4 && (reinterpret_cast<uintptr_t>(xj) & 15u) == 0) {
-            const float4 *src = reinterpret_cast<const float4 *>(xj + tid * 16);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const float4 f = src[q4];
-                first[4 * q4] = f.x;
-                first[4 * q4 + 1] = f.y;
-                first[4 * q4 + 2] = f.z;
-                first[4 * q4 + 3] = f.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) first[i] = ld_x(xj + tid * 16 + i);
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(first[i]));
-    }
-    for (int k = (kPrepThreads + tid) * 16; k < K; k += kPrepThreads * 16)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(ld_x(xj + k + i)));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    __shared__ float red[kPrepThreads / 32];
-    if ((tid & 31) == 0) red[tid >> 5] = m;
-    __syncthreads();
-    float amax = red[0];
-#pragma unroll
-    for (int w = 1; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
-    int s = 0;
-    if (amax > 0.0f && amax <= 3.4e38f) {
-        int e;
-        frexpf(amax, &e);  // amax = f * 2^e, f in [0.5, 1)
-        s = min(max(15 - e, -100), 126);
-    }
-    float *out_scale = reinterpret_cast<float *>(J.prep);
-    if (tid == 0) out_scale[j] = ldexpf(1.0f, 24 - s);
-    if (j == 0 && tid < 8 && tid >= ncols) out_scale[tid] = 0.0f;
-
-    // 2) fragments. Thread handles (block b, word c): the 16 elements 16c..16c+15.
-    const float fscale[4] = {ldexpf(1.0f, s), ldexpf(1.0f, s - 2), ldexpf(1.0f, s - 4),
-                             ldexpf(1.0f, s - 6)};
-    const int lane = tid & 31;
-    const int su = used_slots(ncols), rb = rec_bytes(ncols);
-    const int t = j >> 2, jc = j & 3;  // n-tile and column within it
-    for (int idx = tid; idx < nb * 4; idx += kPrepThreads) {
-        const int b = idx >> 2, c = idx & 3;
-        const XT *xe = xj + b * 64 + c * 16;
-        __half hi[16], lo[16];
-        float base_hi = 0.0f, base_lo = 0.0f;  // sum over the block of part * 4^m * 2^-24
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float xv = idx == tid ? first[i] : ld_x(xe + i);
-            const float v = xv * fscale[i & 3];
-            hi[i] = __float2half_rn(v);
-            lo[i] = __float2half_rn(v - __half2float(hi[i]));
-            const float wgt = ldexpf(1.0f, 2 * (i & 3) - 24);
-            base_hi += __half2float(hi[i]) * wgt;
-            base_lo += __half2float(lo[i]) * wgt;
-        }
-        uint32_t rh[8], rl[8];
-#pragma unroll
-        for (int mm = 0; mm < 4; ++mm) {
-            rh[2 * mm] = pack_half2(hi[mm], hi[8 + mm]);
-            rh[2 * mm + 1] = pack_half2(hi[4 + mm], hi[12 + mm]);
-            rl[2 * mm] = pack_half2(lo[mm], lo[8 + mm]);
-            rl[2 * mm + 1] = pack_half2(lo[4 + mm], lo[12 + mm]);
-        }
-        // full-block sums over the 4 threads (b, c = 0..3) = consecutive lanes
-        const unsigned grp = 0xFu << (lane & ~3);
-        base_hi += __shfl_xor_sync(grp, base_hi, 1);
-        base_hi += __shfl_xor_sync(grp, base_hi, 2);
-        base_lo += __shfl_xor_sync(grp, base_lo, 1);
-        base_lo += __shfl_xor_sync(grp, base_lo, 2);
-
-        // B column 2*jc (hi) is lane group 2*jc, column 2*jc+1 (lo) group 2*jc+1.
-        uint8_t *rec = J.prep + kPrepHeader + (size_t(b) * NT + t) * rb;
-        const int l_hi = 4 * (2 * jc) + c, l_lo = 4 * (2 * jc + 1) + c;
-        *reinterpret_cast<uint4 *>(rec + l_hi * 16) = make_uint4(rh[0], rh[1], rh[2], rh[3]);
-        *reinterpret_cast<uint4 *>(rec + 16 * su + l_hi * 16) = make_uint4(rh[4], rh[5], rh[6], rh[7]);
-        *reinterpret_cast<uint4 *>(rec + l_lo * 16) = make_uint4(rl[0], rl[1], rl[2], rl[3]);
-        *reinterpret_cast<uint4 *>(rec + 16 * su + l_lo * 16) = make_uint4(rl[4], rl[5], rl[6], rl[7]);
-        if (c == 0)
-            *reinterpret_cast<float2 *>(rec + 32 * su + 8 * jc) = make_float2(-base_hi, -base_lo);
-        // Column 0's CTA also clears the slots and starts of columns past ncols
-        // in the last tile (the tiles of ncols 5..8 share the 32-slot layout).
-        if (j == 0) {
-            const int last_t = NT - 1;
-            uint8_t *rl_rec = J.prep + kPrepHeader + (size_t(b) * NT + last_t) * rb;
-            for (int jj = ncols - 4 * last_t; jj < 4; ++jj) {
-                if (8 * jj + 8 > su) break;
-                for (int part = 0; part < 2; ++part) {
-                    const int l = 4 * (2 * jj + part) + c;
-                    *reinterpret_cast<uint4 *>(rl_rec + l * 16) = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4 *>(rl_rec + 16 * su + l * 16) = make_uint4(0, 0, 0, 0);
-                }
-            }
-            if (c == 0)
-                for (int jj = ncols - 4 * last_t; jj < 4; ++jj)
-                    *reinterpret_cast<float2 *>(rl_rec + 32 * su + 8 * jj) = make_float2(0.f, 0.f);
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Tensor-core mat-vec kernel
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                          uint32_t a3, uint32_t b0, uint32_t b1, float c0, float c1,
-                                          float c2, float c3) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%10,%11,%12,%13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2),
-          "f"(c3));
-}
-
-__device__ __forceinline__ uint32_t pick(const uint4 &a, const uint4 &b, int r) {
-    switch (r) {
-        case 0: return a.x;
-        case 1: return a.y;
-        case 2: return a.z;
-        case 3: return a.w;
-        case 4: return b.x;
-        case 5: return b.y;
-        case 6: return b.z;
-        default: return b.w;
-    }
-}
 
 // fp16 scale at a shared-memory address, as f32.
 __device__ __forceinline__ float lds_half_as_float(const uint8_t *p) {
     return __half2float(*reinterpret_cast<const __half *>(p));
 }
 
-// Code words and scales of one block pair for a thread's two rows (a, b):
-// element u = 0 is the even block (words straddle two aligned words), u = 1 the
-// odd block (words aligned).
-struct PairRegs {
-    uint32_t wa[2], wb[2];
-    float da[2], db[2];
-};
-
-__device__ __forceinline__ PairRegs load_pair(const uint8_t *row_a, const uint8_t *row_b, int pr,
-                                              int c) {
-    PairRegs r;
-    const uint8_t *pa = row_a + 36 * pr;
-    const uint8_t *pb = row_b + 36 * pr;
-    r.wa[0] = __byte_perm(*reinterpret_cast<const uint32_t *>(pa + 4 * c),
-                          *reinterpret_cast<const uint32_t *>(pa + 4 * c + 4), 0x5432);
-    r.wb[0] = __byte_perm(*reinterpret_cast<const uint32_t *>(pb + 4 * c),
-                          *reinterpret_cast<const uint32_t *>(pb + 4 * c + 4), 0x5432);
-    r.wa[1] = *reinterpret_cast<const uint32_t *>(pa + 20 + 4 * c);
-    r.wb[1] = *reinterpret_cast<const uint32_t *>(pb + 20 + 4 * c);
-    r.da[0] = lds_half_as_float(pa);
-    r.db[0] = lds_half_as_float(pb);
-    r.da[1] = lds_half_as_float(pa + 18);
-    r.db[1] = lds_half_as_float(pb + 18);
-    return r;
-}
-
-// One pipeline stage (8 blocks of a thread's rows a = row_a, b = row_a + 8) as
-// straight-line code: per block pair, the B fragments (data lanes only) and
-// accumulator starts, the two code words and scales per row, then the four MMA
-// steps issued step-major across the pair's two chains, then the scaling.
-template <int NT>
-__device__ __forceinline__ void mv_stage(float (&acc)[NT][4], uint4 (&fr0)[2][NT],
-                                         uint4 (&fr1)[2][NT], const uint8_t *row_a,
-                                         const uint8_t *rs, int rec_bytes, int su, int lane, int c,
-                                         const bool (&lane_used)[NT]) {
-    const uint8_t *row_b = row_a + 8 * kChunkBytes;
-#pragma unroll
-    for (int pr = 0; pr < kChunkBlocks / 2; ++pr) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u)
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                const uint8_t *rec = rs + ((2 * pr + u) * NT + t) * rec_bytes;
-                if (lane_used[t]) {  // other lanes keep their zero registers
-                    fr0[u][t] = *reinterpret_cast<const uint4 *>(rec + lane * 16);
-                    fr1[u][t] = *reinterpret_cast<const uint4 *>(rec + 16 * su + lane * 16);
-                }
-            }
-        const PairRegs cur = load_pair(row_a, row_b, pr, c);
-        uint32_t sa[2], sb[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            sa[u] = cur.wa[u] >> 8;
-            sb[u] = cur.wb[u] >> 8;
-        }
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            float2 st[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-                st[u] = *reinterpret_cast<const float2 *>(rs + ((2 * pr + u) * NT + t) * rec_bytes +
-                                                          32 * su + 8 * c);
-            float cc[2][4];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                cc[u][0] = st[u].x;
-                cc[u][1] = st[u].y;
-                cc[u][2] = st[u].x;
-                cc[u][3] = st[u].y;
-            }
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const uint32_t mask = 0x00030003u << (2 * m);
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    float dd[4];
-                    mma_16816(dd, cur.wa[u] & mask, cur.wb[u] & mask, sa[u] & mask, sb[u] & mask,
-                              pick(fr0[u][t], fr1[u][t], 2 * m), pick(fr0[u][t], fr1[u][t], 2 * m + 1),
-                              cc[u][0], cc[u][1], cc[u][2], cc[u][3]);
-                    cc[u][0] = dd[0];
-                    cc[u][1] = dd[1];
-                    cc[u][2] = dd[2];
-                    cc[u][3] = dd[3];
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                acc[t][0] = fmaf(cur.da[u], cc[u][0], acc[t][0]);
-                acc[t][1] = fmaf(cur.da[u], cc[u][1], acc[t][1]);
-                acc[t][2] = fmaf(cur.db[u], cc[u][2], acc[t][2]);
-                acc[t][3] = fmaf(cur.db[u], cc[u][3], acc[t][3]);
-            }
-        }
-    }
-}
-
 __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-constexpr int kConsumerWarps = kTileRows / 16;  // one 16-row MMA group per warp
-constexpr int kCtaThreads = (kConsumerWarps + 1) * 32;
-
-// NT: MMA n-tiles (1 for ncols <= 4, 2 for 5..8).
-template <int NT>
-__global__ void __launch_bounds__(kCtaThreads, 1)
-    mv_tc_kernel(const __grid_constant__ MvJob single, const MvParams p) {
-    // The next prep launch on the stream may become resident now; it waits for
-    // this grid before it touches any buffer this kernel reads.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    constexpr int kCW = kConsumerWarps;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const int kStages = p.n_stages;
-    const int su = used_slots(p.ncols), kRecBytes = rec_bytes(p.ncols);
-    const int kRStageBytes = kChunkBlocks * NT * kRecBytes;
-    uint8_t *w_stage = smem;                               // kStages x kWStageBytes
-    uint8_t *r_stage = smem + kStages * kWStageBytes;      // kStages x kRStageBytes
-    uint64_t *full = reinterpret_cast<uint64_t *>(r_stage + kStages * kRStageBytes);
-    uint64_t *empty = full + kMaxStages;
-    __shared__ int s_abort;
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kCW);
-        }
-        s_abort = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    // This CTA's work list.
-    int n_items, item_base = 0;
-    if (p.jobs) {
-        item_base = p.cta_begin[blockIdx.x];
-        n_items = p.cta_begin[blockIdx.x + 1] - item_base;
-    } else {
-        n_items = blockIdx.x < unsigned(single.n_tiles)
-                      ? (single.n_tiles - 1 - int(blockIdx.x)) / int(gridDim.x) + 1
-                      : 0;
-    }
-    auto item_at = [&](int i, const MvJob *&J, int &tile) {
-        if (p.jobs) {
-            const MvItem it = p.items[item_base + i];
-            J = &p.jobs[it.job];
-            tile = it.tile;
-        } else {
-            J = &single;
-            tile = int(blockIdx.x) + i * int(gridDim.x);
-        }
-    };
-
-    if (warp == kCW) {
-        // ------------------------------ producer ------------------------------
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t ph = 0;
-            int issued = 0;
-            bool ok = true, prep_ready = false;
-            for (int i = 0; i < n_items && ok; ++i) {
-                const MvJob *J;
-                int tile;
-                item_at(i, J, tile);
-                const int nch = J->n_chunks;
-                for (int ch = 0; ch < nch; ++ch) {
-                    if (!mbar_wait(&empty[stage], ph ^ 1u, p.err, kTagMvEmpty) ||
-                        *(volatile int *)&s_abort) {
-                        ok = false;
-                        s_abort = 1;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&full[stage], kWStageBytes + kRStageBytes);
-                    tma_load_2d(w_stage + stage * kWStageBytes, &J->tmap, ch * kChunkBytes,
-                                tile * kTileRows, &full[stage]);
-                    if (!prep_ready) {
-                        // The activation fragments come from the preceding kernel.
-                        grid_dependency_wait();
-                        prep_ready = true;
-                    }
-                    bulk_g2s(r_stage + stage * kRStageBytes,
-                             J->prep + kPrepHeader + size_t(ch) * kRStageBytes, kRStageBytes,
-                             &full[stage]);
-                    ++issued;
-                    if (++stage == kStages) {
-                        stage = 0;
-                        ph ^= 1u;
-                    }
-                }
-            }
-            if (!ok) {
-                // Let copies already issued land before the CTA exits (bounded).
-                int st = stage, pp = ph;
-                for (int k = 0; k < kStages && k < issued; ++k) {
-                    if (--st < 0) {
-                        st = kStages - 1;
-                        pp ^= 1;
-                    }
-                    mbar_wait(&full[st], uint32_t(pp), p.err, kTagMvFull);
-                }
-            }
-        }
-        return;
-    }
-
-    // ------------------------------ consumers ------------------------------
-    grid_dependency_wait();  // the epilogue reads the column scales written by prep
-    const int g = lane >> 2, c = lane & 3;
-    // Lane groups g < 2 * (columns of tile t) carry B data.
-    bool lane_used[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) lane_used[t] = g < 2 * min(4, p.ncols - 4 * t);
-
-    // B-fragment registers of a block pair; lanes that carry no column keep zeros.
-    uint4 fr0[2][NT], fr1[2][NT];
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-#pragma unroll
-        for (int t = 0; t < NT; ++t) fr0[u][t] = fr1[u][t] = make_uint4(0, 0, 0, 0);
-
-    int stage = 0;
-    uint32_t ph = 0;
-    for (int i = 0; i < n_items; ++i) {
-        const MvJob *J;
-        int tile;
-        item_at(i, J, tile);
-        const int n_chunks = J->n_chunks;
-        float acc[NT][4];
-#pragma unroll
-        for (int t = 0; t < NT; ++t)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) acc[t][k] = 0.0f;
-
-        bool ok = true;
-        for (int ch = 0; ch < n_chunks; ++ch) {
-            const bool got = mbar_wait(&full[stage], ph, p.err, kTagMvFull) &&
-                             !*(volatile int *)&s_abort;
-            if (!__all_sync(0xffffffffu, got)) {  // warp-uniform decision
-                s_abort = 1;
-                ok = false;
-                break;
-            }
-            mv_stage<NT>(acc, fr0, fr1, w_stage + stage * kWStageBytes + (warp * 16 + g) * kChunkBytes,
-                         r_stage + stage * kRStageBytes, kRecBytes, su, lane, c, lane_used);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
-            if (++stage == kStages) {
-                stage = 0;
-                ph ^= 1u;
-            }
-        }
-        if (!ok) break;
-
-        // ---- epilogue: hi + lo of column 4t + c, undo the column scale, store ----
-        const float *out_scale = reinterpret_cast<const float *>(J->prep);
-        const int N = J->N;
-        const int row_a = tile * kTileRows + warp * 16 + g;
-        const int row_b = row_a + 8;
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            const int col = 4 * t + c;
-            if (col < p.ncols) {
-                const float sc = out_scale[col];
-                if (row_a < N) J->y[size_t(col) * N + row_a] = (acc[t][0] + acc[t][1]) * sc;
-                if (row_b < N) J->y[size_t(col) * N + row_b] = (acc[t][2] + acc[t][3]) * sc;
-            }
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// tcgen05 mat-vec (ncols 1..3)
-//
-// The codes become tensor-core operands without any arithmetic: byte j of a
-// code word holds elements 4j..4j+3 at bits 0-1, 2-3, 4-5, 6-7, and read as
-// e4m3 a byte whose only set bits are 0-1 is the subnormal q * 2^-9, one whose
-// only set bits are 2-3 is q * 2^-7 (bit 2 is the top mantissa bit, bit 3 the
-// lowest exponent bit: 0, 2^-7, 2^-6, 1.5 * 2^-6). So word & 0x03030303,
-// word & 0x0C0C0C0C, (word >> 4) & 0x03030303 and (word >> 4) & 0x0C0C0C0C are
-// four registers of exact e4m3 weights, one logic op each. Four expansion
-// warps per 128-row tile store them into tensor memory (one row per TMEM lane)
-// and one thread issues tcgen05.mma kind::f8f6f4 (M = 128, N = 16, K = 32)
-// with A in TMEM and B = the activations as e4m3 pieces in shared memory.
-//
-// Activations as e4m3 pieces. Per column j, u = x * 2^s_j with max|u| in
-// [2^-2, 2^-1); element e gives v = u * 2^9 (codes at bits 0-1) or u * 2^7
-// (bits 2-3), split into kT5Pieces e4m3 values: piece p = e4m3(r_p * 2^4p),
-// r_0 = v, r_{p+1} = r_p - piece_p * 2^-4p; each rounding keeps 4 significant
-// bits, so the residual after 5 pieces is below 2^-20 |v|. Piece p of column j
-// is B row n = 5j + p. A block's MMA result per row is then C_n = sum q *
-// piece_n / (2^9 or 2^7).
-//
-// Per block accumulators. d changes every 64 weights of a row, so each block
-// gets its own accumulator columns; the epilogue loads them and forms, per
-// row and column,
-//   t = sum_p 2^-4p C_(5j+p) - beta_j,   acc_j += d * t,
-// where beta_j is the same sum for all-ones codes (the "- 1" of (q - 1)),
-// computed by the preparation kernel with the same f32 operations from exact
-// per-piece sums, so that all-ones blocks give exactly 0. With one column
-// (5 pieces) two blocks share a 16-column accumulator: the even block's pieces
-// are B rows 0-4 and the odd block's rows 8-12, each block's other rows zero,
-// and the odd block's MMAs accumulate onto the even block's result. With 2-3
-// columns each block has its own 16 columns.
-//
-// Pipeline per CTA (persistent over 128-row tiles), stage = 8 blocks:
-//   warp 2      streams the stage's TMA box (144 B x 128 rows) and, by bulk
-//               copy, its B image and betas into an 8-deep shared-memory ring;
-//   warps 4-11  expand the stage's codes into a TMEM A buffer (3 buffers with
-//               one column, 2 with 2-3; warps 4-7 blocks 0-3, warps 8-11 blocks
-//               4-7; warp w owns TMEM lanes 32 (w % 4) .. +31, i.e. those rows);
-//   warp 3      issues the stage's 16 MMAs into one of two TMEM D buffers and
-//               commits them to the expansion (A free) and epilogue (D full)
-//               barriers. The whole warp runs the loop and waits, and the
-//               elected lane issues: from a lone lane each MMA cost ~70 cycles
-//               to issue, and a warp diverged around the waits took ~200 cycles
-//               to reconverge;
-//   warps 12-15 epilogue, one row per thread: D, the row's d values from the
-//               ring and the betas; they release the D buffer and the ring slot.
-// The expansion of a stage waits for the MMAs that last read its A buffer, so
-// the A buffer count sets how far expansion runs ahead of the tensor core.
-// ---------------------------------------------------------------------------
-constexpr int kT5Rows = 128;
-constexpr int kT5Pieces = 5;
-constexpr int kT5MaxCols = 3;                         // 5 * 3 pieces fit N = 16
-constexpr int kT5N = 16;
-constexpr int kT5Stages = 8;
-constexpr int kT5RawBytes = kT5Rows * kChunkBytes;   // 18432
-constexpr int kT5ImgBytes = kT5N * kChunkBlocks * 64; // 8192: 16 rows x 512 K bytes, SW128
-constexpr int kT5BetaBytes = kChunkBlocks * 4 * 4;   // beta[8 blocks][4 columns] f32
-constexpr int kT5PrepHeader = 1024;                  // int col_shift[8], images 1024-aligned
-constexpr int kT5ExpWarps = 4;
-constexpr int kT5EpiWarps = 4;
-// Warp roles. A warp reaches only the TMEM lanes of its quarter (warp % 4), so
-// each quarter hosts 1 expansion warp and 1 epilogue warp (12 warps in all: a
-// second expansion warp per quarter measured slower at ncols 2 and no faster
-// at 3). Two MMA issuers (even and odd stages) sit on warps 1 and 3, the
-// producer on warp 2.
-constexpr int kT5ProdWarp = 2;
-constexpr int kT5MmaWarp = 3;    // even stages; allocates TMEM
-constexpr int kT5MmaWarp2 = 1;   // odd stages
-constexpr int kT5ExpWarp0 = 4;   // warps 4-7
-constexpr int kT5EpiWarp0 = 8;   // warps 8-11
-constexpr int kT5Warps = kT5EpiWarp0 + kT5EpiWarps;
-constexpr int kT5Threads = kT5Warps * 32;
-constexpr int kT5MaxABufs = 3;
-constexpr int kT5Smem = 1024 /* alignment slack */ +
-                        kT5Stages * (kT5ImgBytes + kT5RawBytes + kT5BetaBytes) +
-                        (2 * kT5Stages + 2 * kT5MaxABufs + 4) * 8;
-// TMEM columns (512): A buffers of 128 (8 blocks x 16 columns of 4 e4m3), then
-// two D buffers of 64 (one column: 4 block pairs x 16) or 128 (8 blocks x 16).
-__host__ __device__ constexpr int t5_abufs(int nc) { return nc == 1 ? 3 : 2; }
-__host__ __device__ constexpr int t5_dcols(int nc) { return nc == 1 ? 64 : 128; }
-static_assert(t5_abufs(1) * 128 + 2 * t5_dcols(1) <= 512, "TMEM budget");
-static_assert(t5_abufs(2) * 128 + 2 * t5_dcols(2) <= 512, "TMEM budget");
-constexpr int kTagT5Full = 111;
-constexpr int kTagT5Empty = 112;
-constexpr int kTagT5AFull = 113;
-constexpr int kTagT5DFull = 114;
-constexpr int kTagT5DEmpty = 115;
-
-size_t t5_prep_bytes(int64_t K) {
-    const size_t n_chunks = size_t(K / 512);
-    size_t b = kT5PrepHeader + n_chunks * (kT5ImgBytes + kT5BetaBytes);
-    return (b + 255) & ~size_t(255);
-}
-
-// Byte offset of element (row n, K position kc) of one stage's B image: K-major
-// rows of 128 bytes in atoms of 8 rows (1024 B); the 16-byte chunk index is
-// XOR-ed with the row within the atom (128-byte swizzle); 4 atom columns of
-// 128 K bytes (2 KB each: rows 0-7, then rows 8-15).
-__host__ __device__ constexpr int t5_img_offset(int n, int kc) {
-    return (kc >> 7) * 2048 + (n >> 3) * 1024 + (n & 7) * 128 +
+// Byte offset of element (row n, K byte kc) of one stage's activation image of
+// `rows` rows: K-major rows of 128 bytes in atoms of 8 rows (1024 B); the
+// 16-byte chunk index is XOR-ed with the row within the atom (128-byte
+// swizzle); the K extent is split into atom columns of 128 bytes, each holding
+// all rows (rows * 128 bytes).
+__host__ __device__ constexpr int img_offset(int rows, int n, int kc) {
+    return (kc >> 7) * (rows * 128) + (n >> 3) * 1024 + (n & 7) * 128 +
            ((((kc & 127) >> 4) ^ (n & 7)) << 4) + (kc & 15);
 }
 
-// Preparation: grid (ncols, n_jobs), kPrepThreads threads. Thread (block b,
-// word c, r) handles the 4 elements 16c + 4jj + r (jj = 0..3) of block b and
-// writes, per piece, one 32-bit word of the B image: K positions 64 (b % 8) +
-// 16c + 4r + jj (the order the expansion warps store codes in TMEM: column
-// 4c + r of a block holds elements 16c + 4jj + r in byte jj). The per-piece
-// all-ones sums are exact integers in units of 2^-18 (a piece is a multiple of
-// 2^-9, divided by 2^9 or 2^7; |sum| < 64 * 448 * 2^-7), rounded once to f32.
-constexpr int kT5PrepThreads = 256;
-
-template <typename XT>
-__global__ void __launch_bounds__(kT5PrepThreads) t5_prep_kernel(
-    const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs, int ncols) {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // Launched as a programmatic dependent of the kernel before it on the stream
-    // (a mat-vec that may still read this buffer, or the producer of x): wait
-    // for that grid before reading x or writing the prep buffer.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const MvPrepJob &J = jobs ? jobs[blockIdx.y] : single;
-    const int K = J.K;
-    const int j = blockIdx.x;
-    const XT *xj = static_cast<const XT *>(J.x) + size_t(j) * K;
-    const int tid = threadIdx.x;
-    const int nb = K / 64;
-    const int n_chunks = K / 512;
-    // grid z splits a column's 16 * nb items (one per thread, grid-stride for
-    // very long columns); the CTAs past this column's items have nothing to do
-    if (int(blockIdx.z) * kT5PrepThreads >= nb * 16) return;
-
-    // 1) column scale 2^s with max|x * 2^s| in [2^-2, 2^-1) (each CTA of the
-    //    column reads the whole column)
-    float m = 0.0f;
-    if (sizeof(XT) == 4 && (reinterpret_cast<uintptr_t>(xj) & 15u) == 0) {
-        const float4 *x4 = reinterpret_cast<const float4 *>(xj);
-        for (int k = tid; k < K / 4; k += kT5PrepThreads) {
-            const float4 f = x4[k];
-            m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
-        }
-    } else {
-        for (int k = tid; k < K; k += kT5PrepThreads) m = fmaxf(m, fabsf(ld_x(xj + k)));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    __shared__ float red[kT5PrepThreads / 32];
-    if ((tid & 31) == 0) red[tid >> 5] = m;
-    __syncthreads();
-    float amax = red[0];
-#pragma unroll
-    for (int w = 1; w < kT5PrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
-    int s = 0;
-    if (amax > 0.0f && amax <= 3.4e38f) {
-        int e;
-        frexpf(amax, &e);  // amax = f * 2^e, f in [0.5, 1)
-        s = -e - 1;
-    }
-    int *col_shift = reinterpret_cast<int *>(J.prep);
-    if (blockIdx.z == 0 && tid == 0) col_shift[j] = s;
-
-    // 2) pieces
-    uint8_t *img = J.prep + kT5PrepHeader;
-    float *beta = reinterpret_cast<float *>(img + size_t(n_chunks) * kT5ImgBytes);
-    const int lane = tid & 31;
-    const unsigned grp = 0xFFFFu << (lane & 16);  // the block's 16 threads
-    for (int idx = int(blockIdx.z) * kT5PrepThreads + tid; idx < nb * 16;
-         idx += int(gridDim.z) * kT5PrepThreads) {
-        const int b = idx >> 4, c = (idx >> 2) & 3, r = idx & 3;
-        const XT *xe = xj + b * 64 + c * 16 + r;
-        const int e_in = s + ((r & 1) ? 7 : 9);    // v = x * 2^e_in
-        const float to_int = (r & 1) ? 2048.0f : 512.0f;  // piece / (2^7 or 2^9) in 2^-18 units
-        float v[4];
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) v[jj] = mul_pow2(ld_x(xe + 4 * jj), e_in);
-        uint8_t *bimg = img + size_t(b >> 3) * kT5ImgBytes;
-        const int kc = 64 * (b & 7) + 16 * c;
-        int isum[kT5Pieces];
-#pragma unroll
-        for (int p = 0; p < kT5Pieces; ++p) {
-            const float up = __int_as_float((127 + 4 * p) << 23);
-            const float down = __int_as_float((127 - 4 * p) << 23);
-            const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                make_float2(v[0] * up, v[1] * up), __NV_SATFINITE, __NV_E4M3);
-            const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                make_float2(v[2] * up, v[3] * up), __NV_SATFINITE, __NV_E4M3);
-            const float2 plo = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3)));
-            const float2 phi = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
-            v[0] -= plo.x * down;
-            v[1] -= plo.y * down;
-            v[2] -= phi.x * down;
-            v[3] -= phi.y * down;
-            isum[p] = __float2int_rn(plo.x * to_int) + __float2int_rn(plo.y * to_int) +
-                      __float2int_rn(phi.x * to_int) + __float2int_rn(phi.y * to_int);
-            // one column: the block's pieces are rows 0-4 (even block) or 8-12 (odd)
-            const int n = ncols == 1 ? 8 * (b & 1) + p : kT5Pieces * j + p;
-            *reinterpret_cast<uint32_t *>(bimg + t5_img_offset(n, kc) + 4 * r) =
-                uint32_t(lo) | (uint32_t(hi) << 16);
-        }
-        if (ncols == 1) {
-            // the rows the other block of the pair reads its result from stay zero
-            for (int n = 8 * (1 - (b & 1)); n < 8 * (1 - (b & 1)) + 8; ++n)
-                *reinterpret_cast<uint32_t *>(bimg + t5_img_offset(n, kc) + 4 * r) = 0u;
-        }
-        float base[kT5Pieces];
-#pragma unroll
-        for (int p = 0; p < kT5Pieces; ++p) {
-            int t = isum[p];
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1) t += __shfl_xor_sync(grp, t, o);
-            base[p] = float(t) * 0x1p-18f;
-        }
-        if ((idx & 15) == 0) {
-            // the epilogue's combination, applied to the all-ones results
-            float t = base[4] * 0x1p-16f;
-            t = fmaf(base[3], 0x1p-12f, t);
-            t = fmaf(base[2], 0x1p-8f, t);
-            t = fmaf(base[1], 0x1p-4f, t);
-            t = t + base[0];
-            beta[size_t(b >> 3) * (kT5BetaBytes / 4) + (b & 7) * 4 + j] = t;
-        }
-    }
-}
-
-// kind::f8f6f4 instruction descriptor: D f32, A and B e4m3, both K-major, N, M.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n) {
-    return (1u << 4) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
-}
-
-// NC: activation columns (1..3).
-template <int NC>
-__global__ void __launch_bounds__(kT5Threads, 1)
-    mv_t5_kernel(const __grid_constant__ MvJob single, const MvParams p) {
-    // The next prep launch on the stream may become resident now; it waits for
-    // this grid before it touches any buffer this kernel reads.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    constexpr int kABufs = t5_abufs(NC);
-    constexpr int kDCols = t5_dcols(NC);
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
-    uint8_t *img_ring = smem;                                      // kT5Stages x 8 KB
-    uint8_t *raw_ring = img_ring + kT5Stages * kT5ImgBytes;         // kT5Stages x 18 KB
-    uint8_t *beta_ring = raw_ring + kT5Stages * kT5RawBytes;        // kT5Stages x 128 B
-    uint64_t *full = reinterpret_cast<uint64_t *>(beta_ring + kT5Stages * kT5BetaBytes);
-    uint64_t *empty = full + kT5Stages;        // arrived by the 4 epilogue warps
-    uint64_t *a_full = empty + kT5Stages;      // [kABufs] arrived by the 8 expansion warps
-    uint64_t *a_empty = a_full + kT5MaxABufs;  // [kABufs] tcgen05.commit
-    uint64_t *d_full = a_empty + kT5MaxABufs;  // [2] tcgen05.commit
-    uint64_t *d_empty = d_full + 2;            // [2] arrived by the 4 epilogue warps
-    __shared__ uint32_t s_tmem;
-    __shared__ int s_abort;
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kT5Stages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kT5EpiWarps);
-        }
-        for (int i = 0; i < kABufs; ++i) {
-            mbar_init(&a_full[i], kT5ExpWarps);
-            mbar_init(&a_empty[i], 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&d_full[i], 1);
-            mbar_init(&d_empty[i], kT5EpiWarps);
-        }
-        s_abort = 0;
-        fence_barrier_init();
-    }
-    if (warp == kT5MmaWarp) {
-        tmem_alloc(&s_tmem, 512);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = s_tmem;
-
-    int n_items, item_base = 0;
-    if (p.jobs) {
-        item_base = p.cta_begin[blockIdx.x];
-        n_items = p.cta_begin[blockIdx.x + 1] - item_base;
-    } else {
-        n_items = blockIdx.x < unsigned(single.n_tiles)
-                      ? (single.n_tiles - 1 - int(blockIdx.x)) / int(gridDim.x) + 1
-                      : 0;
-    }
-    auto item_at = [&](int i, const MvJob *&J, int &tile) {
-        if (p.jobs) {
-            const MvItem it = p.items[item_base + i];
-            J = &p.jobs[it.job];
-            tile = it.tile;
-        } else {
-            J = &single;
-            tile = int(blockIdx.x) + i * int(gridDim.x);
-        }
-    };
-    auto stage_parity = [](int s) { return uint32_t(s / kT5Stages) & 1u; };
-    // A buffer of stage s and the parity of its use; D buffer likewise
-    auto a_buf = [](int s) { return s % kABufs; };
-    auto a_use = [](int s) { return uint32_t(s / kABufs) & 1u; };
-    auto a_col = [&](int s) { return uint32_t(a_buf(s) * 128); };
-    auto d_col = [&](int s) { return uint32_t(kABufs * 128 + (s & 1) * kDCols); };
-
-    if (warp == kT5ProdWarp) {
-        // ------------------------------ producer ------------------------------
-        if (lane == 0) {
-            int s = 0;
-            bool ok = true, prep_ready = false;
-            for (int i = 0; i < n_items && ok; ++i) {
-                const MvJob *J;
-                int tile;
-                item_at(i, J, tile);
-                const uint8_t *img = J->prep + kT5PrepHeader;
-                const uint8_t *beta = img + size_t(J->n_chunks) * kT5ImgBytes;
-                const int nch = J->n_chunks;
-                for (int ch = 0; ch < nch; ++ch, ++s) {
-                    const int st = s % kT5Stages;
-                    if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagT5Empty, true) ||
-                        *(volatile int *)&s_abort) {
-                        ok = false;
-                        s_abort = 1;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&full[st], kT5RawBytes + kT5ImgBytes + kT5BetaBytes);
-                    tma_load_2d(raw_ring + st * kT5RawBytes, &J->tmap, ch * kChunkBytes,
-                                tile * kT5Rows, &full[st]);
-                    if (!prep_ready) {
-                        grid_dependency_wait();  // the B images come from the prep kernel
-                        prep_ready = true;
-                    }
-                    bulk_g2s(img_ring + st * kT5ImgBytes, img + size_t(ch) * kT5ImgBytes,
-                             kT5ImgBytes, &full[st]);
-                    bulk_g2s(beta_ring + st * kT5BetaBytes, beta + size_t(ch) * kT5BetaBytes,
-                             kT5BetaBytes, &full[st]);
-                }
-            }
-            if (!ok) {
-                // let copies already issued land (bounded) before the CTA exits
-                for (int k = 1; k <= kT5Stages && s - k >= 0; ++k)
-                    mbar_wait(&full[(s - k) % kT5Stages], stage_parity(s - k), p.err, kTagT5Full);
-            }
-        }
-    } else if (warp == kT5MmaWarp || warp == kT5MmaWarp2) {
-        // ------------------------------ MMA issuers ------------------------------
-        // Each issuer's per-stage control path (barrier checks, fence, issue,
-        // commits) takes about a stage's worth of time, so two issuers take
-        // the even and the odd stages (D buffer = stage parity; consecutive
-        // uses of an A buffer are ordered through its expansion). The whole
-        // warp runs the loop and waits (addresses and descriptors stay
-        // warp-uniform, and the warp stays converged); the elected lane issues
-        // the MMAs and commits them.
-        constexpr uint32_t idesc = idesc_e4m3(kT5Rows, kT5N);
-        const bool leader = elect_one();
-        const int parity = warp == kT5MmaWarp ? 0 : 1;
-        const uint64_t desc0 = sw128_desc(smem_addr(img_ring));
-        int s = 0, last = -1;
-        bool ok = true;
-        for (int i = 0; i < n_items && ok; ++i) {
-            const MvJob *J;
-            int tile;
-            item_at(i, J, tile);
-            const int nch = J->n_chunks;
-            for (int ch = 0; ch < nch; ++ch, ++s) {
-                if ((s & 1) != parity) continue;
-                const int st = s % kT5Stages;
-                const bool got =
-                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
-                    mbar_wait(&a_full[a_buf(s)], a_use(s), p.err, kTagT5AFull) &&
-                    mbar_wait(&d_empty[s & 1], (uint32_t(s >> 1) & 1u) ^ 1u, p.err,
-                              kTagT5DEmpty) &&
-                    !*(volatile int *)&s_abort;
-                if (!__all_sync(0xffffffffu, got)) {
-                    ok = false;
-                    s_abort = 1;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t a_base = tmem + a_col(s);
-                const uint32_t d_base = tmem + d_col(s);
-                // descriptor start-address field advanced by the byte offset / 16
-                const uint64_t dst = desc0 + uint64_t((st * kT5ImgBytes) >> 4);
-                if (leader) {
-#pragma unroll
-                    for (int b = 0; b < kChunkBlocks; ++b)
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk) {
-                            // one column: blocks 2i, 2i+1 share accumulator i
-                            const uint32_t dcol = NC == 1 ? (b >> 1) * kT5N : b * kT5N;
-                            const uint32_t accum = NC == 1 ? uint32_t((b & 1) | kk) : uint32_t(kk);
-                            tc_mma_f8f6f4_ta(d_base + dcol, a_base + b * 16 + kk * 8,
-                                             dst + uint64_t(((b >> 1) * 2048 + (b & 1) * 64 +
-                                                             kk * 32) >> 4),
-                                             idesc, accum);
-                        }
-                    tc_commit(&a_empty[a_buf(s)]);
-                    tc_commit(&d_full[s & 1]);
-                }
-                __syncwarp();
-                last = s;
-            }
-        }
-        if (last >= 0)  // TMEM is freed only after the last MMAs completed
-            mbar_wait(&d_full[last & 1], uint32_t(last >> 1) & 1u, p.err, kTagT5DFull);
-    } else if (warp >= kT5ExpWarp0 && warp < kT5ExpWarp0 + kT5ExpWarps) {
-        // ------------------------------ expansion ------------------------------
-        // warp w: TMEM lane quarter w % 4 (rows 32 (w % 4) ..), all 8 blocks
-        const int qd = warp & 3;
-        const int row = 32 * qd + lane;
-        const uint32_t lane_base = uint32_t(32 * qd) << 16;
-        int s = 0;
-        bool ok = true;
-        for (int i = 0; i < n_items && ok; ++i) {
-            const MvJob *J;
-            int tile;
-            item_at(i, J, tile);
-            const int nch = J->n_chunks;
-            for (int ch = 0; ch < nch; ++ch, ++s) {
-                const int st = s % kT5Stages;
-                const bool got =
-                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
-                    mbar_wait(&a_empty[a_buf(s)], a_use(s) ^ 1u, p.err, kTagT5AFull) &&
-                    !*(volatile int *)&s_abort;
-                if (!__all_sync(0xffffffffu, got)) {
-                    s_abort = 1;
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int G = 0; G < 2; ++G) {
-                    const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes + G * 72;
-                    uint32_t u[18];
-#pragma unroll
-                    for (int k = 0; k < 9; ++k) {
-                        const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * k);
-                        u[2 * k] = v.x;
-                        u[2 * k + 1] = v.y;
-                    }
-                    const uint32_t a_base = tmem + lane_base + a_col(s) + 4 * G * 16;
-#pragma unroll
-                    for (int bi = 0; bi < 4; ++bi) {
-                        uint32_t a[16];
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint32_t w;
-                            if (bi == 0) w = __byte_perm(u[c], u[c + 1], 0x5432);
-                            else if (bi == 1) w = u[5 + c];
-                            else if (bi == 2) w = __byte_perm(u[9 + c], u[10 + c], 0x5432);
-                            else w = u[14 + c];
-                            const uint32_t hw = w >> 4;
-                            a[4 * c + 0] = w & 0x03030303u;
-                            a[4 * c + 1] = w & 0x0C0C0C0Cu;
-                            a[4 * c + 2] = hw & 0x03030303u;
-                            a[4 * c + 3] = hw & 0x0C0C0C0Cu;
-                        }
-                        tmem_st16(a_base + bi * 16, a);
-                    }
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[a_buf(s)]);
-            }
-        }
-    } else if (warp >= kT5EpiWarp0) {
-        // ------------------------------ epilogue ------------------------------
-        // warp w: TMEM lane quarter w % 4; one row per thread, all 8 blocks.
-        grid_dependency_wait();  // reads the column shifts written by prep
-        const int qd = warp & 3;
-        const int row = 32 * qd + lane;
-        const uint32_t lane_base = uint32_t(32 * qd) << 16;
-        float acc[NC];
-#pragma unroll
-        for (int j = 0; j < NC; ++j) acc[j] = 0.0f;
-        int s = 0;
-        bool ok = true;
-        for (int i = 0; i < n_items && ok; ++i) {
-            const MvJob *J;
-            int tile;
-            item_at(i, J, tile);
-            const int nch = J->n_chunks;
-            for (int ch = 0; ch < nch; ++ch, ++s) {
-                const int st = s % kT5Stages;
-                const bool got =
-                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
-                    mbar_wait(&d_full[s & 1], uint32_t(s >> 1) & 1u, p.err, kTagT5DFull) &&
-                    !*(volatile int *)&s_abort;
-                if (!__all_sync(0xffffffffu, got)) {
-                    s_abort = 1;
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_base = tmem + lane_base + d_col(s);
-                const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes;
-                const float *bt = reinterpret_cast<const float *>(beta_ring + st * kT5BetaBytes);
-#pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    // blocks 4hb .. 4hb+3: C[bi][n] = accumulator column n of block 4hb+bi
-                    float C[4][NC * 5];
-                    if (NC == 1) {
-                        uint32_t r[2][16];
-#pragma unroll
-                        for (int pi = 0; pi < 2; ++pi)
-                            tmem_ld16(d_base + (2 * hb + pi) * kT5N, r[pi]);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int bi = 0; bi < 4; ++bi)
-#pragma unroll
-                            for (int n = 0; n < 5; ++n)
-                                C[bi][n] = __uint_as_float(r[bi >> 1][8 * (bi & 1) + n]);
-                    } else {
-                        uint32_t r[4][16];
-#pragma unroll
-                        for (int bi = 0; bi < 4; ++bi)
-                            tmem_ld16(d_base + (4 * hb + bi) * kT5N, r[bi]);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int bi = 0; bi < 4; ++bi)
-#pragma unroll
-                            for (int n = 0; n < NC * 5; ++n) C[bi][n] = __uint_as_float(r[bi][n]);
-                    }
-#pragma unroll
-                    for (int bi = 0; bi < 4; ++bi) {
-                        const int b = 4 * hb + bi;
-                        const float d = lds_half_as_float(rp + 18 * b);
-#pragma unroll
-                        for (int j = 0; j < NC; ++j) {
-                            const float *c = &C[bi][5 * j];
-                            float t = c[4] * 0x1p-16f;
-                            t = fmaf(c[3], 0x1p-12f, t);
-                            t = fmaf(c[2], 0x1p-8f, t);
-                            t = fmaf(c[1], 0x1p-4f, t);
-                            t = t + c[0];
-                            acc[j] = fmaf(d, t - bt[b * 4 + j], acc[j]);
-                        }
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&d_empty[s & 1]);
-                    mbar_arrive(&empty[st]);
-                }
-                if (ch == nch - 1) {
-                    const int *col_shift = reinterpret_cast<const int *>(J->prep);
-                    const int r = tile * kT5Rows + row;
-                    if (r < J->N)
-#pragma unroll
-                        for (int j = 0; j < NC; ++j)
-                            J->y[size_t(j) * J->N + r] = mul_pow2(acc[j], -col_shift[j]);
-#pragma unroll
-                    for (int j = 0; j < NC; ++j) acc[j] = 0.0f;
-                }
-            }
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == kT5MmaWarp) {
-        tc_fence_after();
-        tmem_dealloc(tmem, 512);
-    }
+// The 18 bytes of block 4G + bi of a row's stage slice as four code words,
+// from the 72-byte half G loaded as u[0..17]: even blocks start 2 bytes into a
+// 4-byte word (d first), so their words straddle two aligned words.
+__device__ __forceinline__ uint32_t block_word(const uint32_t (&u)[18], int bi, int c) {
+    if (bi == 0) return __byte_perm(u[c], u[c + 1], 0x5432);
+    if (bi == 1) return u[5 + c];
+    if (bi == 2) return __byte_perm(u[9 + c], u[10 + c], 0x5432);
+    return u[14 + c];
 }
 
 // ---------------------------------------------------------------------------
@@ -1198,7 +203,9 @@ __global__ void __launch_bounds__(kT5Threads, 1)
 // does not grow with K.
 // ---------------------------------------------------------------------------
 constexpr int kT4Pieces = 16;
-constexpr int kT4ImgBytes = kT5N * kChunkBlocks * 32;  // 4096: 16 rows x 256 bytes (512 e2m1)
+constexpr int kT4N = 16;                               // MMA N: one B row per piece
+constexpr int kT4Stages = 8;
+constexpr int kT4ImgBytes = kT4N * kChunkBlocks * 32;  // 4096: 16 rows x 256 bytes (512 e2m1)
 // per block of a stage: float {2^(e - 1), H, M, L}
 constexpr int kT4BlockRec = 4;
 constexpr int kT4BetaBytes = kChunkBlocks * kT4BlockRec * 4;  // 128
@@ -1207,15 +214,20 @@ constexpr int kT4ACol = 256;                           // A buffers at 256 + 64 
 constexpr int kT4ScaleCol = 448;                       // scales A 448..451, B 452..455
 // mbarriers: full / empty per stage, a_full / a_empty per A buffer, d_full /
 // d_empty per D buffer, a drain per MMA issuer
-constexpr int kT4Barriers = 2 * kT5Stages + 2 * kT4ABufs + 2 * 2 + 2;
+constexpr int kT4Barriers = 2 * kT4Stages + 2 * kT4ABufs + 2 * 2 + 2;
 constexpr int kT4Smem = 1024 /* alignment slack */ +
-                        kT5Stages * (kT4ImgBytes + kT5RawBytes + kT4BetaBytes) +
+                        kT4Stages * (kT4ImgBytes + kRawBytes + kT4BetaBytes) +
                         kT4Barriers * 8;
-static_assert(kT4Pieces == kT5N, "one B row per piece");
+static_assert(kT4Pieces == kT4N, "one B row per piece");
+constexpr int kTagT4Full = 111;
+constexpr int kTagT4Empty = 112;
+constexpr int kTagT4AFull = 113;
+constexpr int kTagT4DFull = 114;
+constexpr int kTagT4DEmpty = 115;
 
 size_t t4_prep_bytes(int64_t K) {
     const size_t n_chunks = size_t(K / 512);
-    size_t b = kT5PrepHeader + n_chunks * (kT4ImgBytes + kT4BetaBytes);
+    size_t b = kPrepHeader + n_chunks * (kT4ImgBytes + kT4BetaBytes);
     return (b + 255) & ~size_t(255);
 }
 
@@ -1225,19 +237,14 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int m, int n) {
            (uint32_t(m >> 4) << 24);
 }
 
-// 2^k as a float for k in [-149, 127] (subnormal below -126).
-__device__ __forceinline__ float pow2f(int k) {
-    return k >= -126 ? __int_as_float((127 + k) << 23) : __int_as_float(1 << (149 + k));
-}
-
-// Preparation: grid (1, n_jobs, z), kT5PrepThreads threads. Item (block b,
+// Preparation: grid (1, n_jobs, z), kPrepThreads threads. Item (block b,
 // word c, parity h): the 8 elements 16c + 2j + h (j = 0..7) of block b, one
 // 32-bit word of the B image per piece (K positions 64 (b % 8) + 16c + 8h + j,
 // nibble j). The 8 items of a block are 8 consecutive lanes: they share the
 // block maximum and sum the all-ones groups H, M, L by shuffles (every partial
 // sum is exact).
 template <typename XT>
-__global__ void __launch_bounds__(kT5PrepThreads) t4_prep_kernel(
+__global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
     const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // Launched as a programmatic dependent of the kernel before it on the stream
@@ -1253,14 +260,14 @@ __global__ void __launch_bounds__(kT5PrepThreads) t4_prep_kernel(
     const XT *xj = static_cast<const XT *>(J.x);
     const int nb = K / 64;
     const int n_chunks = K / 512;
-    uint8_t *img = J.prep + kT5PrepHeader;
+    uint8_t *img = J.prep + kPrepHeader;
     float *brec = reinterpret_cast<float *>(img + size_t(n_chunks) * kT4ImgBytes);
     const int lane = threadIdx.x & 31;
     const unsigned grp = 0xFFu << (lane & 24);  // the block's 8 threads
     // 8 items per block and nb blocks: whole warps share a block range, so the
     // shuffles below always run with all 8 lanes of a block present
-    for (int idx = int(blockIdx.z) * kT5PrepThreads + int(threadIdx.x); idx < nb * 8;
-         idx += int(gridDim.z) * kT5PrepThreads) {
+    for (int idx = int(blockIdx.z) * kPrepThreads + int(threadIdx.x); idx < nb * 8;
+         idx += int(gridDim.z) * kPrepThreads) {
         const int b = idx >> 3, c = (idx >> 1) & 3, h = idx & 1;
         const XT *xe = xj + b * 64 + c * 16 + h;
         float v[8];
@@ -1298,7 +305,7 @@ __global__ void __launch_bounds__(kT5PrepThreads) t4_prep_kernel(
                 acc2 += __float2int_rn(2.0f * pv.x) + __float2int_rn(2.0f * pv.y);
                 word |= uint32_t(pc) << (8 * q2);
             }
-            *reinterpret_cast<uint32_t *>(bimg + t5_img_offset(p, kbyte)) = word;
+            *reinterpret_cast<uint32_t *>(bimg + img_offset(kT4N, p, kbyte)) = word;
             // sum of piece / 2 = acc2 / 4, weighted by 4^-p, into its group
             const int gi = p < 6 ? 0 : p < 12 ? 1 : 2;
             grp_sum[gi] = fmaf(float(acc2) * 0.25f, down, grp_sum[gi]);
@@ -1313,36 +320,8 @@ __global__ void __launch_bounds__(kT5PrepThreads) t4_prep_kernel(
     }
 }
 
-// Where the epilogue writes the tile a ring stage belongs to; the producer fills
-// one per slot before the slot's barrier arrive.
-struct T4StageMeta {
-    float *y;              // nullptr: the tile is not written (an expert id out of range)
-    int row0;              // first row of the tile
-    int n_rows;            // rows of the matrix
-    int flags;             // kT4FirstOfTile | kT4LastOfTile
-    int pad;
-};
-constexpr int kT4FirstOfTile = 1;
-constexpr int kT4LastOfTile = 2;
-
-// Warp roles of the fp4 kernel. A warp reaches only the TMEM lanes of its
-// quarter (warp % 4, which is also its SM sub-partition):
-//   warp 2       producer;
-//   warps 3, 1   MMA issuers of the even / odd stages (warp 3 allocates TMEM);
-//   warps 4-7    expansion, one per lane quarter, all 8 blocks of a stage;
-//   warps 8-11   epilogue, one per lane quarter, all 8 blocks of a stage.
-// Measured: more warps per sub-partition (two expansion or two epilogue warps
-// per quarter) lengthened the stage period; 12 warps gave the shortest.
-constexpr int kT4SplitCodeBytes = kT5Rows * 128;  // 16 KB of codes, then 2 KB of scales
-static_assert(kT4SplitCodeBytes + kT5Rows * 16 == kT5RawBytes, "split stage = block stage bytes");
-constexpr int kT4ProdWarp = 2;
-constexpr int kT4MmaWarp = 3;
-constexpr int kT4MmaWarp2 = 1;
-constexpr int kT4ExpWarp0 = 4;
-constexpr int kT4ExpWarps = 4;
-constexpr int kT4EpiWarp0 = 8;
-constexpr int kT4EpiWarps = 4;
-constexpr int kT4Threads = 12 * 32;
+constexpr int kT4SplitCodeBytes = kTcRows * 128;  // 16 KB of codes, then 2 KB of scales
+static_assert(kT4SplitCodeBytes + kTcRows * 16 == kRawBytes, "split stage = block stage bytes");
 
 // kSplit: the weights are in the split layout (codes [N][K/64][16], scales
 // [N][K/64]); the stage's code box is 128 bytes x 128 rows with 128-byte swizzle
@@ -1360,43 +339,43 @@ __global__ void __maxnreg__(128)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    uint8_t *img_ring = smem;                                      // kT5Stages x 4 KB
-    uint8_t *raw_ring = img_ring + kT5Stages * kT4ImgBytes;         // kT5Stages x 18 KB
-    uint8_t *beta_ring = raw_ring + kT5Stages * kT5RawBytes;        // kT5Stages x 32 B
-    uint64_t *full = reinterpret_cast<uint64_t *>(beta_ring + kT5Stages * kT4BetaBytes);
-    uint64_t *empty = full + kT5Stages;
-    uint64_t *a_full = empty + kT5Stages;
-    uint64_t *a_empty = a_full + kT5MaxABufs;
-    uint64_t *d_full = a_empty + kT5MaxABufs;
+    uint8_t *img_ring = smem;                                      // kT4Stages x 4 KB
+    uint8_t *raw_ring = img_ring + kT4Stages * kT4ImgBytes;         // kT4Stages x 18 KB
+    uint8_t *beta_ring = raw_ring + kT4Stages * kRawBytes;        // kT4Stages x 32 B
+    uint64_t *full = reinterpret_cast<uint64_t *>(beta_ring + kT4Stages * kT4BetaBytes);
+    uint64_t *empty = full + kT4Stages;
+    uint64_t *a_full = empty + kT4Stages;
+    uint64_t *a_empty = a_full + kT4ABufs;
+    uint64_t *d_full = a_empty + kT4ABufs;
     uint64_t *d_empty = d_full + 2;
     uint64_t *drain = d_empty + 2;  // [2] one per MMA issuer: its final commit
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     // per ring slot, written by the producer before the slot's barrier arrive:
     // where the epilogue writes the tile that the stage belongs to
-    __shared__ T4StageMeta s_meta[kT5Stages];
+    __shared__ StageMeta s_meta[kT4Stages];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kT5Stages; ++i) {
+        for (int i = 0; i < kT4Stages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kT4EpiWarps);
+            mbar_init(&empty[i], kEpiWarps);
         }
         for (int i = 0; i < kT4ABufs; ++i) {
-            mbar_init(&a_full[i], kT4ExpWarps);
+            mbar_init(&a_full[i], kExpWarps);
             mbar_init(&a_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&d_full[i], 1);
-            mbar_init(&d_empty[i], kT4EpiWarps);
+            mbar_init(&d_empty[i], kEpiWarps);
         }
         for (int i = 0; i < 2; ++i) mbar_init(&drain[i], 1);
         s_abort = 0;
         fence_barrier_init();
     }
-    if (warp == kT4MmaWarp) {
+    if (warp == kMmaWarp) {
         tmem_alloc(&s_tmem, 512);
         tmem_relinquish();
     }
@@ -1427,13 +406,13 @@ __global__ void __maxnreg__(128)
     };
     // stages of this CTA (every role but the producer runs a flat stage loop)
     const int n_stages = p.jobs ? p.cta_stages[blockIdx.x] : n_items * single.n_chunks;
-    auto stage_parity = [](int s) { return uint32_t(s / kT5Stages) & 1u; };
+    auto stage_parity = [](int s) { return uint32_t(s / kT4Stages) & 1u; };
     auto a_buf = [](int s) { return s % kT4ABufs; };
     auto a_use = [](int s) { return uint32_t(s / kT4ABufs) & 1u; };
     auto a_col = [](int s) { return uint32_t(kT4ACol + (s % kT4ABufs) * 64); };
     auto d_col = [](int s) { return uint32_t((s & 1) * 128); };
 
-    if (warp == kT4ProdWarp) {
+    if (warp == kProdWarp) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
             int s = 0, last = -1;
@@ -1462,31 +441,31 @@ __global__ void __maxnreg__(128)
                     const int xv = p.moe.n_x == 1 ? v / p.moe.n_used : v;
                     prep += size_t(xv) * p.moe.prep_stride;
                 }
-                const uint8_t *img = prep + kT5PrepHeader;
+                const uint8_t *img = prep + kPrepHeader;
                 const uint8_t *beta = img + size_t(J->n_chunks) * kT4ImgBytes;
                 const int nch = J->n_chunks;
                 for (int ch = 0; ch < nch; ++ch, ++s) {
-                    const int st = s % kT5Stages;
-                    if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagT5Empty, true) ||
+                    const int st = s % kT4Stages;
+                    if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagT4Empty, true) ||
                         *(volatile int *)&s_abort) {
                         ok = false;
                         s_abort = 1;
                         break;
                     }
-                    T4StageMeta &m = s_meta[st];
+                    StageMeta &m = s_meta[st];
                     m.y = y_out;
-                    m.row0 = tile * kT5Rows;
+                    m.row0 = tile * kTcRows;
                     m.n_rows = J->N;
-                    m.flags = (ch == 0 ? kT4FirstOfTile : 0) | (ch == nch - 1 ? kT4LastOfTile : 0);
-                    mbar_arrive_expect_tx(&full[st], kT5RawBytes + kT4ImgBytes + kT4BetaBytes);
+                    m.flags = ch == nch - 1 ? kLastOfTile : 0;
+                    mbar_arrive_expect_tx(&full[st], kRawBytes + kT4ImgBytes + kT4BetaBytes);
                     if (kSplit) {
-                        tma_load_2d(raw_ring + st * kT5RawBytes, &J->tmap, ch * 128,
-                                    row_base + tile * kT5Rows, &full[st]);
-                        tma_load_2d(raw_ring + st * kT5RawBytes + kT4SplitCodeBytes, &J->tmap_d,
-                                    ch * 16, row_base + tile * kT5Rows, &full[st]);
+                        tma_load_2d(raw_ring + st * kRawBytes, &J->tmap, ch * 128,
+                                    row_base + tile * kTcRows, &full[st]);
+                        tma_load_2d(raw_ring + st * kRawBytes + kT4SplitCodeBytes, &J->tmap_d,
+                                    ch * 16, row_base + tile * kTcRows, &full[st]);
                     } else {
-                        tma_load_2d(raw_ring + st * kT5RawBytes, &J->tmap, ch * kChunkBytes,
-                                    row_base + tile * kT5Rows, &full[st]);
+                        tma_load_2d(raw_ring + st * kRawBytes, &J->tmap, ch * kChunkBytes,
+                                    row_base + tile * kTcRows, &full[st]);
                     }
                     if (!prep_ready) {
                         grid_dependency_wait();  // the B images come from the prep kernel
@@ -1501,28 +480,28 @@ __global__ void __maxnreg__(128)
             }
             if (!ok) {
                 // let the copies in flight land (bounded) before the CTA exits
-                for (int t = last; t >= 0 && t > last - kT5Stages; --t)
-                    mbar_wait(&full[t % kT5Stages], stage_parity(t), p.err, kTagT5Full);
+                for (int t = last; t >= 0 && t > last - kT4Stages; --t)
+                    mbar_wait(&full[t % kT4Stages], stage_parity(t), p.err, kTagT4Full);
             }
         }
-    } else if (warp == kT4MmaWarp || warp == kT4MmaWarp2) {
+    } else if (warp == kMmaWarp || warp == kMmaWarp2) {
         // ------------------------------ MMA issuers ------------------------------
         // even / odd stages; the whole warp runs the loop and waits (so it stays
         // converged), the elected lane issues (one K = 64 MMA per block) and commits
-        constexpr uint32_t idesc = idesc_mxf4(kT5Rows, kT5N);
+        constexpr uint32_t idesc = idesc_mxf4(kTcRows, kT4N);
         const bool leader = elect_one();
-        const int mine = warp == kT4MmaWarp ? 0 : 1;
+        const int mine = warp == kMmaWarp ? 0 : 1;
         const uint64_t desc0 = sw128_desc(smem_addr(img_ring));
         const uint32_t sfa = tmem + kT4ScaleCol, sfb = tmem + kT4ScaleCol + 4;
         int last = -1;
         {
             for (int s = mine; s < n_stages; s += 2) {
-                const int st = s % kT5Stages;
+                const int st = s % kT4Stages;
                 const bool got =
-                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
-                    mbar_wait(&a_full[a_buf(s)], a_use(s), p.err, kTagT5AFull) &&
+                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full) &&
+                    mbar_wait(&a_full[a_buf(s)], a_use(s), p.err, kTagT4AFull) &&
                     mbar_wait(&d_empty[s & 1], (uint32_t(s >> 1) & 1u) ^ 1u, p.err,
-                              kTagT5DEmpty) &&
+                              kTagT4DEmpty) &&
                     !*(volatile int *)&s_abort;
                 if (!__all_sync(0xffffffffu, got)) {
                     s_abort = 1;
@@ -1535,7 +514,7 @@ __global__ void __maxnreg__(128)
                 if (leader) {
 #pragma unroll
                     for (int b = 0; b < kChunkBlocks; ++b)
-                        tc_mma_mxf4_ta(d_base + b * kT5N, a_base + b * 8,
+                        tc_mma_mxf4_ta(d_base + b * kT4N, a_base + b * 8,
                                        dst + uint64_t(((b >> 2) * 2048 + (b & 3) * 32) >> 4), idesc,
                                        sfa, sfb, 0u);
                     tc_commit(&a_empty[a_buf(s)]);
@@ -1550,10 +529,10 @@ __global__ void __maxnreg__(128)
         if (last >= 0) {
             if (leader) tc_commit(&drain[mine]);
             __syncwarp();
-            if (leader) mbar_wait(&drain[mine], 0u, p.err, kTagT5DFull);
+            if (leader) mbar_wait(&drain[mine], 0u, p.err, kTagT4DFull);
             __syncwarp();
         }
-    } else if (warp >= kT4ExpWarp0 && warp < kT4ExpWarp0 + kT4ExpWarps) {
+    } else if (warp >= kExpWarp0 && warp < kExpWarp0 + kExpWarps) {
         // ------------------------------ expansion ------------------------------
         // warp w: TMEM lane quarter w % 4 (rows 32 (w % 4) ..), all 8 blocks
         const int qd = warp & 3;
@@ -1566,10 +545,10 @@ __global__ void __maxnreg__(128)
         }
         {
             for (int s = 0; s < n_stages; ++s) {
-                const int st = s % kT5Stages;
+                const int st = s % kT4Stages;
                 const bool got =
-                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
-                    mbar_wait(&a_empty[a_buf(s)], a_use(s) ^ 1u, p.err, kTagT5AFull) &&
+                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full) &&
+                    mbar_wait(&a_empty[a_buf(s)], a_use(s) ^ 1u, p.err, kTagT4AFull) &&
                     !*(volatile int *)&s_abort;
                 if (!__all_sync(0xffffffffu, got)) {
                     s_abort = 1;
@@ -1582,7 +561,7 @@ __global__ void __maxnreg__(128)
                     if (kSplit) {
                         // block 4G+bi is 16-byte chunk 4G+bi of the row, stored at
                         // chunk (4G+bi) ^ (row % 8) by the 128-byte swizzle
-                        const uint8_t *rp = raw_ring + st * kT5RawBytes + row * 128;
+                        const uint8_t *rp = raw_ring + st * kRawBytes + row * 128;
 #pragma unroll
                         for (int bi = 0; bi < 4; ++bi) {
                             const uint4 v = *reinterpret_cast<const uint4 *>(
@@ -1596,7 +575,7 @@ __global__ void __maxnreg__(128)
                         }
                     } else {
                         const uint8_t *rp =
-                            raw_ring + st * kT5RawBytes + row * kChunkBytes + G * 72;
+                            raw_ring + st * kRawBytes + row * kChunkBytes + G * 72;
                         uint32_t u[18];
 #pragma unroll
                         for (int k = 0; k < 9; ++k) {
@@ -1626,7 +605,7 @@ __global__ void __maxnreg__(128)
                 if (lane == 0) mbar_arrive(&a_full[a_buf(s)]);
             }
         }
-    } else if (warp >= kT4EpiWarp0 && warp < kT4EpiWarp0 + kT4EpiWarps) {
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
         // ------------------------------ epilogue ------------------------------
         // warp w: TMEM lane quarter w % 4, all 8 blocks of each stage; it writes y
         // at the tile's last stage. Every wait is bounded; a warp whose wait
@@ -1636,18 +615,18 @@ __global__ void __maxnreg__(128)
         const uint32_t lane_base = uint32_t(32 * qd) << 16;
         float acc = 0.0f, comp = 0.0f;  // compensated sum of the stage sums
         for (int s = 0; s < n_stages; ++s) {
-            const int st = s % kT5Stages;
+            const int st = s % kT4Stages;
             const bool got = !*(volatile int *)&s_abort &&
-                             mbar_wait(&full[st], stage_parity(s), p.err, kTagT5Full) &&
-                             mbar_wait(&d_full[s & 1], uint32_t(s >> 1) & 1u, p.err, kTagT5DFull);
+                             mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full) &&
+                             mbar_wait(&d_full[s & 1], uint32_t(s >> 1) & 1u, p.err, kTagT4DFull);
             if (!__all_sync(0xffffffffu, got)) {
                 s_abort = 1;
                 break;
             }
             tc_fence_after();
-            const T4StageMeta m = s_meta[st];
+            const StageMeta m = s_meta[st];
             const uint32_t d_base = tmem + lane_base + d_col(s);
-            const uint8_t *rp = raw_ring + st * kT5RawBytes + row * kChunkBytes;
+            const uint8_t *rp = raw_ring + st * kRawBytes + row * kChunkBytes;
             const float4 *brec = reinterpret_cast<const float4 *>(beta_ring + st * kT4BetaBytes);
             float stage_sum = 0.0f;
             // blocks 4 hb .. 4 hb + 3: their 16 pieces each (64 registers)
@@ -1655,7 +634,7 @@ __global__ void __maxnreg__(128)
             for (int hb = 0; hb < 2; ++hb) {
                 uint32_t r[4][16];
 #pragma unroll
-                for (int bi = 0; bi < 4; ++bi) tmem_ld16(d_base + (4 * hb + bi) * kT5N, r[bi]);
+                for (int bi = 0; bi < 4; ++bi) tmem_ld16(d_base + (4 * hb + bi) * kT4N, r[bi]);
                 tmem_wait_ld();
                 if (hb == 1) {  // the stage's accumulators are all in registers
                     tc_fence_before();
@@ -1677,7 +656,7 @@ __global__ void __maxnreg__(128)
                     const float4 br = brec[b];  // {2^(e - 1), H, M, L}
                     const float t = ((gh - br.y) + (gm - br.z)) + (gl - br.w);
                     const float d =
-                        kSplit ? lds_half_as_float(raw_ring + st * kT5RawBytes + kT4SplitCodeBytes +
+                        kSplit ? lds_half_as_float(raw_ring + st * kRawBytes + kT4SplitCodeBytes +
                                                    row * 16 + 2 * b)
                                : lds_half_as_float(rp + 18 * b);
                     stage_sum = fmaf(d, t * br.x, stage_sum);
@@ -1692,7 +671,7 @@ __global__ void __maxnreg__(128)
                 comp += (acc - (sum - bb)) + (stage_sum - bb);
                 acc = sum;
             }
-            if (m.flags & kT4LastOfTile) {
+            if (m.flags & kLastOfTile) {
                 const int rr = m.row0 + row;
                 if (m.y && rr < m.n_rows) m.y[rr] = acc + comp;
                 acc = 0.0f;
@@ -1703,7 +682,468 @@ __global__ void __maxnreg__(128)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kT4MmaWarp) {
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+
+// ---------------------------------------------------------------------------
+// tcgen05 mat-vec on signed e4m3 codes (ncols 2..8)
+//
+// Codes. The expansion warps turn each 2-bit code into the e4m3 value q - 1
+// (-1, 0, 1, 2 are exact e4m3 values) with one byte-permute lookup per 4 codes:
+// selecting byte q of the constant 0x403800B8 gives 0xB8 (-1), 0x00, 0x38 (+1)
+// or 0x40 (+2). From a code word w, the selectors w, w >> 2, w >> 16 and
+// w >> 18 (masked to their low two bits per nibble) give elements {0,2,4,6},
+// {1,3,5,7}, {8,10,12,14} and {9,11,13,15}; tensor-memory column 4c + r of a
+// block holds register r of word c, i.e. K byte 16c + 4r + j of the block is
+// element 16c + 8 (r >> 1) + (r & 1) + 2j. A weight of code 1 is an exact zero
+// operand: it contributes nothing however large its activation is.
+//
+// Activations, block by block and column by column. For block b of column j
+// with M = max |x| over the block, M = f * 2^e (f in [0.5, 1)), the prep kernel
+// forms v = x * 2^(8 - e) (max |v| in [128, 256)) and splits it into 5 e4m3
+// pieces: piece p = e4m3(r_p * 16^p), r_0 = v, r_(p+1) = r_p - piece_p * 16^-p.
+// e4m3 keeps 4 significant bits of each element's own magnitude, every
+// subtraction is exact, and |r_5| <= 2^-20 |v| + 2^-26 (the last term from
+// e4m3's subnormal step, i.e. 2^-33 of the block maximum). Piece p of column j
+// is B row n = 5j + p; the MMA's N is 5 * ncols rounded up to 16.
+//
+// Per-block accumulators. d and the activation scale change every block, so
+// each block has its own accumulator columns (N per block). The 512 tensor-
+// memory columns hold two A buffers of 128 (a stage's 8 blocks x 64 e4m3 codes)
+// and two accumulator buffers of 128; a stage's 8 blocks are issued in
+// sub-stages of 128 / N blocks (8, 4 or 2), each committed to its own
+// accumulator buffer, so the epilogue drains one sub-stage while the tensor
+// core fills the other. The epilogue forms t_j = sum_p 16^-p C_(5j+p) per
+// block and column and adds d * 2^(e - 8) * t_j; the stage sums are accumulated
+// with a two-sum.
+// ---------------------------------------------------------------------------
+constexpr int kS8Pieces = 5;
+constexpr int kS8RecBytes = 256;  // per stage: float scale[8 blocks][ncols]
+__host__ __device__ constexpr int s8_n(int nc) { return (kS8Pieces * nc + 15) / 16 * 16; }
+__host__ __device__ constexpr int s8_bs(int nc) { return 128 / s8_n(nc); }
+__host__ __device__ constexpr int s8_subs(int nc) { return kChunkBlocks / s8_bs(nc); }
+__host__ __device__ constexpr int s8_img_bytes(int nc) { return s8_n(nc) * kChunkBlocks * 64; }
+constexpr int kS8Barriers = 2 * 8 + 2 * 2 + 2 * 2 + 2;
+__host__ __device__ constexpr int s8_stages(int nc) {
+    return (kSmemOptIn - 2048 - kS8Barriers * 8) / (kRawBytes + s8_img_bytes(nc) + kS8RecBytes) < 8
+               ? (kSmemOptIn - 2048 - kS8Barriers * 8) / (kRawBytes + s8_img_bytes(nc) + kS8RecBytes)
+               : 8;
+}
+__host__ __device__ constexpr int s8_smem(int nc) {
+    return 1024 /* alignment slack */ +
+           s8_stages(nc) * (s8_img_bytes(nc) + kRawBytes + kS8RecBytes) + kS8Barriers * 8;
+}
+static_assert(s8_bs(2) == 8 && s8_bs(4) == 4 && s8_bs(8) == 2, "sub-stage sizes");
+static_assert(s8_stages(8) >= 4 && s8_smem(8) <= kSmemOptIn - 1024, "shared memory");
+constexpr int kS8ACol = 0;    // A buffers at 0 and 128
+constexpr int kS8DCol = 256;  // accumulator buffers at 256 and 384
+constexpr uint32_t kS8Lut = 0x403800B8u;  // e4m3 of q - 1 in byte q
+constexpr int kTagS8Full = 121;
+constexpr int kTagS8Empty = 122;
+constexpr int kTagS8AFull = 123;
+constexpr int kTagS8DFull = 124;
+constexpr int kTagS8DEmpty = 125;
+
+size_t s8_prep_bytes(int64_t K, int ncols) {
+    const size_t n_chunks = size_t(K / 512);
+    size_t b = kPrepHeader + n_chunks * (s8_img_bytes(ncols) + kS8RecBytes);
+    return (b + 255) & ~size_t(255);
+}
+
+// kind::f8f6f4 instruction descriptor: D f32, A and B e4m3, both K-major, N, M.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n) {
+    return (1u << 4) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+
+// Preparation: grid (ncols, n_jobs, z), kPrepThreads threads. Item (block b,
+// word c, register r) of column j = blockIdx.x: the 4 elements
+// 16c + 8 (r >> 1) + (r & 1) + 2i (i = 0..3) of block b, which sit at K bytes
+// 64 (b % 8) + 16c + 4r + i of the stage; one 32-bit word of the image per
+// piece. The 16 items of a block are 16 consecutive lanes; they share the
+// block maximum by shuffles.
+template <typename XT>
+__global__ void __launch_bounds__(kPrepThreads) s8_prep_kernel(
+    const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs, int ncols) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Launched as a programmatic dependent of the kernel before it on the stream
+    // (a mat-vec that may still read this buffer, or the producer of x): wait
+    // for that grid before reading x or writing the prep buffer.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const MvPrepJob &J = jobs ? jobs[blockIdx.y] : single;
+    const int K = J.K;
+    const int j = blockIdx.x;
+    const XT *xj = static_cast<const XT *>(J.x) + size_t(j) * K;
+    const int nb = K / 64;
+    const int rows = s8_n(ncols);
+    const size_t stage_bytes = size_t(s8_img_bytes(ncols)) + kS8RecBytes;
+    const int lane = threadIdx.x & 31;
+    const unsigned grp = 0xFFFFu << (lane & 16);  // the block's 16 threads
+    // 16 items per block: whole half-warps share a block, so the shuffles below
+    // always run with all 16 lanes of a block present
+    for (int idx = int(blockIdx.z) * kPrepThreads + int(threadIdx.x); idx < nb * 16;
+         idx += int(gridDim.z) * kPrepThreads) {
+        const int b = idx >> 4, c = (idx >> 2) & 3, r = idx & 3;
+        const XT *xe = xj + b * 64 + 16 * c + 8 * (r >> 1) + (r & 1);
+        float v[4];
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[i] = ld_x(xe + 2 * i);
+            m = fmaxf(m, fabsf(v[i]));
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(grp, m, o));
+        // v = x * 2^(8 - e), max |v| over the block in [128, 256); all-zero (or
+        // non-finite) blocks keep e = 0
+        int e = 0;
+        if (m > 0.0f && m <= 3.402823466e38f) frexpf(m, &e);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = mul_pow2(v[i], 8 - e);
+        uint8_t *st_base = J.prep + kPrepHeader + size_t(b >> 3) * stage_bytes;
+        const int kc = 64 * (b & 7) + 16 * c + 4 * r;
+#pragma unroll
+        for (int p = 0; p < kS8Pieces; ++p) {
+            const float up = __int_as_float((127 + 4 * p) << 23);
+            const float down = __int_as_float((127 - 4 * p) << 23);
+            const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                make_float2(v[0] * up, v[1] * up), __NV_SATFINITE, __NV_E4M3);
+            const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                make_float2(v[2] * up, v[3] * up), __NV_SATFINITE, __NV_E4M3);
+            const float2 plo = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3)));
+            const float2 phi = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
+            v[0] -= plo.x * down;
+            v[1] -= plo.y * down;
+            v[2] -= phi.x * down;
+            v[3] -= phi.y * down;
+            *reinterpret_cast<uint32_t *>(st_base + img_offset(rows, kS8Pieces * j + p, kc)) =
+                uint32_t(lo) | (uint32_t(hi) << 16);
+        }
+        // column 0 clears the rows past the last column's pieces
+        if (j == 0)
+            for (int n = kS8Pieces * ncols; n < rows; ++n)
+                *reinterpret_cast<uint32_t *>(st_base + img_offset(rows, n, kc)) = 0u;
+        if ((idx & 15) == 0)
+            reinterpret_cast<float *>(st_base + s8_img_bytes(ncols))[(b & 7) * ncols + j] =
+                pow2f(e - 8);
+    }
+}
+
+// NC: activation columns (2..8).
+template <int NC>
+__global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob single,
+                                              const MvParams p) {
+    // The next prep launch on the stream may become resident now; it waits for
+    // this grid before it touches any buffer this kernel reads.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    constexpr int kN = s8_n(NC), kBS = s8_bs(NC), kSub = s8_subs(NC);
+    constexpr int kImg = s8_img_bytes(NC), kStages = s8_stages(NC);
+    constexpr int kRecCopy = kChunkBlocks * NC * 4;  // bytes of the stage's block scales
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *img_ring = smem;                                 // kStages x kImg (1024-aligned)
+    uint8_t *raw_ring = img_ring + kStages * kImg;            // kStages x 18 KB
+    uint8_t *rec_ring = raw_ring + kStages * kRawBytes;       // kStages x 256 B
+    uint64_t *full = reinterpret_cast<uint64_t *>(rec_ring + kStages * kS8RecBytes);
+    uint64_t *empty = full + 8;
+    uint64_t *a_full = empty + 8;
+    uint64_t *a_empty = a_full + 2;
+    uint64_t *d_full = a_empty + 2;
+    uint64_t *d_empty = d_full + 2;
+    uint64_t *drain = d_empty + 2;  // [2] one per MMA issuer: its final commit
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    __shared__ StageMeta s_meta[kStages];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kEpiWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&a_full[i], kExpWarps);
+            mbar_init(&a_empty[i], kSub >= 2 ? 2 : 1);  // one commit per issuer on the stage
+            mbar_init(&d_full[i], 1);
+            mbar_init(&d_empty[i], kEpiWarps);
+            mbar_init(&drain[i], 1);
+        }
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&s_tmem, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    int n_items, item_base = 0;
+    if (p.jobs) {
+        item_base = p.cta_begin[blockIdx.x];
+        n_items = p.cta_begin[blockIdx.x + 1] - item_base;
+    } else {
+        n_items = blockIdx.x < unsigned(single.n_tiles)
+                      ? (single.n_tiles - 1 - int(blockIdx.x)) / int(gridDim.x) + 1
+                      : 0;
+    }
+    auto item_at = [&](int i, const MvJob *&J, int &tile) {
+        if (p.jobs) {
+            const MvItem it = p.items[item_base + i];
+            J = &p.jobs[it.job];
+            tile = it.tile;
+        } else {
+            J = &single;
+            tile = int(blockIdx.x) + i * int(gridDim.x);
+        }
+    };
+    const int n_stages = p.jobs ? p.cta_stages[blockIdx.x] : n_items * single.n_chunks;
+    auto stage_parity = [](int s) { return uint32_t(s / kStages) & 1u; };
+
+    if (warp == kProdWarp) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            int s = 0, last = -1;
+            bool ok = true, prep_ready = false;
+            for (int i = 0; i < n_items && ok; ++i) {
+                const MvJob *J;
+                int tile;
+                item_at(i, J, tile);
+                const uint8_t *prep = J->prep + kPrepHeader;
+                const int nch = J->n_chunks;
+                for (int ch = 0; ch < nch; ++ch, ++s) {
+                    const int st = s % kStages;
+                    if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagS8Empty, true) ||
+                        *(volatile int *)&s_abort) {
+                        ok = false;
+                        s_abort = 1;
+                        break;
+                    }
+                    StageMeta &m = s_meta[st];
+                    m.y = J->y;
+                    m.row0 = tile * kTcRows;
+                    m.n_rows = J->N;
+                    m.flags = ch == nch - 1 ? kLastOfTile : 0;
+                    mbar_arrive_expect_tx(&full[st], kRawBytes + kImg + kRecCopy);
+                    tma_load_2d(raw_ring + st * kRawBytes, &J->tmap, ch * kChunkBytes,
+                                tile * kTcRows, &full[st]);
+                    if (!prep_ready) {
+                        grid_dependency_wait();  // the images come from the prep kernel
+                        prep_ready = true;
+                    }
+                    const uint8_t *src = prep + size_t(ch) * (kImg + kS8RecBytes);
+                    bulk_g2s(img_ring + st * kImg, src, kImg, &full[st]);
+                    bulk_g2s(rec_ring + st * kS8RecBytes, src + kImg, kRecCopy, &full[st]);
+                    last = s;
+                }
+            }
+            if (!ok) {
+                // let the copies in flight land (bounded) before the CTA exits
+                for (int t = last; t >= 0 && t > last - kStages; --t)
+                    mbar_wait(&full[t % kStages], stage_parity(t), p.err, kTagS8Full);
+            }
+        }
+    } else if (warp == kMmaWarp || warp == kMmaWarp2) {
+        // ------------------------------ MMA issuers ------------------------------
+        // Issuer i takes the sub-stages g = i, i + 2, ... (g = s * kSub + ss) and
+        // always fills accumulator buffer i, so each of its barrier waits is at
+        // most one phase ahead of the barrier. The whole warp runs the loop and
+        // waits (so it stays converged); the elected lane issues (two K = 32
+        // MMAs per block) and commits the sub-stage to its buffer, and, after
+        // its last sub-stage of a stage, the stage's A buffer (with kSub >= 2
+        // both issuers work on every stage, and a_empty counts both commits).
+        constexpr uint32_t idesc = idesc_e4m3(kTcRows, kN);
+        const bool leader = elect_one();
+        const int mine = warp == kMmaWarp ? 0 : 1;
+        const uint64_t desc0 = sw128_desc(smem_addr(img_ring));
+        const uint32_t d_base = tmem + kS8DCol + mine * 128;
+        bool issued = false;
+        for (int g = mine; g < n_stages * kSub; g += 2) {
+            const int s = g / kSub, ss = g - s * kSub;
+            const int st = s % kStages;
+            const bool first = ss < 2, last_of_stage = ss + 2 >= kSub;
+            const bool got =
+                (!first ||
+                 (mbar_wait(&full[st], stage_parity(s), p.err, kTagS8Full) &&
+                  mbar_wait(&a_full[s & 1], uint32_t(s >> 1) & 1u, p.err, kTagS8AFull))) &&
+                mbar_wait(&d_empty[mine], (uint32_t(g >> 1) & 1u) ^ 1u, p.err, kTagS8DEmpty) &&
+                !*(volatile int *)&s_abort;
+            if (!__all_sync(0xffffffffu, got)) {
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a_base = tmem + kS8ACol + (s & 1) * 128;
+            const uint64_t dst = desc0 + uint64_t((st * kImg) >> 4);
+            if (leader) {
+#pragma unroll
+                for (int bi = 0; bi < kBS; ++bi) {
+                    const int b = ss * kBS + bi;
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk)
+                        tc_mma_f8f6f4_ta(d_base + bi * kN, a_base + b * 16 + kk * 8,
+                                         dst + uint64_t(((b >> 1) * (kN * 128) + (b & 1) * 64 +
+                                                         kk * 32) >> 4),
+                                         idesc, uint32_t(kk));
+                }
+                tc_commit(&d_full[mine]);
+                if (last_of_stage) tc_commit(&a_empty[s & 1]);
+            }
+            __syncwarp();
+            issued = true;
+        }
+        // TMEM is freed only after this issuer's MMAs completed: one more commit
+        // tracks all of them
+        if (issued) {
+            if (leader) tc_commit(&drain[mine]);
+            __syncwarp();
+            if (leader) mbar_wait(&drain[mine], 0u, p.err, kTagS8DFull);
+            __syncwarp();
+        }
+    } else if (warp >= kExpWarp0 && warp < kExpWarp0 + kExpWarps) {
+        // ------------------------------ expansion ------------------------------
+        // warp w: TMEM lane quarter w % 4 (rows 32 (w % 4) ..), all 8 blocks
+        const int qd = warp & 3;
+        const int row = 32 * qd + lane;
+        const uint32_t lane_base = uint32_t(32 * qd) << 16;
+        for (int s = 0; s < n_stages; ++s) {
+            const int st = s % kStages;
+            const bool got =
+                mbar_wait(&full[st], stage_parity(s), p.err, kTagS8Full) &&
+                mbar_wait(&a_empty[s & 1], (uint32_t(s >> 1) & 1u) ^ 1u, p.err, kTagS8AFull) &&
+                !*(volatile int *)&s_abort;
+            if (!__all_sync(0xffffffffu, got)) {
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int G = 0; G < 2; ++G) {
+                const uint8_t *rp = raw_ring + st * kRawBytes + row * kChunkBytes + G * 72;
+                uint32_t u[18];
+#pragma unroll
+                for (int k = 0; k < 9; ++k) {
+                    const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * k);
+                    u[2 * k] = v.x;
+                    u[2 * k + 1] = v.y;
+                }
+#pragma unroll
+                for (int bi = 0; bi < 4; ++bi) {
+                    uint32_t a[16];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t w = block_word(u, bi, c);
+                        a[4 * c + 0] = __byte_perm(kS8Lut, 0u, w & 0x3333u);
+                        a[4 * c + 1] = __byte_perm(kS8Lut, 0u, (w >> 2) & 0x3333u);
+                        a[4 * c + 2] = __byte_perm(kS8Lut, 0u, (w >> 16) & 0x3333u);
+                        a[4 * c + 3] = __byte_perm(kS8Lut, 0u, (w >> 18) & 0x3333u);
+                    }
+                    tmem_st16(tmem + lane_base + kS8ACol + (s & 1) * 128 + (4 * G + bi) * 16, a);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[s & 1]);
+        }
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
+        // ------------------------------ epilogue ------------------------------
+        // warp w: TMEM lane quarter w % 4, all 8 blocks of each stage; it writes
+        // y at the tile's last stage. Every wait is bounded; a warp whose wait
+        // fails leaves the loop.
+        const int qd = warp & 3;
+        const int row = 32 * qd + lane;
+        const uint32_t lane_base = uint32_t(32 * qd) << 16;
+        float acc[NC], comp[NC];
+#pragma unroll
+        for (int j = 0; j < NC; ++j) acc[j] = comp[j] = 0.0f;
+        bool ok = true;
+        for (int s = 0; s < n_stages && ok; ++s) {
+            const int st = s % kStages;
+            const bool got = !*(volatile int *)&s_abort &&
+                             mbar_wait(&full[st], stage_parity(s), p.err, kTagS8Full);
+            if (!__all_sync(0xffffffffu, got)) {
+                s_abort = 1;
+                break;
+            }
+            const StageMeta m = s_meta[st];
+            const uint8_t *rp = raw_ring + st * kRawBytes + row * kChunkBytes;
+            const float *sc = reinterpret_cast<const float *>(rec_ring + st * kS8RecBytes);
+            float ssum[NC];
+#pragma unroll
+            for (int j = 0; j < NC; ++j) ssum[j] = 0.0f;
+#pragma unroll 1
+            for (int ss = 0; ss < kSub; ++ss) {
+                const int g = s * kSub + ss;
+                const bool have = mbar_wait(&d_full[g & 1], uint32_t(g >> 1) & 1u, p.err,
+                                            kTagS8DFull) &&
+                                  !*(volatile int *)&s_abort;
+                if (!__all_sync(0xffffffffu, have)) {
+                    s_abort = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_base = tmem + lane_base + kS8DCol + (g & 1) * 128;
+#pragma unroll 1
+                for (int bi = 0; bi < kBS; ++bi) {
+                    const int b = ss * kBS + bi;
+                    uint32_t r[kN];
+#pragma unroll
+                    for (int q16 = 0; q16 < kN / 16; ++q16)
+                        tmem_ld16(d_base + bi * kN + 16 * q16,
+                                  *reinterpret_cast<uint32_t(*)[16]>(&r[16 * q16]));
+                    tmem_wait_ld();
+                    if (bi == kBS - 1) {  // the sub-stage's accumulators are all read
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&d_empty[g & 1]);
+                    }
+                    const float d = lds_half_as_float(rp + 18 * b);
+#pragma unroll
+                    for (int j = 0; j < NC; ++j) {
+                        const uint32_t *c = &r[kS8Pieces * j];
+                        float t = __uint_as_float(c[4]) * 0x1p-16f;
+                        t = fmaf(__uint_as_float(c[3]), 0x1p-12f, t);
+                        t = fmaf(__uint_as_float(c[2]), 0x1p-8f, t);
+                        t = fmaf(__uint_as_float(c[1]), 0x1p-4f, t);
+                        t = t + __uint_as_float(c[0]);
+                        ssum[j] = fmaf(d * sc[b * NC + j], t, ssum[j]);
+                    }
+                }
+            }
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+#pragma unroll
+            for (int j = 0; j < NC; ++j) {  // acc + comp += ssum (two-sum)
+                const float sum = acc[j] + ssum[j];
+                const float bb = sum - acc[j];
+                comp[j] += (acc[j] - (sum - bb)) + (ssum[j] - bb);
+                acc[j] = sum;
+            }
+            if (m.flags & kLastOfTile) {
+                const int rr = m.row0 + row;
+                if (rr < m.n_rows)
+#pragma unroll
+                    for (int j = 0; j < NC; ++j) m.y[size_t(j) * m.n_rows + rr] = acc[j] + comp[j];
+#pragma unroll
+                for (int j = 0; j < NC; ++j) acc[j] = comp[j] = 0.0f;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -1794,17 +1234,10 @@ __global__ void __launch_bounds__(256) moe_generic_kernel(
     if (lane == 0) y[size_t(v) * N + row] = acc;
 }
 
+
 std::mutex g_attr_mu;
-bool g_attr_done[64][2];
-bool g_t5_attr_done[64][kT5MaxCols];
-
-template <int NC>
-cudaError_t set_t5_attr() {
-    return cudaFuncSetAttribute(mv_t5_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kT5Smem);
-}
-
 bool g_t4_attr_done[64];
+bool g_s8_attr_done[64][9];
 
 cudaError_t ensure_t4_attr() {
     int dev = 0;
@@ -1821,87 +1254,67 @@ cudaError_t ensure_t4_attr() {
     return e;
 }
 
-cudaError_t ensure_t5_attrs(int ncols) {
+template <int NC>
+cudaError_t launch_s8_nc(cudaLaunchConfig_t &cfg, const MvJob &single, const MvParams &prm) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lk(g_attr_mu);
-    if (dev < 64 && g_t5_attr_done[dev][ncols - 1]) return cudaSuccess;
-    e = ncols == 1 ? set_t5_attr<1>() : ncols == 2 ? set_t5_attr<2>() : set_t5_attr<3>();
-    if (e == cudaSuccess && dev < 64) g_t5_attr_done[dev][ncols - 1] = true;
-    return e;
+    {
+        std::lock_guard<std::mutex> lk(g_attr_mu);
+        if (!(dev < 64 && g_s8_attr_done[dev][NC])) {
+            e = cudaFuncSetAttribute(mv_s8_kernel<NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     s8_smem(NC));
+            if (e != cudaSuccess) return e;
+            if (dev < 64) g_s8_attr_done[dev][NC] = true;
+        }
+    }
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = s8_smem(NC);
+    return cudaLaunchKernelEx(&cfg, mv_s8_kernel<NC>, single, prm);
 }
 
-cudaError_t ensure_attrs(int nt) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lk(g_attr_mu);
-    if (dev < 64 && g_attr_done[dev][nt - 1]) return cudaSuccess;
-    if (nt == 1)
-        e = cudaFuncSetAttribute(mv_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBudget + 2 * kMaxStages * 8);
-    else
-        e = cudaFuncSetAttribute(mv_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemBudget + 2 * kMaxStages * 8);
-    if (e == cudaSuccess && dev < 64) g_attr_done[dev][nt - 1] = true;
-    return e;
-}
-
-// ncols = 1 runs the fp4 tcgen05 kernel, ncols 2-3 the e4m3 one (both 128-row
-// tiles); more columns run the mma.sync kernel (256-row tiles).
+// ncols = 1 runs the fp4 kernel, ncols 2..8 the signed-e4m3 one.
 bool use_t4(int ncols) { return ncols == 1; }
-bool use_t5(int ncols) { return ncols <= kT5MaxCols; }
-int tile_rows_for(int ncols) { return use_t5(ncols) ? kT5Rows : kTileRows; }
 
-bool make_job(MvJob &J, const uint8_t *w, const uint8_t *prep, float *y, int64_t N, int64_t K,
-              int rows) {
+bool make_job(MvJob &J, const uint8_t *w, const uint8_t *prep, float *y, int64_t N, int64_t K) {
     std::memset(&J, 0, sizeof(J));
     const uint64_t row_bytes = uint64_t(K / 64) * 18;
     if (!encode_tmap_2d(&J.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row_bytes, uint64_t(N), row_bytes,
-                        kChunkBytes, rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+                        kChunkBytes, kTcRows, CU_TENSOR_MAP_SWIZZLE_NONE))
         return false;
     J.prep = prep;
     J.y = y;
     J.N = int(N);
     J.nb = int(K / 64);
     J.n_chunks = int(K / 512);
-    J.n_tiles = int((N + rows - 1) / rows);
+    J.n_tiles = int((N + kTcRows - 1) / kTcRows);
     return true;
 }
 
-// max_k: the largest K among the jobs (sets the t5 prep's grid z).
-template <typename XT>
 // The prep kernels are launched as programmatic dependents of whatever precedes
 // them on the stream: their launch overlaps that kernel's tail, and they wait
 // for it (griddepcontrol.wait) before reading x or writing their buffers.
+// max_k: the largest K among the jobs (sets the grid's z extent).
+template <typename XT>
 cudaError_t launch_prep_t(const MvPrepJob &single, const MvPrepJob *jobs, int n_jobs, int ncols,
                           int64_t max_k, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(ncols, n_jobs);
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    cfg.blockDim = dim3(kPrepThreads);
+    const int64_t items = max_k / 64 * (use_t4(ncols) ? 8 : 16);
+    const unsigned z =
+        unsigned(std::min<int64_t>((items + kPrepThreads - 1) / kPrepThreads, 65535));
     if (use_t4(ncols)) {
-        const int64_t items = max_k / 64 * 8;
-        cfg.gridDim.z =
-            unsigned(std::min<int64_t>((items + kT5PrepThreads - 1) / kT5PrepThreads, 65535));
-        cfg.blockDim = dim3(kT5PrepThreads);
+        cfg.gridDim = dim3(1, n_jobs, z);
         return cudaLaunchKernelEx(&cfg, t4_prep_kernel<XT>, single, jobs);
     }
-    if (use_t5(ncols)) {
-        const int64_t items = max_k / 64 * 16;
-        cfg.gridDim.z =
-            unsigned(std::min<int64_t>((items + kT5PrepThreads - 1) / kT5PrepThreads, 65535));
-        cfg.blockDim = dim3(kT5PrepThreads);
-        return cudaLaunchKernelEx(&cfg, t5_prep_kernel<XT>, single, jobs, ncols);
-    }
-    cfg.blockDim = dim3(kPrepThreads);
-    if (n_tiles_for(ncols) == 1) return cudaLaunchKernelEx(&cfg, mv_prep_kernel<1, XT>, single, jobs, ncols);
-    return cudaLaunchKernelEx(&cfg, mv_prep_kernel<2, XT>, single, jobs, ncols);
+    cfg.gridDim = dim3(ncols, n_jobs, z);
+    return cudaLaunchKernelEx(&cfg, s8_prep_kernel<XT>, single, jobs, ncols);
 }
 
 cudaError_t launch_prep(const MvPrepJob &single, const MvPrepJob *jobs, int n_jobs, int ncols,
@@ -1912,13 +1325,8 @@ cudaError_t launch_prep(const MvPrepJob &single, const MvPrepJob *jobs, int n_jo
 
 // The tensor-core kernel is launched as a programmatic dependent of the prep
 // kernel: its prologue and first weight loads overlap the prep's tail; its
-// producer waits for the prep grid before loading any activation fragment.
+// producer waits for the prep grid before loading any activation image.
 cudaError_t launch_tc(const MvJob &single, const MvParams &prm, int grid, cudaStream_t s) {
-    const int nt = n_tiles_for(prm.ncols);
-    cudaError_t e = use_t4(prm.ncols)   ? ensure_t4_attr()
-                    : use_t5(prm.ncols) ? ensure_t5_attrs(prm.ncols)
-                                        : ensure_attrs(nt);
-    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1927,28 +1335,24 @@ cudaError_t launch_tc(const MvJob &single, const MvParams &prm, int grid, cudaSt
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    cudaError_t e;
     if (use_t4(prm.ncols)) {
-        cfg.blockDim = dim3(kT4Threads);
+        e = ensure_t4_attr();
+        if (e != cudaSuccess) return e;
+        cfg.blockDim = dim3(kTcThreads);
         cfg.dynamicSmemBytes = kT4Smem;
         e = prm.split ? cudaLaunchKernelEx(&cfg, mv_t4_kernel<true>, single, prm)
                       : cudaLaunchKernelEx(&cfg, mv_t4_kernel<false>, single, prm);
-    } else if (use_t5(prm.ncols)) {
-        cfg.blockDim = dim3(kT5Threads);
-        cfg.dynamicSmemBytes = kT5Smem;
-        if (prm.ncols == 1)
-            e = cudaLaunchKernelEx(&cfg, mv_t5_kernel<1>, single, prm);
-        else if (prm.ncols == 2)
-            e = cudaLaunchKernelEx(&cfg, mv_t5_kernel<2>, single, prm);
-        else
-            e = cudaLaunchKernelEx(&cfg, mv_t5_kernel<3>, single, prm);
-    } else if (nt == 1) {
-        cfg.blockDim = dim3(kCtaThreads);
-        cfg.dynamicSmemBytes = smem_bytes_for(prm.ncols);
-        e = cudaLaunchKernelEx(&cfg, mv_tc_kernel<1>, single, prm);
     } else {
-        cfg.blockDim = dim3(kCtaThreads);
-        cfg.dynamicSmemBytes = smem_bytes_for(prm.ncols);
-        e = cudaLaunchKernelEx(&cfg, mv_tc_kernel<2>, single, prm);
+        switch (prm.ncols) {
+            case 2: e = launch_s8_nc<2>(cfg, single, prm); break;
+            case 3: e = launch_s8_nc<3>(cfg, single, prm); break;
+            case 4: e = launch_s8_nc<4>(cfg, single, prm); break;
+            case 5: e = launch_s8_nc<5>(cfg, single, prm); break;
+            case 6: e = launch_s8_nc<6>(cfg, single, prm); break;
+            case 7: e = launch_s8_nc<7>(cfg, single, prm); break;
+            default: e = launch_s8_nc<8>(cfg, single, prm); break;
+        }
     }
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -1969,8 +1373,7 @@ cudaError_t launch_generic(const uint8_t *w, const void *x, int xtype, float *y,
 }  // namespace
 
 size_t matvec_workspace_bytes(int64_t K, int ncols) {
-    return use_t4(ncols) ? t4_prep_bytes(K) : use_t5(ncols) ? t5_prep_bytes(K)
-                                                            : prep_bytes_for(K, ncols);
+    return use_t4(ncols) ? t4_prep_bytes(K) : s8_prep_bytes(K, ncols);
 }
 
 bool matvec_fast_path_ok(const void *w, int64_t K) {
@@ -1989,8 +1392,8 @@ int matvec_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, 
     cudaError_t e = launch_prep(pj, nullptr, 1, ncols, K, xtype, s);
     if (e != cudaSuccess) return Q2_0_ECUDA;
     MvJob J;
-    if (!make_job(J, w, prep, y, N, K, tile_rows_for(ncols))) return Q2_0_ECUDA;
-    MvParams prm{nullptr, nullptr, nullptr, nullptr, ncols, n_stages_for(ncols), err};
+    if (!make_job(J, w, prep, y, N, K)) return Q2_0_ECUDA;
+    MvParams prm{nullptr, nullptr, nullptr, nullptr, ncols, err};
     const int grid = std::max(1, std::min(J.n_tiles, sm_count()));
     return cuda_status(launch_tc(J, prm, grid, s));
 }
@@ -2012,17 +1415,17 @@ int matvec_split_run(const uint8_t *soa, const float *x, float *y, int64_t N, in
     // codes: 128 bytes (8 blocks) x 128 rows per box, 128-byte swizzle;
     // scales: 16 bytes x 128 rows per box
     if (!encode_tmap_2d(&J.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, soa, nb * 16, uint64_t(N), nb * 16,
-                        128, kT5Rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                        128, kTcRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tmap_2d(&J.tmap_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, dsc, nb * 2, uint64_t(N), nb * 2,
-                        16, kT5Rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+                        16, kTcRows, CU_TENSOR_MAP_SWIZZLE_NONE))
         return Q2_0_ECUDA;
     J.prep = prep;
     J.y = y;
     J.N = int(N);
     J.nb = int(nb);
     J.n_chunks = int(K / 512);
-    J.n_tiles = int((N + kT5Rows - 1) / kT5Rows);
-    MvParams prm{nullptr, nullptr, nullptr, nullptr, 1, n_stages_for(1), err, MvMoe{}, 1};
+    J.n_tiles = int((N + kTcRows - 1) / kTcRows);
+    MvParams prm{nullptr, nullptr, nullptr, nullptr, 1, err, MvMoe{}, 1};
     const int grid = std::max(1, std::min(J.n_tiles, sm_count()));
     return cuda_status(launch_tc(J, prm, grid, s));
 }
@@ -2052,10 +1455,10 @@ int matvec_moe_run(const uint8_t *w, int64_t n_expert, int64_t N, int64_t K, con
     if (launch_prep(pj, nullptr, int(n_xvec), 1, K, kXF32, s) != cudaSuccess) return Q2_0_ECUDA;
     // the tensor map spans all experts' rows; the kernel picks expert ids[v]
     MvJob J;
-    if (!make_job(J, w, prep, y, n_expert * N, K, kT5Rows)) return Q2_0_ECUDA;
+    if (!make_job(J, w, prep, y, n_expert * N, K)) return Q2_0_ECUDA;
     J.N = int(N);
-    J.n_tiles = int((N + kT5Rows - 1) / kT5Rows);
-    MvParams prm{nullptr, nullptr, nullptr, nullptr, 1, n_stages_for(1), err,
+    J.n_tiles = int((N + kTcRows - 1) / kTcRows);
+    MvParams prm{nullptr, nullptr, nullptr, nullptr, 1, err,
                  MvMoe{ids, int(n_vec), int(n_used), int(n_x), int(n_expert), stride}};
     const int64_t items = n_vec * J.n_tiles;
     const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items, sm_count())));
@@ -2132,7 +1535,7 @@ int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **o
         for (int j = 0; j < P->n_fast && st == Q2_0_OK; ++j) {
             const q2_0_mv_desc &d = descs[fast[j]];
             if (!make_job(jobs[j], static_cast<const uint8_t *>(d.w), P->d_prep + off[j], d.y, d.N,
-                          d.K, tile_rows_for(ncols)))
+                          d.K))
                 st = Q2_0_ECUDA;
             pjobs[j] = MvPrepJob{d.x, P->d_prep + off[j], int(d.K)};
             P->max_k = std::max<int64_t>(P->max_k, d.K);
@@ -2250,9 +1653,7 @@ int mv_plan_execute(const q2_0_mv_plan *P, cudaStream_t s) {
             return Q2_0_ECUDA;
         MvJob dummy;
         std::memset(&dummy, 0, sizeof(dummy));
-        MvParams prm{P->d_jobs, P->d_items, P->d_cta_begin, P->d_cta_stages, P->ncols,
-                     n_stages_for(P->ncols),
-                     P->err};
+        MvParams prm{P->d_jobs, P->d_items, P->d_cta_begin, P->d_cta_stages, P->ncols, P->err};
         if (launch_tc(dummy, prm, P->grid, s) != cudaSuccess) return Q2_0_ECUDA;
     }
     for (const q2_0_mv_desc &d : P->generic)

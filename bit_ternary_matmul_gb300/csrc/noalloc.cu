@@ -18,8 +18,8 @@ namespace q2 {
 namespace {
 
 // Q2_0_NOALLOC_SCRATCH_BYTES (1 MiB): enough for K up to 126,976 at ncols = 1,
-// 64,000 at ncols 2..3, 63,488 at ncols = 4 and 31,744 at ncols 5..8 (the scratch
-// grows with K and ncols).
+// 63,488 at ncols 2..3, 31,744 at ncols 4..6 and 21,504 at ncols 7..8 (the
+// scratch grows with K and ncols).
 constexpr size_t kNoAllocScratchBytes = Q2_0_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) uint8_t g_mv_noalloc_scratch[kNoAllocScratchBytes];
@@ -54,8 +54,11 @@ extern "C" int q2_0_mul_mat_vec_noalloc(const void *w, const float *x, float *y,
     if (!w || !x || !y || N < 1 || N > (int64_t(1) << 31) - 1 || K < 64 || K % 64 != 0 ||
         K > (int64_t(1) << 30) || ncols < 1 || ncols > 8)
         return Q2_0_EINVAL;
-    // The scratch this call needs must fit the static array.
-    if (q2::matvec_workspace_bytes(K, ncols) > q2::kNoAllocScratchBytes) return Q2_0_ENOSPACE;
+    // The tensor-core path's scratch must fit the static array; the CUDA-core
+    // path (K % 512 != 0 or w not 16-byte aligned) uses none.
+    if (q2::matvec_fast_path_ok(w, K) &&
+        q2::matvec_workspace_bytes(K, ncols) > q2::kNoAllocScratchBytes)
+        return Q2_0_ENOSPACE;
     int st = q2::check_device(nullptr);
     if (st != Q2_0_OK) return st;
     void *scratch = nullptr;

@@ -122,13 +122,17 @@ int q2_0_mul_mat_vec_ws(const void *w, const float *x, float *y, int64_t N, int6
  *   all. This call allocates nothing: its scratch (the prepared activation
  *   fragments) lives in a static device array of Q2_0_NOALLOC_SCRATCH_BYTES
  *   that every GPU which loads the library holds until the process exits.
- *   Limit: if q2_0_mul_mat_vec_workspace_size(K, ncols) exceeds
- *   Q2_0_NOALLOC_SCRATCH_BYTES the call returns Q2_0_ENOSPACE (1 MiB covers K up
- *   to 126,976 for ncols = 1, 64,000 for ncols 2..3, 63,488 for ncols = 4 and 31,744
- *   for ncols 5..8).
+ *   Limit: shapes on the tensor-core path (K % 512 == 0 and w 16-byte
+ *   aligned) need q2_0_mul_mat_vec_workspace_size(K, ncols) bytes of scratch;
+ *   if that exceeds Q2_0_NOALLOC_SCRATCH_BYTES the call returns Q2_0_ENOSPACE
+ *   and launches nothing (1 MiB covers K up to 126,976 for ncols = 1, 63,488
+ *   for ncols 2..3, 31,744 for ncols 4..6 and 21,504 for ncols 7..8). Other
+ *   shapes run the CUDA-core kernel, which needs no scratch, at any K.
  *   Set-up: the first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   (cudaGetSymbolAddress) with that device current and keeps it for the life
+ *   of the process; make that first call before any stream capture, and do not
+ *   call the entry point again after a cudaDeviceReset of that device (the
+ *   kept address belongs to the context the reset destroyed).
  *   Sharing: every call uses the same array and leaves its contents behind.
  *   Each call rewrites all of the scratch it reads, so nothing needs clearing,
  *   but calls whose executions overlap on the GPU (e.g. on two streams) race

@@ -97,7 +97,7 @@ def test_argument_validation_without_gpu(L):
     # the allocation-free entry's documented K limits (largest K that fits, then the next
     # multiple of 512) against its scratch size
     cap = q.Q2_0_NOALLOC_SCRATCH_BYTES
-    for ncols, k_max in [(1, 126976), (2, 64000), (3, 64000), (4, 63488), (5, 31744), (8, 31744)]:
+    for ncols, k_max in [(1, 126976), (2, 63488), (3, 63488), (4, 31744), (6, 31744), (7, 21504), (8, 21504)]:
         assert L.q2_0_mul_mat_vec_workspace_size(k_max, ncols) <= cap, ncols
         assert L.q2_0_mul_mat_vec_workspace_size(k_max + 512, ncols) > cap, ncols
     # GEMM: bad precision, bad K, small workspace
