@@ -22,8 +22,8 @@
 // 128-row tiles of one matrix or of a plan's many matrices; a pipeline stage is
 // one 2-D TMA box of 128 rows x 144 bytes (8 blocks = 512 weights per row) plus
 // the stage's activation image (bulk copy), in an 8-deep shared-memory ring.
-// Warp 2 streams the stages, warps 3 and 1 issue the MMAs of the even and odd
-// stages, warps 4-7 expand the codes of a stage into tensor memory (one warp
+// Warps 0 and 2 stream the even and odd stages, warps 3 and 1 issue the MMAs
+// of the even and odd stages, warps 4-7 expand the codes of a stage into tensor memory (one warp
 // per 32-lane quarter: a warp reaches only the lanes of its quarter) and warps
 // 8-11 combine the accumulators, apply d and write y. Activations are F32 or
 // F16 (the prep kernels and the generic kernel read either; F16 values are
@@ -52,8 +52,13 @@ constexpr int kRawBytes = kTcRows * kChunkBytes; // 18432: one stage's TMA box
 constexpr int kPrepHeader = 1024;                // activation images start 1024-aligned
 constexpr int kPrepThreads = 256;
 constexpr int kTcThreads = 12 * 32;
-// Warp roles of both tensor-core kernels (see the file comment).
+// Warp roles of both tensor-core kernels (see the file comment). Two producers
+// (warps 0 and 2) take the even and odd stages: issuing a stage's copies slows
+// the other warps of the producer's SM sub-partition, and the stage period is
+// set by the slowest expansion warp, so the issue work is split over two
+// sub-partitions.
 constexpr int kProdWarp = 2;
+constexpr int kProdWarp2 = 0;
 constexpr int kMmaWarp = 3;    // even stages; allocates TMEM
 constexpr int kMmaWarp2 = 1;   // odd stages
 constexpr int kExpWarp0 = 4;   // warps 4-7
@@ -215,8 +220,11 @@ constexpr int kT4ScaleCol = 448;                       // scales A 448..451, B 4
 // mbarriers: full / empty per stage, a_full / a_empty per A buffer, d_full /
 // d_empty per D buffer, a drain per MMA issuer
 constexpr int kT4Barriers = 2 * kT4Stages + 2 * kT4ABufs + 2 * 2 + 2;
-constexpr int kT4Smem = 1024 /* alignment slack */ +
-                        kT4Stages * (kT4ImgBytes + kRawBytes + kT4BetaBytes) +
+// a stage's activation data (image, then block records) is one bulk copy; in
+// shared memory its slots stay 1024-aligned for the swizzled image
+constexpr int kT4ActBytes = kT4ImgBytes + kT4BetaBytes;  // 4224, the stride in the prep buffer
+constexpr int kT4ActSlot = 5120;
+constexpr int kT4Smem = 1024 /* alignment slack */ + kT4Stages * (kT4ActSlot + kRawBytes) +
                         kT4Barriers * 8;
 static_assert(kT4Pieces == kT4N, "one B row per piece");
 constexpr int kTagT4Full = 111;
@@ -227,7 +235,7 @@ constexpr int kTagT4DEmpty = 115;
 
 size_t t4_prep_bytes(int64_t K) {
     const size_t n_chunks = size_t(K / 512);
-    size_t b = kPrepHeader + n_chunks * (kT4ImgBytes + kT4BetaBytes);
+    size_t b = kPrepHeader + n_chunks * kT4ActBytes;
     return (b + 255) & ~size_t(255);
 }
 
@@ -259,9 +267,7 @@ __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
     const int K = J.K;
     const XT *xj = static_cast<const XT *>(J.x);
     const int nb = K / 64;
-    const int n_chunks = K / 512;
-    uint8_t *img = J.prep + kPrepHeader;
-    float *brec = reinterpret_cast<float *>(img + size_t(n_chunks) * kT4ImgBytes);
+    uint8_t *act = J.prep + kPrepHeader;  // per stage: image, then block records
     const int lane = threadIdx.x & 31;
     const unsigned grp = 0xFFu << (lane & 24);  // the block's 8 threads
     // 8 items per block and nb blocks: whole warps share a block range, so the
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
         if (m > 0.0f && m <= 3.402823466e38f) frexpf(m, &e);
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) v[jj] = mul_pow2(v[jj], 2 - e);
-        uint8_t *bimg = img + size_t(b >> 3) * kT4ImgBytes;
+        uint8_t *bimg = act + size_t(b >> 3) * kT4ActBytes;
         const int kbyte = 32 * (b & 7) + 8 * c + 4 * h;  // byte of K position 64(b%8)+16c+8h
         float grp_sum[3] = {0.0f, 0.0f, 0.0f};  // this item's share of H, M, L
 #pragma unroll
@@ -315,7 +321,7 @@ __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
 #pragma unroll
             for (int o = 1; o < 8; o <<= 1) grp_sum[gi] += __shfl_xor_sync(grp, grp_sum[gi], o);
         if ((idx & 7) == 0)
-            *reinterpret_cast<float4 *>(brec + size_t(b) * kT4BlockRec) =
+            *reinterpret_cast<float4 *>(bimg + kT4ImgBytes + (b & 7) * kT4BlockRec * 4) =
                 make_float4(pow2f(e - 1), grp_sum[0], grp_sum[1], grp_sum[2]);
     }
 }
@@ -339,10 +345,9 @@ __global__ void __maxnreg__(128)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    uint8_t *img_ring = smem;                                      // kT4Stages x 4 KB
-    uint8_t *raw_ring = img_ring + kT4Stages * kT4ImgBytes;         // kT4Stages x 18 KB
-    uint8_t *beta_ring = raw_ring + kT4Stages * kRawBytes;        // kT4Stages x 32 B
-    uint64_t *full = reinterpret_cast<uint64_t *>(beta_ring + kT4Stages * kT4BetaBytes);
+    uint8_t *act_ring = smem;                                   // kT4Stages x 5 KB slots
+    uint8_t *raw_ring = act_ring + kT4Stages * kT4ActSlot;      // kT4Stages x 18 KB
+    uint64_t *full = reinterpret_cast<uint64_t *>(raw_ring + kT4Stages * kRawBytes);
     uint64_t *empty = full + kT4Stages;
     uint64_t *a_full = empty + kT4Stages;
     uint64_t *a_empty = a_full + kT4ABufs;
@@ -412,8 +417,10 @@ __global__ void __maxnreg__(128)
     auto a_col = [](int s) { return uint32_t(kT4ACol + (s % kT4ABufs) * 64); };
     auto d_col = [](int s) { return uint32_t((s & 1) * 128); };
 
-    if (warp == kProdWarp) {
-        // ------------------------------ producer ------------------------------
+    if (warp == kProdWarp || warp == kProdWarp2) {
+        // ------------------------------ producers ------------------------------
+        // warp 0 issues the even stages, warp 2 the odd ones; both walk every item
+        const int pmine = warp == kProdWarp2 ? 0 : 1;
         if (lane == 0) {
             int s = 0, last = -1;
             bool ok = true, prep_ready = false;
@@ -441,10 +448,10 @@ __global__ void __maxnreg__(128)
                     const int xv = p.moe.n_x == 1 ? v / p.moe.n_used : v;
                     prep += size_t(xv) * p.moe.prep_stride;
                 }
-                const uint8_t *img = prep + kPrepHeader;
-                const uint8_t *beta = img + size_t(J->n_chunks) * kT4ImgBytes;
+                const uint8_t *act = prep + kPrepHeader;
                 const int nch = J->n_chunks;
                 for (int ch = 0; ch < nch; ++ch, ++s) {
+                    if ((s & 1) != pmine) continue;
                     const int st = s % kT4Stages;
                     if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagT4Empty, true) ||
                         *(volatile int *)&s_abort) {
@@ -457,7 +464,7 @@ __global__ void __maxnreg__(128)
                     m.row0 = tile * kTcRows;
                     m.n_rows = J->N;
                     m.flags = ch == nch - 1 ? kLastOfTile : 0;
-                    mbar_arrive_expect_tx(&full[st], kRawBytes + kT4ImgBytes + kT4BetaBytes);
+                    mbar_arrive_expect_tx(&full[st], kRawBytes + kT4ActBytes);
                     if (kSplit) {
                         tma_load_2d(raw_ring + st * kRawBytes, &J->tmap, ch * 128,
                                     row_base + tile * kTcRows, &full[st]);
@@ -471,16 +478,14 @@ __global__ void __maxnreg__(128)
                         grid_dependency_wait();  // the B images come from the prep kernel
                         prep_ready = true;
                     }
-                    bulk_g2s(img_ring + st * kT4ImgBytes, img + size_t(ch) * kT4ImgBytes,
-                             kT4ImgBytes, &full[st]);
-                    bulk_g2s(beta_ring + st * kT4BetaBytes, beta + size_t(ch) * kT4BetaBytes,
-                             kT4BetaBytes, &full[st]);
+                    bulk_g2s(act_ring + st * kT4ActSlot, act + size_t(ch) * kT4ActBytes,
+                             kT4ActBytes, &full[st]);
                     last = s;
                 }
             }
             if (!ok) {
-                // let the copies in flight land (bounded) before the CTA exits
-                for (int t = last; t >= 0 && t > last - kT4Stages; --t)
+                // let this producer's copies in flight land (bounded) before the CTA exits
+                for (int t = last; t >= 0 && t > last - kT4Stages; t -= 2)
                     mbar_wait(&full[t % kT4Stages], stage_parity(t), p.err, kTagT4Full);
             }
         }
@@ -491,7 +496,7 @@ __global__ void __maxnreg__(128)
         constexpr uint32_t idesc = idesc_mxf4(kTcRows, kT4N);
         const bool leader = elect_one();
         const int mine = warp == kMmaWarp ? 0 : 1;
-        const uint64_t desc0 = sw128_desc(smem_addr(img_ring));
+        const uint64_t desc0 = sw128_desc(smem_addr(act_ring));
         const uint32_t sfa = tmem + kT4ScaleCol, sfb = tmem + kT4ScaleCol + 4;
         int last = -1;
         {
@@ -510,7 +515,7 @@ __global__ void __maxnreg__(128)
                 tc_fence_after();
                 const uint32_t a_base = tmem + a_col(s);
                 const uint32_t d_base = tmem + d_col(s);
-                const uint64_t dst = desc0 + uint64_t((st * kT4ImgBytes) >> 4);
+                const uint64_t dst = desc0 + uint64_t((st * kT4ActSlot) >> 4);
                 if (leader) {
 #pragma unroll
                     for (int b = 0; b < kChunkBlocks; ++b)
@@ -627,7 +632,8 @@ __global__ void __maxnreg__(128)
             const StageMeta m = s_meta[st];
             const uint32_t d_base = tmem + lane_base + d_col(s);
             const uint8_t *rp = raw_ring + st * kRawBytes + row * kChunkBytes;
-            const float4 *brec = reinterpret_cast<const float4 *>(beta_ring + st * kT4BetaBytes);
+            const float4 *brec =
+                reinterpret_cast<const float4 *>(act_ring + st * kT4ActSlot + kT4ImgBytes);
             float stage_sum = 0.0f;
             // blocks 4 hb .. 4 hb + 3: their 16 pieces each (64 registers)
 #pragma unroll
@@ -728,17 +734,25 @@ __host__ __device__ constexpr int s8_bs(int nc) { return 128 / s8_n(nc); }
 __host__ __device__ constexpr int s8_subs(int nc) { return kChunkBlocks / s8_bs(nc); }
 __host__ __device__ constexpr int s8_img_bytes(int nc) { return s8_n(nc) * kChunkBlocks * 64; }
 constexpr int kS8Barriers = 2 * 8 + 2 * 2 + 2 * 2 + 2;
+// shared-memory slot of a stage's activation data (image, then block scales:
+// one bulk copy), 1024-aligned for the swizzled image
+__host__ __device__ constexpr int s8_act_slot(int nc) { return s8_img_bytes(nc) + 1024; }
+// An even number of stages: each ring slot is then always filled by the same
+// producer (stage parity), so no producer waits two barrier phases ahead.
 __host__ __device__ constexpr int s8_stages(int nc) {
-    return (kSmemOptIn - 2048 - kS8Barriers * 8) / (kRawBytes + s8_img_bytes(nc) + kS8RecBytes) < 8
-               ? (kSmemOptIn - 2048 - kS8Barriers * 8) / (kRawBytes + s8_img_bytes(nc) + kS8RecBytes)
+    return (kSmemOptIn - 2048 - kS8Barriers * 8) / (kRawBytes + s8_act_slot(nc)) < 8
+               ? (kSmemOptIn - 2048 - kS8Barriers * 8) / (kRawBytes + s8_act_slot(nc)) / 2 * 2
                : 8;
 }
 __host__ __device__ constexpr int s8_smem(int nc) {
-    return 1024 /* alignment slack */ +
-           s8_stages(nc) * (s8_img_bytes(nc) + kRawBytes + kS8RecBytes) + kS8Barriers * 8;
+    return 1024 /* alignment slack */ + s8_stages(nc) * (s8_act_slot(nc) + kRawBytes) +
+           kS8Barriers * 8;
 }
 static_assert(s8_bs(2) == 8 && s8_bs(4) == 4 && s8_bs(8) == 2, "sub-stage sizes");
 static_assert(s8_stages(8) >= 4 && s8_smem(8) <= kSmemOptIn - 1024, "shared memory");
+static_assert(s8_stages(2) % 2 == 0 && s8_stages(4) % 2 == 0 && s8_stages(8) % 2 == 0 &&
+                  kT4Stages % 2 == 0,
+              "an even number of ring stages (two producers)");
 constexpr int kS8ACol = 0;    // A buffers at 0 and 128
 constexpr int kS8DCol = 256;  // accumulator buffers at 256 and 384
 constexpr uint32_t kS8Lut = 0x403800B8u;  // e4m3 of q - 1 in byte q
@@ -842,13 +856,15 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
     constexpr int kN = s8_n(NC), kBS = s8_bs(NC), kSub = s8_subs(NC);
     constexpr int kImg = s8_img_bytes(NC), kStages = s8_stages(NC);
     constexpr int kRecCopy = kChunkBlocks * NC * 4;  // bytes of the stage's block scales
+    constexpr int kGB = kN <= 16 ? 4 : kN <= 32 ? 2 : 1;  // blocks per tensor-memory wait
+    static_assert(kBS % kGB == 0, "whole load groups per sub-stage");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    uint8_t *img_ring = smem;                                 // kStages x kImg (1024-aligned)
-    uint8_t *raw_ring = img_ring + kStages * kImg;            // kStages x 18 KB
-    uint8_t *rec_ring = raw_ring + kStages * kRawBytes;       // kStages x 256 B
-    uint64_t *full = reinterpret_cast<uint64_t *>(rec_ring + kStages * kS8RecBytes);
+    constexpr int kSlot = s8_act_slot(NC);
+    uint8_t *act_ring = smem;                                 // kStages x kSlot (1024-aligned)
+    uint8_t *raw_ring = act_ring + kStages * kSlot;           // kStages x 18 KB
+    uint64_t *full = reinterpret_cast<uint64_t *>(raw_ring + kStages * kRawBytes);
     uint64_t *empty = full + 8;
     uint64_t *a_full = empty + 8;
     uint64_t *a_empty = a_full + 2;
@@ -908,8 +924,10 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
     const int n_stages = p.jobs ? p.cta_stages[blockIdx.x] : n_items * single.n_chunks;
     auto stage_parity = [](int s) { return uint32_t(s / kStages) & 1u; };
 
-    if (warp == kProdWarp) {
-        // ------------------------------ producer ------------------------------
+    if (warp == kProdWarp || warp == kProdWarp2) {
+        // ------------------------------ producers ------------------------------
+        // warp 0 issues the even stages, warp 2 the odd ones; both walk every item
+        const int pmine = warp == kProdWarp2 ? 0 : 1;
         if (lane == 0) {
             int s = 0, last = -1;
             bool ok = true, prep_ready = false;
@@ -920,6 +938,7 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
                 const uint8_t *prep = J->prep + kPrepHeader;
                 const int nch = J->n_chunks;
                 for (int ch = 0; ch < nch; ++ch, ++s) {
+                    if ((s & 1) != pmine) continue;
                     const int st = s % kStages;
                     if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagS8Empty, true) ||
                         *(volatile int *)&s_abort) {
@@ -939,15 +958,14 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
                         grid_dependency_wait();  // the images come from the prep kernel
                         prep_ready = true;
                     }
-                    const uint8_t *src = prep + size_t(ch) * (kImg + kS8RecBytes);
-                    bulk_g2s(img_ring + st * kImg, src, kImg, &full[st]);
-                    bulk_g2s(rec_ring + st * kS8RecBytes, src + kImg, kRecCopy, &full[st]);
+                    bulk_g2s(act_ring + st * kSlot, prep + size_t(ch) * (kImg + kS8RecBytes),
+                             kImg + kRecCopy, &full[st]);
                     last = s;
                 }
             }
             if (!ok) {
-                // let the copies in flight land (bounded) before the CTA exits
-                for (int t = last; t >= 0 && t > last - kStages; --t)
+                // let this producer's copies in flight land (bounded) before the CTA exits
+                for (int t = last; t >= 0 && t > last - kStages; t -= 2)
                     mbar_wait(&full[t % kStages], stage_parity(t), p.err, kTagS8Full);
             }
         }
@@ -963,7 +981,7 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
         constexpr uint32_t idesc = idesc_e4m3(kTcRows, kN);
         const bool leader = elect_one();
         const int mine = warp == kMmaWarp ? 0 : 1;
-        const uint64_t desc0 = sw128_desc(smem_addr(img_ring));
+        const uint64_t desc0 = sw128_desc(smem_addr(act_ring));
         const uint32_t d_base = tmem + kS8DCol + mine * 128;
         bool issued = false;
         for (int g = mine; g < n_stages * kSub; g += 2) {
@@ -982,7 +1000,7 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
             }
             tc_fence_after();
             const uint32_t a_base = tmem + kS8ACol + (s & 1) * 128;
-            const uint64_t dst = desc0 + uint64_t((st * kImg) >> 4);
+            const uint64_t dst = desc0 + uint64_t((st * kSlot) >> 4);
             if (leader) {
 #pragma unroll
                 for (int bi = 0; bi < kBS; ++bi) {
@@ -1076,7 +1094,7 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
             }
             const StageMeta m = s_meta[st];
             const uint8_t *rp = raw_ring + st * kRawBytes + row * kChunkBytes;
-            const float *sc = reinterpret_cast<const float *>(rec_ring + st * kS8RecBytes);
+            const float *sc = reinterpret_cast<const float *>(act_ring + st * kSlot + kImg);
             float ssum[NC];
 #pragma unroll
             for (int j = 0; j < NC; ++j) ssum[j] = 0.0f;
@@ -1093,30 +1111,36 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
                 }
                 tc_fence_after();
                 const uint32_t d_base = tmem + lane_base + kS8DCol + (g & 1) * 128;
+                // kGB blocks' accumulators (at most 64 registers) per tensor-memory wait
 #pragma unroll 1
-                for (int bi = 0; bi < kBS; ++bi) {
-                    const int b = ss * kBS + bi;
-                    uint32_t r[kN];
+                for (int gb = 0; gb < kBS; gb += kGB) {
+                    uint32_t r[kGB][kN];
 #pragma unroll
-                    for (int q16 = 0; q16 < kN / 16; ++q16)
-                        tmem_ld16(d_base + bi * kN + 16 * q16,
-                                  *reinterpret_cast<uint32_t(*)[16]>(&r[16 * q16]));
+                    for (int bi = 0; bi < kGB; ++bi)
+#pragma unroll
+                        for (int q16 = 0; q16 < kN / 16; ++q16)
+                            tmem_ld16(d_base + (gb + bi) * kN + 16 * q16,
+                                      *reinterpret_cast<uint32_t(*)[16]>(&r[bi][16 * q16]));
                     tmem_wait_ld();
-                    if (bi == kBS - 1) {  // the sub-stage's accumulators are all read
+                    if (gb + kGB == kBS) {  // the sub-stage's accumulators are all read
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&d_empty[g & 1]);
                     }
-                    const float d = lds_half_as_float(rp + 18 * b);
 #pragma unroll
-                    for (int j = 0; j < NC; ++j) {
-                        const uint32_t *c = &r[kS8Pieces * j];
-                        float t = __uint_as_float(c[4]) * 0x1p-16f;
-                        t = fmaf(__uint_as_float(c[3]), 0x1p-12f, t);
-                        t = fmaf(__uint_as_float(c[2]), 0x1p-8f, t);
-                        t = fmaf(__uint_as_float(c[1]), 0x1p-4f, t);
-                        t = t + __uint_as_float(c[0]);
-                        ssum[j] = fmaf(d * sc[b * NC + j], t, ssum[j]);
+                    for (int bi = 0; bi < kGB; ++bi) {
+                        const int b = ss * kBS + gb + bi;
+                        const float d = lds_half_as_float(rp + 18 * b);
+#pragma unroll
+                        for (int j = 0; j < NC; ++j) {
+                            const uint32_t *c = &r[bi][kS8Pieces * j];
+                            float t = __uint_as_float(c[4]) * 0x1p-16f;
+                            t = fmaf(__uint_as_float(c[3]), 0x1p-12f, t);
+                            t = fmaf(__uint_as_float(c[2]), 0x1p-8f, t);
+                            t = fmaf(__uint_as_float(c[1]), 0x1p-4f, t);
+                            t = t + __uint_as_float(c[0]);
+                            ssum[j] = fmaf(d * sc[b * NC + j], t, ssum[j]);
+                        }
                     }
                 }
             }
