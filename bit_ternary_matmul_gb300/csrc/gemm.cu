@@ -99,7 +99,7 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
 // never overflows fp16, and the lo parts of small elements stay above fp16's
 // subnormal range down to 2^-29 of the row maximum. F16 rows are only scaled
 // up (s >= 0), which keeps them exact. The scaling is exact and undone on the
-// f32 result (y = acc * 2^-s). One warp per row; X 16-byte aligned.
+// f32 result (y = acc * 2^-s). One CTA per row; X 16-byte aligned.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void load16(const float *p, float (&v)[16]) {
     const float4 *src = reinterpret_cast<const float4 *>(p);
@@ -133,22 +133,22 @@ __device__ __forceinline__ float mul_pow2(float v, int e) {
     return v * __int_as_float((127 + e1) << 23) * __int_as_float((127 + e2) << 23);
 }
 
-constexpr int kPrepRowsPerCta = 8;
+constexpr int kPrepThreads = 128;
 
+// One CTA per row: the row maximum by a block reduction, then the conversion.
 template <typename XT>
-__global__ void __launch_bounds__(kPrepRowsPerCta * 32) gemm_prep_kernel(
+__global__ void __launch_bounds__(kPrepThreads) gemm_prep_kernel(
     const XT *__restrict__ x, __half *__restrict__ xh, __half *__restrict__ xl,
     int *__restrict__ row_shift, int M, int K, int split) {
     // The GEMM kernel that follows may start its prologue and weight loads now;
     // it waits for this grid before reading X.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int m = blockIdx.x * kPrepRowsPerCta + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (m >= M) return;
+    const int m = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31;
     const XT *xr = x + size_t(m) * K;
     const int groups = K / 16;
     float amax = 0.0f;
-    for (int gi = lane; gi < groups; gi += 32) {
+    for (int gi = tid; gi < groups; gi += kPrepThreads) {
         float v[16];
         load16(xr + gi * 16, v);
 #pragma unroll
@@ -156,6 +156,11 @@ __global__ void __launch_bounds__(kPrepRowsPerCta * 32) gemm_prep_kernel(
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    __shared__ float red[kPrepThreads / 32];
+    if (lane == 0) red[tid >> 5] = amax;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kPrepThreads / 32; ++w) amax = fmaxf(amax, red[w]);
     int sh = 0;
     if (amax > 0.0f && amax <= 3.402823466e38f) {
         int e;
@@ -163,10 +168,10 @@ __global__ void __launch_bounds__(kPrepRowsPerCta * 32) gemm_prep_kernel(
         sh = 15 - e;
         if (sizeof(XT) == 2 && sh < 0) sh = 0;
     }
-    if (lane == 0) row_shift[m] = sh;
+    if (tid == 0) row_shift[m] = sh;
     __half *hr = xh + size_t(m) * K;
     __half *lr = split ? xl + size_t(m) * K : nullptr;
-    for (int gi = lane; gi < groups; gi += 32) {
+    for (int gi = tid; gi < groups; gi += kPrepThreads) {
         float v[16];
         load16(xr + gi * 16, v);
         uint32_t hw[8], lw[8];
@@ -717,12 +722,11 @@ int gemm_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, in
     __half *xl = split ? reinterpret_cast<__half *>(wsb + L.part) : nullptr;
     float *partials = reinterpret_cast<float *>(wsb + L.partials);
     int *row_shift = reinterpret_cast<int *>(wsb + L.shifts);
-    const unsigned pg = unsigned((M + kPrepRowsPerCta - 1) / kPrepRowsPerCta);
     if (xtype == kXF16)
-        gemm_prep_kernel<__half><<<pg, kPrepRowsPerCta * 32, 0, s>>>(
+        gemm_prep_kernel<__half><<<unsigned(M), kPrepThreads, 0, s>>>(
             static_cast<const __half *>(x), xh, xl, row_shift, int(M), int(K), split);
     else
-        gemm_prep_kernel<float><<<pg, kPrepRowsPerCta * 32, 0, s>>>(
+        gemm_prep_kernel<float><<<unsigned(M), kPrepThreads, 0, s>>>(
             static_cast<const float *>(x), xh, xl, row_shift, int(M), int(K), split);
     if (cudaGetLastError() != cudaSuccess) return Q2_0_ECUDA;
 
