@@ -47,7 +47,8 @@ _STATUS = {0: "Q2_0_OK", 1: "Q2_0_EINVAL", 2: "Q2_0_ECUDA", 3: "Q2_0_EUNSUPPORTE
 # Every symbol include/q2_0.h declares.
 EXPORTS = (
     "q2_0_version", "q2_0_device_check", "q2_0_mul_mat_vec", "q2_0_mul_mat_vec_workspace_size",
-    "q2_0_mul_mat_vec_ws", "q2_0_mul_mat_vec_noalloc", "q2_0_mv_plan_create", "q2_0_mv_plan_execute",
+    "q2_0_mul_mat_vec_ws", "q2_0_mul_mat_vec_noalloc", "q2_0_test_inject_stall",
+    "q2_0_mv_plan_create", "q2_0_mv_plan_execute",
     "q2_0_mv_plan_launches", "q2_0_mv_plan_destroy", "q2_0_mul_mat_workspace_size",
     "q2_0_mul_mat", "q2_0_get_rows", "q2_0_quantize_ref", "q2_0_get_error",
     "q2_0_mul_mat_vec_f16", "q2_0_mul_mat_f16",
@@ -102,6 +103,8 @@ def lib():
             L.q2_0_mul_mat_vec_ws.restype = i32
             L.q2_0_mul_mat_vec_noalloc.argtypes = [vp, vp, vp, i64, i64, i32, vp]
             L.q2_0_mul_mat_vec_noalloc.restype = i32
+            L.q2_0_test_inject_stall.argtypes = [i32, ctypes.c_uint64]
+            L.q2_0_test_inject_stall.restype = i32
             L.q2_0_mv_plan_create.argtypes = [ctypes.POINTER(_MvDesc), i32, i32,
                                               ctypes.POINTER(vp)]
             L.q2_0_mv_plan_create.restype = i32
@@ -432,6 +435,12 @@ def q2_0_quantize_ref(src: torch.Tensor, nrows: int, K: int, dst: torch.Tensor |
                                  _stream(stream))
     _check("q2_0_quantize_ref", st)
     return dst
+
+
+def q2_0_test_inject_stall(stage: int, wait_limit_ns: int) -> None:
+    """Test only: the next fp4 mat-vec launch on the current device stalls before
+    pipeline stage `stage` and its waits give up after wait_limit_ns."""
+    _check("q2_0_test_inject_stall", lib().q2_0_test_inject_stall(int(stage), int(wait_limit_ns)))
 
 
 def q2_0_get_error(stream=None):

@@ -115,6 +115,11 @@ struct MvParams {
     unsigned long long *err;
     MvMoe moe;
     int split;                // fp4 kernel only: 1 = the split layout (codes and scales apart)
+    // fp4 kernel, test hook (q2_0_test_inject_stall): when stall_stage > 0 the
+    // producers stop before stage stall_stage - 1, so the consumers' waits on it
+    // run out after wait_ns (0: the default limit)
+    int stall_stage;
+    unsigned long long wait_ns;
 };
 
 // Where the epilogue writes the tile a ring stage belongs to; the producer fills
@@ -360,6 +365,7 @@ __global__ void __maxnreg__(128)
     // where the epilogue writes the tile that the stage belongs to
     __shared__ StageMeta s_meta[kT4Stages];
 
+    const uint64_t wl = p.wait_ns ? p.wait_ns : kWaitLimitNs;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
@@ -452,8 +458,12 @@ __global__ void __maxnreg__(128)
                 const int nch = J->n_chunks;
                 for (int ch = 0; ch < nch; ++ch, ++s) {
                     if ((s & 1) != pmine) continue;
+                    if (p.stall_stage && s >= p.stall_stage - 1) {  // test hook
+                        ok = false;
+                        break;
+                    }
                     const int st = s % kT4Stages;
-                    if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagT4Empty, true) ||
+                    if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagT4Empty, true, wl) ||
                         *(volatile int *)&s_abort) {
                         ok = false;
                         s_abort = 1;
@@ -486,7 +496,7 @@ __global__ void __maxnreg__(128)
             if (!ok) {
                 // let this producer's copies in flight land (bounded) before the CTA exits
                 for (int t = last; t >= 0 && t > last - kT4Stages; t -= 2)
-                    mbar_wait(&full[t % kT4Stages], stage_parity(t), p.err, kTagT4Full);
+                    mbar_wait(&full[t % kT4Stages], stage_parity(t), p.err, kTagT4Full, false, wl);
             }
         }
     } else if (warp == kMmaWarp || warp == kMmaWarp2) {
@@ -503,10 +513,10 @@ __global__ void __maxnreg__(128)
             for (int s = mine; s < n_stages; s += 2) {
                 const int st = s % kT4Stages;
                 const bool got =
-                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full) &&
-                    mbar_wait(&a_full[a_buf(s)], a_use(s), p.err, kTagT4AFull) &&
+                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full, false, wl) &&
+                    mbar_wait(&a_full[a_buf(s)], a_use(s), p.err, kTagT4AFull, false, wl) &&
                     mbar_wait(&d_empty[s & 1], (uint32_t(s >> 1) & 1u) ^ 1u, p.err,
-                              kTagT4DEmpty) &&
+                              kTagT4DEmpty, false, wl) &&
                     !*(volatile int *)&s_abort;
                 if (!__all_sync(0xffffffffu, got)) {
                     s_abort = 1;
@@ -534,7 +544,7 @@ __global__ void __maxnreg__(128)
         if (last >= 0) {
             if (leader) tc_commit(&drain[mine]);
             __syncwarp();
-            if (leader) mbar_wait(&drain[mine], 0u, p.err, kTagT4DFull);
+            if (leader) mbar_wait(&drain[mine], 0u, p.err, kTagT4DFull, false, wl);
             __syncwarp();
         }
     } else if (warp >= kExpWarp0 && warp < kExpWarp0 + kExpWarps) {
@@ -552,8 +562,8 @@ __global__ void __maxnreg__(128)
             for (int s = 0; s < n_stages; ++s) {
                 const int st = s % kT4Stages;
                 const bool got =
-                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full) &&
-                    mbar_wait(&a_empty[a_buf(s)], a_use(s) ^ 1u, p.err, kTagT4AFull) &&
+                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full, false, wl) &&
+                    mbar_wait(&a_empty[a_buf(s)], a_use(s) ^ 1u, p.err, kTagT4AFull, false, wl) &&
                     !*(volatile int *)&s_abort;
                 if (!__all_sync(0xffffffffu, got)) {
                     s_abort = 1;
@@ -622,8 +632,8 @@ __global__ void __maxnreg__(128)
         for (int s = 0; s < n_stages; ++s) {
             const int st = s % kT4Stages;
             const bool got = !*(volatile int *)&s_abort &&
-                             mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full) &&
-                             mbar_wait(&d_full[s & 1], uint32_t(s >> 1) & 1u, p.err, kTagT4DFull);
+                             mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full, false, wl) &&
+                             mbar_wait(&d_full[s & 1], uint32_t(s >> 1) & 1u, p.err, kTagT4DFull, false, wl);
             if (!__all_sync(0xffffffffu, got)) {
                 s_abort = 1;
                 break;
@@ -1261,6 +1271,23 @@ __global__ void __launch_bounds__(256) moe_generic_kernel(
 
 std::mutex g_attr_mu;
 bool g_t4_attr_done[64];
+
+// Test hook (q2_0_test_inject_stall): a one-shot stall for the next fp4 mat-vec
+// launch on a device.
+std::mutex g_stall_mu;
+int g_stall_stage[64];
+unsigned long long g_stall_wait_ns[64];
+
+void take_stall(MvParams &prm) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
+    std::lock_guard<std::mutex> lk(g_stall_mu);
+    if (g_stall_stage[dev] > 0) {
+        prm.stall_stage = g_stall_stage[dev];
+        prm.wait_ns = g_stall_wait_ns[dev];
+        g_stall_stage[dev] = 0;
+    }
+}
 bool g_s8_attr_done[64][9];
 
 cudaError_t ensure_t4_attr() {
@@ -1365,8 +1392,10 @@ cudaError_t launch_tc(const MvJob &single, const MvParams &prm, int grid, cudaSt
         if (e != cudaSuccess) return e;
         cfg.blockDim = dim3(kTcThreads);
         cfg.dynamicSmemBytes = kT4Smem;
-        e = prm.split ? cudaLaunchKernelEx(&cfg, mv_t4_kernel<true>, single, prm)
-                      : cudaLaunchKernelEx(&cfg, mv_t4_kernel<false>, single, prm);
+        MvParams prm2 = prm;
+        take_stall(prm2);
+        e = prm2.split ? cudaLaunchKernelEx(&cfg, mv_t4_kernel<true>, single, prm2)
+                       : cudaLaunchKernelEx(&cfg, mv_t4_kernel<false>, single, prm2);
     } else {
         switch (prm.ncols) {
             case 2: e = launch_s8_nc<2>(cfg, single, prm); break;
@@ -1689,3 +1718,17 @@ int mv_plan_execute(const q2_0_mv_plan *P, cudaStream_t s) {
 }
 
 }  // namespace q2
+
+// Test hook: the next fp4 mat-vec launch (ncols = 1 on the tensor-core path) on
+// the current device stops feeding its pipeline before the given stage, and
+// every pipeline wait of that launch gives up after wait_limit_ns.
+extern "C" int q2_0_test_inject_stall(int stage, uint64_t wait_limit_ns) {
+    int dev = 0;
+    if (stage < 0 || wait_limit_ns == 0 || wait_limit_ns > 10000000000ull) return Q2_0_EINVAL;
+    if (cudaGetDevice(&dev) != cudaSuccess) return Q2_0_ECUDA;
+    if (dev < 0 || dev >= 64) return Q2_0_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lk(q2::g_stall_mu);
+    q2::g_stall_stage[dev] = stage + 1;
+    q2::g_stall_wait_ns[dev] = wait_limit_ns;
+    return Q2_0_OK;
+}

@@ -85,8 +85,9 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t pa
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete. Gives up after about
-// one second: records the timeout (tag identifies the wait) and returns false.
+// Wait for the phase with the given parity to complete. Gives up after
+// limit_ns (about one second unless a kernel passes a shorter limit): records
+// the timeout (tag identifies the wait) and returns false.
 // Between checks the thread backs off for a few tens of nanoseconds, so that a
 // waiting warp takes few issue slots from the warps that share its SM
 // sub-partition while still waking within ~100 cycles; sleep = true suspends
@@ -97,7 +98,8 @@ constexpr uint32_t kWaitSuspendNs = 20000;
 constexpr uint32_t kWaitBackoffNs = 32;
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned long long *err,
-                                          int tag, bool sleep = false) {
+                                          int tag, bool sleep = false,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = globaltimer_ns();
     while (true) {
@@ -107,7 +109,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
             __nanosleep(kWaitBackoffNs);
             if (mbar_try_wait(bar, parity)) return true;
         }
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             record_error(err, Q2_0_DEVERR_TIMEOUT, tag);
             return false;
         }

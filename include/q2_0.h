@@ -305,6 +305,22 @@ int q2_0_quantize_ref(const float *src, void *dst, int64_t nrows, int64_t K, voi
  */
 int q2_0_get_error(void *stream, int64_t *info);
 
+/*
+ * q2_0_test_inject_stall — TEST ONLY: exercises the bounded pipeline waits.
+ * (No counterpart on the pages: the failure-detection path of this library.)
+ * The next fp4 mat-vec launch on the current device (ncols = 1 on the
+ * tensor-core path: q2_0_mul_mat_vec, _ws, _noalloc, _f16, _split, a plan or
+ * q2_0_mul_mat_id) stops feeding its pipeline before pipeline stage `stage`
+ * of each CTA (0 = the first), and every pipeline wait of that launch gives up
+ * after wait_limit_ns instead of about one second. The consumers' waits on
+ * the missing stage then run out: the kernel records Q2_0_DEVERR_TIMEOUT with
+ * info 111 (the wait for a stage's copies), lets the copies it issued land,
+ * frees its tensor memory and returns; its outputs are incomplete. Later
+ * launches are unaffected. Returns Q2_0_EINVAL for stage < 0 or a limit of 0
+ * or above 10 s.
+ */
+int q2_0_test_inject_stall(int stage, uint64_t wait_limit_ns);
+
 #ifdef __cplusplus
 }
 #endif
