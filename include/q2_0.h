@@ -60,11 +60,18 @@ typedef enum q2_0_status {
 #define Q2_0_DEVERR_TIMEOUT 2 /* a pipeline wait gave up; info = kernel tag */
 
 /* GEMM activation precision. F32 activations are used by the tensor cores as
- * fp16 operands (the weights (q-1)*d are exact in fp16):
+ * fp16 operands (the weights (q-1)*d are exact in fp16). Each token row is first
+ * scaled by an exact power of two that puts its largest |x| in [2^14, 2^15), and
+ * the f32 result is scaled back, so any finite x is in range:
  *   Q2_0_PREC_F16_SPLIT: x = hi + lo with hi = fp16(x), lo = fp16(x - hi); two
- *     tensor-core products. Bound: |y - exact| <= 1e-5 * sum|w*x| + 1e-7.
- *   Q2_0_PREC_F16: x rounded once to fp16. Bound: <= 4e-3 * sum|w*x|.
- * Precondition of both: finite x with |x| < 65504 and |2d| <= 65504. */
+ *     tensor-core products. Each element keeps 22 bits of its own value (down to
+ *     2^-29 of its row's largest |x|); tolerance |y - exact| <= 1e-5 * sum|w*x|
+ *     + 1e-7. The products are exact; the f32 accumulation over K/16 tensor-core
+ *     steps adds rounding that is far below that in practice, but whose
+ *     worst-case bound grows as (K/16) * 2^-24 * sum|w*x|.
+ *   Q2_0_PREC_F16: x rounded once to fp16 (11 bits). Tolerance <= 4e-3 * sum|w*x|.
+ * Precondition of both: finite x, and |2d| <= 65504 (so that (q-1)*d is finite
+ * in fp16). */
 typedef enum q2_0_prec { Q2_0_PREC_F16_SPLIT = 0, Q2_0_PREC_F16 = 1 } q2_0_prec;
 
 /* Library version string (static storage). */
@@ -82,7 +89,21 @@ int q2_0_device_check(void);
  *   w      N x K Q2_0 matrix (N*K/64*18 bytes), any alignment.
  *   x      F32 [ncols][K].   y  F32 [ncols][N] (written, not accumulated).
  *   N >= 1, K >= 64 with K % 64 == 0, 1 <= ncols <= 8.
- * Error bound: |y - exact| <= 1e-5 * sum_k |W[n][k] X[c][k]| + 1e-7 for finite x.
+ * Precision (finite x; M_b = the largest |x| of the activation block of 64
+ * that holds element k; the tensor-core paths have K % 512 == 0 and w 16-byte
+ * aligned, other shapes run f32 on CUDA cores):
+ *   ncols 1, tensor cores: each element of x is represented to within
+ *     2^-33 M_b; zero weights contribute exactly nothing; the rest is f32
+ *     rounding: |y - exact| <= 2^-33 sum_k |W[n][k]| M_b + 2^-20 sum_k |W X|;
+ *   ncols 2..8, tensor cores: each element keeps 20 bits of its own value,
+ *     with a floor of 2^-33 M_b: |y - exact| <= 2^-33 sum_k |W[n][k]| M_b +
+ *     2^-17 sum_k |W X|;
+ *   CUDA cores: f32 products and sums, |y - exact| <= 2^-17 sum_k |W X| for
+ *     K <= 65536.
+ * The tensor-core paths meet the tolerance |y - exact| <= 1e-5 *
+ * sum_k |W[n][k] X[c][k]| + 1e-7 unless, weighted by |W|, the activations sit
+ * on average more than ~2e4 times below the largest element of their own block
+ * of 64.
  * Scratch: the call takes q2_0_mul_mat_vec_workspace_size(K, ncols) bytes of
  * stream-ordered memory from the device's default memory pool
  * (cudaMallocAsync/cudaFreeAsync on `stream`); use q2_0_mul_mat_vec_ws to
@@ -96,8 +117,8 @@ int q2_0_mul_mat_vec(const void *w, const float *x, float *y, int64_t N, int64_t
  * activations x [ncols][K], any alignment; y F32. The pages' WebGPU port
  * supports F32 activations only and lists F16 ones as missing ("WebGPU: add
  * Q2_0 support", limitations paragraph); this is that variant. Each fp16
- * value is used exactly, so the F32 error bound applies with x read as the
- * exact fp16 values. Scratch as q2_0_mul_mat_vec (default memory pool).
+ * value is read exactly, so the F32 precision statement applies with x read
+ * as the exact fp16 values. Scratch as q2_0_mul_mat_vec (default memory pool).
  */
 int q2_0_mul_mat_vec_f16(const void *w, const void *x, float *y, int64_t N, int64_t K, int ncols,
                          void *stream);
