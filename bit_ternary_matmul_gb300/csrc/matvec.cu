@@ -50,7 +50,7 @@ constexpr int kChunkBytes = kChunkBlocks * 18;   // 144 bytes of a row per stage
 constexpr int kTcRows = 128;                     // rows per tile (MMA M)
 constexpr int kRawBytes = kTcRows * kChunkBytes; // 18432: one stage's TMA box
 constexpr int kPrepHeader = 1024;                // activation images start 1024-aligned
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 128;
 constexpr int kTcThreads = 12 * 32;
 // Warp roles of both tensor-core kernels (see the file comment). Two producers
 // (warps 0 and 2) take the even and odd stages: issuing a stage's copies slows
@@ -299,27 +299,44 @@ __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
         uint8_t *bimg = act + size_t(b >> 3) * kT4ActBytes;
         const int kbyte = 32 * (b & 7) + 8 * c + 4 * h;  // byte of K position 64(b%8)+16c+8h
         float grp_sum[3] = {0.0f, 0.0f, 0.0f};  // this item's share of H, M, L
+        // Rounding to the e2m1 grid without format conversions. With M = 2^23,
+        // fma(|s|, 2, M) rounds 2|s| to the nearest integer (ties to even) and
+        // keeps it in its low mantissa bits. On [0, 2] the e2m1 values are the
+        // multiples of 1/2, and round-to-nearest-even on them is exactly that
+        // rounding of 2|s|, whose integer k (0..4) is also the nibble of k/2;
+        // only the first piece can exceed 2 (|s| < 4), where the grid is the
+        // integers 2, 3, 4 (nibbles 4, 5, 6) and |s| + M rounds |s| alike.
+        constexpr float kMagic = 8388608.0f;
 #pragma unroll
         for (int p = 0; p < kT4Pieces; ++p) {
             const float up = __int_as_float((127 + 2 * p) << 23);
             const float down = __int_as_float((127 - 2 * p) << 23);
             uint32_t word = 0;
-            int acc2 = 0;  // sum of 2 * piece (exact small integers)
+            float sum2 = 0.0f;  // sum of 2 * piece over the item's 8 elements (exact)
 #pragma unroll
-            for (int q2 = 0; q2 < 4; ++q2) {
-                const __nv_fp4x2_storage_t pc = __nv_cvt_float2_to_fp4x2(
-                    make_float2(v[2 * q2] * up, v[2 * q2 + 1] * up), __NV_E2M1, cudaRoundNearest);
-                const float2 pv =
-                    __half22float2(__half2(__nv_cvt_fp4x2_to_halfraw2(pc, __NV_E2M1)));
-                v[2 * q2] -= pv.x * down;
-                v[2 * q2 + 1] -= pv.y * down;
-                acc2 += __float2int_rn(2.0f * pv.x) + __float2int_rn(2.0f * pv.y);
-                word |= uint32_t(pc) << (8 * q2);
+            for (int jj = 0; jj < 8; ++jj) {
+                const float sv = v[jj] * up;
+                const float as = fabsf(sv);
+                float two_mag;   // 2 |piece|
+                uint32_t nib;
+                if (p == 0 && as > 2.0f) {
+                    const float a1 = as + kMagic;
+                    nib = (__float_as_uint(a1) & 7u) + 2u;
+                    two_mag = 2.0f * (a1 - kMagic);
+                } else {
+                    const float a2 = fmaf(as, 2.0f, kMagic);
+                    nib = __float_as_uint(a2) & 7u;
+                    two_mag = a2 - kMagic;
+                }
+                const float two_piece = copysignf(two_mag, sv);
+                v[jj] = fmaf(-two_piece, 0.5f * down, v[jj]);
+                sum2 += two_piece;
+                word |= (nib | ((__float_as_uint(sv) >> 28) & 8u)) << (4 * jj);
             }
             *reinterpret_cast<uint32_t *>(bimg + img_offset(kT4N, p, kbyte)) = word;
-            // sum of piece / 2 = acc2 / 4, weighted by 4^-p, into its group
+            // sum of piece / 2 = sum2 / 4, weighted by 4^-p, into its group
             const int gi = p < 6 ? 0 : p < 12 ? 1 : 2;
-            grp_sum[gi] = fmaf(float(acc2) * 0.25f, down, grp_sum[gi]);
+            grp_sum[gi] = fmaf(sum2 * 0.25f, down, grp_sum[gi]);
         }
 #pragma unroll
         for (int gi = 0; gi < 3; ++gi)

@@ -144,3 +144,38 @@ def test_block_groups_exact_and_zero_weights_cancel():
         nonzero = sum(abs(Fraction(int(qq) - 1, 2)) * abs(Fraction(vv))
                       for qq, vv in zip(q, v))
         assert abs(Fraction(float(t)) - exact) <= Fraction(1, 2 ** 22) * nonzero + Fraction(1, 2 ** 40)
+
+
+def _magic_round(s, first_piece):
+    """The prep's rounding in f32: |s| + 2^23 (first piece, |s| > 2) or
+    fma(|s|, 2, 2^23) rounds to an integer in its low mantissa bits; returns
+    (piece value, e2m1 nibble)."""
+    M = F32(8388608.0)
+    a = F32(abs(s))
+    if first_piece and a > 2.0:
+        a1 = F32(a + M)
+        m = int(np.array(a1, dtype=np.float32).view(np.uint32)) & 7
+        mag, nib = float(a1 - M), m + 2
+    else:
+        a2 = F32(Fraction(float(a)) * 2 + Fraction(float(M)))   # one rounding, as fma
+        k = int(np.array(a2, dtype=np.float32).view(np.uint32)) & 7
+        mag, nib = float(a2 - M) / 2.0, k
+    sign = 8 if np.signbit(F32(s)) else 0
+    return float(np.copysign(mag, s)), nib | sign
+
+
+_NIBBLE = {0.0: 0, 0.5: 1, 1.0: 2, 1.5: 3, 2.0: 4, 3.0: 5, 4.0: 6, 6.0: 7}
+
+
+def test_prep_rounding_equals_e2m1_round_to_nearest_even():
+    g = np.random.default_rng(4)
+    first = list(g.uniform(-4.0, 4.0, 4000)) + [2.0, 2.5, 3.5, 3.999999761581421, -2.5, -3.5]
+    later = list(g.uniform(-2.0, 2.0, 4000)) + [0.25, 0.75, 1.25, 1.75, -0.25, -1.75, 2.0, 0.0]
+    for vals, is_first in ((first, True), (later, False)):
+        for v in vals:
+            v = float(F32(v))
+            piece, nib = _magic_round(v, is_first)
+            want = e2m1_rne(v)
+            assert piece == want, (v, piece, want)
+            assert nib & 7 == _NIBBLE[abs(want)], (v, nib)
+            assert (nib & 8 != 0) == bool(np.signbit(F32(v))), v
