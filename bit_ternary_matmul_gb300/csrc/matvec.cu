@@ -760,15 +760,28 @@ __host__ __device__ constexpr int s8_n(int nc) { return (kS8Pieces * nc + 15) / 
 __host__ __device__ constexpr int s8_bs(int nc) { return 128 / s8_n(nc); }
 __host__ __device__ constexpr int s8_subs(int nc) { return kChunkBlocks / s8_bs(nc); }
 __host__ __device__ constexpr int s8_img_bytes(int nc) { return s8_n(nc) * kChunkBlocks * 64; }
-constexpr int kS8Barriers = 2 * 8 + 2 * 2 + 2 * 2 + 2;
+// full/empty per stage, a_full/a_empty, d_full/d_empty, drain, and per lane
+// quarter the two tile-end hand-offs between its epilogue warps
+constexpr int kS8Barriers = 2 * 8 + 2 * 2 + 2 * 2 + 2 + 2 * 4;
+// The fp4 kernel's roles with two epilogue warps per lane quarter (warps 8-11
+// drain accumulator buffer 0, warps 12-15 buffer 1): 16 warps. With one
+// accumulator sub-stage per stage (ncols 2-3) the expansion is the longest
+// role, and it also gets two warps per lane quarter (warps 4-7 expand blocks
+// 0-3 of a stage, warps 16-19 blocks 4-7): 20 warps at most 96 registers each.
+constexpr int kS8EpiWarps = 8;
+constexpr int kS8ExpWarp1 = 16;
+__host__ __device__ constexpr bool s8_exp2(int nc) { return s8_n(nc) <= 16; }
+__host__ __device__ constexpr int s8_threads(int nc) { return (s8_exp2(nc) ? 20 : 16) * 32; }
+constexpr int kS8PairBytes = 4 * 32 * 2 * 8 * 4;  // tile-end exchange, ncols <= 8
 // shared-memory slot of a stage's activation data (image, then block scales:
 // one bulk copy), 1024-aligned for the swizzled image
 __host__ __device__ constexpr int s8_act_slot(int nc) { return s8_img_bytes(nc) + 1024; }
 // An even number of stages: each ring slot is then always filled by the same
 // producer (stage parity), so no producer waits two barrier phases ahead.
 __host__ __device__ constexpr int s8_stages(int nc) {
-    return (kSmemOptIn - 2048 - kS8Barriers * 8) / (kRawBytes + s8_act_slot(nc)) < 8
-               ? (kSmemOptIn - 2048 - kS8Barriers * 8) / (kRawBytes + s8_act_slot(nc)) / 2 * 2
+    return (kSmemOptIn - 2048 - kS8PairBytes - kS8Barriers * 8) / (kRawBytes + s8_act_slot(nc)) < 8
+               ? (kSmemOptIn - 2048 - kS8PairBytes - kS8Barriers * 8) /
+                     (kRawBytes + s8_act_slot(nc)) / 2 * 2
                : 8;
 }
 __host__ __device__ constexpr int s8_smem(int nc) {
@@ -788,6 +801,7 @@ constexpr int kTagS8Empty = 122;
 constexpr int kTagS8AFull = 123;
 constexpr int kTagS8DFull = 124;
 constexpr int kTagS8DEmpty = 125;
+constexpr int kTagS8Pair = 126;
 
 size_t s8_prep_bytes(int64_t K, int ncols) {
     const size_t n_chunks = size_t(K / 512);
@@ -875,7 +889,7 @@ __global__ void __launch_bounds__(kPrepThreads) s8_prep_kernel(
 
 // NC: activation columns (2..8).
 template <int NC>
-__global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob single,
+__global__ void __launch_bounds__(s8_threads(NC), 1) mv_s8_kernel(const __grid_constant__ MvJob single,
                                               const MvParams p) {
     // The next prep launch on the stream may become resident now; it waits for
     // this grid before it touches any buffer this kernel reads.
@@ -898,6 +912,9 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
     uint64_t *d_full = a_empty + 2;
     uint64_t *d_empty = d_full + 2;
     uint64_t *drain = d_empty + 2;  // [2] one per MMA issuer: its final commit
+    uint64_t *tile_w1 = drain + 2;  // [4] per quarter: warp 12+q's tile sums are in s_pair
+    uint64_t *tile_w0 = tile_w1 + 4;  // [4] per quarter: warp 8+q has read them
+    __shared__ float s_pair[4][32][2 * NC];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     __shared__ StageMeta s_meta[kStages];
@@ -908,14 +925,18 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kEpiWarps);
+            mbar_init(&empty[i], kS8EpiWarps);  // both epilogue warps of each quarter
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&a_full[i], kExpWarps);
+            mbar_init(&a_full[i], s8_exp2(NC) ? 2 * kExpWarps : kExpWarps);
             mbar_init(&a_empty[i], kSub >= 2 ? 2 : 1);  // one commit per issuer on the stage
             mbar_init(&d_full[i], 1);
-            mbar_init(&d_empty[i], kEpiWarps);
+            mbar_init(&d_empty[i], kEpiWarps);  // the 4 warps that drain buffer i
             mbar_init(&drain[i], 1);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&tile_w1[i], 1);
+            mbar_init(&tile_w0[i], 1);
         }
         s_abort = 0;
         fence_barrier_init();
@@ -1053,9 +1074,12 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
             if (leader) mbar_wait(&drain[mine], 0u, p.err, kTagS8DFull);
             __syncwarp();
         }
-    } else if (warp >= kExpWarp0 && warp < kExpWarp0 + kExpWarps) {
+    } else if ((warp >= kExpWarp0 && warp < kExpWarp0 + kExpWarps) ||
+               (s8_exp2(NC) && warp >= kS8ExpWarp1)) {
         // ------------------------------ expansion ------------------------------
-        // warp w: TMEM lane quarter w % 4 (rows 32 (w % 4) ..), all 8 blocks
+        // warp w: TMEM lane quarter w % 4 (rows 32 (w % 4) ..): all 8 blocks, or with
+        // two expansion warps per quarter blocks 4G..4G+3, G = 0 for warps 4-7 and 1
+        // for warps 16-19
         const int qd = warp & 3;
         const int row = 32 * qd + lane;
         const uint32_t lane_base = uint32_t(32 * qd) << 16;
@@ -1070,8 +1094,10 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
                 break;
             }
             tc_fence_after();
+            const int g_lo = s8_exp2(NC) ? (warp >= kS8ExpWarp1 ? 1 : 0) : 0;
+            const int g_hi = s8_exp2(NC) ? g_lo + 1 : 2;
 #pragma unroll
-            for (int G = 0; G < 2; ++G) {
+            for (int G = g_lo; G < g_hi; ++G) {
                 const uint8_t *rp = raw_ring + st * kRawBytes + row * kChunkBytes + G * 72;
                 uint32_t u[18];
 #pragma unroll
@@ -1081,17 +1107,22 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
                     u[2 * k + 1] = v.y;
                 }
 #pragma unroll
-                for (int bi = 0; bi < 4; ++bi) {
-                    uint32_t a[16];
+                for (int bp = 0; bp < 2; ++bp) {  // two blocks per tensor-memory store
+                    uint32_t a[32];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t w = block_word(u, bi, c);
-                        a[4 * c + 0] = __byte_perm(kS8Lut, 0u, w & 0x3333u);
-                        a[4 * c + 1] = __byte_perm(kS8Lut, 0u, (w >> 2) & 0x3333u);
-                        a[4 * c + 2] = __byte_perm(kS8Lut, 0u, (w >> 16) & 0x3333u);
-                        a[4 * c + 3] = __byte_perm(kS8Lut, 0u, (w >> 18) & 0x3333u);
-                    }
-                    tmem_st16(tmem + lane_base + kS8ACol + (s & 1) * 128 + (4 * G + bi) * 16, a);
+                    for (int b2 = 0; b2 < 2; ++b2)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            // even and odd codes, one per nibble; the byte permute
+                            // reads only the selector's low 16 bits
+                            const uint32_t w = block_word(u, 2 * bp + b2, c);
+                            const uint32_t me = w & 0x33333333u, mo = (w >> 2) & 0x33333333u;
+                            a[16 * b2 + 4 * c + 0] = __byte_perm(kS8Lut, 0u, me);
+                            a[16 * b2 + 4 * c + 1] = __byte_perm(kS8Lut, 0u, mo);
+                            a[16 * b2 + 4 * c + 2] = __byte_perm(kS8Lut, 0u, me >> 16);
+                            a[16 * b2 + 4 * c + 3] = __byte_perm(kS8Lut, 0u, mo >> 16);
+                        }
+                    tmem_st32(tmem + lane_base + kS8ACol + (s & 1) * 128 + (4 * G + 2 * bp) * 16, a);
                 }
             }
             tmem_wait_st();
@@ -1099,18 +1130,21 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
             __syncwarp();
             if (lane == 0) mbar_arrive(&a_full[s & 1]);
         }
-    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
+    } else if (warp >= kEpiWarp0 && warp < kS8ExpWarp1) {
         // ------------------------------ epilogue ------------------------------
-        // warp w: TMEM lane quarter w % 4, all 8 blocks of each stage; it writes
-        // y at the tile's last stage. Every wait is bounded; a warp whose wait
-        // fails leaves the loop.
-        const int qd = warp & 3;
+        // warp w: TMEM lane quarter q = w % 4 and accumulator buffer e = (w - 8) / 4,
+        // i.e. the sub-stages g = s * kSub + ss with g % 2 == e. Each of the two
+        // warps of a quarter sums its own sub-stages; at a tile's last stage warp
+        // 12+q hands its sums to warp 8+q through s_pair, which adds them and
+        // writes y. Every wait is bounded; a warp whose wait fails leaves the loop.
+        const int qd = warp & 3, e = (warp - kEpiWarp0) >> 2;
         const int row = 32 * qd + lane;
         const uint32_t lane_base = uint32_t(32 * qd) << 16;
         float acc[NC], comp[NC];
 #pragma unroll
         for (int j = 0; j < NC; ++j) acc[j] = comp[j] = 0.0f;
         bool ok = true;
+        int n_tile_ends = 0;
         for (int s = 0; s < n_stages && ok; ++s) {
             const int st = s % kStages;
             const bool got = !*(volatile int *)&s_abort &&
@@ -1128,7 +1162,8 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
 #pragma unroll 1
             for (int ss = 0; ss < kSub; ++ss) {
                 const int g = s * kSub + ss;
-                const bool have = mbar_wait(&d_full[g & 1], uint32_t(g >> 1) & 1u, p.err,
+                if ((g & 1) != e) continue;
+                const bool have = mbar_wait(&d_full[e], uint32_t(g >> 1) & 1u, p.err,
                                             kTagS8DFull) &&
                                   !*(volatile int *)&s_abort;
                 if (!__all_sync(0xffffffffu, have)) {
@@ -1137,7 +1172,7 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_base = tmem + lane_base + kS8DCol + (g & 1) * 128;
+                const uint32_t d_base = tmem + lane_base + kS8DCol + e * 128;
                 // kGB blocks' accumulators (at most 64 registers) per tensor-memory wait
 #pragma unroll 1
                 for (int gb = 0; gb < kBS; gb += kGB) {
@@ -1152,7 +1187,7 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
                     if (gb + kGB == kBS) {  // the sub-stage's accumulators are all read
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&d_empty[g & 1]);
+                        if (lane == 0) mbar_arrive(&d_empty[e]);
                     }
 #pragma unroll
                     for (int bi = 0; bi < kGB; ++bi) {
@@ -1172,6 +1207,9 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
                 }
             }
             if (!ok) break;
+            // every epilogue warp releases every stage once it has read the stage's
+            // record and d values (kept even without a sub-stage of its own, so
+            // the slot is not refilled before both warps of a quarter read it)
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
 #pragma unroll
@@ -1182,10 +1220,41 @@ __global__ void __maxnreg__(128) mv_s8_kernel(const __grid_constant__ MvJob sing
                 acc[j] = sum;
             }
             if (m.flags & kLastOfTile) {
-                const int rr = m.row0 + row;
-                if (rr < m.n_rows)
+                const int t = n_tile_ends++;
+                if (e == 1) {
+                    // wait until warp 8+q has read the previous tile's sums
+                    const bool free_pair =
+                        t == 0 || mbar_wait(&tile_w0[qd], uint32_t(t - 1) & 1u, p.err, kTagS8Pair);
+                    if (!__all_sync(0xffffffffu, free_pair)) {
+                        s_abort = 1;
+                        break;
+                    }
 #pragma unroll
-                    for (int j = 0; j < NC; ++j) m.y[size_t(j) * m.n_rows + rr] = acc[j] + comp[j];
+                    for (int j = 0; j < NC; ++j) {
+                        s_pair[qd][lane][2 * j] = acc[j];
+                        s_pair[qd][lane][2 * j + 1] = comp[j];
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tile_w1[qd]);
+                } else {
+                    const bool have = mbar_wait(&tile_w1[qd], uint32_t(t) & 1u, p.err, kTagS8Pair);
+                    if (!__all_sync(0xffffffffu, have)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    const int rr = m.row0 + row;
+#pragma unroll
+                    for (int j = 0; j < NC; ++j) {
+                        const float o = s_pair[qd][lane][2 * j];
+                        const float sum = acc[j] + o;
+                        const float bb = sum - acc[j];
+                        const float err = (acc[j] - (sum - bb)) + (o - bb);
+                        const float yv = sum + (comp[j] + s_pair[qd][lane][2 * j + 1] + err);
+                        if (rr < m.n_rows) m.y[size_t(j) * m.n_rows + rr] = yv;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tile_w0[qd]);
+                }
 #pragma unroll
                 for (int j = 0; j < NC; ++j) acc[j] = comp[j] = 0.0f;
             }
@@ -1336,7 +1405,7 @@ cudaError_t launch_s8_nc(cudaLaunchConfig_t &cfg, const MvJob &single, const MvP
             if (dev < 64) g_s8_attr_done[dev][NC] = true;
         }
     }
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(s8_threads(NC));
     cfg.dynamicSmemBytes = s8_smem(NC);
     return cudaLaunchKernelEx(&cfg, mv_s8_kernel<NC>, single, prm);
 }

@@ -280,7 +280,7 @@ def _decode_step(dev, mats, seed, ncols):
     return ents, host
 
 
-@pytest.mark.parametrize("ncols", [1, 8])
+@pytest.mark.parametrize("ncols", [1, 2, 3, 4, 8])
 def test_plan_1p7b_decode_step_sampled(dev, ncols):
     """All 196 matrices of the 1.7B-class step; 24 sampled rows of each checked."""
     mats = synth.decode_step_1p7b()
