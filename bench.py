@@ -225,25 +225,26 @@ def run_ours(args):
     # ---- resident inputs -------------------------------------------------
     # Decode activations and outputs live in two contiguous buffers (one slice
     # per matrix), as a runtime would lay out a step's vectors.
-    dec = decode_inputs(1)
+    nc = args.ncols
+    dec = decode_inputs(nc)
     dec_bytes = sum(w.size for _, w, _ in dec)
     x_off, y_off, xo, yo = [], [], 0, 0
     for m, _, _ in dec:
         x_off.append(xo)
         y_off.append(yo)
-        xo += m.K
-        yo += m.N
+        xo += nc * m.K
+        yo += nc * m.N
     d_xall = torch.empty(xo, dtype=torch.float32, device=dev)
     d_yall = torch.empty(yo, dtype=torch.float32, device=dev)
     h_xall = torch.from_numpy(np.concatenate([x.reshape(-1) for _, _, x in dec]))
     d_xall.copy_(h_xall)
     d_dec = []
     for (m, w, _), xo_, yo_ in zip(dec, x_off, y_off):
-        d_dec.append((torch.from_numpy(w).to(dev), d_xall[xo_:xo_ + m.K].view(1, m.K),
-                      d_yall[yo_:yo_ + m.N].view(1, m.N), m.N, m.K))
+        d_dec.append((torch.from_numpy(w).to(dev), d_xall[xo_:xo_ + nc * m.K].view(nc, m.K),
+                      d_yall[yo_:yo_ + nc * m.N].view(nc, m.N), m.N, m.K))
     dec_x_bytes = d_xall.numel() * 4
     dec_y_bytes = d_yall.numel() * 4
-    plan = q.MvPlan(d_dec, 1) if args.only in ("all", "decode") else None
+    plan = q.MvPlan(d_dec, nc) if args.only in ("all", "decode") else None
 
     gm = gemm_inputs()
     d_gm = []
@@ -422,7 +423,8 @@ def run_ours(args):
             "dtype": "u8 weights (2-bit codes), f32 activations; tensor-core operands: decode "
                      "e2m1 (exact codes, 16 block-scaled activation pieces), GEMM fp16 hi+lo",
             "data": "synthetic (seeded; no trained weights)",
-            "config": {"workload": WORKLOAD, "ncols": 1, "decode_matrices": len(d_dec),
+            "config": {"workload": WORKLOAD if nc == 1 else WORKLOAD.replace("ncols=1", f"ncols={nc}"),
+                       "ncols": nc, "decode_matrices": len(d_dec),
                        "decode_weight_bytes": dec_bytes, "prefill_M": PREFILL_M,
                        "gemm_prec": "f16_split", "get_rows_ids": N_IDS,
                        "l2": "inputs larger than L2 (396 MB packed weights streamed per step)",
@@ -868,6 +870,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the side measurements (head mat-vec F32/F16, F16 GEMM)")
+    ap.add_argument("--ncols", type=int, default=1, choices=range(1, 9),
+                    help="activation columns of the decode step (the headline runs 1)")
     ap.add_argument("--only", choices=["all", "decode", "gemm", "get_rows"], default="all",
                     help="run one part of the step (for profiling); the JSON line is the "
                          "benchmark only with the default 'all'")
