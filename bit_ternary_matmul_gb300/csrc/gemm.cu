@@ -134,6 +134,7 @@ __device__ __forceinline__ float mul_pow2(float v, int e) {
 }
 
 constexpr int kPrepThreads = 128;
+constexpr int kPrepCache = 3;
 
 // One CTA per row: the row maximum by a block reduction, then the conversion.
 template <typename XT>
@@ -147,8 +148,20 @@ __global__ void __launch_bounds__(kPrepThreads) gemm_prep_kernel(
     const int tid = threadIdx.x, lane = tid & 31;
     const XT *xr = x + size_t(m) * K;
     const int groups = K / 16;
+    // the first kPrepCache groups of 16 per thread stay in registers between
+    // the maximum and the conversion (all of a row up to K = 6144)
+    float cache[kPrepCache][16];
     float amax = 0.0f;
-    for (int gi = tid; gi < groups; gi += kPrepThreads) {
+#pragma unroll
+    for (int c = 0; c < kPrepCache; ++c) {
+        const int gi = tid + c * kPrepThreads;
+        if (gi < groups) {
+            load16(xr + gi * 16, cache[c]);
+#pragma unroll
+            for (int t = 0; t < 16; ++t) amax = fmaxf(amax, fabsf(cache[c][t]));
+        }
+    }
+    for (int gi = tid + kPrepCache * kPrepThreads; gi < groups; gi += kPrepThreads) {
         float v[16];
         load16(xr + gi * 16, v);
 #pragma unroll
@@ -171,9 +184,7 @@ __global__ void __launch_bounds__(kPrepThreads) gemm_prep_kernel(
     if (tid == 0) row_shift[m] = sh;
     __half *hr = xh + size_t(m) * K;
     __half *lr = split ? xl + size_t(m) * K : nullptr;
-    for (int gi = tid; gi < groups; gi += kPrepThreads) {
-        float v[16];
-        load16(xr + gi * 16, v);
+    auto convert = [&](int gi, const float (&v)[16]) {
         uint32_t hw[8], lw[8];
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
@@ -193,6 +204,16 @@ __global__ void __launch_bounds__(kPrepThreads) gemm_prep_kernel(
             dl[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             dl[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
         }
+    };
+#pragma unroll
+    for (int c = 0; c < kPrepCache; ++c) {
+        const int gi = tid + c * kPrepThreads;
+        if (gi < groups) convert(gi, cache[c]);
+    }
+    for (int gi = tid + kPrepCache * kPrepThreads; gi < groups; gi += kPrepThreads) {
+        float v[16];
+        load16(xr + gi * 16, v);
+        convert(gi, v);
     }
 }
 
@@ -500,14 +521,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                 uint32_t v[32];
                 tmem_ld32(tmem_base + lane_addr + kAccCol + t * kBN + cb, v);
                 if (whole) {
-                    if (n < a.N) {
+                    // the 32 tokens' row exponents: one load per lane, shared by shuffles
+                    const int sh = m0 + cb + lane < a.M ? a.row_shift[m0 + cb + lane] : 0;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int m = m0 + cb + j;
-                            if (m < a.M)
-                                a.y[size_t(m) * a.N + n] =
-                                    mul_pow2(__uint_as_float(v[j]), -a.row_shift[m]);
-                        }
+                    for (int j = 0; j < 32; ++j) {
+                        const int shj = __shfl_sync(0xffffffffu, sh, j);
+                        const int m = m0 + cb + j;
+                        if (n < a.N && m < a.M)
+                            a.y[size_t(m) * a.N + n] = mul_pow2(__uint_as_float(v[j]), -shj);
                     }
                 } else {
 #pragma unroll
