@@ -283,6 +283,23 @@ int q2_0_mul_mat_vec_split(const void *w, const float *x, float *y, int64_t N, i
     return st != Q2_0_OK ? st : st2;
 }
 
+int q2_0_g128_mul_mat_vec(const void *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
+                         void *stream) {
+    if (!w || !x || !y || N < 1 || N > (int64_t(1) << 31) - 1 || K < 128 || K % 128 != 0 ||
+        K > (int64_t(1) << 30) || ncols < 1 || ncols > 8)
+        return Q2_0_EINVAL;
+    int st = check_device(nullptr);
+    if (st != Q2_0_OK) return st;
+    const size_t need = matvec_g128_workspace_bytes(K, ncols);
+    PoolScratch ws;
+    st = ws.alloc(need, as_stream(stream));
+    if (st != Q2_0_OK) return st;
+    st = matvec_g128_run(static_cast<const uint8_t *>(w), x, y, N, K, ncols, ws.ptr, need,
+                         as_stream(stream));
+    int st2 = ws.release();
+    return st != Q2_0_OK ? st : st2;
+}
+
 // Expert mat-vec shapes: n_expert * N rows must fit a tensor-map coordinate,
 // and the activation vectors a grid dimension.
 static bool valid_moe(int64_t n_expert, int64_t N, int64_t K, int64_t n_x, int64_t n_used,

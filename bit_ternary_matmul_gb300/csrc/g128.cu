@@ -9,12 +9,12 @@
 // then eight little-endian words, element 16w+i in bits 2i..2i+1 of word w,
 // code q -> (q - 1) * d.
 //
-// On GB300 the fast kernels are built around 18-byte blocks (TMA boxes of
-// 144-byte rows). A group-128 matrix is therefore repacked once, exactly, into
-// the 64-weight layout (each block becomes two blocks with the same scale, 36
-// bytes instead of 34), after which every fast path applies. get_rows reads the
-// 34-byte blocks directly (get_rows.cu), and a CUDA-core mat-vec serves callers
-// that keep the 128-weight packing.
+// The fast kernels read group-128 matrices in two ways: repacked once, exactly,
+// into the 64-weight layout (each block becomes two blocks with the same scale,
+// 36 bytes instead of 34), after which every fast path applies; or directly,
+// for the ncols = 1 mat-vec, by the fp4 tensor-core kernel of matvec.cu with
+// 272-byte stage boxes. get_rows reads the 34-byte blocks directly
+// (get_rows.cu), and a CUDA-core mat-vec serves the other shapes.
 #include "q2_0_device.cuh"
 #include "q2_0_internal.h"
 
@@ -87,6 +87,13 @@ __global__ void __launch_bounds__(256) g128_mv_kernel(const uint8_t *__restrict_
 inline bool valid_k128(int64_t K) { return K >= 128 && K % 128 == 0 && K <= (int64_t(1) << 30); }
 
 }  // namespace
+
+cudaError_t launch_g128_generic(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K,
+                                int ncols, cudaStream_t s) {
+    g128_mv_kernel<<<unsigned((N + 7) / 8), 256, 0, s>>>(w, x, y, int(N), int(K), ncols);
+    return cudaGetLastError();
+}
+
 }  // namespace q2
 
 using namespace q2;
@@ -119,18 +126,6 @@ int q2_0_g128_get_rows(const void *table, int64_t n_rows, int64_t K, const int32
     if (!err) return Q2_0_ECUDA;
     return cuda_status(launch_get_rows(static_cast<const uint8_t *>(table), n_rows, K, ids, n_ids,
                                        out, err, reinterpret_cast<cudaStream_t>(stream), 128));
-}
-
-int q2_0_g128_mul_mat_vec(const void *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
-                         void *stream) {
-    if (!w || !x || !y || N < 1 || N > (int64_t(1) << 31) - 1 || !valid_k128(K) || ncols < 1 ||
-        ncols > 8)
-        return Q2_0_EINVAL;
-    int st = check_device(nullptr);
-    if (st != Q2_0_OK) return st;
-    g128_mv_kernel<<<unsigned((N + 7) / 8), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint8_t *>(w), x, y, int(N), int(K), ncols);
-    return cuda_status(cudaGetLastError());
 }
 
 }  // extern "C"

@@ -114,7 +114,7 @@ struct MvParams {
     int ncols;
     unsigned long long *err;
     MvMoe moe;
-    int split;                // fp4 kernel only: 1 = the split layout (codes and scales apart)
+    int layout;               // fp4 kernel only: kLayBlocks, kLaySplit or kLayG128
     // fp4 kernel, test hook (q2_0_test_inject_stall): when stall_stage > 0 the
     // producers stop before stage stall_stage - 1, so the consumers' waits on it
     // run out after wait_ns (0: the default limit)
@@ -238,9 +238,46 @@ constexpr int kTagT4AFull = 113;
 constexpr int kTagT4DFull = 114;
 constexpr int kTagT4DEmpty = 115;
 
+// Weight layouts the fp4 kernel streams: 18-byte blocks of 64 weights, the
+// split layout (codes and scales in separate arrays), and group-128 (34-byte
+// blocks of 128 weights under one scale). A group-128 stage is 1024 weights of
+// a row: one 272-byte box per row (eight blocks), two 64-column A buffers, and
+// eight accumulator regions, one per 128-weight block, each the sum of two
+// K = 64 MMAs; the activations are scaled per 128 elements to match, so every
+// region is still exact. Every other quantity is the 64-weight layout's.
+constexpr int kLayBlocks = 0;
+constexpr int kLaySplit = 1;
+constexpr int kLayG128 = 2;
+constexpr int kG128Bytes = 34;
+constexpr int kG128RowBytes = kChunkBlocks * kG128Bytes;  // 272
+
+template <int L>
+struct T4Lay {
+    static constexpr int kStageK = L == kLayG128 ? 1024 : 512;  // weights of a row per stage
+    static constexpr int kAPer = kStageK / 512;                 // 64-column A buffers per stage
+    static constexpr int kRaw = L == kLayG128 ? kTcRows * kG128RowBytes : kRawBytes;
+    static constexpr int kImg = kT4N * kStageK / 2;             // e2m1 B image of a stage
+    static constexpr int kAct = kImg + kT4BetaBytes;            // image, then 8 region records
+    static constexpr int kActSlot = (kAct + 1023) / 1024 * 1024;
+    static constexpr int kStages = L == kLayG128 ? 4 : kT4Stages;
+    static constexpr int kBarriers = 2 * kStages + 2 * kT4ABufs + 2 * 2 + 2;
+    static constexpr int kSmem = 1024 /* alignment slack */ + kStages * (kActSlot + kRaw) +
+                                 kBarriers * 8;
+};
+static_assert(T4Lay<kLayBlocks>::kActSlot == kT4ActSlot && T4Lay<kLayBlocks>::kSmem == kT4Smem,
+              "the 64-weight layout keeps its stage geometry");
+static_assert(T4Lay<kLayG128>::kStages % 2 == 0 && T4Lay<kLayG128>::kSmem <= kSmemOptIn,
+              "group-128 ring: even depth (two producers), within the shared-memory limit");
+
 size_t t4_prep_bytes(int64_t K) {
     const size_t n_chunks = size_t(K / 512);
     size_t b = kPrepHeader + n_chunks * kT4ActBytes;
+    return (b + 255) & ~size_t(255);
+}
+
+size_t g4_prep_bytes(int64_t K) {
+    const size_t n_chunks = size_t(K / 1024);
+    size_t b = kPrepHeader + n_chunks * T4Lay<kLayG128>::kAct;
     return (b + 255) & ~size_t(255);
 }
 
@@ -256,7 +293,12 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int m, int n) {
 // nibble j). The 8 items of a block are 8 consecutive lanes: they share the
 // block maximum and sum the all-ones groups H, M, L by shuffles (every partial
 // sum is exact).
-template <typename XT>
+// kG128: blocks of 128 elements (the group-128 layout's scale blocks), 16 items
+// each; word c of block b falls in the 64-element half c / 4, which the image
+// holds as the K positions 64 (2 (b % 8) + c / 4) + 16 (c % 4) + 8h + j of the
+// 1024-element stage. The sums stay exact: 128 elements add one bit to every
+// group, which still spans fewer than 24 bits.
+template <typename XT, bool kG128>
 __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
     const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -269,18 +311,22 @@ __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
         J.x = static_cast<const uint8_t *>(single.x) + size_t(blockIdx.y) * single.x_stride;
         J.prep = single.prep + size_t(blockIdx.y) * single.prep_stride;
     }
+    using Lt = T4Lay<kG128 ? kLayG128 : kLayBlocks>;
+    constexpr int kBE = kG128 ? 128 : 64;  // elements per scale block
+    constexpr int kIPB = kBE / 8;          // items (lanes) per block
     const int K = J.K;
     const XT *xj = static_cast<const XT *>(J.x);
-    const int nb = K / 64;
+    const int nb = K / kBE;
     uint8_t *act = J.prep + kPrepHeader;  // per stage: image, then block records
     const int lane = threadIdx.x & 31;
-    const unsigned grp = 0xFFu << (lane & 24);  // the block's 8 threads
-    // 8 items per block and nb blocks: whole warps share a block range, so the
-    // shuffles below always run with all 8 lanes of a block present
-    for (int idx = int(blockIdx.z) * kPrepThreads + int(threadIdx.x); idx < nb * 8;
+    // the block's kIPB threads
+    const unsigned grp = kG128 ? 0xFFFFu << (lane & 16) : 0xFFu << (lane & 24);
+    // kIPB items per block and nb blocks: whole warps share a block range, so the
+    // shuffles below always run with all lanes of a block present
+    for (int idx = int(blockIdx.z) * kPrepThreads + int(threadIdx.x); idx < nb * kIPB;
          idx += int(gridDim.z) * kPrepThreads) {
-        const int b = idx >> 3, c = (idx >> 1) & 3, h = idx & 1;
-        const XT *xe = xj + b * 64 + c * 16 + h;
+        const int b = idx / kIPB, c = (idx >> 1) & (kIPB / 2 - 1), h = idx & 1;
+        const XT *xe = xj + b * kBE + c * 16 + h;
         float v[8];
         float m = 0.0f;
 #pragma unroll
@@ -289,15 +335,17 @@ __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
             m = fmaxf(m, fabsf(v[jj]));
         }
 #pragma unroll
-        for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(grp, m, o));
+        for (int o = 1; o < kIPB; o <<= 1) m = fmaxf(m, __shfl_xor_sync(grp, m, o));
         // v = x * 2^(2 - e), max |v| over the block in [2, 4); all-zero (or
         // non-finite) blocks keep e = 0
         int e = 0;
         if (m > 0.0f && m <= 3.402823466e38f) frexpf(m, &e);
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) v[jj] = mul_pow2(v[jj], 2 - e);
-        uint8_t *bimg = act + size_t(b >> 3) * kT4ActBytes;
-        const int kbyte = 32 * (b & 7) + 8 * c + 4 * h;  // byte of K position 64(b%8)+16c+8h
+        uint8_t *bimg = act + size_t(b >> 3) * Lt::kAct;
+        // byte of the item's first K position in the stage image
+        const int kbyte = kG128 ? 32 * (2 * (b & 7) + (c >> 2)) + 8 * (c & 3) + 4 * h
+                                : 32 * (b & 7) + 8 * c + 4 * h;
         float grp_sum[3] = {0.0f, 0.0f, 0.0f};  // this item's share of H, M, L
         // Rounding to the e2m1 grid without format conversions. With M = 2^23,
         // fma(|s|, 2, M) rounds 2|s| to the nearest integer (ties to even) and
@@ -341,9 +389,9 @@ __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
 #pragma unroll
         for (int gi = 0; gi < 3; ++gi)
 #pragma unroll
-            for (int o = 1; o < 8; o <<= 1) grp_sum[gi] += __shfl_xor_sync(grp, grp_sum[gi], o);
-        if ((idx & 7) == 0)
-            *reinterpret_cast<float4 *>(bimg + kT4ImgBytes + (b & 7) * kT4BlockRec * 4) =
+            for (int o = 1; o < kIPB; o <<= 1) grp_sum[gi] += __shfl_xor_sync(grp, grp_sum[gi], o);
+        if ((idx & (kIPB - 1)) == 0)
+            *reinterpret_cast<float4 *>(bimg + Lt::kImg + (b & 7) * kT4BlockRec * 4) =
                 make_float4(pow2f(e - 1), grp_sum[0], grp_sum[1], grp_sum[2]);
     }
 }
@@ -351,26 +399,32 @@ __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
 constexpr int kT4SplitCodeBytes = kTcRows * 128;  // 16 KB of codes, then 2 KB of scales
 static_assert(kT4SplitCodeBytes + kTcRows * 16 == kRawBytes, "split stage = block stage bytes");
 
-// kSplit: the weights are in the split layout (codes [N][K/64][16], scales
-// [N][K/64]); the stage's code box is 128 bytes x 128 rows with 128-byte swizzle
-// and its scale box 16 bytes x 128 rows, together the same 18 KB as the block
-// box of the 18-byte layout.
+// kLay: the weight layout. kLaySplit: codes [N][K/64][16] and scales [N][K/64];
+// the stage's code box is 128 bytes x 128 rows with 128-byte swizzle and its
+// scale box 16 bytes x 128 rows, together the same 18 KB as the block box of the
+// 18-byte layout. kLayG128: 34-byte blocks of 128; the stage's box is 272 bytes
+// (eight blocks) x 128 rows, read through a 16-bit view of the rows because a
+// box holds at most 256 elements a dimension.
 // At most 128 registers a thread (384 x 128 = 48K of the SM's 64K), so a CTA of
 // the next prep kernel (256 threads x 64 registers) can be resident beside it
 // and the programmatic launch overlaps the two.
-template <bool kSplit>
+template <int kLay>
 __global__ void __maxnreg__(128)
     mv_t4_kernel(const __grid_constant__ MvJob single, const MvParams p) {
+    using Lt = T4Lay<kLay>;
+    constexpr bool kSplit = kLay == kLaySplit;
+    constexpr bool kG = kLay == kLayG128;
+    constexpr int kRowBytes = kG ? kG128RowBytes : kChunkBytes;  // a row's bytes in a stage
     // The next prep launch on the stream may become resident now; it waits for
     // this grid before it touches any buffer this kernel reads.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    uint8_t *act_ring = smem;                                   // kT4Stages x 5 KB slots
-    uint8_t *raw_ring = act_ring + kT4Stages * kT4ActSlot;      // kT4Stages x 18 KB
-    uint64_t *full = reinterpret_cast<uint64_t *>(raw_ring + kT4Stages * kRawBytes);
-    uint64_t *empty = full + kT4Stages;
+    uint8_t *act_ring = smem;                                   // Lt::kStages activation slots
+    uint8_t *raw_ring = act_ring + Lt::kStages * Lt::kActSlot;  // Lt::kStages weight boxes
+    uint64_t *full = reinterpret_cast<uint64_t *>(raw_ring + Lt::kStages * Lt::kRaw);
+    uint64_t *empty = full + Lt::kStages;
     uint64_t *a_full = empty + kT4Stages;
     uint64_t *a_empty = a_full + kT4ABufs;
     uint64_t *d_full = a_empty + kT4ABufs;
@@ -380,14 +434,14 @@ __global__ void __maxnreg__(128)
     __shared__ int s_abort;
     // per ring slot, written by the producer before the slot's barrier arrive:
     // where the epilogue writes the tile that the stage belongs to
-    __shared__ StageMeta s_meta[kT4Stages];
+    __shared__ StageMeta s_meta[Lt::kStages];
 
     const uint64_t wl = p.wait_ns ? p.wait_ns : kWaitLimitNs;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kT4Stages; ++i) {
+        for (int i = 0; i < Lt::kStages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kEpiWarps);
         }
@@ -434,10 +488,11 @@ __global__ void __maxnreg__(128)
     };
     // stages of this CTA (every role but the producer runs a flat stage loop)
     const int n_stages = p.jobs ? p.cta_stages[blockIdx.x] : n_items * single.n_chunks;
-    auto stage_parity = [](int s) { return uint32_t(s / kT4Stages) & 1u; };
-    auto a_buf = [](int s) { return s % kT4ABufs; };
-    auto a_use = [](int s) { return uint32_t(s / kT4ABufs) & 1u; };
-    auto a_col = [](int s) { return uint32_t(kT4ACol + (s % kT4ABufs) * 64); };
+    auto stage_parity = [](int s) { return uint32_t(s / Lt::kStages) & 1u; };
+    // A buffers in order of use: unit u = s * Lt::kAPer + h is part h of stage s
+    auto a_buf = [](int u) { return u % kT4ABufs; };
+    auto a_use = [](int u) { return uint32_t(u / kT4ABufs) & 1u; };
+    auto a_col = [](int u) { return uint32_t(kT4ACol + (u % kT4ABufs) * 64); };
     auto d_col = [](int s) { return uint32_t((s & 1) * 128); };
 
     if (warp == kProdWarp || warp == kProdWarp2) {
@@ -479,7 +534,7 @@ __global__ void __maxnreg__(128)
                         ok = false;
                         break;
                     }
-                    const int st = s % kT4Stages;
+                    const int st = s % Lt::kStages;
                     if (!mbar_wait(&empty[st], stage_parity(s) ^ 1u, p.err, kTagT4Empty, true, wl) ||
                         *(volatile int *)&s_abort) {
                         ok = false;
@@ -491,29 +546,32 @@ __global__ void __maxnreg__(128)
                     m.row0 = tile * kTcRows;
                     m.n_rows = J->N;
                     m.flags = ch == nch - 1 ? kLastOfTile : 0;
-                    mbar_arrive_expect_tx(&full[st], kRawBytes + kT4ActBytes);
+                    mbar_arrive_expect_tx(&full[st], Lt::kRaw + Lt::kAct);
                     if (kSplit) {
-                        tma_load_2d(raw_ring + st * kRawBytes, &J->tmap, ch * 128,
+                        tma_load_2d(raw_ring + st * Lt::kRaw, &J->tmap, ch * 128,
                                     row_base + tile * kTcRows, &full[st]);
-                        tma_load_2d(raw_ring + st * kRawBytes + kT4SplitCodeBytes, &J->tmap_d,
+                        tma_load_2d(raw_ring + st * Lt::kRaw + kT4SplitCodeBytes, &J->tmap_d,
                                     ch * 16, row_base + tile * kTcRows, &full[st]);
+                    } else if (kG) {  // 16-bit elements: x = 136 ch (272 bytes, 16-aligned)
+                        tma_load_2d(raw_ring + st * Lt::kRaw, &J->tmap, ch * (kG128RowBytes / 2),
+                                    row_base + tile * kTcRows, &full[st]);
                     } else {
-                        tma_load_2d(raw_ring + st * kRawBytes, &J->tmap, ch * kChunkBytes,
+                        tma_load_2d(raw_ring + st * Lt::kRaw, &J->tmap, ch * kChunkBytes,
                                     row_base + tile * kTcRows, &full[st]);
                     }
                     if (!prep_ready) {
                         grid_dependency_wait();  // the B images come from the prep kernel
                         prep_ready = true;
                     }
-                    bulk_g2s(act_ring + st * kT4ActSlot, act + size_t(ch) * kT4ActBytes,
-                             kT4ActBytes, &full[st]);
+                    bulk_g2s(act_ring + st * Lt::kActSlot, act + size_t(ch) * Lt::kAct,
+                             Lt::kAct, &full[st]);
                     last = s;
                 }
             }
             if (!ok) {
                 // let this producer's copies in flight land (bounded) before the CTA exits
-                for (int t = last; t >= 0 && t > last - kT4Stages; t -= 2)
-                    mbar_wait(&full[t % kT4Stages], stage_parity(t), p.err, kTagT4Full, false, wl);
+                for (int t = last; t >= 0 && t > last - Lt::kStages; t -= 2)
+                    mbar_wait(&full[t % Lt::kStages], stage_parity(t), p.err, kTagT4Full, false, wl);
             }
         }
     } else if (warp == kMmaWarp || warp == kMmaWarp2) {
@@ -528,32 +586,49 @@ __global__ void __maxnreg__(128)
         int last = -1;
         {
             for (int s = mine; s < n_stages; s += 2) {
-                const int st = s % kT4Stages;
-                const bool got =
-                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full, false, wl) &&
-                    mbar_wait(&a_full[a_buf(s)], a_use(s), p.err, kTagT4AFull, false, wl) &&
-                    mbar_wait(&d_empty[s & 1], (uint32_t(s >> 1) & 1u) ^ 1u, p.err,
-                              kTagT4DEmpty, false, wl) &&
-                    !*(volatile int *)&s_abort;
-                if (!__all_sync(0xffffffffu, got)) {
+                const int st = s % Lt::kStages;
+                const uint32_t d_base = tmem + d_col(s);
+                const uint64_t dst = desc0 + uint64_t((st * Lt::kActSlot) >> 4);
+                bool ok = true;
+#pragma unroll
+                for (int h = 0; h < Lt::kAPer; ++h) {
+                    const int u = s * Lt::kAPer + h;
+                    const bool got =
+                        (h > 0 ||
+                         (mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full, false, wl) &&
+                          mbar_wait(&d_empty[s & 1], (uint32_t(s >> 1) & 1u) ^ 1u, p.err,
+                                    kTagT4DEmpty, false, wl))) &&
+                        mbar_wait(&a_full[a_buf(u)], a_use(u), p.err, kTagT4AFull, false, wl) &&
+                        !*(volatile int *)&s_abort;
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    last = s;
+                    const uint32_t a_base = tmem + a_col(u);
+                    if (leader) {
+                        // the A buffer's eight 64-element sub-blocks sb of the stage;
+                        // region = the block that owns d: sb itself, or for
+                        // group-128 block sb / 2 (its second half accumulates)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int sb = 8 * h + i;
+                            const int region = kG ? sb >> 1 : sb;
+                            tc_mma_mxf4_ta(d_base + region * kT4N, a_base + i * 8,
+                                           dst + uint64_t(((sb >> 2) * 2048 + (sb & 3) * 32) >> 4),
+                                           idesc, sfa, sfb, kG ? uint32_t(sb & 1) : 0u);
+                        }
+                        tc_commit(&a_empty[a_buf(u)]);
+                    }
+                    __syncwarp();
+                }
+                if (!ok) {
                     s_abort = 1;
                     break;
                 }
-                tc_fence_after();
-                const uint32_t a_base = tmem + a_col(s);
-                const uint32_t d_base = tmem + d_col(s);
-                const uint64_t dst = desc0 + uint64_t((st * kT4ActSlot) >> 4);
-                if (leader) {
-#pragma unroll
-                    for (int b = 0; b < kChunkBlocks; ++b)
-                        tc_mma_mxf4_ta(d_base + b * kT4N, a_base + b * 8,
-                                       dst + uint64_t(((b >> 2) * 2048 + (b & 3) * 32) >> 4), idesc,
-                                       sfa, sfb, 0u);
-                    tc_commit(&a_empty[a_buf(s)]);
-                    tc_commit(&d_full[s & 1]);
-                }
+                if (leader) tc_commit(&d_full[s & 1]);
                 __syncwarp();
-                last = s;
             }
         }
         // TMEM is freed only after this issuer's MMAs completed: one more commit
@@ -576,17 +651,55 @@ __global__ void __maxnreg__(128)
             tmem_st4(tmem + lane_base + kT4ScaleCol + 4, one, one, one, one);
         }
         {
-            for (int s = 0; s < n_stages; ++s) {
-                const int st = s % kT4Stages;
+            bool ok = true;
+            for (int s = 0; s < n_stages && ok; ++s) {
+                const int st = s % Lt::kStages;
+#pragma unroll 1
+                for (int h = 0; h < Lt::kAPer; ++h) {
+                const int u = s * Lt::kAPer + h;
                 const bool got =
-                    mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full, false, wl) &&
-                    mbar_wait(&a_empty[a_buf(s)], a_use(s) ^ 1u, p.err, kTagT4AFull, false, wl) &&
+                    (h > 0 || mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full, false, wl)) &&
+                    mbar_wait(&a_empty[a_buf(u)], a_use(u) ^ 1u, p.err, kTagT4AFull, false, wl) &&
                     !*(volatile int *)&s_abort;
                 if (!__all_sync(0xffffffffu, got)) {
                     s_abort = 1;
+                    ok = false;
                     break;
                 }
                 tc_fence_after();
+                if constexpr (kG) {
+                    // half h of the row's stage: blocks 4h .. 4h + 3 (136 bytes from an
+                    // 8-byte boundary); block bl's codes start 2 bytes into a word for
+                    // even bl and on a word boundary for odd bl
+                    const uint8_t *rp = raw_ring + st * Lt::kRaw + row * kG128RowBytes + h * 136;
+                    uint32_t w32[34];
+#pragma unroll
+                    for (int k = 0; k < 17; ++k) {
+                        const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * k);
+                        w32[2 * k] = v.x;
+                        w32[2 * k + 1] = v.y;
+                    }
+#pragma unroll
+                    for (int G = 0; G < 2; ++G) {
+                        uint32_t a[32];
+#pragma unroll
+                        for (int b2 = 0; b2 < 2; ++b2) {
+                            const int bl = 2 * G + b2;
+#pragma unroll
+                            for (int wi = 0; wi < 8; ++wi) {
+                                const uint32_t w =
+                                    (bl & 1) ? w32[(34 * bl + 2) / 4 + wi]
+                                             : __byte_perm(w32[34 * bl / 4 + wi],
+                                                           w32[34 * bl / 4 + wi + 1], 0x5432);
+                                // sub-block 2 b2 + wi / 4 of this store, word wi % 4
+                                const int o = 8 * (2 * b2 + (wi >> 2)) + 2 * (wi & 3);
+                                a[o] = w & 0x33333333u;
+                                a[o + 1] = (w >> 2) & 0x33333333u;
+                            }
+                        }
+                        tmem_st32(tmem + lane_base + a_col(u) + 32 * G, a);
+                    }
+                } else {
 #pragma unroll
                 for (int G = 0; G < 2; ++G) {
                     uint32_t a[32];
@@ -629,12 +742,14 @@ __global__ void __maxnreg__(128)
                             }
                         }
                     }
-                    tmem_st32(tmem + lane_base + a_col(s) + 32 * G, a);
+                    tmem_st32(tmem + lane_base + a_col(u) + 32 * G, a);
+                }
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[a_buf(s)]);
+                if (lane == 0) mbar_arrive(&a_full[a_buf(u)]);
+                }
             }
         }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
@@ -647,7 +762,7 @@ __global__ void __maxnreg__(128)
         const uint32_t lane_base = uint32_t(32 * qd) << 16;
         float acc = 0.0f, comp = 0.0f;  // compensated sum of the stage sums
         for (int s = 0; s < n_stages; ++s) {
-            const int st = s % kT4Stages;
+            const int st = s % Lt::kStages;
             const bool got = !*(volatile int *)&s_abort &&
                              mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full, false, wl) &&
                              mbar_wait(&d_full[s & 1], uint32_t(s >> 1) & 1u, p.err, kTagT4DFull, false, wl);
@@ -658,11 +773,11 @@ __global__ void __maxnreg__(128)
             tc_fence_after();
             const StageMeta m = s_meta[st];
             const uint32_t d_base = tmem + lane_base + d_col(s);
-            const uint8_t *rp = raw_ring + st * kRawBytes + row * kChunkBytes;
+            const uint8_t *rp = raw_ring + st * Lt::kRaw + row * kRowBytes;
             const float4 *brec =
-                reinterpret_cast<const float4 *>(act_ring + st * kT4ActSlot + kT4ImgBytes);
+                reinterpret_cast<const float4 *>(act_ring + st * Lt::kActSlot + Lt::kImg);
             float stage_sum = 0.0f;
-            // blocks 4 hb .. 4 hb + 3: their 16 pieces each (64 registers)
+            // regions (blocks of d) 4 hb .. 4 hb + 3: their 16 pieces each (64 registers)
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
                 uint32_t r[4][16];
@@ -689,9 +804,9 @@ __global__ void __maxnreg__(128)
                     const float4 br = brec[b];  // {2^(e - 1), H, M, L}
                     const float t = ((gh - br.y) + (gm - br.z)) + (gl - br.w);
                     const float d =
-                        kSplit ? lds_half_as_float(raw_ring + st * kRawBytes + kT4SplitCodeBytes +
+                        kSplit ? lds_half_as_float(raw_ring + st * Lt::kRaw + kT4SplitCodeBytes +
                                                    row * 16 + 2 * b)
-                               : lds_half_as_float(rp + 18 * b);
+                               : lds_half_as_float(rp + (kG ? kG128Bytes : 18) * b);
                     stage_sum = fmaf(d, t * br.x, stage_sum);
                 }
             }
@@ -1382,11 +1497,16 @@ cudaError_t ensure_t4_attr() {
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(g_attr_mu);
     if (dev < 64 && g_t4_attr_done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(mv_t4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kT4Smem);
+    e = cudaFuncSetAttribute(mv_t4_kernel<kLayBlocks>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             T4Lay<kLayBlocks>::kSmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(mv_t4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kT4Smem);
+        e = cudaFuncSetAttribute(mv_t4_kernel<kLaySplit>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 T4Lay<kLaySplit>::kSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mv_t4_kernel<kLayG128>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 T4Lay<kLayG128>::kSmem);
     if (e == cudaSuccess && dev < 64) g_t4_attr_done[dev] = true;
     return e;
 }
@@ -1434,7 +1554,7 @@ bool make_job(MvJob &J, const uint8_t *w, const uint8_t *prep, float *y, int64_t
 // max_k: the largest K among the jobs (sets the grid's z extent).
 template <typename XT>
 cudaError_t launch_prep_t(const MvPrepJob &single, const MvPrepJob *jobs, int n_jobs, int ncols,
-                          int64_t max_k, cudaStream_t s) {
+                          int64_t max_k, cudaStream_t s, bool g128) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1448,16 +1568,18 @@ cudaError_t launch_prep_t(const MvPrepJob &single, const MvPrepJob *jobs, int n_
         unsigned(std::min<int64_t>((items + kPrepThreads - 1) / kPrepThreads, 65535));
     if (use_t4(ncols)) {
         cfg.gridDim = dim3(1, n_jobs, z);
-        return cudaLaunchKernelEx(&cfg, t4_prep_kernel<XT>, single, jobs);
+        return g128 ? cudaLaunchKernelEx(&cfg, t4_prep_kernel<XT, true>, single, jobs)
+                    : cudaLaunchKernelEx(&cfg, t4_prep_kernel<XT, false>, single, jobs);
     }
     cfg.gridDim = dim3(ncols, n_jobs, z);
     return cudaLaunchKernelEx(&cfg, s8_prep_kernel<XT>, single, jobs, ncols);
 }
 
+// g128: the fp4 preparation in 128-element scale blocks (the group-128 layout)
 cudaError_t launch_prep(const MvPrepJob &single, const MvPrepJob *jobs, int n_jobs, int ncols,
-                        int64_t max_k, int xtype, cudaStream_t s) {
-    return xtype == kXF16 ? launch_prep_t<__half>(single, jobs, n_jobs, ncols, max_k, s)
-                          : launch_prep_t<float>(single, jobs, n_jobs, ncols, max_k, s);
+                        int64_t max_k, int xtype, cudaStream_t s, bool g128 = false) {
+    return xtype == kXF16 ? launch_prep_t<__half>(single, jobs, n_jobs, ncols, max_k, s, g128)
+                          : launch_prep_t<float>(single, jobs, n_jobs, ncols, max_k, s, g128);
 }
 
 // The tensor-core kernel is launched as a programmatic dependent of the prep
@@ -1477,11 +1599,18 @@ cudaError_t launch_tc(const MvJob &single, const MvParams &prm, int grid, cudaSt
         e = ensure_t4_attr();
         if (e != cudaSuccess) return e;
         cfg.blockDim = dim3(kTcThreads);
-        cfg.dynamicSmemBytes = kT4Smem;
         MvParams prm2 = prm;
         take_stall(prm2);
-        e = prm2.split ? cudaLaunchKernelEx(&cfg, mv_t4_kernel<true>, single, prm2)
-                       : cudaLaunchKernelEx(&cfg, mv_t4_kernel<false>, single, prm2);
+        if (prm2.layout == kLaySplit) {
+            cfg.dynamicSmemBytes = T4Lay<kLaySplit>::kSmem;
+            e = cudaLaunchKernelEx(&cfg, mv_t4_kernel<kLaySplit>, single, prm2);
+        } else if (prm2.layout == kLayG128) {
+            cfg.dynamicSmemBytes = T4Lay<kLayG128>::kSmem;
+            e = cudaLaunchKernelEx(&cfg, mv_t4_kernel<kLayG128>, single, prm2);
+        } else {
+            cfg.dynamicSmemBytes = T4Lay<kLayBlocks>::kSmem;
+            e = cudaLaunchKernelEx(&cfg, mv_t4_kernel<kLayBlocks>, single, prm2);
+        }
     } else {
         switch (prm.ncols) {
             case 2: e = launch_s8_nc<2>(cfg, single, prm); break;
@@ -1564,7 +1693,40 @@ int matvec_split_run(const uint8_t *soa, const float *x, float *y, int64_t N, in
     J.nb = int(nb);
     J.n_chunks = int(K / 512);
     J.n_tiles = int((N + kTcRows - 1) / kTcRows);
-    MvParams prm{nullptr, nullptr, nullptr, nullptr, 1, err, MvMoe{}, 1};
+    MvParams prm{nullptr, nullptr, nullptr, nullptr, 1, err, MvMoe{}, kLaySplit};
+    const int grid = std::max(1, std::min(J.n_tiles, sm_count()));
+    return cuda_status(launch_tc(J, prm, grid, s));
+}
+
+size_t matvec_g128_workspace_bytes(int64_t K, int ncols) {
+    return ncols == 1 && K % 1024 == 0 ? g4_prep_bytes(K) : 0;
+}
+
+int matvec_g128_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
+                    void *ws, size_t ws_bytes, cudaStream_t s) {
+    if (matvec_g128_workspace_bytes(K, ncols) == 0 || (reinterpret_cast<uintptr_t>(w) & 15u) != 0)
+        return cuda_status(launch_g128_generic(w, x, y, N, K, ncols, s));
+    if (ws_bytes < g4_prep_bytes(K)) return Q2_0_EINVAL;
+    unsigned long long *err = error_word_ptr();
+    if (!err) return Q2_0_ECUDA;
+    uint8_t *prep = static_cast<uint8_t *>(ws);
+    MvPrepJob pj{x, prep, int(K)};
+    if (launch_prep(pj, nullptr, 1, 1, K, kXF32, s, true) != cudaSuccess) return Q2_0_ECUDA;
+    MvJob J;
+    std::memset(&J, 0, sizeof(J));
+    // rows of K / 128 * 34 bytes seen as 16-bit elements: a box of 136 elements
+    // (one stage, 272 bytes) x 128 rows
+    const uint64_t row_bytes = uint64_t(K / 128) * kG128Bytes;
+    if (!encode_tmap_2d(&J.tmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, w, row_bytes / 2, uint64_t(N),
+                        row_bytes, kG128RowBytes / 2, kTcRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return Q2_0_ECUDA;
+    J.prep = prep;
+    J.y = y;
+    J.N = int(N);
+    J.nb = int(K / 128);
+    J.n_chunks = int(K / 1024);
+    J.n_tiles = int((N + kTcRows - 1) / kTcRows);
+    MvParams prm{nullptr, nullptr, nullptr, nullptr, 1, err, MvMoe{}, kLayG128};
     const int grid = std::max(1, std::min(J.n_tiles, sm_count()));
     return cuda_status(launch_tc(J, prm, grid, s));
 }

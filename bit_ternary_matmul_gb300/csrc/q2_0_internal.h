@@ -62,6 +62,15 @@ cudaError_t launch_soa_generic(const uint8_t *soa, const float *x, float *y, int
 int matvec_split_run(const uint8_t *soa, const float *x, float *y, int64_t N, int64_t K,
                      int ncols, void *ws, size_t ws_bytes, cudaStream_t s);
 
+// group-128 (34-byte blocks) mat-vec: ncols 1 with K % 1024 == 0 and w 16-byte
+// aligned on the fp4 kernel (scratch: matvec_g128_workspace_bytes(K, ncols),
+// 0 for the other shapes, which run on CUDA cores)
+cudaError_t launch_g128_generic(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K,
+                                int ncols, cudaStream_t s);
+size_t matvec_g128_workspace_bytes(int64_t K, int ncols);
+int matvec_g128_run(const uint8_t *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
+                    void *ws, size_t ws_bytes, cudaStream_t s);
+
 // expert mat-vec (mul_mat_id), F32 x: one fp4 prep region per activation vector
 size_t matvec_moe_workspace_bytes(int64_t K, int64_t n_xvec);
 int matvec_moe_run(const uint8_t *w, int64_t n_expert, int64_t N, int64_t K, const float *x,

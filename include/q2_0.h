@@ -301,9 +301,14 @@ int q2_0_g128_to_g64(const void *src, void *dst, int64_t nrows, int64_t K, void 
 int q2_0_g128_get_rows(const void *table, int64_t n_rows, int64_t K, const int32_t *ids,
                       int64_t n_ids, float *out, void *stream);
 
-/* q2_0_g128_mul_mat_vec — as q2_0_mul_mat_vec over a group-128 matrix, on CUDA
- * cores (for callers that keep the 128-weight packing; the repack plus
- * q2_0_mul_mat_vec is the fast route). Same error bound; no scratch. */
+/* q2_0_g128_mul_mat_vec — as q2_0_mul_mat_vec over a group-128 matrix, for
+ * callers that keep the 128-weight packing. ncols = 1 with K % 1024 == 0 and w
+ * 16-byte aligned runs the fp4 tensor-core kernel directly on the 34-byte
+ * blocks (one 272-byte box per row and 1024 weights; activations scaled per
+ * 128 elements), with scratch of 1024 + K/1024 * 8320 bytes (256-aligned) from
+ * the device's default memory pool on `stream`; its bound is the ncols = 1 one
+ * with M_b the largest |x| of the 128-element block. Other shapes run on CUDA
+ * cores (f32, the same error bound as the CUDA-core mat-vec) without scratch. */
 int q2_0_g128_mul_mat_vec(const void *w, const float *x, float *y, int64_t N, int64_t K, int ncols,
                          void *stream);
 

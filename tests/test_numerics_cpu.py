@@ -21,6 +21,7 @@ Nothing here is shared with the CUDA sources.
 from fractions import Fraction
 
 import numpy as np
+import pytest
 
 # e2m1 magnitudes with their mantissa bit (for ties to even)
 _E2M1 = [(0.0, 0), (0.5, 1), (1.0, 0), (1.5, 1), (2.0, 0), (3.0, 1), (4.0, 0), (6.0, 1)]
@@ -118,23 +119,26 @@ def _exact_groups(c):
             sum(Fraction(c[i]) * Fraction(4) ** -i for i in range(12, 16)))
 
 
-def test_block_groups_exact_and_zero_weights_cancel():
-    g = np.random.default_rng(2)
-    for trial in range(60):
-        x = g.standard_normal(64).astype(F32)
-        q = g.integers(0, 4, 64)
+@pytest.mark.parametrize("n", [64, 128])
+def test_block_groups_exact_and_zero_weights_cancel(n):
+    """Blocks of 64 (the 18-byte layout) and of 128 (the group-128 layout, whose
+    activations are scaled per 128 elements)."""
+    g = np.random.default_rng(2 + n)
+    for trial in range(60 if n == 64 else 30):
+        x = g.standard_normal(n).astype(F32)
+        q = g.integers(0, 4, n)
         if trial % 3 == 0:   # a large element under a zero weight
-            k = int(g.integers(0, 64))
+            k = int(g.integers(0, n))
             x[k] = F32(3000.0 * (1 if trial % 2 else -1))
             q[k] = 1
-            x[np.arange(64) != k] *= F32(1e-2)
+            x[np.arange(n) != k] *= F32(1e-2)
         e = block_scale(x)
         v = [float(F32(float(xx) * 2.0 ** (2 - e))) for xx in x]
-        P = np.array([split_pieces(vv)[0] for vv in v])          # [64][16]
+        P = np.array([split_pieces(vv)[0] for vv in v])          # [n][16]
         c = [sum((qq / 2.0) * P[k, i] for k, qq in enumerate(q)) for i in range(16)]
-        b = [sum(0.5 * P[k, i] for k in range(64)) for i in range(16)]
-        # each per-piece sum is an exact f32 (multiples of 1/4 below 2^9)
-        assert all(float(F32(ci)) == ci and abs(ci) < 512 for ci in c + b)
+        b = [sum(0.5 * P[k, i] for k in range(n)) for i in range(16)]
+        # each per-piece sum is an exact f32 (multiples of 1/4 below 2^9 or 2^10)
+        assert all(float(F32(ci)) == ci and abs(ci) < 8 * n for ci in c + b)
         gc, gb = _groups_f32(c), _groups_f32(b)
         ec, eb = _exact_groups(c), _exact_groups(b)
         assert all(Fraction(float(a)) == x_ for a, x_ in zip(gc, ec))

@@ -471,8 +471,12 @@ def test_g128_repack_then_fast_paths(dev):
     _no_device_error()
 
 
-@pytest.mark.parametrize("N,K,ncols", [(300, 1024, 1), (129, 2048, 3), (64, 128, 8), (5, 896, 2)])
+@pytest.mark.parametrize("N,K,ncols", [(300, 1024, 1), (129, 2048, 3), (64, 128, 8), (5, 896, 2),
+                                       (1000, 4096, 1), (257, 2048, 1), (2000, 6144, 1),
+                                       (77, 3072, 1)])
 def test_g128_matvec_direct(dev, N, K, ncols):
+    """ncols 1 with K % 1024 == 0 runs the fp4 tensor-core kernel on 272-byte
+    stage boxes (several tiles, ragged last tile); the rest the CUDA-core kernel."""
     g = synth.rng(4103, N, K, ncols)
     w = _g128_matrix(g, N, K)
     x = synth.activations(g, ncols, K, 0.001, 30.0)
@@ -693,6 +697,68 @@ def test_matvec_f16_wide_range(dev, ncols):
     y = q.q2_0_mul_mat_vec_f16(_to(dev, w), _to(dev, x16), N, K, ncols).cpu().numpy()
     yo, acc = oracle.matmul(w, N, K, x16.astype(np.float32))
     _assert_close(y, yo, acc, TOL_SPLIT, f"mat-vec f16 wide ncols={ncols}")
+    _no_device_error()
+
+
+@pytest.mark.parametrize("kind", wr.WIDE_KINDS)
+def test_g128_matvec_wide_range(dev, kind):
+    """The group-128 tensor-core path scales activations per 128 elements: small
+    elements beside large ones and large elements under zero weights."""
+    g = synth.rng(4104, wr.WIDE_KINDS.index(kind))
+    N, K = 300, 4096
+    w64, x = wr.wide_range_case(kind, g, N, K, 1)
+    w = wr.to_g128(w64, N, K)
+    y = q.q2_0_g128_mul_mat_vec(_to(dev, w), _to(dev, x), N, K, 1).cpu().numpy()
+    yo, acc = oracle.matmul_g128(w, N, K, x)
+    _assert_close(y, yo, acc, TOL_SPLIT, f"g128 mat-vec {kind}")
+    _no_device_error()
+
+
+def test_g128_matvec_edge_blocks(dev):
+    """Blocks with d = +-0, a subnormal d, all code 3 and d = 65504 on the
+    group-128 tensor-core path."""
+    g = synth.rng(4105)
+    N, K = 260, 2048
+    w = _g128_matrix(g, N, K)
+    wb = w.reshape(N, K // 128, 34)
+    for r in range(0, N, 5):
+        b = r % (K // 128)
+        kind = (r // 5) % 4
+        if kind == 0:
+            wb[r, b, :2] = [0x00, 0x80]       # -0
+        elif kind == 1:
+            wb[r, b, :2] = [0x01, 0x00]       # smallest subnormal
+        elif kind == 2:
+            wb[r, b, 2:] = 0xFF               # all code 3
+        else:
+            wb[r, b, :2] = [0xFF, 0x7B]       # 65504
+            wb[r, b, 2:] = 0x24               # codes 0, 1, 2, 0
+    x = synth.activations(g, 1, K, 0.001, 30.0)
+    y = q.q2_0_g128_mul_mat_vec(_to(dev, w), _to(dev, x), N, K, 1).cpu().numpy()
+    yo, acc = oracle.matmul_g128(w, N, K, x)
+    assert np.all(np.isfinite(y))
+    _assert_close(y, yo, acc, TOL_SPLIT, "g128 mat-vec edge blocks")
+    _no_device_error()
+
+
+def test_g128_matvec_head_sampled(dev):
+    """A 151936 x 4096 group-128 head on the tensor-core path, checked on 512
+    sampled rows (first, last, tile edges and random ones)."""
+    g = synth.rng(4106)
+    N, K = 151936, 4096
+    nb = K // 128
+    wb = np.empty((N, nb, 34), dtype=np.uint8)   # uniform codes 0..3 (byte draws)
+    wb[:, :, 2:] = g.integers(0, 256, size=(N, nb, 32), dtype=np.uint8)
+    d = g.uniform(0.005, 0.05, size=(N, nb)).astype(np.float16).view(np.uint16)
+    wb[:, :, 0] = d & 0xFF
+    wb[:, :, 1] = d >> 8
+    w = wb.reshape(-1)
+    x = synth.activations(g, 1, K, 0.001, 30.0)
+    y = q.q2_0_g128_mul_mat_vec(_to(dev, w), _to(dev, x), N, K, 1).cpu().numpy()
+    rows = np.unique(np.concatenate([[0, 127, 128, N - 129, N - 128, N - 1],
+                                     g.integers(0, N, 506)])).astype(np.int64)
+    yo, acc = oracle.matmul_g128(w, N, K, x, rows=rows)
+    _assert_close(y[:, rows], yo, acc, TOL_SPLIT, "g128 head sampled rows")
     _no_device_error()
 
 

@@ -82,3 +82,16 @@ def wide_range_case(kind, g, N, K, ncols):
 
 
 WIDE_KINDS = ["const_outliers", "normal_outliers", "block_outliers", "mixed_scales"]
+
+
+def to_g128(w, N, K):
+    """The same codes in the group-128 packing: blocks 2i and 2i+1 of a row
+    (18 bytes each) become one 34-byte block with block 2i's scale and the two
+    blocks' code bytes in order. The weights of odd blocks change scale with it;
+    the oracle reads the group-128 bytes, so both sides see the same matrix."""
+    b = w.reshape(N, K // 128, 2, 18)
+    out = np.empty((N, K // 128, 34), dtype=np.uint8)
+    out[:, :, 0:2] = b[:, :, 0, 0:2]
+    out[:, :, 2:18] = b[:, :, 0, 2:18]
+    out[:, :, 18:34] = b[:, :, 1, 2:18]
+    return out.reshape(-1)
