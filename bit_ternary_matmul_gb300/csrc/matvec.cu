@@ -106,11 +106,20 @@ struct MvMoe {
     long long prep_stride;  // bytes between consecutive activation vectors' prep
 };
 
+// A plan CTA's share of the schedule in one record, so that a CTA learns its
+// work and its first item with a single load.
+struct MvFirst {
+    int item_base;  // the CTA's first entry in items
+    int n_items;
+    int n_stages;   // stages (512-column chunks) of its items
+    int job0;       // its first item
+    int tile0;
+};
+
 struct MvParams {
     const MvJob *jobs;        // nullptr: the single job passed by value
     const MvItem *items;      // per-CTA work lists (schedule), when jobs != nullptr
-    const int *cta_begin;     // [gridDim.x + 1]
-    const int *cta_stages;    // [gridDim.x] stages (512-column chunks) per CTA, plan only
+    const MvFirst *first;     // [gridDim.x] each CTA's share of the schedule, plan only
     int ncols;
     unsigned long long *err;
     MvMoe moe;
@@ -439,6 +448,10 @@ __global__ void __maxnreg__(128)
     const uint64_t wl = p.wait_ns ? p.wait_ns : kWaitLimitNs;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // a plan CTA's share of the schedule (one load); the first item's tensor map early
+    const MvFirst fst = p.jobs ? p.first[blockIdx.x] : MvFirst{};
+    if (warp == kProdWarp && lane == 0 && p.jobs && fst.n_items > 0)
+        prefetch_tensormap(&p.jobs[fst.job0].tmap);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < Lt::kStages; ++i) {
@@ -468,8 +481,8 @@ __global__ void __maxnreg__(128)
 
     int n_items, item_base = 0;
     if (p.jobs) {
-        item_base = p.cta_begin[blockIdx.x];
-        n_items = p.cta_begin[blockIdx.x + 1] - item_base;
+        item_base = fst.item_base;
+        n_items = fst.n_items;
     } else {
         // one matrix: its tiles; expert mat-vec: (output vector, tile) pairs
         const int total = p.moe.ids ? p.moe.n_vec * single.n_tiles : single.n_tiles;
@@ -478,16 +491,21 @@ __global__ void __maxnreg__(128)
     }
     auto item_at = [&](int i, const MvJob *&J, int &tile) {
         if (p.jobs) {
-            const MvItem it = p.items[item_base + i];
-            J = &p.jobs[it.job];
-            tile = it.tile;
+            if (i == 0) {  // from the CTA's record
+                J = &p.jobs[fst.job0];
+                tile = fst.tile0;
+            } else {
+                const MvItem it = p.items[item_base + i];
+                J = &p.jobs[it.job];
+                tile = it.tile;
+            }
         } else {
             J = &single;
             tile = int(blockIdx.x) + i * int(gridDim.x);
         }
     };
     // stages of this CTA (every role but the producer runs a flat stage loop)
-    const int n_stages = p.jobs ? p.cta_stages[blockIdx.x] : n_items * single.n_chunks;
+    const int n_stages = p.jobs ? fst.n_stages : n_items * single.n_chunks;
     auto stage_parity = [](int s) { return uint32_t(s / Lt::kStages) & 1u; };
     // A buffers in order of use: unit u = s * Lt::kAPer + h is part h of stage s
     auto a_buf = [](int u) { return u % kT4ABufs; };
@@ -1036,6 +1054,10 @@ __global__ void __launch_bounds__(s8_threads(NC), 1) mv_s8_kernel(const __grid_c
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // a plan CTA's share of the schedule (one load); the first item's tensor map early
+    const MvFirst fst = p.jobs ? p.first[blockIdx.x] : MvFirst{};
+    if (warp == kProdWarp && lane == 0 && p.jobs && fst.n_items > 0)
+        prefetch_tensormap(&p.jobs[fst.job0].tmap);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -1067,8 +1089,8 @@ __global__ void __launch_bounds__(s8_threads(NC), 1) mv_s8_kernel(const __grid_c
 
     int n_items, item_base = 0;
     if (p.jobs) {
-        item_base = p.cta_begin[blockIdx.x];
-        n_items = p.cta_begin[blockIdx.x + 1] - item_base;
+        item_base = fst.item_base;
+        n_items = fst.n_items;
     } else {
         n_items = blockIdx.x < unsigned(single.n_tiles)
                       ? (single.n_tiles - 1 - int(blockIdx.x)) / int(gridDim.x) + 1
@@ -1076,15 +1098,20 @@ __global__ void __launch_bounds__(s8_threads(NC), 1) mv_s8_kernel(const __grid_c
     }
     auto item_at = [&](int i, const MvJob *&J, int &tile) {
         if (p.jobs) {
-            const MvItem it = p.items[item_base + i];
-            J = &p.jobs[it.job];
-            tile = it.tile;
+            if (i == 0) {  // from the CTA's record
+                J = &p.jobs[fst.job0];
+                tile = fst.tile0;
+            } else {
+                const MvItem it = p.items[item_base + i];
+                J = &p.jobs[it.job];
+                tile = it.tile;
+            }
         } else {
             J = &single;
             tile = int(blockIdx.x) + i * int(gridDim.x);
         }
     };
-    const int n_stages = p.jobs ? p.cta_stages[blockIdx.x] : n_items * single.n_chunks;
+    const int n_stages = p.jobs ? fst.n_stages : n_items * single.n_chunks;
     auto stage_parity = [](int s) { return uint32_t(s / kStages) & 1u; };
 
     if (warp == kProdWarp || warp == kProdWarp2) {
@@ -1661,7 +1688,7 @@ int matvec_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, 
     if (e != cudaSuccess) return Q2_0_ECUDA;
     MvJob J;
     if (!make_job(J, w, prep, y, N, K)) return Q2_0_ECUDA;
-    MvParams prm{nullptr, nullptr, nullptr, nullptr, ncols, err};
+    MvParams prm{nullptr, nullptr, nullptr, ncols, err};
     const int grid = std::max(1, std::min(J.n_tiles, sm_count()));
     return cuda_status(launch_tc(J, prm, grid, s));
 }
@@ -1693,7 +1720,7 @@ int matvec_split_run(const uint8_t *soa, const float *x, float *y, int64_t N, in
     J.nb = int(nb);
     J.n_chunks = int(K / 512);
     J.n_tiles = int((N + kTcRows - 1) / kTcRows);
-    MvParams prm{nullptr, nullptr, nullptr, nullptr, 1, err, MvMoe{}, kLaySplit};
+    MvParams prm{nullptr, nullptr, nullptr, 1, err, MvMoe{}, kLaySplit};
     const int grid = std::max(1, std::min(J.n_tiles, sm_count()));
     return cuda_status(launch_tc(J, prm, grid, s));
 }
@@ -1726,7 +1753,7 @@ int matvec_g128_run(const uint8_t *w, const float *x, float *y, int64_t N, int64
     J.nb = int(K / 128);
     J.n_chunks = int(K / 1024);
     J.n_tiles = int((N + kTcRows - 1) / kTcRows);
-    MvParams prm{nullptr, nullptr, nullptr, nullptr, 1, err, MvMoe{}, kLayG128};
+    MvParams prm{nullptr, nullptr, nullptr, 1, err, MvMoe{}, kLayG128};
     const int grid = std::max(1, std::min(J.n_tiles, sm_count()));
     return cuda_status(launch_tc(J, prm, grid, s));
 }
@@ -1759,7 +1786,7 @@ int matvec_moe_run(const uint8_t *w, int64_t n_expert, int64_t N, int64_t K, con
     if (!make_job(J, w, prep, y, n_expert * N, K)) return Q2_0_ECUDA;
     J.N = int(N);
     J.n_tiles = int((N + kTcRows - 1) / kTcRows);
-    MvParams prm{nullptr, nullptr, nullptr, nullptr, 1, err,
+    MvParams prm{nullptr, nullptr, nullptr, 1, err,
                  MvMoe{ids, int(n_vec), int(n_used), int(n_x), int(n_expert), stride}};
     const int64_t items = n_vec * J.n_tiles;
     const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items, sm_count())));
@@ -1779,8 +1806,7 @@ struct q2_0_mv_plan {
     int64_t max_k = 0;  // largest K among the TMA-path jobs
     q2::MvJob *d_jobs = nullptr;
     q2::MvItem *d_items = nullptr;
-    int *d_cta_begin = nullptr;
-    int *d_cta_stages = nullptr;  // [grid] stages (512-column chunks) per CTA
+    q2::MvFirst *d_first = nullptr;  // [grid] each CTA's share of the schedule
     q2::MvPrepJob *d_prep_jobs = nullptr;
     uint8_t *d_prep = nullptr;
     unsigned long long *err = nullptr;
@@ -1796,8 +1822,7 @@ void mv_plan_destroy(q2_0_mv_plan *plan) {
     cudaSetDevice(plan->device);
     cudaFree(plan->d_jobs);
     cudaFree(plan->d_items);
-    cudaFree(plan->d_cta_begin);
-    cudaFree(plan->d_cta_stages);
+    cudaFree(plan->d_first);
     cudaFree(plan->d_prep_jobs);
     cudaFree(plan->d_prep);
     cudaSetDevice(cur);
@@ -1912,11 +1937,21 @@ int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **o
         }
         begin[grid] = int(flat.size());
         P->grid = grid;
+        std::vector<MvFirst> first(grid, MvFirst{});
+        for (int c = 0; c < grid; ++c) {
+            MvFirst &f = first[c];
+            f.item_base = begin[c];
+            f.n_items = begin[c + 1] - begin[c];
+            f.n_stages = stages[c];
+            if (f.n_items > 0) {
+                f.job0 = flat[begin[c]].job;
+                f.tile0 = flat[begin[c]].tile;
+            }
+        }
         if (st == Q2_0_OK &&
             (cudaMalloc(&P->d_jobs, sizeof(MvJob) * jobs.size()) != cudaSuccess ||
              cudaMalloc(&P->d_items, sizeof(MvItem) * flat.size()) != cudaSuccess ||
-             cudaMalloc(&P->d_cta_begin, sizeof(int) * begin.size()) != cudaSuccess ||
-             cudaMalloc(&P->d_cta_stages, sizeof(int) * stages.size()) != cudaSuccess ||
+             cudaMalloc(&P->d_first, sizeof(MvFirst) * first.size()) != cudaSuccess ||
              cudaMalloc(&P->d_prep_jobs, sizeof(MvPrepJob) * pjobs.size()) != cudaSuccess))
             st = Q2_0_ECUDA;
         if (st == Q2_0_OK &&
@@ -1924,9 +1959,7 @@ int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **o
                         cudaMemcpyHostToDevice) != cudaSuccess ||
              cudaMemcpy(P->d_items, flat.data(), sizeof(MvItem) * flat.size(),
                         cudaMemcpyHostToDevice) != cudaSuccess ||
-             cudaMemcpy(P->d_cta_begin, begin.data(), sizeof(int) * begin.size(),
-                        cudaMemcpyHostToDevice) != cudaSuccess ||
-             cudaMemcpy(P->d_cta_stages, stages.data(), sizeof(int) * stages.size(),
+             cudaMemcpy(P->d_first, first.data(), sizeof(MvFirst) * first.size(),
                         cudaMemcpyHostToDevice) != cudaSuccess ||
              cudaMemcpy(P->d_prep_jobs, pjobs.data(), sizeof(MvPrepJob) * pjobs.size(),
                         cudaMemcpyHostToDevice) != cudaSuccess))
@@ -1954,7 +1987,7 @@ int mv_plan_execute(const q2_0_mv_plan *P, cudaStream_t s) {
             return Q2_0_ECUDA;
         MvJob dummy;
         std::memset(&dummy, 0, sizeof(dummy));
-        MvParams prm{P->d_jobs, P->d_items, P->d_cta_begin, P->d_cta_stages, P->ncols, P->err};
+        MvParams prm{P->d_jobs, P->d_items, P->d_first, P->ncols, P->err};
         if (launch_tc(dummy, prm, P->grid, s) != cudaSuccess) return Q2_0_ECUDA;
     }
     for (const q2_0_mv_desc &d : P->generic)
