@@ -309,13 +309,18 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int m, int n) {
 // group, which still spans fewer than 24 bits.
 template <typename XT, bool kG128>
 __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
-    const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs) {
+    const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs,
+    const int2 *__restrict__ ctas) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // Launched as a programmatic dependent of the kernel before it on the stream
     // (a mat-vec that may still read this buffer, or the producer of x): wait
     // for that grid before reading x or writing the prep buffer.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    MvPrepJob J = jobs ? jobs[blockIdx.y] : single;
+    // a plan's CTA list: CTA y takes items ctas[y].y .. +127 of job ctas[y].x
+    const int2 cta = ctas ? ctas[blockIdx.y] : make_int2(int(blockIdx.y), 0);
+    const int idx0 = ctas ? cta.y : int(blockIdx.z) * kPrepThreads;
+    const int idx_step = ctas ? (1 << 30) : int(gridDim.z) * kPrepThreads;
+    MvPrepJob J = jobs ? jobs[cta.x] : single;
     if (!jobs) {  // a strided batch of vectors, one per grid row
         J.x = static_cast<const uint8_t *>(single.x) + size_t(blockIdx.y) * single.x_stride;
         J.prep = single.prep + size_t(blockIdx.y) * single.prep_stride;
@@ -332,8 +337,7 @@ __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
     const unsigned grp = kG128 ? 0xFFFFu << (lane & 16) : 0xFFu << (lane & 24);
     // kIPB items per block and nb blocks: whole warps share a block range, so the
     // shuffles below always run with all lanes of a block present
-    for (int idx = int(blockIdx.z) * kPrepThreads + int(threadIdx.x); idx < nb * kIPB;
-         idx += int(gridDim.z) * kPrepThreads) {
+    for (int idx = idx0 + int(threadIdx.x); idx < nb * kIPB; idx += idx_step) {
         const int b = idx / kIPB, c = (idx >> 1) & (kIPB / 2 - 1), h = idx & 1;
         const XT *xe = xj + b * kBE + c * 16 + h;
         float v[8];
@@ -955,13 +959,18 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n) {
 // block maximum by shuffles.
 template <typename XT>
 __global__ void __launch_bounds__(kPrepThreads) s8_prep_kernel(
-    const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs, int ncols) {
+    const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs,
+    const int2 *__restrict__ ctas, int ncols) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // Launched as a programmatic dependent of the kernel before it on the stream
     // (a mat-vec that may still read this buffer, or the producer of x): wait
     // for that grid before reading x or writing the prep buffer.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const MvPrepJob &J = jobs ? jobs[blockIdx.y] : single;
+    // a plan's CTA list: CTA (j, y) takes items ctas[y].y .. +127 of job ctas[y].x
+    const int2 cta = ctas ? ctas[blockIdx.y] : make_int2(int(blockIdx.y), 0);
+    const int idx0 = ctas ? cta.y : int(blockIdx.z) * kPrepThreads;
+    const int idx_step = ctas ? (1 << 30) : int(gridDim.z) * kPrepThreads;
+    const MvPrepJob &J = jobs ? jobs[cta.x] : single;
     const int K = J.K;
     const int j = blockIdx.x;
     const XT *xj = static_cast<const XT *>(J.x) + size_t(j) * K;
@@ -972,8 +981,7 @@ __global__ void __launch_bounds__(kPrepThreads) s8_prep_kernel(
     const unsigned grp = 0xFFFFu << (lane & 16);  // the block's 16 threads
     // 16 items per block: whole half-warps share a block, so the shuffles below
     // always run with all 16 lanes of a block present
-    for (int idx = int(blockIdx.z) * kPrepThreads + int(threadIdx.x); idx < nb * 16;
-         idx += int(gridDim.z) * kPrepThreads) {
+    for (int idx = idx0 + int(threadIdx.x); idx < nb * 16; idx += idx_step) {
         const int b = idx >> 4, c = (idx >> 2) & 3, r = idx & 3;
         const XT *xe = xj + b * 64 + 16 * c + 8 * (r >> 1) + (r & 1);
         float v[4];
@@ -1579,9 +1587,12 @@ bool make_job(MvJob &J, const uint8_t *w, const uint8_t *prep, float *y, int64_t
 // them on the stream: their launch overlaps that kernel's tail, and they wait
 // for it (griddepcontrol.wait) before reading x or writing their buffers.
 // max_k: the largest K among the jobs (sets the grid's z extent).
+// ctas (plans): n_ctas entries (job, first item), 128 items each, instead of the
+// grid (.., n_jobs, z) sized by the largest K.
 template <typename XT>
 cudaError_t launch_prep_t(const MvPrepJob &single, const MvPrepJob *jobs, int n_jobs, int ncols,
-                          int64_t max_k, cudaStream_t s, bool g128) {
+                          int64_t max_k, cudaStream_t s, bool g128, const int2 *ctas,
+                          int n_ctas) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1592,21 +1603,24 @@ cudaError_t launch_prep_t(const MvPrepJob &single, const MvPrepJob *jobs, int n_
     cfg.blockDim = dim3(kPrepThreads);
     const int64_t items = max_k / 64 * (use_t4(ncols) ? 8 : 16);
     const unsigned z =
-        unsigned(std::min<int64_t>((items + kPrepThreads - 1) / kPrepThreads, 65535));
+        ctas ? 1u : unsigned(std::min<int64_t>((items + kPrepThreads - 1) / kPrepThreads, 65535));
+    const unsigned gy = unsigned(ctas ? n_ctas : n_jobs);
     if (use_t4(ncols)) {
-        cfg.gridDim = dim3(1, n_jobs, z);
-        return g128 ? cudaLaunchKernelEx(&cfg, t4_prep_kernel<XT, true>, single, jobs)
-                    : cudaLaunchKernelEx(&cfg, t4_prep_kernel<XT, false>, single, jobs);
+        cfg.gridDim = dim3(1, gy, z);
+        return g128 ? cudaLaunchKernelEx(&cfg, t4_prep_kernel<XT, true>, single, jobs, ctas)
+                    : cudaLaunchKernelEx(&cfg, t4_prep_kernel<XT, false>, single, jobs, ctas);
     }
-    cfg.gridDim = dim3(ncols, n_jobs, z);
-    return cudaLaunchKernelEx(&cfg, s8_prep_kernel<XT>, single, jobs, ncols);
+    cfg.gridDim = dim3(ncols, gy, z);
+    return cudaLaunchKernelEx(&cfg, s8_prep_kernel<XT>, single, jobs, ctas, ncols);
 }
 
 // g128: the fp4 preparation in 128-element scale blocks (the group-128 layout)
 cudaError_t launch_prep(const MvPrepJob &single, const MvPrepJob *jobs, int n_jobs, int ncols,
-                        int64_t max_k, int xtype, cudaStream_t s, bool g128 = false) {
-    return xtype == kXF16 ? launch_prep_t<__half>(single, jobs, n_jobs, ncols, max_k, s, g128)
-                          : launch_prep_t<float>(single, jobs, n_jobs, ncols, max_k, s, g128);
+                        int64_t max_k, int xtype, cudaStream_t s, bool g128 = false,
+                        const int2 *ctas = nullptr, int n_ctas = 0) {
+    return xtype == kXF16
+               ? launch_prep_t<__half>(single, jobs, n_jobs, ncols, max_k, s, g128, ctas, n_ctas)
+               : launch_prep_t<float>(single, jobs, n_jobs, ncols, max_k, s, g128, ctas, n_ctas);
 }
 
 // The tensor-core kernel is launched as a programmatic dependent of the prep
@@ -1808,6 +1822,8 @@ struct q2_0_mv_plan {
     q2::MvItem *d_items = nullptr;
     q2::MvFirst *d_first = nullptr;  // [grid] each CTA's share of the schedule
     q2::MvPrepJob *d_prep_jobs = nullptr;
+    int2 *d_prep_ctas = nullptr;  // the prep kernel's CTAs: (job, first item)
+    int n_prep_ctas = 0;
     uint8_t *d_prep = nullptr;
     unsigned long long *err = nullptr;
     std::vector<q2_0_mv_desc> generic;  // descriptors outside the TMA path
@@ -1824,6 +1840,7 @@ void mv_plan_destroy(q2_0_mv_plan *plan) {
     cudaFree(plan->d_items);
     cudaFree(plan->d_first);
     cudaFree(plan->d_prep_jobs);
+    cudaFree(plan->d_prep_ctas);
     cudaFree(plan->d_prep);
     cudaSetDevice(cur);
     delete plan;
@@ -1866,6 +1883,19 @@ int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **o
             pjobs[j] = MvPrepJob{d.x, P->d_prep + off[j], int(d.K)};
             P->max_k = std::max<int64_t>(P->max_k, d.K);
         }
+        // the prep kernel's CTAs: 128 items (fp4: 8 elements, e4m3: 4 elements
+        // of one column) of one job each, so that no CTA of a short row idles
+        std::vector<int2> pctas;
+        for (int j = 0; j < P->n_fast; ++j) {
+            const int64_t n_it = use_t4(ncols) ? descs[fast[j]].K / 8 : descs[fast[j]].K / 4;
+            for (int64_t i0 = 0; i0 < n_it; i0 += kPrepThreads) pctas.push_back(make_int2(j, int(i0)));
+        }
+        P->n_prep_ctas = int(pctas.size());
+        if (st == Q2_0_OK && (pctas.size() > 65535 ||
+                              cudaMalloc(&P->d_prep_ctas, sizeof(int2) * pctas.size()) != cudaSuccess ||
+                              cudaMemcpy(P->d_prep_ctas, pctas.data(), sizeof(int2) * pctas.size(),
+                                         cudaMemcpyHostToDevice) != cudaSuccess))
+            st = pctas.size() > 65535 ? Q2_0_EINVAL : Q2_0_ECUDA;
         // Schedule of (job, tile) items over one CTA per SM. A tile costs its
         // stage count (K / 512): the pipeline takes the same time per stage
         // whatever the tile's valid rows. Longest-processing-time-first, then
@@ -1982,8 +2012,8 @@ int mv_plan_execute(const q2_0_mv_plan *P, cudaStream_t s) {
     if (cudaGetDevice(&cur) != cudaSuccess || cur != P->device) return Q2_0_EINVAL;
     if (P->n_fast > 0) {
         MvPrepJob none{nullptr, nullptr, 0};
-        if (launch_prep(none, P->d_prep_jobs, P->n_fast, P->ncols, P->max_k, kXF32, s) !=
-            cudaSuccess)
+        if (launch_prep(none, P->d_prep_jobs, P->n_fast, P->ncols, P->max_k, kXF32, s, false,
+                        P->d_prep_ctas, P->n_prep_ctas) != cudaSuccess)
             return Q2_0_ECUDA;
         MvJob dummy;
         std::memset(&dummy, 0, sizeof(dummy));
