@@ -269,6 +269,32 @@ def test_plan_mixed_shapes(dev, ncols):
     _no_device_error()
 
 
+@pytest.mark.parametrize("seed,ncols", [(1, 1), (2, 1), (3, 3), (4, 8), (5, 2)])
+def test_plan_random_shapes(dev, seed, ncols):
+    """Seeded random plans: 24-40 matrices of 1-1500 rows (ragged last tiles,
+    single-row matrices), K a multiple of 512 up to 6144 or off the tensor-core
+    rules; every row checked, executed twice (the scratch and schedule reused)."""
+    g = synth.rng(2010, seed)
+    n_mat = int(g.integers(24, 41))
+    ents, host = [], []
+    for i in range(n_mat):
+        N = int(g.integers(1, 1501)) if i % 5 else int(g.integers(1, 4))
+        K = int(512 * g.integers(1, 13)) if i % 7 else int(64 * g.integers(1, 40))
+        w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+        x = synth.activations(g, ncols, K, 0.001, 30.0)
+        ents.append((_to(dev, w), _to(dev, x), torch.full((ncols, N), float("nan"), device=dev), N, K))
+        host.append((w, x))
+    plan = q.MvPlan(ents, ncols)
+    for rep in range(2):
+        plan.execute()
+        torch.cuda.synchronize()
+        for (w, x), (_, _, yd, N, K) in zip(host, ents):
+            yo, acc = oracle.matmul(w, N, K, x)
+            _assert_close(yd.cpu().numpy(), yo, acc, TOL_SPLIT, f"random plan {N}x{K} rep {rep}")
+    plan.close()
+    _no_device_error()
+
+
 def _decode_step(dev, mats, seed, ncols):
     ents, host = [], []
     for idx, (layer, m) in enumerate(mats):
@@ -317,7 +343,9 @@ def test_plan_8b_decode_step_sampled(dev):
 # prefill GEMM
 # ---------------------------------------------------------------------------
 GEMM_SMALL = [(128, 512, 128), (300, 1024, 70), (1, 512, 1), (200, 1536, 17), (130, 2048, 257),
-              (256, 512, 300), (40, 576, 9), (17, 64, 5)]
+              (256, 512, 300), (40, 576, 9), (17, 64, 5),
+              # few output units over a long K: each unit split over many stream-K CTAs
+              (300, 8192, 64), (513, 4096, 129)]
 
 
 @pytest.mark.parametrize("prec", [q.Q2_0_PREC_F16_SPLIT, q.Q2_0_PREC_F16])
