@@ -672,12 +672,12 @@ __global__ void __maxnreg__(128)
             tmem_st4(tmem + lane_base + kT4ScaleCol, one, one, one, one);
             tmem_st4(tmem + lane_base + kT4ScaleCol + 4, one, one, one, one);
         }
-        {
-            bool ok = true;
-            for (int s = 0; s < n_stages && ok; ++s) {
-                const int st = s % Lt::kStages;
+        bool ok = true;
+        for (int s = 0; s < n_stages && ok; ++s) {
+            const int st = s % Lt::kStages;
+            // one 64-column A buffer per 512 weights of the stage (two for group-128)
 #pragma unroll 1
-                for (int h = 0; h < Lt::kAPer; ++h) {
+            for (int h = 0; h < Lt::kAPer; ++h) {
                 const int u = s * Lt::kAPer + h;
                 const bool got =
                     (h > 0 || mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full, false, wl)) &&
@@ -689,46 +689,43 @@ __global__ void __maxnreg__(128)
                     break;
                 }
                 tc_fence_after();
-                if constexpr (kG) {
-                    // half h of the row's stage: blocks 4h .. 4h + 3 (136 bytes from an
-                    // 8-byte boundary); block bl's codes start 2 bytes into a word for
-                    // even bl and on a word boundary for odd bl
-                    const uint8_t *rp = raw_ring + st * Lt::kRaw + row * kG128RowBytes + h * 136;
-                    uint32_t w32[34];
 #pragma unroll
-                    for (int k = 0; k < 17; ++k) {
-                        const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * k);
-                        w32[2 * k] = v.x;
-                        w32[2 * k + 1] = v.y;
-                    }
+                for (int G = 0; G < 2; ++G) {  // 32 columns of the A buffer per store
+                    uint32_t a[32];
+                    if constexpr (kG) {
+                        // half h of the row's stage: blocks 4h .. 4h + 3 (136 bytes from
+                        // an 8-byte boundary). This store: blocks 2G and 2G + 1 (sub-blocks
+                        // 4G .. 4G + 3 of the A buffer), read as 9 8-byte words from byte
+                        // 64 G of the half (8-byte loads: 2-way bank conflicts at the
+                        // 272-byte row stride). Block 2G + b2 starts at byte 34 b2 + 4 G
+                        // of those words: its codes are word wi at byte 34 b2 + 4 G + 2 +
+                        // 4 wi, 2 bytes into a 32-bit word for b2 = 0 and aligned for b2 = 1.
+                        const uint8_t *rp =
+                            raw_ring + st * Lt::kRaw + row * kG128RowBytes + h * 136 + G * 64;
+                        uint32_t w32[18];
 #pragma unroll
-                    for (int G = 0; G < 2; ++G) {
-                        uint32_t a[32];
+                        for (int k = 0; k < 9; ++k) {
+                            const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * k);
+                            w32[2 * k] = v.x;
+                            w32[2 * k + 1] = v.y;
+                        }
 #pragma unroll
                         for (int b2 = 0; b2 < 2; ++b2) {
-                            const int bl = 2 * G + b2;
 #pragma unroll
                             for (int wi = 0; wi < 8; ++wi) {
                                 const uint32_t w =
-                                    (bl & 1) ? w32[(34 * bl + 2) / 4 + wi]
-                                             : __byte_perm(w32[34 * bl / 4 + wi],
-                                                           w32[34 * bl / 4 + wi + 1], 0x5432);
+                                    b2 ? w32[9 + G + wi]
+                                       : __byte_perm(w32[G + wi], w32[G + wi + 1], 0x5432);
                                 // sub-block 2 b2 + wi / 4 of this store, word wi % 4
                                 const int o = 8 * (2 * b2 + (wi >> 2)) + 2 * (wi & 3);
                                 a[o] = w & 0x33333333u;
                                 a[o + 1] = (w >> 2) & 0x33333333u;
                             }
                         }
-                        tmem_st32(tmem + lane_base + a_col(u) + 32 * G, a);
-                    }
-                } else {
-#pragma unroll
-                for (int G = 0; G < 2; ++G) {
-                    uint32_t a[32];
-                    if (kSplit) {
+                    } else if constexpr (kSplit) {
                         // block 4G+bi is 16-byte chunk 4G+bi of the row, stored at
                         // chunk (4G+bi) ^ (row % 8) by the 128-byte swizzle
-                        const uint8_t *rp = raw_ring + st * kRawBytes + row * 128;
+                        const uint8_t *rp = raw_ring + st * Lt::kRaw + row * 128;
 #pragma unroll
                         for (int bi = 0; bi < 4; ++bi) {
                             const uint4 v = *reinterpret_cast<const uint4 *>(
@@ -741,24 +738,23 @@ __global__ void __maxnreg__(128)
                             }
                         }
                     } else {
-                        const uint8_t *rp =
-                            raw_ring + st * kRawBytes + row * kChunkBytes + G * 72;
-                        uint32_t u[18];
+                        const uint8_t *rp = raw_ring + st * Lt::kRaw + row * kChunkBytes + G * 72;
+                        uint32_t u32[18];
 #pragma unroll
                         for (int k = 0; k < 9; ++k) {
                             const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * k);
-                            u[2 * k] = v.x;
-                            u[2 * k + 1] = v.y;
+                            u32[2 * k] = v.x;
+                            u32[2 * k + 1] = v.y;
                         }
 #pragma unroll
                         for (int bi = 0; bi < 4; ++bi) {
 #pragma unroll
                             for (int c = 0; c < 4; ++c) {
                                 uint32_t w;
-                                if (bi == 0) w = __byte_perm(u[c], u[c + 1], 0x5432);
-                                else if (bi == 1) w = u[5 + c];
-                                else if (bi == 2) w = __byte_perm(u[9 + c], u[10 + c], 0x5432);
-                                else w = u[14 + c];
+                                if (bi == 0) w = __byte_perm(u32[c], u32[c + 1], 0x5432);
+                                else if (bi == 1) w = u32[5 + c];
+                                else if (bi == 2) w = __byte_perm(u32[9 + c], u32[10 + c], 0x5432);
+                                else w = u32[14 + c];
                                 a[8 * bi + 2 * c + 0] = w & 0x33333333u;
                                 a[8 * bi + 2 * c + 1] = (w >> 2) & 0x33333333u;
                             }
@@ -766,12 +762,10 @@ __global__ void __maxnreg__(128)
                     }
                     tmem_st32(tmem + lane_base + a_col(u) + 32 * G, a);
                 }
-                }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&a_full[a_buf(u)]);
-                }
             }
         }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {

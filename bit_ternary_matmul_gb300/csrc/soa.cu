@@ -13,7 +13,7 @@
 // On GB300 the split gives 128-byte code rows per 8 blocks, a width the TMA
 // engine can swizzle, so the fp4 mat-vec reads them with
 // conflict-free 16-byte shared-memory loads and no byte shuffles
-// (mv_t4_kernel<true>). This file holds the layout kernels and the CUDA-core
+// (mv_t4_kernel<kLaySplit>). This file holds the layout kernels and the CUDA-core
 // mat-vec used off that fast path.
 #include "q2_0_device.cuh"
 #include "q2_0_internal.h"
