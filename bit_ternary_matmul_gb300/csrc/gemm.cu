@@ -380,8 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             }
             tc_fence_after();
             for (int kk = kb; kk < ke; ++kk) {
-                const bool got = mbar_wait(&x_full[st], ph, a.err, kTagGemm + 4) &&
-                                 mbar_wait(&a_full[st], ph, a.err, kTagGemm + 5);
+                const bool got = mbar_wait2(&x_full[st], ph, kTagGemm + 4, &a_full[st], ph,
+                                            kTagGemm + 5, a.err, kWaitLimitNs);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
@@ -435,9 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const int ke = seg_end(n_slabs, kb, g_end - g);
             g += ke - kb;
             for (int kk = kb; kk < ke; ++kk) {
-                bool got = true;
-                if ((kk & 7) == 0 || kk == kb) got = mbar_wait(&w_full[wst], wph, a.err, kTagGemm + 6);
-                got = got && mbar_wait(&slot_free[st], ph ^ 1u, a.err, kTagGemm + 7);
+                const bool got =
+                    (kk & 7) == 0 || kk == kb
+                        ? mbar_wait2(&w_full[wst], wph, kTagGemm + 6, &slot_free[st], ph ^ 1u,
+                                     kTagGemm + 7, a.err, kWaitLimitNs)
+                        : mbar_wait(&slot_free[st], ph ^ 1u, a.err, kTagGemm + 7);
                 if (!__all_sync(0xffffffffu, got)) {  // warp-uniform decision
                     ok = false;
                     break;

@@ -616,12 +616,12 @@ __global__ void __maxnreg__(128)
                 for (int h = 0; h < Lt::kAPer; ++h) {
                     const int u = s * Lt::kAPer + h;
                     const bool got =
-                        (h > 0 ||
-                         (mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full, false, wl) &&
-                          mbar_wait(&d_empty[s & 1], (uint32_t(s >> 1) & 1u) ^ 1u, p.err,
-                                    kTagT4DEmpty, false, wl))) &&
-                        mbar_wait(&a_full[a_buf(u)], a_use(u), p.err, kTagT4AFull, false, wl) &&
-                        !*(volatile int *)&s_abort;
+                        h > 0 ? mbar_wait(&a_full[a_buf(u)], a_use(u), p.err, kTagT4AFull, false, wl) &&
+                                    !*(volatile int *)&s_abort
+                              : mbar_wait3(&full[st], stage_parity(s), kTagT4Full, &d_empty[s & 1],
+                                           (uint32_t(s >> 1) & 1u) ^ 1u, kTagT4DEmpty,
+                                           &a_full[a_buf(u)], a_use(u), kTagT4AFull, p.err, wl,
+                                           &s_abort);
                     if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
                         break;
@@ -673,90 +673,108 @@ __global__ void __maxnreg__(128)
             tmem_st4(tmem + lane_base + kT4ScaleCol + 4, one, one, one, one);
         }
         bool ok = true;
+        // The next stage's barriers are tested (without blocking) while this
+        // stage's codes are expanded; when both had completed, the next stage
+        // starts without a wait. An incomplete one takes the bounded wait.
+        bool ready = false;
         for (int s = 0; s < n_stages && ok; ++s) {
             const int st = s % Lt::kStages;
             // one 64-column A buffer per 512 weights of the stage (two for group-128)
 #pragma unroll 1
             for (int h = 0; h < Lt::kAPer; ++h) {
                 const int u = s * Lt::kAPer + h;
-                const bool got =
-                    (h > 0 || mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full, false, wl)) &&
-                    mbar_wait(&a_empty[a_buf(u)], a_use(u) ^ 1u, p.err, kTagT4AFull, false, wl) &&
-                    !*(volatile int *)&s_abort;
+                bool got = h == 0 && __all_sync(0xffffffffu, ready);
+                if (!got)
+                    got = h > 0 ? mbar_wait(&a_empty[a_buf(u)], a_use(u) ^ 1u, p.err, kTagT4AFull,
+                                            false, wl) &&
+                                      !*(volatile int *)&s_abort
+                                : mbar_wait2(&full[st], stage_parity(s), kTagT4Full,
+                                             &a_empty[a_buf(u)], a_use(u) ^ 1u, kTagT4AFull, p.err,
+                                             wl, &s_abort);
                 if (!__all_sync(0xffffffffu, got)) {
                     s_abort = 1;
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                // This A buffer's code words, both 32-column halves G, loaded first.
+                // Blocks layout: half G is bytes 72 G .. 72 G + 71 of the row's stage
+                // slice, 9 8-byte words; even blocks start 2 bytes into a 4-byte word
+                // (d first). Group-128: half h of the stage is blocks 4h .. 4h + 3
+                // (136 bytes from an 8-byte boundary); its half G is 9 8-byte words
+                // from byte 64 G (8-byte loads: 2-way bank conflicts at the 272-byte
+                // row stride). Split layout: four 16-byte chunks per half, chunk 4G+bi
+                // at (4G+bi) ^ (row % 8) under the 128-byte swizzle.
+                uint32_t w32[2][18];
 #pragma unroll
-                for (int G = 0; G < 2; ++G) {  // 32 columns of the A buffer per store
-                    uint32_t a[32];
-                    if constexpr (kG) {
-                        // half h of the row's stage: blocks 4h .. 4h + 3 (136 bytes from
-                        // an 8-byte boundary). This store: blocks 2G and 2G + 1 (sub-blocks
-                        // 4G .. 4G + 3 of the A buffer), read as 9 8-byte words from byte
-                        // 64 G of the half (8-byte loads: 2-way bank conflicts at the
-                        // 272-byte row stride). Block 2G + b2 starts at byte 34 b2 + 4 G
-                        // of those words: its codes are word wi at byte 34 b2 + 4 G + 2 +
-                        // 4 wi, 2 bytes into a 32-bit word for b2 = 0 and aligned for b2 = 1.
-                        const uint8_t *rp =
-                            raw_ring + st * Lt::kRaw + row * kG128RowBytes + h * 136 + G * 64;
-                        uint32_t w32[18];
-#pragma unroll
-                        for (int k = 0; k < 9; ++k) {
-                            const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * k);
-                            w32[2 * k] = v.x;
-                            w32[2 * k + 1] = v.y;
-                        }
-#pragma unroll
-                        for (int b2 = 0; b2 < 2; ++b2) {
-#pragma unroll
-                            for (int wi = 0; wi < 8; ++wi) {
-                                const uint32_t w =
-                                    b2 ? w32[9 + G + wi]
-                                       : __byte_perm(w32[G + wi], w32[G + wi + 1], 0x5432);
-                                // sub-block 2 b2 + wi / 4 of this store, word wi % 4
-                                const int o = 8 * (2 * b2 + (wi >> 2)) + 2 * (wi & 3);
-                                a[o] = w & 0x33333333u;
-                                a[o + 1] = (w >> 2) & 0x33333333u;
-                            }
-                        }
-                    } else if constexpr (kSplit) {
-                        // block 4G+bi is 16-byte chunk 4G+bi of the row, stored at
-                        // chunk (4G+bi) ^ (row % 8) by the 128-byte swizzle
+                for (int G = 0; G < 2; ++G) {
+                    if constexpr (kSplit) {
                         const uint8_t *rp = raw_ring + st * Lt::kRaw + row * 128;
 #pragma unroll
                         for (int bi = 0; bi < 4; ++bi) {
                             const uint4 v = *reinterpret_cast<const uint4 *>(
                                 rp + (((4 * G + bi) ^ (row & 7)) << 4));
-                            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                a[8 * bi + 2 * c + 0] = wv[c] & 0x33333333u;
-                                a[8 * bi + 2 * c + 1] = (wv[c] >> 2) & 0x33333333u;
-                            }
+                            w32[G][4 * bi + 0] = v.x;
+                            w32[G][4 * bi + 1] = v.y;
+                            w32[G][4 * bi + 2] = v.z;
+                            w32[G][4 * bi + 3] = v.w;
                         }
                     } else {
-                        const uint8_t *rp = raw_ring + st * Lt::kRaw + row * kChunkBytes + G * 72;
-                        uint32_t u32[18];
+                        const uint8_t *rp =
+                            kG ? raw_ring + st * Lt::kRaw + row * kG128RowBytes + h * 136 + G * 64
+                               : raw_ring + st * Lt::kRaw + row * kChunkBytes + G * 72;
 #pragma unroll
                         for (int k = 0; k < 9; ++k) {
                             const uint2 v = *reinterpret_cast<const uint2 *>(rp + 8 * k);
-                            u32[2 * k] = v.x;
-                            u32[2 * k + 1] = v.y;
+                            w32[G][2 * k] = v.x;
+                            w32[G][2 * k + 1] = v.y;
                         }
+                    }
+                }
+                if (h == Lt::kAPer - 1) {  // the next stage's barriers, tested now
+                    const int s1 = s + 1, u1 = s1 * Lt::kAPer;
+                    const bool r1 = mbar_test_wait(&full[s1 % Lt::kStages], stage_parity(s1));
+                    const bool r2 = mbar_test_wait(&a_empty[a_buf(u1)], a_use(u1) ^ 1u);
+                    ready = s1 < n_stages && r1 && r2;
+                }
+#pragma unroll
+                for (int G = 0; G < 2; ++G) {  // 32 columns of the A buffer per store
+                    uint32_t a[32];
+                    const uint32_t(&w)[18] = w32[G];
+                    if constexpr (kG) {
+                        // this store: blocks 2G and 2G + 1 (sub-blocks 4G .. 4G + 3 of
+                        // the A buffer). Block 2G + b2 starts at byte 34 b2 + 4 G of the
+                        // words: its codes are word wi at byte 34 b2 + 4 G + 2 + 4 wi,
+                        // 2 bytes into a 32-bit word for b2 = 0 and aligned for b2 = 1.
+#pragma unroll
+                        for (int b2 = 0; b2 < 2; ++b2) {
+#pragma unroll
+                            for (int wi = 0; wi < 8; ++wi) {
+                                const uint32_t cw =
+                                    b2 ? w[9 + G + wi] : __byte_perm(w[G + wi], w[G + wi + 1], 0x5432);
+                                // sub-block 2 b2 + wi / 4 of this store, word wi % 4
+                                const int o = 8 * (2 * b2 + (wi >> 2)) + 2 * (wi & 3);
+                                a[o] = cw & 0x33333333u;
+                                a[o + 1] = (cw >> 2) & 0x33333333u;
+                            }
+                        }
+                    } else if constexpr (kSplit) {
 #pragma unroll
                         for (int bi = 0; bi < 4; ++bi) {
 #pragma unroll
                             for (int c = 0; c < 4; ++c) {
-                                uint32_t w;
-                                if (bi == 0) w = __byte_perm(u32[c], u32[c + 1], 0x5432);
-                                else if (bi == 1) w = u32[5 + c];
-                                else if (bi == 2) w = __byte_perm(u32[9 + c], u32[10 + c], 0x5432);
-                                else w = u32[14 + c];
-                                a[8 * bi + 2 * c + 0] = w & 0x33333333u;
-                                a[8 * bi + 2 * c + 1] = (w >> 2) & 0x33333333u;
+                                a[8 * bi + 2 * c + 0] = w[4 * bi + c] & 0x33333333u;
+                                a[8 * bi + 2 * c + 1] = (w[4 * bi + c] >> 2) & 0x33333333u;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int bi = 0; bi < 4; ++bi) {
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const uint32_t cw = block_word(w, bi, c);
+                                a[8 * bi + 2 * c + 0] = cw & 0x33333333u;
+                                a[8 * bi + 2 * c + 1] = (cw >> 2) & 0x33333333u;
                             }
                         }
                     }
@@ -779,9 +797,8 @@ __global__ void __maxnreg__(128)
         float acc = 0.0f, comp = 0.0f;  // compensated sum of the stage sums
         for (int s = 0; s < n_stages; ++s) {
             const int st = s % Lt::kStages;
-            const bool got = !*(volatile int *)&s_abort &&
-                             mbar_wait(&full[st], stage_parity(s), p.err, kTagT4Full, false, wl) &&
-                             mbar_wait(&d_full[s & 1], uint32_t(s >> 1) & 1u, p.err, kTagT4DFull, false, wl);
+            const bool got = mbar_wait2(&full[st], stage_parity(s), kTagT4Full, &d_full[s & 1],
+                                        uint32_t(s >> 1) & 1u, kTagT4DFull, p.err, wl, &s_abort);
             if (!__all_sync(0xffffffffu, got)) {
                 s_abort = 1;
                 break;
@@ -1181,11 +1198,12 @@ __global__ void __launch_bounds__(s8_threads(NC), 1) mv_s8_kernel(const __grid_c
             const int st = s % kStages;
             const bool first = ss < 2, last_of_stage = ss + 2 >= kSub;
             const bool got =
-                (!first ||
-                 (mbar_wait(&full[st], stage_parity(s), p.err, kTagS8Full) &&
-                  mbar_wait(&a_full[s & 1], uint32_t(s >> 1) & 1u, p.err, kTagS8AFull))) &&
-                mbar_wait(&d_empty[mine], (uint32_t(g >> 1) & 1u) ^ 1u, p.err, kTagS8DEmpty) &&
-                !*(volatile int *)&s_abort;
+                first ? mbar_wait3(&full[st], stage_parity(s), kTagS8Full, &a_full[s & 1],
+                                   uint32_t(s >> 1) & 1u, kTagS8AFull, &d_empty[mine],
+                                   (uint32_t(g >> 1) & 1u) ^ 1u, kTagS8DEmpty, p.err, kWaitLimitNs,
+                                   &s_abort)
+                      : mbar_wait(&d_empty[mine], (uint32_t(g >> 1) & 1u) ^ 1u, p.err, kTagS8DEmpty) &&
+                            !*(volatile int *)&s_abort;
             if (!__all_sync(0xffffffffu, got)) {
                 s_abort = 1;
                 break;
@@ -1229,10 +1247,9 @@ __global__ void __launch_bounds__(s8_threads(NC), 1) mv_s8_kernel(const __grid_c
         const uint32_t lane_base = uint32_t(32 * qd) << 16;
         for (int s = 0; s < n_stages; ++s) {
             const int st = s % kStages;
-            const bool got =
-                mbar_wait(&full[st], stage_parity(s), p.err, kTagS8Full) &&
-                mbar_wait(&a_empty[s & 1], (uint32_t(s >> 1) & 1u) ^ 1u, p.err, kTagS8AFull) &&
-                !*(volatile int *)&s_abort;
+            const bool got = mbar_wait2(&full[st], stage_parity(s), kTagS8Full, &a_empty[s & 1],
+                                        (uint32_t(s >> 1) & 1u) ^ 1u, kTagS8AFull, p.err,
+                                        kWaitLimitNs, &s_abort);
             if (!__all_sync(0xffffffffu, got)) {
                 s_abort = 1;
                 break;

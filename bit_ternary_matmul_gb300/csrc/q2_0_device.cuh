@@ -85,6 +85,18 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t pa
     return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete. Gives up after
 // limit_ns (about one second unless a kernel passes a shorter limit): records
 // the timeout (tag identifies the wait) and returns false.
@@ -114,6 +126,36 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
             return false;
         }
     }
+}
+
+// Two or three waits whose phases are usually complete by the time they are
+// checked: the non-blocking tests are all issued before any result is used, so
+// their latencies overlap; a phase not yet complete takes the bounded wait. A
+// set *abort flag (read alongside; optional) makes them return false at once.
+__device__ __forceinline__ bool mbar_wait2(uint64_t *b1, uint32_t p1, int tag1, uint64_t *b2,
+                                           uint32_t p2, int tag2, unsigned long long *err,
+                                           uint64_t limit_ns, const volatile int *abort = nullptr) {
+    const int ab = abort ? *abort : 0;
+    const bool r1 = mbar_test_wait(b1, p1);
+    const bool r2 = mbar_test_wait(b2, p2);
+    if (ab) return false;
+    if (r1 && r2) return true;
+    return (r1 || mbar_wait(b1, p1, err, tag1, false, limit_ns)) &&
+           (r2 || mbar_wait(b2, p2, err, tag2, false, limit_ns));
+}
+__device__ __forceinline__ bool mbar_wait3(uint64_t *b1, uint32_t p1, int tag1, uint64_t *b2,
+                                           uint32_t p2, int tag2, uint64_t *b3, uint32_t p3,
+                                           int tag3, unsigned long long *err, uint64_t limit_ns,
+                                           const volatile int *abort = nullptr) {
+    const int ab = abort ? *abort : 0;
+    const bool r1 = mbar_test_wait(b1, p1);
+    const bool r2 = mbar_test_wait(b2, p2);
+    const bool r3 = mbar_test_wait(b3, p3);
+    if (ab) return false;
+    if (r1 && r2 && r3) return true;
+    return (r1 || mbar_wait(b1, p1, err, tag1, false, limit_ns)) &&
+           (r2 || mbar_wait(b2, p2, err, tag2, false, limit_ns)) &&
+           (r3 || mbar_wait(b3, p3, err, tag3, false, limit_ns));
 }
 
 // ---------------------------------------------------------------------------
