@@ -112,8 +112,12 @@ struct MvFirst {
     int item_base;  // the CTA's first entry in items
     int n_items;
     int n_stages;   // stages (512-column chunks) of its items
-    int job0;       // its first item
-    int tile0;
+    int job0;       // its first item: job, tile, and the job's fields the producer
+    int tile0;      // needs, so that the first copies wait on no further load
+    int n_chunks0;
+    int n0;
+    const uint8_t *prep0;
+    float *y0;
 };
 
 struct MvParams {
@@ -152,6 +156,35 @@ __device__ __forceinline__ float mul_pow2(float v, int e) {
 __device__ __forceinline__ float pow2f(int k) {
     return k >= -126 ? __int_as_float((127 + k) << 23)
                      : k >= -149 ? __int_as_float(1 << (149 + k)) : 0.0f;
+}
+
+// Eight f32 values rounded to e2m1 (round to nearest, ties to even; the
+// values here never reach the saturation bound 6), packed as nibbles: value i
+// in bits 4i .. 4i + 3.
+__device__ __forceinline__ uint32_t e2m1x8_rn(const float (&w)[8]) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q3, %8, %7;\n\t"
+        "mov.b32 %0, {q0, q1, q2, q3};\n\t}"
+        : "=r"(r)
+        : "f"(w[0]), "f"(w[1]), "f"(w[2]), "f"(w[3]), "f"(w[4]), "f"(w[5]), "f"(w[6]), "f"(w[7]));
+    return r;
+}
+
+// The e2m1 values of nibbles 2k (lo) and 2k + 1 (hi) of a packed word, exactly.
+__device__ __forceinline__ void e2m1x2_values(uint32_t word, int k, float &lo, float &hi) {
+    uint32_t h2;
+    asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+        "mov.b32 {q0, q1, q2, q3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, q0;\n\t}"
+        : "=r"(h2)
+        : "r"(word >> (8 * k)));
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
 }
 
 // Activation element load: F32 as is, F16 (IEEE binary16) converted exactly.
@@ -360,44 +393,27 @@ __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
         const int kbyte = kG128 ? 32 * (2 * (b & 7) + (c >> 2)) + 8 * (c & 3) + 4 * h
                                 : 32 * (b & 7) + 8 * c + 4 * h;
         float grp_sum[3] = {0.0f, 0.0f, 0.0f};  // this item's share of H, M, L
-        // Rounding to the e2m1 grid without format conversions. With M = 2^23,
-        // fma(|s|, 2, M) rounds 2|s| to the nearest integer (ties to even) and
-        // keeps it in its low mantissa bits. On [0, 2] the e2m1 values are the
-        // multiples of 1/2, and round-to-nearest-even on them is exactly that
-        // rounding of 2|s|, whose integer k (0..4) is also the nibble of k/2;
-        // only the first piece can exceed 2 (|s| < 4), where the grid is the
-        // integers 2, 3, 4 (nibbles 4, 5, 6) and |s| + M rounds |s| alike.
-        constexpr float kMagic = 8388608.0f;
+        // Piece p of element jj is e2m1(w), w = r_p * 4^p the scaled residual
+        // (w = v for p = 0), rounded to nearest even by the conversion; then
+        // w <- 4 (w - piece), exact: |w| < 4 at p = 0 (grid spacing 1 on [2, 4],
+        // 1/2 below) and |w| <= 2 after it, so every residual is a multiple of
+        // the grid's spacing far inside f32's precision.
 #pragma unroll
         for (int p = 0; p < kT4Pieces; ++p) {
-            const float up = __int_as_float((127 + 2 * p) << 23);
-            const float down = __int_as_float((127 - 2 * p) << 23);
-            uint32_t word = 0;
-            float sum2 = 0.0f;  // sum of 2 * piece over the item's 8 elements (exact)
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                const float sv = v[jj] * up;
-                const float as = fabsf(sv);
-                float two_mag;   // 2 |piece|
-                uint32_t nib;
-                if (p == 0 && as > 2.0f) {
-                    const float a1 = as + kMagic;
-                    nib = (__float_as_uint(a1) & 7u) + 2u;
-                    two_mag = 2.0f * (a1 - kMagic);
-                } else {
-                    const float a2 = fmaf(as, 2.0f, kMagic);
-                    nib = __float_as_uint(a2) & 7u;
-                    two_mag = a2 - kMagic;
-                }
-                const float two_piece = copysignf(two_mag, sv);
-                v[jj] = fmaf(-two_piece, 0.5f * down, v[jj]);
-                sum2 += two_piece;
-                word |= (nib | ((__float_as_uint(sv) >> 28) & 8u)) << (4 * jj);
-            }
+            const uint32_t word = e2m1x8_rn(v);
             *reinterpret_cast<uint32_t *>(bimg + img_offset(kT4N, p, kbyte)) = word;
-            // sum of piece / 2 = sum2 / 4, weighted by 4^-p, into its group
+            float psum = 0.0f;  // sum of the item's 8 pieces (exact)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float lo, hi;
+                e2m1x2_values(word, k, lo, hi);
+                v[2 * k] = fmaf(v[2 * k], 4.0f, -4.0f * lo);
+                v[2 * k + 1] = fmaf(v[2 * k + 1], 4.0f, -4.0f * hi);
+                psum += lo + hi;
+            }
+            // sum of piece / 2, weighted by 4^-p, into its group
             const int gi = p < 6 ? 0 : p < 12 ? 1 : 2;
-            grp_sum[gi] = fmaf(sum2 * 0.25f, down, grp_sum[gi]);
+            grp_sum[gi] = fmaf(psum * 0.5f, __int_as_float((127 - 2 * p) << 23), grp_sum[gi]);
         }
 #pragma unroll
         for (int gi = 0; gi < 3; ++gi)
@@ -528,8 +544,11 @@ __global__ void __maxnreg__(128)
                 const MvJob *J;
                 int tile;
                 item_at(i, J, tile);
-                const uint8_t *prep = J->prep;
-                float *y_out = J->y;
+                // a plan's first item: the fields come with the CTA's record
+                const bool rec = p.jobs && i == 0;
+                const uint8_t *prep = rec ? fst.prep0 : J->prep;
+                float *y_out = rec ? fst.y0 : J->y;
+                const int n_rows = rec ? fst.n0 : J->N;
                 int row_base = 0;  // first tensor-map row of the matrix
                 if (p.moe.ids) {
                     // item = (output vector v, tile): expert ids[v], that expert's
@@ -549,7 +568,7 @@ __global__ void __maxnreg__(128)
                     prep += size_t(xv) * p.moe.prep_stride;
                 }
                 const uint8_t *act = prep + kPrepHeader;
-                const int nch = J->n_chunks;
+                const int nch = rec ? fst.n_chunks0 : J->n_chunks;
                 for (int ch = 0; ch < nch; ++ch, ++s) {
                     if ((s & 1) != pmine) continue;
                     if (p.stall_stage && s >= p.stall_stage - 1) {  // test hook
@@ -566,7 +585,7 @@ __global__ void __maxnreg__(128)
                     StageMeta &m = s_meta[st];
                     m.y = y_out;
                     m.row0 = tile * kTcRows;
-                    m.n_rows = J->N;
+                    m.n_rows = n_rows;
                     m.flags = ch == nch - 1 ? kLastOfTile : 0;
                     mbar_arrive_expect_tx(&full[st], Lt::kRaw + Lt::kAct);
                     if (kSplit) {
@@ -1144,8 +1163,12 @@ __global__ void __launch_bounds__(s8_threads(NC), 1) mv_s8_kernel(const __grid_c
                 const MvJob *J;
                 int tile;
                 item_at(i, J, tile);
-                const uint8_t *prep = J->prep + kPrepHeader;
-                const int nch = J->n_chunks;
+                // a plan's first item: the fields come with the CTA's record
+                const bool rec = p.jobs && i == 0;
+                const uint8_t *prep = (rec ? fst.prep0 : J->prep) + kPrepHeader;
+                const int nch = rec ? fst.n_chunks0 : J->n_chunks;
+                float *y_out = rec ? fst.y0 : J->y;
+                const int n_rows = rec ? fst.n0 : J->N;
                 for (int ch = 0; ch < nch; ++ch, ++s) {
                     if ((s & 1) != pmine) continue;
                     const int st = s % kStages;
@@ -1156,9 +1179,9 @@ __global__ void __launch_bounds__(s8_threads(NC), 1) mv_s8_kernel(const __grid_c
                         break;
                     }
                     StageMeta &m = s_meta[st];
-                    m.y = J->y;
+                    m.y = y_out;
                     m.row0 = tile * kTcRows;
-                    m.n_rows = J->N;
+                    m.n_rows = n_rows;
                     m.flags = ch == nch - 1 ? kLastOfTile : 0;
                     mbar_arrive_expect_tx(&full[st], kRawBytes + kImg + kRecCopy);
                     tma_load_2d(raw_ring + st * kRawBytes, &J->tmap, ch * kChunkBytes,
@@ -1987,6 +2010,11 @@ int mv_plan_create(const q2_0_mv_desc *descs, int n, int ncols, q2_0_mv_plan **o
             if (f.n_items > 0) {
                 f.job0 = flat[begin[c]].job;
                 f.tile0 = flat[begin[c]].tile;
+                const MvJob &j0 = jobs[f.job0];
+                f.n_chunks0 = j0.n_chunks;
+                f.n0 = j0.N;
+                f.prep0 = j0.prep;
+                f.y0 = j0.y;
             }
         }
         if (st == Q2_0_OK &&
