@@ -257,19 +257,17 @@ __device__ __forceinline__ uint32_t block_word(const uint32_t (&u)[18], int bi, 
 constexpr int kT4Pieces = 16;
 constexpr int kT4N = 16;                               // MMA N: one B row per piece
 constexpr int kT4Stages = 8;
-constexpr int kT4ImgBytes = kT4N * kChunkBlocks * 32;  // 4096: 16 rows x 256 bytes (512 e2m1)
 // per block of a stage: float {2^(e - 1), H, M, L}
 constexpr int kT4BlockRec = 4;
 constexpr int kT4BetaBytes = kChunkBlocks * kT4BlockRec * 4;  // 128
 constexpr int kT4ABufs = 3;
 constexpr int kT4ACol = 256;                           // A buffers at 256 + 64 i
-constexpr int kT4ScaleCol = 448;                       // scales A 448..451, B 452..455
+constexpr int kT4ScaleCol = 448;  // scales A 448..451, B 452..455 (448..463 all hold 1.0)
 // mbarriers: full / empty per stage, a_full / a_empty per A buffer, d_full /
 // d_empty per D buffer, a drain per MMA issuer
 constexpr int kT4Barriers = 2 * kT4Stages + 2 * kT4ABufs + 2 * 2 + 2;
 // a stage's activation data (image, then block records) is one bulk copy; in
 // shared memory its slots stay 1024-aligned for the swizzled image
-constexpr int kT4ActBytes = kT4ImgBytes + kT4BetaBytes;  // 4224, the stride in the prep buffer
 constexpr int kT4ActSlot = 5120;
 constexpr int kT4Smem = 1024 /* alignment slack */ + kT4Stages * (kT4ActSlot + kRawBytes) +
                         kT4Barriers * 8;
@@ -279,6 +277,7 @@ constexpr int kTagT4Empty = 112;
 constexpr int kTagT4AFull = 113;
 constexpr int kTagT4DFull = 114;
 constexpr int kTagT4DEmpty = 115;
+constexpr int kTagT4Pair = 116;
 
 // Weight layouts the fp4 kernel streams: 18-byte blocks of 64 weights, the
 // split layout (codes and scales in separate arrays), and group-128 (34-byte
@@ -293,27 +292,40 @@ constexpr int kLayG128 = 2;
 constexpr int kG128Bytes = 34;
 constexpr int kG128RowBytes = kChunkBlocks * kG128Bytes;  // 272
 
-template <int L>
+// NC: activation columns (1, or 2 for the 64-weight layout). Column j's pieces
+// are B rows 16 j .. 16 j + 15, and each region has one record per column.
+template <int L, int NC = 1>
 struct T4Lay {
     static constexpr int kStageK = L == kLayG128 ? 1024 : 512;  // weights of a row per stage
     static constexpr int kAPer = kStageK / 512;                 // 64-column A buffers per stage
     static constexpr int kRaw = L == kLayG128 ? kTcRows * kG128RowBytes : kRawBytes;
-    static constexpr int kImg = kT4N * kStageK / 2;             // e2m1 B image of a stage
-    static constexpr int kAct = kImg + kT4BetaBytes;            // image, then 8 region records
+    static constexpr int kN = kT4N * NC;                        // MMA N: B rows
+    static constexpr int kImg = kN * kStageK / 2;               // e2m1 B image of a stage
+    static constexpr int kAct = kImg + kT4BetaBytes * NC;       // image, then the region records
     static constexpr int kActSlot = (kAct + 1023) / 1024 * 1024;
     static constexpr int kStages = L == kLayG128 ? 4 : kT4Stages;
-    static constexpr int kBarriers = 2 * kStages + 2 * kT4ABufs + 2 * 2 + 2;
+    // two columns: per lane quarter, the tile-end hand-off between its two
+    // epilogue warps (sums ready, sums read)
+    static constexpr int kBarriers = 2 * kStages + 2 * kT4ABufs + 2 * 2 + 2 + (NC == 2 ? 8 : 0);
     static constexpr int kSmem = 1024 /* alignment slack */ + kStages * (kActSlot + kRaw) +
                                  kBarriers * 8;
+    static constexpr int kEpi = kEpiWarps * NC;   // epilogue warps
+    static constexpr int kThreads = kTcThreads + (NC - 1) * kEpiWarps * 32;
 };
 static_assert(T4Lay<kLayBlocks>::kActSlot == kT4ActSlot && T4Lay<kLayBlocks>::kSmem == kT4Smem,
               "the 64-weight layout keeps its stage geometry");
 static_assert(T4Lay<kLayG128>::kStages % 2 == 0 && T4Lay<kLayG128>::kSmem <= kSmemOptIn,
               "group-128 ring: even depth (two producers), within the shared-memory limit");
+static_assert(T4Lay<kLayBlocks, 2>::kSmem <= kSmemOptIn - 4096,
+              "two-column ring (and the static hand-off buffer) within the shared-memory limit");
+static_assert(T4Lay<kLayBlocks>::kThreads == kTcThreads && T4Lay<kLaySplit>::kThreads == kTcThreads &&
+                  T4Lay<kLayG128>::kThreads == kTcThreads && T4Lay<kLayBlocks, 2>::kThreads == 16 * 32,
+              "fp4 kernel block sizes: 12 warps, 16 with two epilogue warps per lane quarter");
 
-size_t t4_prep_bytes(int64_t K) {
+size_t t4_prep_bytes(int64_t K, int ncols = 1) {
     const size_t n_chunks = size_t(K / 512);
-    size_t b = kPrepHeader + n_chunks * kT4ActBytes;
+    size_t b = kPrepHeader +
+               n_chunks * (ncols == 2 ? T4Lay<kLayBlocks, 2>::kAct : T4Lay<kLayBlocks>::kAct);
     return (b + 255) & ~size_t(255);
 }
 
@@ -343,7 +355,7 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int m, int n) {
 template <typename XT, bool kG128>
 __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
     const __grid_constant__ MvPrepJob single, const MvPrepJob *__restrict__ jobs,
-    const int2 *__restrict__ ctas) {
+    const int2 *__restrict__ ctas, int ncols) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // Launched as a programmatic dependent of the kernel before it on the stream
     // (a mat-vec that may still read this buffer, or the producer of x): wait
@@ -362,9 +374,15 @@ __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
     constexpr int kBE = kG128 ? 128 : 64;  // elements per scale block
     constexpr int kIPB = kBE / 8;          // items (lanes) per block
     const int K = J.K;
-    const XT *xj = static_cast<const XT *>(J.x);
+    // grid x: the activation column j (pieces in B rows 16 j .., one record per
+    // region and column)
+    const int j = int(blockIdx.x);
+    const XT *xj = static_cast<const XT *>(J.x) + size_t(j) * K;
     const int nb = K / kBE;
-    uint8_t *act = J.prep + kPrepHeader;  // per stage: image, then block records
+    const int rows = kT4N * ncols;
+    const int img_bytes = rows * Lt::kStageK / 2;
+    const int act_bytes = img_bytes + kT4BetaBytes * ncols;
+    uint8_t *act = J.prep + kPrepHeader;  // per stage: image, then region records
     const int lane = threadIdx.x & 31;
     // the block's kIPB threads
     const unsigned grp = kG128 ? 0xFFFFu << (lane & 16) : 0xFFu << (lane & 24);
@@ -388,7 +406,7 @@ __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
         if (m > 0.0f && m <= 3.402823466e38f) frexpf(m, &e);
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) v[jj] = mul_pow2(v[jj], 2 - e);
-        uint8_t *bimg = act + size_t(b >> 3) * Lt::kAct;
+        uint8_t *bimg = act + size_t(b >> 3) * act_bytes;
         // byte of the item's first K position in the stage image
         const int kbyte = kG128 ? 32 * (2 * (b & 7) + (c >> 2)) + 8 * (c & 3) + 4 * h
                                 : 32 * (b & 7) + 8 * c + 4 * h;
@@ -401,7 +419,7 @@ __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
 #pragma unroll
         for (int p = 0; p < kT4Pieces; ++p) {
             const uint32_t word = e2m1x8_rn(v);
-            *reinterpret_cast<uint32_t *>(bimg + img_offset(kT4N, p, kbyte)) = word;
+            *reinterpret_cast<uint32_t *>(bimg + img_offset(rows, kT4N * j + p, kbyte)) = word;
             float psum = 0.0f;  // sum of the item's 8 pieces (exact)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -420,7 +438,7 @@ __global__ void __launch_bounds__(kPrepThreads) t4_prep_kernel(
 #pragma unroll
             for (int o = 1; o < kIPB; o <<= 1) grp_sum[gi] += __shfl_xor_sync(grp, grp_sum[gi], o);
         if ((idx & (kIPB - 1)) == 0)
-            *reinterpret_cast<float4 *>(bimg + Lt::kImg + (b & 7) * kT4BlockRec * 4) =
+            *reinterpret_cast<float4 *>(bimg + img_bytes + ((b & 7) * ncols + j) * kT4BlockRec * 4) =
                 make_float4(pow2f(e - 1), grp_sum[0], grp_sum[1], grp_sum[2]);
     }
 }
@@ -437,10 +455,11 @@ static_assert(kT4SplitCodeBytes + kTcRows * 16 == kRawBytes, "split stage = bloc
 // At most 128 registers a thread (384 x 128 = 48K of the SM's 64K), so a CTA of
 // the next prep kernel (256 threads x 64 registers) can be resident beside it
 // and the programmatic launch overlaps the two.
-template <int kLay>
-__global__ void __maxnreg__(128)
+template <int kLay, int kNc = 1>
+__global__ void __maxnreg__(kNc == 1 ? 128 : 112)
     mv_t4_kernel(const __grid_constant__ MvJob single, const MvParams p) {
-    using Lt = T4Lay<kLay>;
+    using Lt = T4Lay<kLay, kNc>;
+    static_assert(kNc == 1 || (kNc == 2 && kLay == kLayBlocks), "two columns: 64-weight blocks");
     constexpr bool kSplit = kLay == kLaySplit;
     constexpr bool kG = kLay == kLayG128;
     constexpr int kRowBytes = kG ? kG128RowBytes : kChunkBytes;  // a row's bytes in a stage
@@ -459,6 +478,9 @@ __global__ void __maxnreg__(128)
     uint64_t *d_full = a_empty + kT4ABufs;
     uint64_t *d_empty = d_full + 2;
     uint64_t *drain = d_empty + 2;  // [2] one per MMA issuer: its final commit
+    uint64_t *tile_w1 = drain + 2;  // two columns, [4] per quarter: warp 12+q's tile sums are in s_pair
+    uint64_t *tile_w0 = tile_w1 + 4;  // [4] per quarter: warp 8+q has read them
+    __shared__ float s_pair[kNc == 2 ? 4 * 32 * 4 : 1];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
     // per ring slot, written by the producer before the slot's barrier arrive:
@@ -476,8 +498,13 @@ __global__ void __maxnreg__(128)
     if (threadIdx.x == 0) {
         for (int i = 0; i < Lt::kStages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kEpiWarps);
+            mbar_init(&empty[i], Lt::kEpi);
         }
+        if (kNc == 2)
+            for (int i = 0; i < 4; ++i) {
+                mbar_init(&tile_w1[i], 1);
+                mbar_init(&tile_w0[i], 1);
+            }
         for (int i = 0; i < kT4ABufs; ++i) {
             mbar_init(&a_full[i], kExpWarps);
             mbar_init(&a_empty[i], 1);
@@ -619,13 +646,56 @@ __global__ void __maxnreg__(128)
         // ------------------------------ MMA issuers ------------------------------
         // even / odd stages; the whole warp runs the loop and waits (so it stays
         // converged), the elected lane issues (one K = 64 MMA per block) and commits
-        constexpr uint32_t idesc = idesc_mxf4(kTcRows, kT4N);
+        constexpr uint32_t idesc = idesc_mxf4(kTcRows, Lt::kN);
         const bool leader = elect_one();
         const int mine = warp == kMmaWarp ? 0 : 1;
         const uint64_t desc0 = sw128_desc(smem_addr(act_ring));
         const uint32_t sfa = tmem + kT4ScaleCol, sfb = tmem + kT4ScaleCol + 4;
         int last = -1;
-        {
+        if constexpr (kNc == 2) {
+            // One issuer (warp kMmaWarp) takes every stage. A stage fills both
+            // accumulator buffers in turn, blocks 0-3 into buffer 0 and 4-7 into
+            // buffer 1 (each block 32 columns: 16 pieces of 2 columns), so each
+            // buffer's waits come in stage order.
+            for (int s = mine == 0 ? 0 : n_stages; s < n_stages; ++s) {
+                const int st = s % Lt::kStages;
+                const uint64_t dst = desc0 + uint64_t((st * Lt::kActSlot) >> 4);
+                const uint32_t dpar = uint32_t(s & 1) ^ 1u;  // buffer released by stage s - 1
+                bool ok = true;
+#pragma unroll
+                for (int ss = 0; ss < 2; ++ss) {
+                    const bool got =
+                        ss == 0 ? mbar_wait3(&full[st], stage_parity(s), kTagT4Full, &a_full[a_buf(s)],
+                                             a_use(s), kTagT4AFull, &d_empty[0], dpar, kTagT4DEmpty,
+                                             p.err, wl, &s_abort)
+                                : mbar_wait(&d_empty[1], dpar, p.err, kTagT4DEmpty, false, wl) &&
+                                      !*(volatile int *)&s_abort;
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    last = s;
+                    if (leader) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int sb = 4 * ss + i;
+                            tc_mma_mxf4_ta(tmem + ss * 128 + i * Lt::kN, tmem + a_col(s) + sb * 8,
+                                           dst + uint64_t(((sb >> 2) * (Lt::kN * 128) + (sb & 3) * 32) >> 4),
+                                           idesc, sfa, sfb, 0u);
+                        }
+                        tc_commit(&d_full[ss]);
+                    }
+                    __syncwarp();
+                }
+                if (!ok) {
+                    s_abort = 1;
+                    break;
+                }
+                if (leader) tc_commit(&a_empty[a_buf(s)]);
+                __syncwarp();
+            }
+        } else {
             for (int s = mine; s < n_stages; s += 2) {
                 const int st = s % Lt::kStages;
                 const uint32_t d_base = tmem + d_col(s);
@@ -686,10 +756,10 @@ __global__ void __maxnreg__(128)
         const int qd = warp & 3;
         const int row = 32 * qd + lane;
         const uint32_t lane_base = uint32_t(32 * qd) << 16;
-        {  // scale factors 1.0 (ue8m0 127) for this quarter's lanes
+        {  // scale factors 1.0 (ue8m0 127) for this quarter's lanes, columns 448-463
             const uint32_t one = 0x7F7F7F7Fu;
-            tmem_st4(tmem + lane_base + kT4ScaleCol, one, one, one, one);
-            tmem_st4(tmem + lane_base + kT4ScaleCol + 4, one, one, one, one);
+#pragma unroll
+            for (int c = 0; c < 16; c += 4) tmem_st4(tmem + lane_base + kT4ScaleCol + c, one, one, one, one);
         }
         bool ok = true;
         // The next stage's barriers are tested (without blocking) while this
@@ -805,7 +875,7 @@ __global__ void __maxnreg__(128)
                 if (lane == 0) mbar_arrive(&a_full[a_buf(u)]);
             }
         }
-    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + Lt::kEpi) {
         // ------------------------------ epilogue ------------------------------
         // warp w: TMEM lane quarter w % 4, all 8 blocks of each stage; it writes y
         // at the tile's last stage. Every wait is bounded; a warp whose wait
@@ -813,6 +883,7 @@ __global__ void __maxnreg__(128)
         const int qd = warp & 3;
         const int row = 32 * qd + lane;
         const uint32_t lane_base = uint32_t(32 * qd) << 16;
+        if constexpr (kNc == 1) {
         float acc = 0.0f, comp = 0.0f;  // compensated sum of the stage sums
         for (int s = 0; s < n_stages; ++s) {
             const int st = s % Lt::kStages;
@@ -877,6 +948,112 @@ __global__ void __maxnreg__(128)
                 acc = 0.0f;
                 comp = 0.0f;
             }
+        }
+        } else {
+        // Two columns: the stage's blocks 0-3 arrive in accumulator buffer 0 and
+        // 4-7 in buffer 1, each block 32 columns (column jc's pieces at 16 jc ..).
+        // Warp 8+q drains buffer 0 and warp 12+q buffer 1 of lane quarter q; at a
+        // tile's end warp 12+q hands its sums to warp 8+q through s_pair, which
+        // adds them and writes y.
+        const int e = (warp - kEpiWarp0) >> 2;
+        float *pair = s_pair + (qd * 32 + lane) * 4;
+        float acc[2] = {0.0f, 0.0f}, comp[2] = {0.0f, 0.0f};
+        int n_tile_ends = 0;
+        for (int s = 0; s < n_stages; ++s) {
+            const int st = s % Lt::kStages;
+            const bool got = mbar_wait2(&full[st], stage_parity(s), kTagT4Full, &d_full[e],
+                                        uint32_t(s & 1), kTagT4DFull, p.err, wl, &s_abort);
+            if (!__all_sync(0xffffffffu, got)) {
+                s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const StageMeta m = s_meta[st];
+            const uint8_t *rp = raw_ring + st * Lt::kRaw + row * kRowBytes;
+            const float4 *brec =
+                reinterpret_cast<const float4 *>(act_ring + st * Lt::kActSlot + Lt::kImg);
+            const uint32_t d_base = tmem + lane_base + e * 128;
+            float stage_sum[2] = {0.0f, 0.0f};
+#pragma unroll
+            for (int bi = 0; bi < 4; ++bi) {  // block 4 e + bi: 32 registers
+                uint32_t r[32];
+                tmem_ld32(d_base + bi * Lt::kN, r);
+                tmem_wait_ld();
+                if (bi == 3) {  // the buffer's accumulators are all in registers
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&d_empty[e]);
+                }
+                const int b = 4 * e + bi;
+                const float d = lds_half_as_float(rp + 18 * b);
+#pragma unroll
+                for (int jc = 0; jc < 2; ++jc) {
+                    auto C = [&](int pp) { return __uint_as_float(r[kT4N * jc + pp]); };
+                    float gh = C(5) * 0x1p-10f, gm = C(11) * 0x1p-22f, gl = C(15) * 0x1p-30f;
+#pragma unroll
+                    for (int pp = 4; pp >= 0; --pp) gh = fmaf(C(pp), __int_as_float((127 - 2 * pp) << 23), gh);
+#pragma unroll
+                    for (int pp = 10; pp >= 6; --pp) gm = fmaf(C(pp), __int_as_float((127 - 2 * pp) << 23), gm);
+#pragma unroll
+                    for (int pp = 14; pp >= 12; --pp) gl = fmaf(C(pp), __int_as_float((127 - 2 * pp) << 23), gl);
+                    const float4 br = brec[2 * b + jc];  // {2^(e - 1), H, M, L}
+                    const float t = ((gh - br.y) + (gm - br.z)) + (gl - br.w);
+                    stage_sum[jc] = fmaf(d, t * br.x, stage_sum[jc]);
+                }
+            }
+            // both warps of a quarter release every stage once they have read its
+            // records and d values
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+#pragma unroll
+            for (int jc = 0; jc < 2; ++jc) {  // acc + comp += stage_sum (two-sum)
+                const float sum = acc[jc] + stage_sum[jc];
+                const float bb = sum - acc[jc];
+                comp[jc] += (acc[jc] - (sum - bb)) + (stage_sum[jc] - bb);
+                acc[jc] = sum;
+            }
+            if (m.flags & kLastOfTile) {
+                const int t = n_tile_ends++;
+                if (e == 1) {
+                    // wait until warp 8+q has read the previous tile's sums
+                    const bool free_pair =
+                        t == 0 || mbar_wait(&tile_w0[qd], uint32_t(t - 1) & 1u, p.err, kTagT4Pair,
+                                            false, wl);
+                    if (!__all_sync(0xffffffffu, free_pair)) {
+                        s_abort = 1;
+                        break;
+                    }
+#pragma unroll
+                    for (int jc = 0; jc < 2; ++jc) {
+                        pair[2 * jc] = acc[jc];
+                        pair[2 * jc + 1] = comp[jc];
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tile_w1[qd]);
+                } else {
+                    const bool have =
+                        mbar_wait(&tile_w1[qd], uint32_t(t) & 1u, p.err, kTagT4Pair, false, wl);
+                    if (!__all_sync(0xffffffffu, have)) {
+                        s_abort = 1;
+                        break;
+                    }
+                    const int rr = m.row0 + row;
+#pragma unroll
+                    for (int jc = 0; jc < 2; ++jc) {
+                        const float o = pair[2 * jc];
+                        const float sum = acc[jc] + o;
+                        const float bb = sum - acc[jc];
+                        const float err = (acc[jc] - (sum - bb)) + (o - bb);
+                        const float yv = sum + (comp[jc] + pair[2 * jc + 1] + err);
+                        if (m.y && rr < m.n_rows) m.y[size_t(jc) * m.n_rows + rr] = yv;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tile_w0[qd]);
+                }
+#pragma unroll
+                for (int jc = 0; jc < 2; ++jc) acc[jc] = comp[jc] = 0.0f;
+            }
+        }
         }
     }
 
@@ -1576,6 +1753,10 @@ cudaError_t ensure_t4_attr() {
         e = cudaFuncSetAttribute(mv_t4_kernel<kLayG128>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  T4Lay<kLayG128>::kSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mv_t4_kernel<kLayBlocks, 2>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 T4Lay<kLayBlocks, 2>::kSmem);
     if (e == cudaSuccess && dev < 64) g_t4_attr_done[dev] = true;
     return e;
 }
@@ -1599,8 +1780,8 @@ cudaError_t launch_s8_nc(cudaLaunchConfig_t &cfg, const MvJob &single, const MvP
     return cudaLaunchKernelEx(&cfg, mv_s8_kernel<NC>, single, prm);
 }
 
-// ncols = 1 runs the fp4 kernel, ncols 2..8 the signed-e4m3 one.
-bool use_t4(int ncols) { return ncols == 1; }
+// ncols 1 and 2 run the fp4 kernel, ncols 3..8 the signed-e4m3 one.
+bool use_t4(int ncols) { return ncols <= 2; }
 
 bool make_job(MvJob &J, const uint8_t *w, const uint8_t *prep, float *y, int64_t N, int64_t K) {
     std::memset(&J, 0, sizeof(J));
@@ -1640,9 +1821,9 @@ cudaError_t launch_prep_t(const MvPrepJob &single, const MvPrepJob *jobs, int n_
         ctas ? 1u : unsigned(std::min<int64_t>((items + kPrepThreads - 1) / kPrepThreads, 65535));
     const unsigned gy = unsigned(ctas ? n_ctas : n_jobs);
     if (use_t4(ncols)) {
-        cfg.gridDim = dim3(1, gy, z);
-        return g128 ? cudaLaunchKernelEx(&cfg, t4_prep_kernel<XT, true>, single, jobs, ctas)
-                    : cudaLaunchKernelEx(&cfg, t4_prep_kernel<XT, false>, single, jobs, ctas);
+        cfg.gridDim = dim3(ncols, gy, z);
+        return g128 ? cudaLaunchKernelEx(&cfg, t4_prep_kernel<XT, true>, single, jobs, ctas, 1)
+                    : cudaLaunchKernelEx(&cfg, t4_prep_kernel<XT, false>, single, jobs, ctas, ncols);
     }
     cfg.gridDim = dim3(ncols, gy, z);
     return cudaLaunchKernelEx(&cfg, s8_prep_kernel<XT>, single, jobs, ctas, ncols);
@@ -1673,7 +1854,7 @@ cudaError_t launch_tc(const MvJob &single, const MvParams &prm, int grid, cudaSt
     if (use_t4(prm.ncols)) {
         e = ensure_t4_attr();
         if (e != cudaSuccess) return e;
-        cfg.blockDim = dim3(kTcThreads);
+        cfg.blockDim = dim3(prm.ncols == 2 ? T4Lay<kLayBlocks, 2>::kThreads : kTcThreads);
         MvParams prm2 = prm;
         take_stall(prm2);
         if (prm2.layout == kLaySplit) {
@@ -1682,6 +1863,9 @@ cudaError_t launch_tc(const MvJob &single, const MvParams &prm, int grid, cudaSt
         } else if (prm2.layout == kLayG128) {
             cfg.dynamicSmemBytes = T4Lay<kLayG128>::kSmem;
             e = cudaLaunchKernelEx(&cfg, mv_t4_kernel<kLayG128>, single, prm2);
+        } else if (prm2.ncols == 2) {
+            cfg.dynamicSmemBytes = T4Lay<kLayBlocks, 2>::kSmem;
+            e = cudaLaunchKernelEx(&cfg, mv_t4_kernel<kLayBlocks, 2>, single, prm2);
         } else {
             cfg.dynamicSmemBytes = T4Lay<kLayBlocks>::kSmem;
             e = cudaLaunchKernelEx(&cfg, mv_t4_kernel<kLayBlocks>, single, prm2);
@@ -1716,7 +1900,7 @@ cudaError_t launch_generic(const uint8_t *w, const void *x, int xtype, float *y,
 }  // namespace
 
 size_t matvec_workspace_bytes(int64_t K, int ncols) {
-    return use_t4(ncols) ? t4_prep_bytes(K) : s8_prep_bytes(K, ncols);
+    return use_t4(ncols) ? t4_prep_bytes(K, ncols) : s8_prep_bytes(K, ncols);
 }
 
 bool matvec_fast_path_ok(const void *w, int64_t K) {

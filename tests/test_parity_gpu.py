@@ -178,6 +178,7 @@ MV_CASES = [
     (2048, 2048, 1),   # the 2048 x 2048 single-matrix workload
     (1, 512, 1), (3, 1024, 2), (127, 512, 3), (300, 2048, 4), (257, 1536, 5),
     (64, 512, 8), (1000, 6144, 7), (513, 4096, 6),
+    (300, 2048, 2), (1000, 6144, 2), (129, 512, 2), (257, 4608, 2),   # fp4 path, two columns
     (33, 576, 1), (5, 64, 3), (130, 1088, 8),   # K % 512 != 0: CUDA-core path
 ]
 
@@ -670,7 +671,7 @@ def test_matvec_wide_range(dev, kind, ncols):
     _no_device_error()
 
 
-@pytest.mark.parametrize("ncols", [1, 3, 8])
+@pytest.mark.parametrize("ncols", [1, 2, 3, 8])
 def test_plan_wide_range(dev, ncols):
     g = synth.rng(2203, ncols)
     ents, host = [], []
@@ -716,7 +717,7 @@ def test_matvec_split_wide_range(dev, kind):
     _no_device_error()
 
 
-@pytest.mark.parametrize("ncols", [1, 4])
+@pytest.mark.parametrize("ncols", [1, 2, 4])
 def test_matvec_f16_wide_range(dev, ncols):
     g = synth.rng(2206, ncols)
     N, K = 260, 2048
@@ -841,7 +842,7 @@ def test_gemm_wide_range(dev, kind):
     _no_device_error()
 
 
-@pytest.mark.parametrize("ncols", [1, 4])
+@pytest.mark.parametrize("ncols", [1, 2, 4])
 @pytest.mark.parametrize("scale", [1e-30, 1e30])
 def test_matvec_activation_magnitude(dev, ncols, scale):
     g = synth.rng(2207, ncols, int(np.log10(scale)) + 40)
