@@ -8,18 +8,20 @@
 // application of d per block, and moves the multiply-accumulate onto the
 // 5th-generation tensor cores (tcgen05.mma, accumulators in tensor memory):
 //
-//   ncols = 1     mv_t4_kernel: codes as packed e2m1 (q / 2, two logic ops per
-//                 16 weights), activations as 16 block-scaled e2m1 pieces,
-//                 kind::mxf4 with K = 64 = one block per MMA; the "- 1" is an
-//                 exact per-block correction (see the fp4 section);
-//   ncols 2..8    mv_s8_kernel<NC>: codes as signed e4m3 (q - 1, one byte-permute
+//   ncols 1, 2    mv_t4_kernel: codes as packed e2m1 (q / 2, two logic ops per
+//                 16 weights), activations as 16 block-scaled e2m1 pieces per
+//                 column, kind::mxf4 with K = 64 = one block per MMA; the "- 1"
+//                 is an exact per-block correction (see the fp4 section);
+//   ncols 3..8    mv_s8_kernel<NC>: codes as signed e4m3 (q - 1, one byte-permute
 //                 lookup per 4 weights), activations as 5 block-scaled e4m3
 //                 pieces per column, kind::f8f6f4 with K = 32;
 //   other shapes  mv_generic_kernel: CUDA cores, f32 (K % 512 != 0 or W not
 //                 16-byte aligned).
 //
-// Both tensor-core kernels are persistent, one CTA of 12 warps per SM, over
-// 128-row tiles of one matrix or of a plan's many matrices; a pipeline stage is
+// Both tensor-core kernels are persistent, one CTA per SM of 12 warps (16 with
+// two epilogue warps per lane quarter: the fp4 kernel at two columns, the e4m3
+// kernel), over 128-row tiles of one matrix or of a plan's many matrices; a
+// pipeline stage is
 // one 2-D TMA box of 128 rows x 144 bytes (8 blocks = 512 weights per row) plus
 // the stage's activation image (bulk copy), in an 8-deep shared-memory ring.
 // Warps 0 and 2 stream the even and odd stages, warps 3 and 1 issue the MMAs
@@ -221,7 +223,7 @@ __device__ __forceinline__ uint32_t block_word(const uint32_t (&u)[18], int bi, 
 }
 
 // ---------------------------------------------------------------------------
-// tcgen05 mat-vec on packed fp4 (ncols = 1)
+// tcgen05 mat-vec on packed fp4 (ncols 1 and 2)
 //
 // The codes are exact e2m1 values without arithmetic as well: e2m1 is sign,
 // two exponent bits, one mantissa bit, and a nibble whose only set bits are
@@ -1067,7 +1069,7 @@ __global__ void __maxnreg__(kNc == 1 ? 128 : 112)
 
 
 // ---------------------------------------------------------------------------
-// tcgen05 mat-vec on signed e4m3 codes (ncols 2..8)
+// tcgen05 mat-vec on signed e4m3 codes (ncols 3..8)
 //
 // Codes. The expansion warps turn each 2-bit code into the e4m3 value q - 1
 // (-1, 0, 1, 2 are exact e4m3 values) with one byte-permute lookup per 4 codes:
@@ -1109,7 +1111,7 @@ __host__ __device__ constexpr int s8_img_bytes(int nc) { return s8_n(nc) * kChun
 constexpr int kS8Barriers = 2 * 8 + 2 * 2 + 2 * 2 + 2 + 2 * 4;
 // The fp4 kernel's roles with two epilogue warps per lane quarter (warps 8-11
 // drain accumulator buffer 0, warps 12-15 buffer 1): 16 warps. With one
-// accumulator sub-stage per stage (ncols 2-3) the expansion is the longest
+// accumulator sub-stage per stage (ncols 3) the expansion is the longest
 // role, and it also gets two warps per lane quarter (warps 4-7 expand blocks
 // 0-3 of a stage, warps 16-19 blocks 4-7): 20 warps at most 96 registers each.
 constexpr int kS8EpiWarps = 8;
@@ -1872,7 +1874,6 @@ cudaError_t launch_tc(const MvJob &single, const MvParams &prm, int grid, cudaSt
         }
     } else {
         switch (prm.ncols) {
-            case 2: e = launch_s8_nc<2>(cfg, single, prm); break;
             case 3: e = launch_s8_nc<3>(cfg, single, prm); break;
             case 4: e = launch_s8_nc<4>(cfg, single, prm); break;
             case 5: e = launch_s8_nc<5>(cfg, single, prm); break;

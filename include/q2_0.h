@@ -92,10 +92,10 @@ int q2_0_device_check(void);
  * Precision (finite x; M_b = the largest |x| of the activation block of 64
  * that holds element k; the tensor-core paths have K % 512 == 0 and w 16-byte
  * aligned, other shapes run f32 on CUDA cores):
- *   ncols 1, tensor cores: each element of x is represented to within
- *     2^-33 M_b; zero weights contribute exactly nothing; the rest is f32
- *     rounding: |y - exact| <= 2^-33 sum_k |W[n][k]| M_b + 2^-20 sum_k |W X|;
- *   ncols 2..8, tensor cores: each element keeps 20 bits of its own value,
+ *   ncols 1 and 2, tensor cores (fp4): each element of x is represented to
+ *     within 2^-33 M_b; zero weights contribute exactly nothing; the rest is
+ *     f32 rounding: |y - exact| <= 2^-33 sum_k |W[n][k]| M_b + 2^-20 sum_k |W X|;
+ *   ncols 3..8, tensor cores (e4m3): each element keeps 20 bits of its own value,
  *     with a floor of 2^-33 M_b: |y - exact| <= 2^-33 sum_k |W[n][k]| M_b +
  *     2^-17 sum_k |W X|;
  *   CUDA cores: f32 products and sums, |y - exact| <= 2^-17 sum_k |W X| for
@@ -334,9 +334,9 @@ int q2_0_get_error(void *stream, int64_t *info);
 /*
  * q2_0_test_inject_stall — TEST ONLY: exercises the bounded pipeline waits.
  * (No counterpart on the pages: the failure-detection path of this library.)
- * The next fp4 mat-vec launch on the current device (ncols = 1 on the
- * tensor-core path: q2_0_mul_mat_vec, _ws, _noalloc, _f16, _split, a plan or
- * q2_0_mul_mat_id) stops feeding its pipeline before pipeline stage `stage`
+ * The next fp4 mat-vec launch on the current device (ncols 1 or 2 on the
+ * tensor-core path: q2_0_mul_mat_vec, _ws, _noalloc, _f16, a plan; ncols 1:
+ * _split or q2_0_mul_mat_id) stops feeding its pipeline before pipeline stage `stage`
  * of each CTA (0 = the first), and every pipeline wait of that launch gives up
  * after wait_limit_ns instead of about one second. The consumers' waits on
  * the missing stage then run out: the kernel records Q2_0_DEVERR_TIMEOUT with
