@@ -266,8 +266,9 @@ constexpr int kT4ABufs = 3;
 constexpr int kT4ACol = 256;                           // A buffers at 256 + 64 i
 constexpr int kT4ScaleCol = 448;  // scales A 448..451, B 452..455 (448..463 all hold 1.0)
 // mbarriers: full / empty per stage, a_full / a_empty per A buffer, d_full /
-// d_empty per D buffer, a drain per MMA issuer
-constexpr int kT4Barriers = 2 * kT4Stages + 2 * kT4ABufs + 2 * 2 + 2;
+// d_empty per D buffer, a drain per MMA issuer, and the two-column kernel's
+// tile-end hand-offs (4 + 4, placed in every layout)
+constexpr int kT4Barriers = 2 * kT4Stages + 2 * kT4ABufs + 2 * 2 + 2 + 8;
 // a stage's activation data (image, then block records) is one bulk copy; in
 // shared memory its slots stay 1024-aligned for the swizzled image
 constexpr int kT4ActSlot = 5120;
@@ -306,9 +307,8 @@ struct T4Lay {
     static constexpr int kAct = kImg + kT4BetaBytes * NC;       // image, then the region records
     static constexpr int kActSlot = (kAct + 1023) / 1024 * 1024;
     static constexpr int kStages = L == kLayG128 ? 4 : kT4Stages;
-    // two columns: per lane quarter, the tile-end hand-off between its two
-    // epilogue warps (sums ready, sums read)
-    static constexpr int kBarriers = 2 * kStages + 2 * kT4ABufs + 2 * 2 + 2 + (NC == 2 ? 8 : 0);
+    // as kT4Barriers (the two-column hand-offs are counted for every layout)
+    static constexpr int kBarriers = 2 * kStages + 2 * kT4ABufs + 2 * 2 + 2 + 8;
     static constexpr int kSmem = 1024 /* alignment slack */ + kStages * (kActSlot + kRaw) +
                                  kBarriers * 8;
     static constexpr int kEpi = kEpiWarps * NC;   // epilogue warps
@@ -475,7 +475,7 @@ __global__ void __maxnreg__(kNc == 1 ? 128 : 112)
     uint8_t *raw_ring = act_ring + Lt::kStages * Lt::kActSlot;  // Lt::kStages weight boxes
     uint64_t *full = reinterpret_cast<uint64_t *>(raw_ring + Lt::kStages * Lt::kRaw);
     uint64_t *empty = full + Lt::kStages;
-    uint64_t *a_full = empty + kT4Stages;
+    uint64_t *a_full = empty + Lt::kStages;
     uint64_t *a_empty = a_full + kT4ABufs;
     uint64_t *d_full = a_empty + kT4ABufs;
     uint64_t *d_empty = d_full + 2;
