@@ -33,28 +33,30 @@ def dev():
     return d
 
 
-def _case(dev, seed, N, K):
+def _case(dev, seed, N, K, ncols=1):
     g = synth.rng(seed, N, K)
     w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
-    x = synth.activations(g, 1, K)
+    x = synth.activations(g, ncols, K)
     return w, x, torch.from_numpy(w).to(dev), torch.from_numpy(x).to(dev)
 
 
-@pytest.mark.parametrize("stage", [0, 3])
-def test_stalled_pipeline_times_out_and_recovers(dev, stage):
+@pytest.mark.parametrize("stage,ncols", [(0, 1), (3, 1), (0, 2), (5, 2)])
+def test_stalled_pipeline_times_out_and_recovers(dev, stage, ncols):
+    """ncols 1 and 2 (the two-column fp4 kernel, whose epilogue warps also hand
+    their tile sums over through bounded waits)."""
     N, K = 1000, 4096
-    w, x, wd, xd = _case(dev, 6101, N, K)
+    w, x, wd, xd = _case(dev, 6101, N, K, ncols)
     yo, acc = oracle.matmul(w, N, K, x)
     q.q2_0_test_inject_stall(stage, 2_000_000)          # 2 ms
     t0 = time.perf_counter()
-    q.q2_0_mul_mat_vec(wd, xd, N, K, 1)
+    q.q2_0_mul_mat_vec(wd, xd, N, K, ncols)
     code, info = q.q2_0_get_error()                     # synchronises
     elapsed = time.perf_counter() - t0
     assert code == q.Q2_0_DEVERR_TIMEOUT and info == TAG_STAGE_COPIES, (code, info)
     assert elapsed < 5.0
     # the next calls run normally on the same context
     for _ in range(2):
-        y = q.q2_0_mul_mat_vec(wd, xd, N, K, 1).cpu().numpy()
+        y = q.q2_0_mul_mat_vec(wd, xd, N, K, ncols).cpu().numpy()
         assert oracle.within_tolerance(y, yo, acc, 1e-5, 1e-7).all()
         code, info = q.q2_0_get_error()
         assert code == 0, (code, info)
