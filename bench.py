@@ -5,7 +5,9 @@ One step = one pass of the whole hot path over one batch of synthetic input of
 the 1.7B-class decoder (hidden 2048, 28 layers):
   1. get_rows: 512 seeded token ids from a 151936 x 2048 Q2_0 embedding table;
   2. prefill GEMM at M = 512 tokens over the layer's Q2_0 shapes gate/up
-     (6144 x 2048) and down (2048 x 6144), F32 activations, split fp16 hi+lo;
+     (6144 x 2048, both reading one X) and down (2048 x 6144), F32
+     activations, split fp16 hi+lo, as one grouped plan (the extras time the
+     same products as separate calls and as two plans, gate+up then down);
   3. decode step: the 196 Q2_0 mat-vecs (q, k, v, o, gate, up, down x 28) at
      ncols = 1, each matrix with its own activation vector, as one batched plan.
 value = packed-weight bytes of the decode step / the decode part's device time
@@ -188,13 +190,34 @@ def decode_inputs(ncols: int = 1):
 
 
 def gemm_inputs():
+    """The M = 512 prefill products (name, N, K, w, x). Gate and up read the same
+    X, as both projections of a layer read its normed hidden state; down reads
+    its own."""
+    xs = {}
     out = []
     for i, (name, N, K) in enumerate(GEMM_SHAPES):
         g = synth.rng(SEED + 3, i)
         w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
-        x = synth.activations(g, PREFILL_M, K, synth.PREFILL_OUTLIER_FRAC, synth.PREFILL_OUTLIER)
-        out.append((name, N, K, w, x))
+        if K not in xs:
+            xs[K] = synth.activations(synth.rng(SEED + 4, K), PREFILL_M, K,
+                                      synth.PREFILL_OUTLIER_FRAC, synth.PREFILL_OUTLIER)
+        out.append((name, N, K, w, xs[K]))
     return out
+
+
+def gemm_flops_512():
+    return sum(2.0 * PREFILL_M * N * K for _, N, K in GEMM_SHAPES)
+
+
+def gemm_device_entries(torch, dev, gm, M):
+    """MmPlan entries (w, x, y, N, K, M) on the device; a shared X is copied once."""
+    d_x, ents = {}, []
+    for _, N, K, w, x in gm:
+        if id(x) not in d_x:
+            d_x[id(x)] = torch.from_numpy(x).to(dev)
+        ents.append((torch.from_numpy(w).to(dev), d_x[id(x)],
+                     torch.empty((M, N), dtype=torch.float32, device=dev), N, K, M))
+    return ents
 
 
 def rows_inputs():
@@ -246,14 +269,13 @@ def run_ours(args):
     dec_y_bytes = d_yall.numel() * 4
     plan = q.MvPlan(d_dec, nc) if args.only in ("all", "decode") else None
 
+    # The prefill part: the three M = 512 products as one grouped plan (one
+    # prepass for the two distinct X, one tensor-core launch over all output
+    # tiles, one stream-K reduction).
     gm = gemm_inputs()
-    d_gm = []
-    for name, N, K, w, x in gm:
-        ws = torch.empty(q.q2_0_mul_mat_workspace_size(PREFILL_M, N, K), dtype=torch.uint8,
-                         device=dev)
-        d_gm.append((torch.from_numpy(w).to(dev), torch.from_numpy(x).to(dev),
-                     torch.empty((PREFILL_M, N), dtype=torch.float32, device=dev), N, K, ws))
+    d_gm = gemm_device_entries(torch, dev, gm, PREFILL_M)
     gemm_flops = sum(2.0 * PREFILL_M * N * K for _, N, K, _, _ in gm)
+    mm_plan = q.MmPlan(d_gm, q.Q2_0_PREC_F16_SPLIT) if args.only in ("all", "gemm") else None
 
     table, ids = rows_inputs()
     d_table = torch.from_numpy(table).to(dev)
@@ -264,7 +286,7 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     launches_per_step = (1 if args.only in ("all", "get_rows") else 0) + \
-        (3 * len(d_gm) if args.only in ("all", "gemm") else 0) + \
+        (mm_plan.launches if mm_plan is not None else 0) + \
         (plan.launches if plan is not None else 0)
 
     run_rows = args.only in ("all", "get_rows")
@@ -280,9 +302,7 @@ def run_ours(args):
             if ev:
                 ev[1].record(stream)
             if run_gemm:
-                for w, x, y, N, K, ws in d_gm:
-                    q.q2_0_mul_mat(w, x, N, K, PREFILL_M, q.Q2_0_PREC_F16_SPLIT, y=y,
-                                   workspace=ws, stream=stream)
+                mm_plan.execute(stream)
             if ev:
                 ev[2].record(stream)
             if run_dec:
@@ -319,11 +339,7 @@ def run_ours(args):
             graphs.append(("rows", capture(lambda: q.q2_0_get_rows(
                 d_table, VOCAB, HIDDEN, d_ids, out=d_rows, stream=stream))))
         if run_gemm:
-            def gemms():
-                for w, x, y, N, K, ws in d_gm:
-                    q.q2_0_mul_mat(w, x, N, K, PREFILL_M, q.Q2_0_PREC_F16_SPLIT, y=y,
-                                   workspace=ws, stream=stream)
-            graphs.append(("gemm", capture(gemms)))
+            graphs.append(("gemm", capture(lambda: mm_plan.execute(stream))))
         if flush_buf is not None:
             graphs.append(("flush", capture(lambda: torch.sum(flush_buf, dim=0, out=flush_out))))
         if run_dec:
@@ -426,10 +442,11 @@ def run_ours(args):
                  "unit": "TFLOP/s", "frac": round(per_gpu_gemm / tpk, 4),
                  "traffic": committed_traffic("gemm_tc_kernel/prefill_1p7b_m512"),
                  "tensor_frac_hi_lo": round(2 * per_gpu_gemm / tpk, 4),
-                 "kernel": "gemm_tc_kernel (M=512, fp16 hi+lo split, incl. prepass)",
+                 "kernel": "gemm_tc_kernel (one grouped plan over the three M=512 products, "
+                           "fp16 hi+lo split, incl. its prepass and stream-K reduction)",
                  "peak_source": peaks["source"] + " bf16 (fp16 dense rate is the same)"}
     # The dominant kernel: the decode mat-vec kernel has the largest single-kernel
-    # share of the step's launch list (each GEMM part is three kernels: prepass,
+    # share of the step's launch list (the GEMM part is three kernels: prepass,
     # tensor-core kernel, stream-K reduction), and it carries the headline metric.
     dominant, other = roof_mv, roof_gemm
 
@@ -448,7 +465,10 @@ def run_ours(args):
             "config": {"workload": WORKLOAD if nc == 1 else WORKLOAD.replace("ncols=1", f"ncols={nc}"),
                        "ncols": nc, "decode_matrices": len(d_dec),
                        "decode_weight_bytes": dec_bytes, "prefill_M": PREFILL_M,
-                       "gemm_prec": "f16_split", "get_rows_ids": N_IDS,
+                       "gemm_prec": "f16_split",
+                       "gemm": "gate and up (6144x2048, one shared X) and down (2048x6144) as "
+                               "one grouped plan",
+                       "get_rows_ids": N_IDS,
                        "l2": "inputs larger than L2 (396 MB packed weights streamed per step); "
                              "a 256 MB read between the GEMM part and the decode part writes the "
                              "GEMM outputs back before the decode part (timed in the step, in "
@@ -469,6 +489,8 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if plan is not None:
         plan.close()
+    if mm_plan is not None:
+        mm_plan.close()
     if dist is not None:
         dist.destroy_process_group()
 
@@ -481,12 +503,14 @@ def measure_extras(torch, q, stream, dev, hbm_peak: float, reps: int = 20):
       - the same head mat-vec on the split layout (codes and scales in
         separate arrays), against the 18-byte layout, and the split itself;
       - the M = 512 prefill GEMMs with F16 activations (q2_0_mul_mat_f16);
+      - the M = 512 split products as three q2_0_mul_mat calls, and as two
+        plans in a layer's order (gate and up, then down);
       - the group-128 packing of the head-sized matrix: exact repack to the
         64-weight layout (bytes read + written) and the direct mat-vec;
       - the 8B-class decode step (253 matrices with the 151936 x 4096 head,
         2,128,527,360 packed bytes, ncols 1) as one plan;
       - the 8B-class prefill GEMMs at M = 2048 (4096x4096, 12288x4096,
-        4096x12288), split fp16 hi+lo;
+        4096x12288), split fp16 hi+lo, as three calls and as one plan;
       - the expert mat-vec (q2_0_mul_mat_id) of one 128-expert layer with
         768 x 2048 experts, 8 experts per token, at 1 and 64 tokens.
     The 8B-class weights and activations are drawn on the device
@@ -544,6 +568,31 @@ def measure_extras(torch, q, stream, dev, hbm_peak: float, reps: int = 20):
     msg = timed(gemms)
     gemm_shapes = [[PREFILL_M, Ng, Kg] for _, _, _, Ng, Kg, _ in gm]
     del gm
+    # The M = 512 split products of the step's prefill part two other ways: as
+    # three separate calls (a prepass, a tensor-core launch and a reduction
+    # each), and as a layer's MLP orders them: gate and up in one plan, then
+    # down in a second (down reads the gated product, so it cannot share the
+    # first launch).
+    ents = gemm_device_entries(torch, dev, gemm_inputs(), PREFILL_M)
+    wss = [torch.empty(q.q2_0_mul_mat_workspace_size(PREFILL_M, Ng, Kg), dtype=torch.uint8,
+                       device=dev) for _, _, _, Ng, Kg, _ in ents]
+
+    def per_call():
+        for (wg, xg, yg, Ng, Kg, Mg), ws in zip(ents, wss):
+            q.q2_0_mul_mat(wg, xg, Ng, Kg, Mg, q.Q2_0_PREC_F16_SPLIT, y=yg, workspace=ws,
+                           stream=stream)
+
+    ms_pc = timed(per_call)
+    plan_gu, plan_dn = q.MmPlan(ents[:2]), q.MmPlan(ents[2:])
+
+    def two_plans():
+        plan_gu.execute(stream)
+        plan_dn.execute(stream)
+
+    ms_2p = timed(two_plans)
+    plan_gu.close()
+    plan_dn.close()
+    del ents, wss
     # group-128 packing: the exact repack to the 64-weight layout, and the direct
     # CUDA-core mat-vec, on the head-sized matrix
     w128 = torch.from_numpy(synth.packed_matrix_g128(g, N, K, *synth.DECODE_SCALE)).to(dev)
@@ -590,6 +639,9 @@ def measure_extras(torch, q, stream, dev, hbm_peak: float, reps: int = 20):
                            stream=stream)
 
     ms2 = timed(gemms2)
+    plan2 = q.MmPlan([(wg, xg, yg, Ng, Kg, M2) for wg, xg, yg, Ng, Kg, _ in g2])
+    ms2p = timed(lambda: plan2.execute(stream))
+    plan2.close()
     del g2
 
     # expert mat-vec: 128 experts of 768 x 2048, 8 per token
@@ -620,7 +672,14 @@ def measure_extras(torch, q, stream, dev, hbm_peak: float, reps: int = 20):
                                   "matrices": 253},
         "gemm_split_m2048_8b": {"tflops": round(flops2 / (ms2 * 1e-3) / 1e12, 2),
                                 "us": round(ms2 * 1e3, 2),
+                                "plan_tflops": round(flops2 / (ms2p * 1e-3) / 1e12, 2),
+                                "plan_us": round(ms2p * 1e3, 2),
                                 "shapes": [[M2, 4096, 4096], [M2, 12288, 4096], [M2, 4096, 12288]]},
+        "gemm_split_m512_per_call": {"tflops": round(gemm_flops_512() / (ms_pc * 1e-3) / 1e12, 2),
+                                     "us": round(ms_pc * 1e3, 2), "launches": 9},
+        "gemm_split_m512_two_plans": {"tflops": round(gemm_flops_512() / (ms_2p * 1e-3) / 1e12, 2),
+                                      "us": round(ms_2p * 1e3, 2), "launches": 6,
+                                      "plans": "gate+up, then down"},
         "head_matvec_split_layout_151936x4096": {
             "split_bytes": split_bytes, "us": round(ms_sp * 1e3, 2),
             "gbs": round(head_bytes / (ms_sp * 1e-3) / 1e9, 1),

@@ -55,6 +55,8 @@ EXPORTS = (
     "q2_0_g128_to_g64", "q2_0_g128_get_rows", "q2_0_g128_mul_mat_vec",
     "q2_0_mul_mat_id_workspace_size", "q2_0_mul_mat_id",
     "q2_0_split_bytes", "q2_0_split_layout", "q2_0_join_layout", "q2_0_mul_mat_vec_split",
+    "q2_0_mm_plan_create", "q2_0_mm_plan_execute", "q2_0_mm_plan_launches",
+    "q2_0_mm_plan_destroy",
 )
 
 
@@ -67,6 +69,11 @@ class Q2Error(RuntimeError):
 class _MvDesc(ctypes.Structure):
     _fields_ = [("w", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
                 ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+class _MmDesc(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("M", ctypes.c_int64)]
 
 
 _lock = threading.Lock()
@@ -118,6 +125,15 @@ def lib():
             L.q2_0_mul_mat_workspace_size.restype = sz
             L.q2_0_mul_mat.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, sz, vp]
             L.q2_0_mul_mat.restype = i32
+            L.q2_0_mm_plan_create.argtypes = [ctypes.POINTER(_MmDesc), i32, i32,
+                                              ctypes.POINTER(vp)]
+            L.q2_0_mm_plan_create.restype = i32
+            L.q2_0_mm_plan_execute.argtypes = [vp, vp]
+            L.q2_0_mm_plan_execute.restype = i32
+            L.q2_0_mm_plan_launches.argtypes = [vp]
+            L.q2_0_mm_plan_launches.restype = i32
+            L.q2_0_mm_plan_destroy.argtypes = [vp]
+            L.q2_0_mm_plan_destroy.restype = None
             L.q2_0_mul_mat_vec_f16.argtypes = [vp, vp, vp, i64, i64, i32, vp]
             L.q2_0_mul_mat_vec_f16.restype = i32
             L.q2_0_mul_mat_f16.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
@@ -315,6 +331,45 @@ def q2_0_mul_mat(w: torch.Tensor, x: torch.Tensor, N: int, K: int, M: int | None
                             _stream(stream))
     _check("q2_0_mul_mat", st)
     return y
+
+
+class MmPlan:
+    """A grouped GEMM plan (q2_0_mm_plan_*): keeps references to its tensors."""
+
+    def __init__(self, entries, prec: int = Q2_0_PREC_F16_SPLIT):
+        """entries: iterable of (w uint8, x f32 [M][K], y f32 [M][N], N, K, M)."""
+        self._keep = []
+        descs = []
+        for (w, x, y, N, K, M) in entries:
+            descs.append(_MmDesc(_dev(w, "w", torch.uint8, packed_bytes(N, K)),
+                                 _dev(x, "x", torch.float32, M * K),
+                                 _dev(y, "y", torch.float32, M * N), N, K, M))
+            self._keep.append((w, x, y))
+        arr = (_MmDesc * len(descs))(*descs)
+        h = ctypes.c_void_p()
+        _check("q2_0_mm_plan_create",
+               lib().q2_0_mm_plan_create(arr, len(descs), prec, ctypes.byref(h)))
+        self._h = h
+        self.prec = prec
+        self.n = len(descs)
+
+    @property
+    def launches(self) -> int:
+        return int(lib().q2_0_mm_plan_launches(self._h))
+
+    def execute(self, stream=None):
+        _check("q2_0_mm_plan_execute", lib().q2_0_mm_plan_execute(self._h, _stream(stream)))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().q2_0_mm_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def q2_0_mul_mat_f16(w: torch.Tensor, x: torch.Tensor, N: int, K: int, M: int | None = None,

@@ -245,6 +245,33 @@ int q2_0_mul_mat_f16(const void *w, const void *x, float *y, int64_t N, int64_t 
     return mul_mat_impl(w, x, kXF16, y, N, K, M, Q2_0_PREC_F16, workspace, workspace_bytes, stream);
 }
 
+int q2_0_mm_plan_create(const q2_0_mm_desc *descs, int n_desc, int prec, q2_0_mm_plan **plan) {
+    if (!plan) return Q2_0_EINVAL;
+    *plan = nullptr;
+    if (!descs || n_desc < 1 || (prec != Q2_0_PREC_F16_SPLIT && prec != Q2_0_PREC_F16))
+        return Q2_0_EINVAL;
+    for (int i = 0; i < n_desc; ++i) {
+        const q2_0_mm_desc &d = descs[i];
+        if (!d.w || !d.x || !d.y || d.N < 1 || d.M < 1 || d.N > (int64_t(1) << 31) - 1 ||
+            d.M > (int64_t(1) << 31) - 1 || !valid_k(d.K))
+            return Q2_0_EINVAL;
+    }
+    int st = check_device(nullptr);
+    if (st != Q2_0_OK) return st;
+    return mm_plan_create(descs, n_desc, prec, plan);
+}
+
+int q2_0_mm_plan_execute(const q2_0_mm_plan *plan, void *stream) {
+    if (!plan) return Q2_0_EINVAL;
+    return mm_plan_execute(plan, as_stream(stream));
+}
+
+int q2_0_mm_plan_launches(const q2_0_mm_plan *plan) { return plan ? mm_plan_launches(plan) : 0; }
+
+void q2_0_mm_plan_destroy(q2_0_mm_plan *plan) {
+    if (plan) mm_plan_destroy(plan);
+}
+
 size_t q2_0_split_bytes(int64_t N, int64_t K) {
     if (N < 1 || N > (int64_t(1) << 31) - 1 || !valid_k(K)) return 0;
     return soa_bytes(N, K);

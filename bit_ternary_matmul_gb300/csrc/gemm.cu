@@ -29,6 +29,7 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "q2_0_device.cuh"
 #include "q2_0_tcgen05.cuh"
@@ -57,19 +58,54 @@ constexpr int kPartialBytes = kBN * kWT * kBM * 4;  // one fp32 unit tile
 
 constexpr int kTagGemm = 200;
 
-struct GemmArgs {
-    CUtensorMap w_map;   // uint8 [N][K/64*18], box {144, 256}
-    CUtensorMap xh_map;  // fp16 [M][K], box {64, 128}, 128B swizzle
+// One product of a launch: Y = W X^T with its own tensor maps and its place in
+// the launch's slab order. A q2_0_mul_mat call is a launch of one product; a
+// plan (q2_0_mm_plan_*) pools several, e.g. the projections that share one X.
+struct GemmJob {  // 64-byte aligned through its CUtensorMap members
+    CUtensorMap w_map;     // uint8 [N][K/64*18], box {144, 256}
+    CUtensorMap xh_map;    // fp16 [M][K], box {64, 128}, 128B swizzle
     CUtensorMap xl_map;
-    float *y;
+    float *y;              // [M][N]
+    const int *row_shift;  // [M]: X row m entered the MMA as X * 2^row_shift[m]
+    long long slab0;       // the product's first slab in the launch's slab order
     int M, N, K;
-    int split;  // 1: hi + lo, 0: hi only
-    int n_units, n_mtiles;  // units = (N / 256 rounded up) x (M / 128 rounded up)
-    long long total_slabs;  // n_units * K / 64: the stream-K iteration space
+    int n_mtiles;          // units = (N / 256 rounded up) x n_mtiles (M / 128 rounded up)
+};
+
+struct GemmArgs {
+    GemmJob single;         // the product of a single call
+    const GemmJob *jobs;    // a plan's products in device memory, slab0 ascending; or null
+    int n_jobs;
+    int split;              // 1: hi + lo, 0: hi only
+    long long total_slabs;  // sum over the products of units * K / 64: the stream-K space
     float *partials;        // 2 slots per CTA of kBN x (kWT * kBM) fp32
-    const int *row_shift;   // [M]: X row m entered the MMA as X * 2^row_shift[m]
     unsigned long long *err;
 };
+
+// Where global slab g lies: its product, unit, slab within the unit and the
+// unit's first global slab. Products are concatenated in the slab order, each
+// unit-major (a unit's K slabs consecutive).
+struct SlabPos {
+    const GemmJob *job;
+    int u, kb, n_slabs;
+    long long ustart;
+};
+__device__ __forceinline__ SlabPos locate(const GemmArgs &a, long long g) {
+    const GemmJob *J = &a.single;
+    if (a.jobs) {
+        int j = 0;
+        while (j + 1 < a.n_jobs && a.jobs[j + 1].slab0 <= g) ++j;
+        J = a.jobs + j;
+    }
+    SlabPos p;
+    p.job = J;
+    p.n_slabs = J->K / kSlabK;
+    const long long local = g - J->slab0;
+    p.u = int(local / p.n_slabs);
+    p.kb = int(local % p.n_slabs);
+    p.ustart = J->slab0 + (long long)p.u * p.n_slabs;
+    return p;
+}
 
 // Stream-K: CTA c owns global slabs [T*c/G, T*(c+1)/G) of the unit-major slab
 // order. A unit whose slabs span several CTAs is summed afterwards by
@@ -99,8 +135,20 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
 // never overflows fp16, and the lo parts of small elements stay above fp16's
 // subnormal range down to 2^-29 of the row maximum. F16 rows are only scaled
 // up (s >= 0), which keeps them exact. The scaling is exact and undone on the
-// f32 result (y = acc * 2^-s). One CTA per row; X 16-byte aligned.
+// f32 result (y = acc * 2^-s). One CTA per row and grid row y per activation
+// matrix of the launch; X 16-byte aligned.
 // ---------------------------------------------------------------------------
+constexpr int kMaxPrepX = 8;
+struct GemmPrepSet {  // the distinct activation matrices of one prep launch
+    const void *x[kMaxPrepX];
+    __half *xh[kMaxPrepX];
+    __half *xl[kMaxPrepX];  // null unless split
+    int *row_shift[kMaxPrepX];
+    int M[kMaxPrepX];
+    int K[kMaxPrepX];
+    int split;
+};
+
 __device__ __forceinline__ void load16(const float *p, float (&v)[16]) {
     const float4 *src = reinterpret_cast<const float4 *>(p);
 #pragma unroll
@@ -139,12 +187,17 @@ constexpr int kPrepCache = 3;
 // One CTA per row: the row maximum by a block reduction, then the conversion.
 template <typename XT>
 __global__ void __launch_bounds__(kPrepThreads) gemm_prep_kernel(
-    const XT *__restrict__ x, __half *__restrict__ xh, __half *__restrict__ xl,
-    int *__restrict__ row_shift, int M, int K, int split) {
+    const __grid_constant__ GemmPrepSet ps) {
     // The GEMM kernel that follows may start its prologue and weight loads now;
     // it waits for this grid before reading X.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int m = blockIdx.x;
+    const int e = blockIdx.y, m = blockIdx.x;
+    if (m >= ps.M[e]) return;  // grid x covers the set's largest M
+    const XT *__restrict__ x = static_cast<const XT *>(ps.x[e]);
+    __half *__restrict__ xh = ps.xh[e];
+    __half *__restrict__ xl = ps.xl[e];
+    int *__restrict__ row_shift = ps.row_shift[e];
+    const int K = ps.K[e], split = ps.split;
     const int tid = threadIdx.x, lane = tid & 31;
     const XT *xr = x + size_t(m) * K;
     const int groups = K / 16;
@@ -254,7 +307,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n_slabs = a.K / kSlabK;
     const long long g_begin = sk_begin(blockIdx.x, a.total_slabs, gridDim.x);
     const long long g_end = sk_begin(blockIdx.x + 1, a.total_slabs, gridDim.x);
 
@@ -282,11 +334,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    // Unit u -> (row pair, token tile) with the token tile fastest, so CTAs running
-    // together share weight rows in L2.
-    auto unit_coords = [&](int u, int &n0, int &m0) {
-        n0 = (u / a.n_mtiles) * (kWT * kBM);
-        m0 = (u % a.n_mtiles) * kBN;
+    // Unit u of a product -> (row pair, token tile) with the token tile fastest,
+    // so CTAs running together share weight rows in L2.
+    auto unit_coords = [&](const SlabPos &p, int &n0, int &m0) {
+        n0 = (p.u / p.job->n_mtiles) * (kWT * kBM);
+        m0 = (p.u % p.job->n_mtiles) * kBN;
     };
 
     if (warp == 0) {
@@ -297,11 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t ph = 0, wph = 0;
             bool ok = true, prep_done = false;
             for (long long g = g_begin; g < g_end && ok;) {
-                const int u = int(g / n_slabs), kb = int(g % n_slabs);
-                const int ke = seg_end(n_slabs, kb, g_end - g);
+                const SlabPos p = locate(a, g);
+                const int kb = p.kb;
+                const int ke = seg_end(p.n_slabs, kb, g_end - g);
                 g += ke - kb;
                 int n0, m0;
-                unit_coords(u, n0, m0);
+                unit_coords(p, n0, m0);
+                const GemmJob *J = p.job;
                 for (int kk = kb; kk < ke; ++kk) {
                     if ((kk & 7) == 0 || kk == kb) {
                         if (!mbar_wait(&w_free[wst], wph ^ 1u, a.err, kTagGemm + 1)) {
@@ -309,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                             break;
                         }
                         mbar_arrive_expect_tx(&w_full[wst], kWBoxBytes);
-                        tma_load_2d(w_s + wst * kWBoxBytes, &a.w_map, (kk >> 3) * 144, n0,
+                        tma_load_2d(w_s + wst * kWBoxBytes, &J->w_map, (kk >> 3) * 144, n0,
                                     &w_full[wst]);
                     }
                     if (!mbar_wait(&slot_free[st], ph ^ 1u, a.err, kTagGemm + 2)) {
@@ -321,9 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                         prep_done = true;
                     }
                     mbar_arrive_expect_tx(&x_full[st], x_bytes);
-                    tma_load_2d(xh_s + st * kXTileBytes, &a.xh_map, kk * kSlabK, m0, &x_full[st]);
+                    tma_load_2d(xh_s + st * kXTileBytes, &J->xh_map, kk * kSlabK, m0, &x_full[st]);
                     if (a.split)
-                        tma_load_2d(xl_s + st * kXTileBytes, &a.xl_map, kk * kSlabK, m0,
+                        tma_load_2d(xl_s + st * kXTileBytes, &J->xl_map, kk * kSlabK, m0,
                                     &x_full[st]);
                     if (++st == kStages) {
                         st = 0;
@@ -369,8 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         bool ok = true;
         int nu = 0;
         for (long long g = g_begin; g < g_end && ok; ++nu) {
-            const int kb = int(g % n_slabs);
-            const int ke = seg_end(n_slabs, kb, g_end - g);
+            const SlabPos p = locate(a, g);
+            const int kb = p.kb;
+            const int ke = seg_end(p.n_slabs, kb, g_end - g);
             g += ke - kb;
             if (nu > 0 &&
                 !__all_sync(0xffffffffu,
@@ -431,8 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         uint32_t ph = 0, wph = 0;
         bool ok = true;
         for (long long g = g_begin; g < g_end && ok;) {
-            const int kb = int(g % n_slabs);
-            const int ke = seg_end(n_slabs, kb, g_end - g);
+            const SlabPos p = locate(a, g);
+            const int kb = p.kb;
+            const int ke = seg_end(p.n_slabs, kb, g_end - g);
             g += ke - kb;
             for (int kk = kb; kk < ke; ++kk) {
                 const bool got =
@@ -501,36 +557,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         bool dead = false;
         int nu = 0;
         for (long long g = g_begin; g < g_end; ++nu) {
-            const int u = int(g / n_slabs), kb = int(g % n_slabs);
-            const int ke = seg_end(n_slabs, kb, g_end - g);
+            const SlabPos p = locate(a, g);
+            const int kb = p.kb;
+            const int ke = seg_end(p.n_slabs, kb, g_end - g);
             g += ke - kb;
             int n0, m0;
-            unit_coords(u, n0, m0);
+            unit_coords(p, n0, m0);
+            const int jM = p.job->M, jN = p.job->N;
+            float *const jy = p.job->y;
+            const int *const jshift = p.job->row_shift;
             if (!dead) {
                 const bool got = mbar_wait(acc_full, uint32_t(nu & 1), a.err, kTagGemm + 8);
                 dead = !__all_sync(0xffffffffu, got);
             }
             if (dead) continue;
-            const bool whole = kb == 0 && ke == n_slabs;
+            const bool whole = kb == 0 && ke == p.n_slabs;
             tc_fence_after();
             const int n = n0 + rloc;
             // partial tiles: slot 2c for a CTA's first segment, 2c + 1 for its last
-            const long long ustart = (long long)u * n_slabs;
             float *mine = a.partials +
-                          size_t(2 * blockIdx.x + (g_begin >= ustart ? 0 : 1)) * (kPartialBytes / 4);
+                          size_t(2 * blockIdx.x + (g_begin >= p.ustart ? 0 : 1)) * (kPartialBytes / 4);
 #pragma unroll 1
             for (int cb = 0; cb < kBN; cb += 32) {
                 uint32_t v[32];
                 tmem_ld32(tmem_base + lane_addr + kAccCol + t * kBN + cb, v);
                 if (whole) {
                     // the 32 tokens' row exponents: one load per lane, shared by shuffles
-                    const int sh = m0 + cb + lane < a.M ? a.row_shift[m0 + cb + lane] : 0;
+                    const int sh = m0 + cb + lane < jM ? jshift[m0 + cb + lane] : 0;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int shj = __shfl_sync(0xffffffffu, sh, j);
                         const int m = m0 + cb + j;
-                        if (n < a.N && m < a.M)
-                            a.y[size_t(m) * a.N + n] = mul_pow2(__uint_as_float(v[j]), -shj);
+                        if (n < jN && m < jM)
+                            jy[size_t(m) * jN + n] = mul_pow2(__uint_as_float(v[j]), -shj);
                     }
                 } else {
 #pragma unroll
@@ -564,19 +623,23 @@ constexpr int kReduceSlices = 8;
 constexpr int kReduceThreads = 256;
 
 __global__ void __launch_bounds__(kReduceThreads) gemm_reduce_kernel(
-    const float *__restrict__ partials, const int *__restrict__ row_shift, float *__restrict__ y,
-    int M, int N, int n_mtiles, int n_slabs, long long total_slabs) {
+    const __grid_constant__ GemmArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int G = int(gridDim.y), c = int(blockIdx.y);
+    const long long total_slabs = a.total_slabs;
     const long long gb = sk_begin(c, total_slabs, G);
-    const int u = int(gb / n_slabs);
-    const long long ustart = (long long)u * n_slabs;
+    const SlabPos p = locate(a, gb);
+    const long long ustart = p.ustart;
     if (gb == ustart) return;  // c begins its first unit: not a split unit's finisher
     const int c_first = sk_owner(ustart, total_slabs, G);
-    const int c_last = sk_owner(ustart + n_slabs - 1, total_slabs, G);
+    const int c_last = sk_owner(ustart + p.n_slabs - 1, total_slabs, G);
     if (c != c_last) return;
-    const int n0 = (u / n_mtiles) * (kWT * kBM);
-    const int m0 = (u % n_mtiles) * kBN;
+    const int M = p.job->M, N = p.job->N;
+    float *const y = p.job->y;
+    const int *const row_shift = p.job->row_shift;
+    const float *const partials = a.partials;
+    const int n0 = (p.u / p.job->n_mtiles) * (kWT * kBM);
+    const int m0 = (p.u % p.job->n_mtiles) * kBN;
     constexpr int kRowVec = kWT * kBM / 4;          // float4 per token row
     constexpr int kTileVec = kBN * kRowVec;         // float4 per tile
     constexpr int kSliceVec = kTileVec / kReduceSlices;
@@ -693,26 +756,99 @@ struct GemmLayout {
     size_t partials;  // offset of the partial tiles
     size_t shifts;    // offset of the per-row exponents (int [M])
     size_t total;
-    int n_units, n_mtiles, grid;
+    int n_mtiles, grid;
     long long total_slabs;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+int mtiles_of(int64_t M) { return int((M + kBN - 1) / kBN); }
+
+// Slabs of one product: units (256 weight rows x 128 tokens) times K / 64.
+long long slabs_of(int64_t M, int64_t N, int64_t K) {
+    const long long units = (long long)((N + kWT * kBM - 1) / (kWT * kBM)) * mtiles_of(M);
+    return units * (K / kSlabK);
+}
+
+// Stream-K grid: one CTA per SM (at most kMaxGrid), at least 8 slabs each.
+int grid_of(long long total_slabs, int sms) {
+    const long long by_work = std::max<long long>(1, total_slabs / 8);
+    return int(std::min<long long>(std::min<long long>(sms > 0 ? sms : kMaxGrid, kMaxGrid), by_work));
+}
+
 // Workspace: [X_hi][X_lo (split)][2 partial tiles per stream-K CTA][row exponents].
-// The grid is at most kMaxGrid CTAs, at least 8 slabs each.
 GemmLayout gemm_layout(int64_t M, int64_t N, int64_t K, int prec, int sms) {
     GemmLayout L;
     L.part = align256(size_t(M) * K * 2);
-    L.n_mtiles = int((M + kBN - 1) / kBN);
-    L.n_units = int((N + kWT * kBM - 1) / (kWT * kBM)) * L.n_mtiles;
-    L.total_slabs = (long long)L.n_units * (K / kSlabK);
-    const long long by_work = std::max<long long>(1, L.total_slabs / 8);
-    L.grid = int(std::min<long long>(std::min<long long>(sms > 0 ? sms : kMaxGrid, kMaxGrid), by_work));
+    L.n_mtiles = mtiles_of(M);
+    L.total_slabs = slabs_of(M, N, K);
+    L.grid = grid_of(L.total_slabs, sms);
     L.partials = (prec == Q2_0_PREC_F16_SPLIT ? 2 : 1) * L.part;
     L.shifts = L.partials + size_t(2) * L.grid * kPartialBytes;
     L.total = L.shifts + align256(size_t(M) * 4);
     return L;
+}
+
+// A product's tensor maps and scalars: W [N][K/64*18] bytes, X_hi and X_lo fp16
+// [M][K] (xl null for the hi-only precision).
+bool make_gemm_job(GemmJob &J, const uint8_t *w, const __half *xh, const __half *xl, float *y,
+                   const int *row_shift, int64_t M, int64_t N, int64_t K, long long slab0) {
+    std::memset(&J, 0, sizeof(J));
+    const uint64_t row_bytes = uint64_t(K / 64) * 18;
+    if (!encode_tmap_2d(&J.w_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row_bytes, uint64_t(N),
+                        row_bytes, 144, kWT * kBM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tmap_2d(&J.xh_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, uint64_t(K), uint64_t(M),
+                        uint64_t(K) * 2, kSlabK, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return false;
+    if (xl && !encode_tmap_2d(&J.xl_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xl, uint64_t(K),
+                              uint64_t(M), uint64_t(K) * 2, kSlabK, kBN,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+        return false;
+    J.y = y;
+    J.row_shift = row_shift;
+    J.slab0 = slab0;
+    J.M = int(M);
+    J.N = int(N);
+    J.K = int(K);
+    J.n_mtiles = mtiles_of(M);
+    return true;
+}
+
+template <typename XT>
+cudaError_t launch_prep(const GemmPrepSet &ps, int n_x, int max_m, cudaStream_t s) {
+    gemm_prep_kernel<XT><<<dim3(unsigned(max_m), unsigned(n_x)), kPrepThreads, 0, s>>>(ps);
+    return cudaGetLastError();
+}
+
+// The tensor-core kernel and its stream-K reduction, each a programmatic
+// dependent of the launch before it on the stream.
+cudaError_t launch_gemm_pair(const GemmArgs &args, int grid, cudaStream_t s) {
+    cudaError_t e = ensure_attr();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = gemm_smem_bytes();
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel, args);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(kReduceSlices, unsigned(grid));
+    cfg.blockDim = dim3(kReduceThreads);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, gemm_reduce_kernel, args);
+}
+
+template <typename XT>
+cudaError_t launch_generic(const uint8_t *w, const XT *x, float *y, int64_t N, int64_t K,
+                           int64_t M, cudaStream_t s) {
+    dim3 grid(unsigned((N + 31) / 32), unsigned((M + 7) / 8));
+    gemm_generic_kernel<XT><<<grid, dim3(32, 8), 0, s>>>(w, x, y, int(M), int(N), int(K));
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -725,14 +861,11 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int prec) {
 int gemm_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, int64_t K,
              int64_t M, int prec, void *ws, size_t ws_bytes, cudaStream_t s) {
     if (!tc_path_ok(w, x, K)) {
-        dim3 grid(unsigned((N + 31) / 32), unsigned((M + 7) / 8));
-        if (xtype == kXF16)
-            gemm_generic_kernel<__half><<<grid, dim3(32, 8), 0, s>>>(
-                w, static_cast<const __half *>(x), y, int(M), int(N), int(K));
-        else
-            gemm_generic_kernel<float><<<grid, dim3(32, 8), 0, s>>>(
-                w, static_cast<const float *>(x), y, int(M), int(N), int(K));
-        return cuda_status(cudaGetLastError());
+        const cudaError_t e =
+            xtype == kXF16
+                ? launch_generic(w, static_cast<const __half *>(x), y, N, K, M, s)
+                : launch_generic(w, static_cast<const float *>(x), y, N, K, M, s);
+        return cuda_status(e);
     }
     // F16 activations are exact fp16 operands: no lo part
     const int split = (prec == Q2_0_PREC_F16_SPLIT && xtype == kXF32) ? 1 : 0;
@@ -745,59 +878,186 @@ int gemm_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, in
     __half *xl = split ? reinterpret_cast<__half *>(wsb + L.part) : nullptr;
     float *partials = reinterpret_cast<float *>(wsb + L.partials);
     int *row_shift = reinterpret_cast<int *>(wsb + L.shifts);
-    if (xtype == kXF16)
-        gemm_prep_kernel<__half><<<unsigned(M), kPrepThreads, 0, s>>>(
-            static_cast<const __half *>(x), xh, xl, row_shift, int(M), int(K), split);
-    else
-        gemm_prep_kernel<float><<<unsigned(M), kPrepThreads, 0, s>>>(
-            static_cast<const float *>(x), xh, xl, row_shift, int(M), int(K), split);
-    if (cudaGetLastError() != cudaSuccess) return Q2_0_ECUDA;
+    GemmPrepSet ps;
+    std::memset(&ps, 0, sizeof(ps));
+    ps.x[0] = x;
+    ps.xh[0] = xh;
+    ps.xl[0] = xl;
+    ps.row_shift[0] = row_shift;
+    ps.M[0] = int(M);
+    ps.K[0] = int(K);
+    ps.split = split;
+    const cudaError_t pe = xtype == kXF16 ? launch_prep<__half>(ps, 1, int(M), s)
+                                          : launch_prep<float>(ps, 1, int(M), s);
+    if (pe != cudaSuccess) return Q2_0_ECUDA;
 
     GemmArgs args;
     std::memset(&args, 0, sizeof(args));
-    const uint64_t row_bytes = uint64_t(K / 64) * 18;
-    if (!encode_tmap_2d(&args.w_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row_bytes, uint64_t(N),
-                        row_bytes, 144, kWT * kBM, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_tmap_2d(&args.xh_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, uint64_t(K), uint64_t(M),
-                        uint64_t(K) * 2, kSlabK, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
-        return Q2_0_ECUDA;
-    if (split && !encode_tmap_2d(&args.xl_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xl, uint64_t(K),
-                                 uint64_t(M), uint64_t(K) * 2, kSlabK, kBN,
-                                 CU_TENSOR_MAP_SWIZZLE_128B))
-        return Q2_0_ECUDA;
-    args.y = y;
-    args.M = int(M);
-    args.N = int(N);
-    args.K = int(K);
+    if (!make_gemm_job(args.single, w, xh, xl, y, row_shift, M, N, K, 0)) return Q2_0_ECUDA;
+    args.jobs = nullptr;
+    args.n_jobs = 1;
     args.split = split;
-    args.err = err;
-    args.n_mtiles = L.n_mtiles;
-    args.n_units = L.n_units;
     args.total_slabs = L.total_slabs;
     args.partials = partials;
-    args.row_shift = row_shift;
-    if (ensure_attr() != cudaSuccess) return Q2_0_ECUDA;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(L.grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = gemm_smem_bytes();
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemm_tc_kernel, args) != cudaSuccess) return Q2_0_ECUDA;
-    // the stream-K reduction, as a programmatic dependent of the GEMM
-    cfg.gridDim = dim3(kReduceSlices, L.grid);
-    cfg.blockDim = dim3(kReduceThreads);
-    cfg.dynamicSmemBytes = 0;
-    if (cudaLaunchKernelEx(&cfg, gemm_reduce_kernel, static_cast<const float *>(partials),
-                           static_cast<const int *>(row_shift), y, int(M), int(N), L.n_mtiles,
-                           int(K / kSlabK), L.total_slabs) !=
-        cudaSuccess)
+    args.err = err;
+    return cuda_status(launch_gemm_pair(args, L.grid, s));
+}
+
+}  // namespace q2
+
+// ---------------------------------------------------------------------------
+// Grouped GEMM plans
+// ---------------------------------------------------------------------------
+struct q2_0_mm_plan {
+    int device = 0;
+    int grid = 0;
+    int n_fast = 0;
+    q2::GemmArgs args;                       // the tensor-core launch (jobs in device memory)
+    q2::GemmJob *d_jobs = nullptr;
+    uint8_t *d_mem = nullptr;                // X copies and row exponents, then partial tiles
+    std::vector<q2::GemmPrepSet> prep;       // up to 8 distinct X per prep launch
+    std::vector<int> prep_n, prep_max_m;
+    std::vector<q2_0_mm_desc> generic;       // descriptors outside the TMA path
+};
+
+namespace q2 {
+
+void mm_plan_destroy(q2_0_mm_plan *plan) {
+    if (!plan) return;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(plan->device);
+    cudaFree(plan->d_jobs);
+    cudaFree(plan->d_mem);
+    cudaSetDevice(cur);
+    delete plan;
+}
+
+int mm_plan_create(const q2_0_mm_desc *descs, int n, int prec, q2_0_mm_plan **out) {
+    q2_0_mm_plan *P = new q2_0_mm_plan();
+    cudaGetDevice(&P->device);
+    std::memset(&P->args, 0, sizeof(P->args));
+    P->args.err = error_word_ptr();
+    if (!P->args.err) {
+        delete P;
         return Q2_0_ECUDA;
-    return cuda_status(cudaGetLastError());
+    }
+    const int split = prec == Q2_0_PREC_F16_SPLIT ? 1 : 0;
+    std::vector<int> fast;
+    for (int i = 0; i < n; ++i) {
+        if (tc_path_ok(descs[i].w, descs[i].x, descs[i].K))
+            fast.push_back(i);
+        else
+            P->generic.push_back(descs[i]);
+    }
+    P->n_fast = int(fast.size());
+    if (P->n_fast == 0) {
+        *out = P;
+        return Q2_0_OK;
+    }
+    // Distinct activation matrices: products with the same (x, M, K) share the
+    // prepass output. Memory per X: X_hi, X_lo (split), row exponents.
+    struct XEnt {
+        const float *x;
+        int64_t M, K;
+        size_t off_h, off_l, off_s;
+    };
+    std::vector<XEnt> xs;
+    std::vector<int> x_of(P->n_fast);
+    size_t total = 0;
+    for (int j = 0; j < P->n_fast; ++j) {
+        const q2_0_mm_desc &d = descs[fast[j]];
+        int hit = -1;
+        for (int e = 0; e < int(xs.size()); ++e)
+            if (xs[e].x == d.x && xs[e].M == d.M && xs[e].K == d.K) hit = e;
+        if (hit < 0) {
+            XEnt e;
+            e.x = d.x;
+            e.M = d.M;
+            e.K = d.K;
+            const size_t part = align256(size_t(d.M) * d.K * 2);
+            e.off_h = total;
+            e.off_l = total + part;
+            e.off_s = total + (split ? 2 : 1) * part;
+            total = e.off_s + align256(size_t(d.M) * 4);
+            hit = int(xs.size());
+            xs.push_back(e);
+        }
+        x_of[j] = hit;
+    }
+    long long total_slabs = 0;
+    std::vector<long long> slab0(P->n_fast);
+    for (int j = 0; j < P->n_fast; ++j) {
+        const q2_0_mm_desc &d = descs[fast[j]];
+        slab0[j] = total_slabs;
+        total_slabs += slabs_of(d.M, d.N, d.K);
+    }
+    P->grid = grid_of(total_slabs, sm_count());
+    const size_t partials_off = total;
+    total += size_t(2) * P->grid * kPartialBytes;
+    int st = Q2_0_OK;
+    if (cudaMalloc(&P->d_mem, total) != cudaSuccess ||
+        cudaMalloc(&P->d_jobs, sizeof(GemmJob) * P->n_fast) != cudaSuccess)
+        st = Q2_0_ECUDA;
+    std::vector<GemmJob> jobs(P->n_fast);
+    for (int j = 0; j < P->n_fast && st == Q2_0_OK; ++j) {
+        const q2_0_mm_desc &d = descs[fast[j]];
+        const XEnt &e = xs[x_of[j]];
+        const __half *xh = reinterpret_cast<const __half *>(P->d_mem + e.off_h);
+        const __half *xl = split ? reinterpret_cast<const __half *>(P->d_mem + e.off_l) : nullptr;
+        const int *rs = reinterpret_cast<const int *>(P->d_mem + e.off_s);
+        if (!make_gemm_job(jobs[j], static_cast<const uint8_t *>(d.w), xh, xl, d.y, rs, d.M, d.N,
+                           d.K, slab0[j]))
+            st = Q2_0_ECUDA;
+    }
+    if (st == Q2_0_OK && cudaMemcpy(P->d_jobs, jobs.data(), sizeof(GemmJob) * P->n_fast,
+                                    cudaMemcpyHostToDevice) != cudaSuccess)
+        st = Q2_0_ECUDA;
+    if (st != Q2_0_OK) {
+        mm_plan_destroy(P);
+        return st;
+    }
+    for (int e0 = 0; e0 < int(xs.size()); e0 += kMaxPrepX) {
+        GemmPrepSet ps;
+        std::memset(&ps, 0, sizeof(ps));
+        ps.split = split;
+        int cnt = 0, max_m = 0;
+        for (int e = e0; e < int(xs.size()) && cnt < kMaxPrepX; ++e, ++cnt) {
+            ps.x[cnt] = xs[e].x;
+            ps.xh[cnt] = reinterpret_cast<__half *>(P->d_mem + xs[e].off_h);
+            ps.xl[cnt] = split ? reinterpret_cast<__half *>(P->d_mem + xs[e].off_l) : nullptr;
+            ps.row_shift[cnt] = reinterpret_cast<int *>(P->d_mem + xs[e].off_s);
+            ps.M[cnt] = int(xs[e].M);
+            ps.K[cnt] = int(xs[e].K);
+            max_m = std::max(max_m, int(xs[e].M));
+        }
+        P->prep.push_back(ps);
+        P->prep_n.push_back(cnt);
+        P->prep_max_m.push_back(max_m);
+    }
+    P->args.jobs = P->d_jobs;
+    P->args.n_jobs = P->n_fast;
+    P->args.split = split;
+    P->args.total_slabs = total_slabs;
+    P->args.partials = reinterpret_cast<float *>(P->d_mem + partials_off);
+    *out = P;
+    return Q2_0_OK;
+}
+
+int mm_plan_execute(const q2_0_mm_plan *P, cudaStream_t s) {
+    for (size_t i = 0; i < P->prep.size(); ++i)
+        if (launch_prep<float>(P->prep[i], P->prep_n[i], P->prep_max_m[i], s) != cudaSuccess)
+            return Q2_0_ECUDA;
+    if (P->n_fast > 0 && launch_gemm_pair(P->args, P->grid, s) != cudaSuccess) return Q2_0_ECUDA;
+    for (const q2_0_mm_desc &d : P->generic)
+        if (launch_generic(static_cast<const uint8_t *>(d.w), d.x, d.y, d.N, d.K, d.M, s) !=
+            cudaSuccess)
+            return Q2_0_ECUDA;
+    return Q2_0_OK;
+}
+
+int mm_plan_launches(const q2_0_mm_plan *P) {
+    return int(P->prep.size()) + (P->n_fast > 0 ? 2 : 0) + int(P->generic.size());
 }
 
 }  // namespace q2

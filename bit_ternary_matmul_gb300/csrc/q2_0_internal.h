@@ -88,4 +88,10 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int prec);
 int gemm_run(const uint8_t *w, const void *x, int xtype, float *y, int64_t N, int64_t K,
              int64_t M, int prec, void *ws, size_t ws_bytes, cudaStream_t s);
 
+// grouped GEMM plans (opaque to the C ABI); F32 x
+int mm_plan_create(const q2_0_mm_desc *descs, int n, int prec, q2_0_mm_plan **plan);
+int mm_plan_execute(const q2_0_mm_plan *plan, cudaStream_t s);
+int mm_plan_launches(const q2_0_mm_plan *plan);
+void mm_plan_destroy(q2_0_mm_plan *plan);
+
 }  // namespace q2

@@ -217,6 +217,45 @@ int q2_0_mul_mat_f16(const void *w, const void *x, float *y, int64_t N, int64_t 
                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Grouped prefill GEMM: several independent products Y = W X^T (e.g. the
+ * gate and up projections of one layer, which read the same X) run as one
+ * launch of the tensor-core kernel over the pooled output tiles, with one
+ * activation prepass and one stream-K reduction for all of them.
+ * q2_0_mm_plan_create records the descriptors (the pointers are kept, not the
+ * data), prepares each distinct activation matrix once (descriptors with the
+ * same x, M and K share it), encodes the TMA descriptors and allocates the
+ * plan's device memory: per distinct X, the fp16 hi (and lo) copies and the
+ * row exponents; the stream-K partial tiles (2 x 128 KB per SM). Each
+ * descriptor obeys q2_0_mul_mat's rules and its bound; all share prec. A
+ * descriptor outside the fast path (K % 512 != 0, w or x not 16-byte aligned)
+ * runs the CUDA-core kernel inside execute. q2_0_mm_plan_execute launches the
+ * work on `stream` (the prepass, one launch per 8 distinct X; the tensor-core
+ * kernel; the reduction; one launch per CUDA-core descriptor); it allocates
+ * nothing and may be captured in a CUDA graph. Products must not write to
+ * memory that another product of the same plan reads or writes.
+ * Errors: Q2_0_EINVAL for a null pointer, n_desc < 1, N or M outside
+ * [1, 2^31), K not a positive multiple of 64 or an unknown prec;
+ * Q2_0_EUNSUPPORTED for a device that is not compute capability 10.3;
+ * Q2_0_ECUDA when an allocation, a copy or a TMA descriptor fails.
+ */
+typedef struct q2_0_mm_desc {
+    const void *w;  /* N x K Q2_0 matrix */
+    const float *x; /* F32 [M][K] */
+    float *y;       /* F32 [M][N] */
+    int64_t N;
+    int64_t K;
+    int64_t M;
+} q2_0_mm_desc;
+
+typedef struct q2_0_mm_plan q2_0_mm_plan;
+
+int q2_0_mm_plan_create(const q2_0_mm_desc *descs, int n_desc, int prec, q2_0_mm_plan **plan);
+int q2_0_mm_plan_execute(const q2_0_mm_plan *plan, void *stream);
+/* Number of kernel launches one execute performs. */
+int q2_0_mm_plan_launches(const q2_0_mm_plan *plan);
+void q2_0_mm_plan_destroy(q2_0_mm_plan *plan);
+
+/*
  * Split layout — scales and codes in separate arrays, as the loader in
  * "kopitiam_runtime::gpu_offload" (section "Why the weight has to stay
  * quantized") splits a block format's scales from its quants. For an N x K

@@ -122,3 +122,21 @@ def test_argument_validation_without_gpu(L):
     assert L.q2_0_mv_plan_execute(null, null) == EINVAL
     assert L.q2_0_mv_plan_launches(null) == 0
     L.q2_0_mv_plan_destroy(null)
+    # grouped GEMM plans: null arguments, no descriptors, bad precision, and a
+    # descriptor with a bad K / M / null pointer are refused before any device call
+    assert L.q2_0_mm_plan_create(None, 1, 0, ctypes.byref(h)) == EINVAL
+    d = q._MmDesc(0x100000, 0x100000, 0x100000, 4, 512, 4)
+    arr = (q._MmDesc * 1)(d)
+    assert L.q2_0_mm_plan_create(arr, 1, 0, None) == EINVAL
+    assert L.q2_0_mm_plan_create(arr, 0, 0, ctypes.byref(h)) == EINVAL
+    assert L.q2_0_mm_plan_create(arr, 1, 2, ctypes.byref(h)) == EINVAL
+    for bad in (q._MmDesc(0x100000, 0x100000, 0x100000, 4, 100, 4),
+                q._MmDesc(0x100000, 0x100000, 0x100000, 4, 512, 0),
+                q._MmDesc(0x100000, 0x100000, 0x100000, 0, 512, 4),
+                q._MmDesc(0x100000, None, 0x100000, 4, 512, 4)):
+        two = (q._MmDesc * 2)(d, bad)
+        assert L.q2_0_mm_plan_create(two, 2, 0, ctypes.byref(h)) == EINVAL
+        assert not h.value
+    assert L.q2_0_mm_plan_execute(null, null) == EINVAL
+    assert L.q2_0_mm_plan_launches(null) == 0
+    L.q2_0_mm_plan_destroy(null)

@@ -395,6 +395,138 @@ def test_gemm_prefill_shapes_sampled(dev, N, K, M, prec):
 
 
 # ---------------------------------------------------------------------------
+# grouped GEMM plans: several products in one prepass, one tensor-core launch
+# over the pooled tiles and one stream-K reduction
+# ---------------------------------------------------------------------------
+def _mm_case(g, N, K, M, x=None):
+    w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+    if x is None:
+        x = synth.activations(g, M, K, synth.PREFILL_OUTLIER_FRAC, synth.PREFILL_OUTLIER)
+    return w, x
+
+
+@pytest.mark.parametrize("prec", [q.Q2_0_PREC_F16_SPLIT, q.Q2_0_PREC_F16])
+def test_mm_plan_parity_small(dev, prec):
+    """Five products: two share one X (one prepass for both), one has K % 512 != 0
+    (the CUDA-core kernel inside execute), ragged N and M everywhere; the pooled
+    slab order is cut into few-slab stream-K ranges that cross unit and product
+    boundaries."""
+    g = synth.rng(3401, prec)
+    shapes = [(300, 1024, 70), (513, 1024, 70), (130, 2048, 257), (40, 576, 9), (256, 512, 128)]
+    cases = []
+    for i, (N, K, M) in enumerate(shapes):
+        x_shared = cases[0][1] if i == 1 else None
+        cases.append(_mm_case(g, N, K, M, x_shared))
+    xs = {}
+    entries, ys = [], []
+    for (w, x), (N, K, M) in zip(cases, shapes):
+        xd = xs.setdefault(id(x), _to(dev, x))
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
+        entries.append((_to(dev, w), xd, y, N, K, M))
+        ys.append(y)
+    plan = q.MmPlan(entries, prec)
+    # one prepass launch (4 distinct X on the tensor-core path), the GEMM and its
+    # reduction, one CUDA-core launch
+    assert plan.launches == 4
+    plan.execute()
+    tol = TOL_SPLIT if prec == q.Q2_0_PREC_F16_SPLIT else TOL_F16
+    first = [y.clone() for y in ys]
+    for (w, x), (N, K, M), y in zip(cases, shapes, ys):
+        yo, acc = oracle.matmul(w, N, K, x)
+        _assert_close(y.cpu().numpy(), yo, acc, tol, f"GEMM plan {N}x{K} M={M} prec={prec}")
+    # deterministic: a second execute, and a CUDA-graph replay, give the same bits
+    for y in ys:
+        y.fill_(float("nan"))
+    plan.execute()
+    for a, b in zip(first, ys):
+        assert torch.equal(a, b)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=s):
+        plan.execute(s)
+    for y in ys:
+        y.fill_(float("nan"))
+    gr.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(first, ys):
+        assert torch.equal(a, b)
+    plan.close()
+    _no_device_error()
+
+
+def test_mm_plan_many_activations(dev):
+    """Ten products with ten distinct X: two prepass launches of up to 8 each."""
+    g = synth.rng(3402)
+    shapes = [(64 + 37 * i, 512 * (1 + i % 3), 3 + 11 * i) for i in range(10)]
+    cases = [_mm_case(g, N, K, M) for (N, K, M) in shapes]
+    entries, ys = [], []
+    for (w, x), (N, K, M) in zip(cases, shapes):
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        entries.append((_to(dev, w), _to(dev, x), y, N, K, M))
+        ys.append(y)
+    plan = q.MmPlan(entries)
+    assert plan.launches == 4
+    plan.execute()
+    for (w, x), (N, K, M), y in zip(cases, shapes, ys):
+        yo, acc = oracle.matmul(w, N, K, x)
+        _assert_close(y.cpu().numpy(), yo, acc, TOL_SPLIT, f"GEMM plan {N}x{K} M={M}")
+    plan.close()
+    _no_device_error()
+
+
+@pytest.mark.parametrize("prec", [q.Q2_0_PREC_F16_SPLIT, q.Q2_0_PREC_F16])
+def test_mm_plan_prefill_sampled(dev, prec):
+    """The 1.7B-class prefill products as one plan: gate and up (6144 x 2048)
+    on one X of 512 tokens, down (2048 x 6144) on its own X; 96 sampled weight
+    rows of each x all tokens."""
+    g = synth.rng(3403, prec)
+    M = 512
+    shapes = [(6144, 2048), (6144, 2048), (2048, 6144)]
+    x1 = synth.activations(g, M, 2048, synth.PREFILL_OUTLIER_FRAC, synth.PREFILL_OUTLIER)
+    x2 = synth.activations(g, M, 6144, synth.PREFILL_OUTLIER_FRAC, synth.PREFILL_OUTLIER)
+    xd1, xd2 = _to(dev, x1), _to(dev, x2)
+    ws, entries, ys = [], [], []
+    for i, (N, K) in enumerate(shapes):
+        w = synth.packed_matrix(g, N, K, *synth.DECODE_SCALE, synth.DECODE_FRAC_CODE3)
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        entries.append((_to(dev, w), xd2 if i == 2 else xd1, y, N, K, M))
+        ws.append(w)
+        ys.append(y)
+    plan = q.MmPlan(entries, prec)
+    assert plan.launches == 3
+    plan.execute()
+    tol = TOL_SPLIT if prec == q.Q2_0_PREC_F16_SPLIT else TOL_F16
+    for i, ((N, K), w, y) in enumerate(zip(shapes, ws, ys)):
+        x = x2 if i == 2 else x1
+        rows = np.unique(np.concatenate([[0, 255, 256, N - 1], g.integers(0, N, 92)]))
+        yo, acc = oracle.matmul(w, N, K, x, rows=rows)
+        got = y[:, torch.from_numpy(rows).to(dev)].cpu().numpy()
+        _assert_close(got, yo, acc, tol, f"GEMM plan {N}x{K} M={M} prec={prec}")
+    plan.close()
+    _no_device_error()
+
+
+def test_mm_plan_wide_range(dev):
+    """The wide-range activation kinds, one product each, in one plan."""
+    N, K, M = 260, 2048, 24
+    cases = [wr.wide_range_case(kind, synth.rng(3404, i), N, K, M)
+             for i, kind in enumerate(wr.WIDE_KINDS)]
+    entries, ys = [], []
+    for w, x in cases:
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        entries.append((_to(dev, w), _to(dev, x), y, N, K, M))
+        ys.append(y)
+    plan = q.MmPlan(entries)
+    plan.execute()
+    for kind, (w, x), y in zip(wr.WIDE_KINDS, cases, ys):
+        yo, acc = oracle.matmul(w, N, K, x)
+        _assert_close(y.cpu().numpy(), yo, acc, TOL_SPLIT, f"GEMM plan {kind}")
+    plan.close()
+    _no_device_error()
+
+
+# ---------------------------------------------------------------------------
 # F16 activations (the missing path of the WebGPU port's limitations paragraph)
 # ---------------------------------------------------------------------------
 F16_MV_CASES = [(2048, 2048, 1), (300, 2048, 2), (257, 1536, 3), (1000, 6144, 4),
