@@ -231,10 +231,16 @@ int q2_0_mul_mat_f16(const void *w, const void *x, float *y, int64_t N, int64_t 
  * runs the CUDA-core kernel inside execute. q2_0_mm_plan_execute launches the
  * work on `stream` (the prepass, one launch per 8 distinct X; the tensor-core
  * kernel; the reduction; one launch per CUDA-core descriptor); it allocates
- * nothing and may be captured in a CUDA graph. Products must not write to
- * memory that another product of the same plan reads or writes.
+ * nothing and may be captured in a CUDA graph. Each execute reads the
+ * current contents of every w and x and writes every y, so the caller may
+ * refill x between executes. Products must not write to memory that another
+ * product of the same plan reads or writes, and two executes of one plan must
+ * not overlap on the GPU (they share the plan's scratch).
+ * Ownership: the plan belongs to the device current at creation; execute it
+ * on a stream of that device. q2_0_mm_plan_destroy frees its device memory;
+ * call it after the last execute has completed.
  * Errors: Q2_0_EINVAL for a null pointer, n_desc < 1, N or M outside
- * [1, 2^31), K not a positive multiple of 64 or an unknown prec;
+ * [1, 2^31), K not a multiple of 64 in [64, 2^30] or an unknown prec;
  * Q2_0_EUNSUPPORTED for a device that is not compute capability 10.3;
  * Q2_0_ECUDA when an allocation, a copy or a TMA descriptor fails.
  */
