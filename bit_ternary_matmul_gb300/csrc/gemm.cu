@@ -132,8 +132,8 @@ __host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
 // hi (and lo) [M][K] in the permuted K order, each row scaled by a power of
 // two first. Row m with M_m = max |x| = f * 2^e (f in [0.5, 1)) is multiplied
 // by 2^s, s = 15 - e, so that its largest element lies in [2^14, 2^15): hi
-// never overflows fp16, and the lo parts of small elements stay above fp16's
-// subnormal range down to 2^-29 of the row maximum. F16 rows are only scaled
+// never overflows fp16, and hi + lo hold each element to 2^-22 of its value
+// plus 2^-39 of the row maximum. F16 rows are only scaled
 // up (s >= 0), which keeps them exact. The scaling is exact and undone on the
 // f32 result (y = acc * 2^-s). One CTA per row and grid row y per activation
 // matrix of the launch; X 16-byte aligned.

@@ -64,12 +64,13 @@ typedef enum q2_0_status {
  * scaled by an exact power of two that puts its largest |x| in [2^14, 2^15), and
  * the f32 result is scaled back, so any finite x is in range:
  *   Q2_0_PREC_F16_SPLIT: x = hi + lo with hi = fp16(x), lo = fp16(x - hi); two
- *     tensor-core products. Each element keeps 22 bits of its own value (down to
- *     2^-29 of its row's largest |x|); tolerance |y - exact| <= 1e-5 * sum|w*x|
- *     + 1e-7. The products are exact; the f32 accumulation over K/16 tensor-core
+ *     tensor-core products. Each element x is held to within 2^-22 |x| + 2^-39 M
+ *     (M its row's largest |x|): 22 bits of its own value down to 2^-18 M;
+ *     tolerance |y - exact| <= 1e-5 * sum|w*x| + 1e-7. The products are exact; the f32 accumulation over K/16 tensor-core
  *     steps adds rounding that is far below that in practice, but whose
  *     worst-case bound grows as (K/16) * 2^-24 * sum|w*x|.
- *   Q2_0_PREC_F16: x rounded once to fp16 (11 bits). Tolerance <= 4e-3 * sum|w*x|.
+ *   Q2_0_PREC_F16: x rounded once to fp16, within 2^-11 |x| + 2^-39 M.
+ *     Tolerance <= 4e-3 * sum|w*x|.
  * Precondition of both: finite x, and |2d| <= 65504 (so that (q-1)*d is finite
  * in fp16). */
 typedef enum q2_0_prec { Q2_0_PREC_F16_SPLIT = 0, Q2_0_PREC_F16 = 1 } q2_0_prec;
