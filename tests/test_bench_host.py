@@ -1,5 +1,6 @@
 """Host logic of bench.py without a GPU: the max/sum reductions over ranks with
-two gloo processes, the clock-sample parser and the traffic bookkeeping."""
+two gloo processes, the clock-sample parser, the traffic bookkeeping and the
+prefill part's inputs."""
 import json
 import os
 import socket
@@ -82,3 +83,22 @@ def test_committed_traffic_tracks_sources():
         got = bench.committed_traffic(name)
         fresh = bench.source_sha256(entry["sources"]) == entry["sha256"]
         assert (got is not None) == fresh
+
+
+def test_prefill_inputs_share_x_between_gate_and_up():
+    """The prefill part's workload: gate and up read one X (M x 2048), down its
+    own (M x 6144); the device entries copy a shared X once and every entry
+    carries its own output of M x N."""
+    gm = bench.gemm_inputs()
+    names = [n for n, *_ in gm]
+    assert names == ["gate", "up", "down"]
+    (_, Ng, Kg, wg, xg), (_, Nu, Ku, wu, xu), (_, Nd, Kd, wd, xd) = gm
+    assert (Ng, Kg, Nu, Ku, Nd, Kd) == (6144, 2048, 6144, 2048, 2048, 6144)
+    assert xg is xu and xd is not xg
+    assert xg.shape == (bench.PREFILL_M, 2048) and xd.shape == (bench.PREFILL_M, 6144)
+    assert wg.size == 6144 * 2048 // 64 * 18 and not (wg == wu).all()
+    ents = bench.gemm_device_entries(torch, torch.device("cpu"), gm, bench.PREFILL_M)
+    assert ents[0][1] is ents[1][1] and ents[2][1] is not ents[0][1]
+    assert [tuple(e[2].shape) for e in ents] == [(bench.PREFILL_M, 6144)] * 2 + [(bench.PREFILL_M, 2048)]
+    assert [e[3:] for e in ents] == [(6144, 2048, bench.PREFILL_M)] * 2 + [(2048, 6144, bench.PREFILL_M)]
+    assert bench.gemm_flops_512() == 2.0 * bench.PREFILL_M * (2 * 6144 * 2048 + 2048 * 6144)
